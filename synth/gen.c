@@ -1,0 +1,142 @@
+/*
+ * Seeded synthetic-input generator for the routed-MoE FFN block.
+ *
+ * This file holds no arithmetic of the block itself: it only draws numbers.
+ * Both the CPU oracle and the CUDA path take their inputs from it.
+ *
+ * Every value is a pure function of (seed, tensor id, attempt, element index):
+ *   key   = mix(mix(seed) ^ mix(tensor << 32 | attempt))
+ *   h_i   = mix(key + (i + 1) * 0x9E3779B97F4A7C15)        (SplitMix64 stream)
+ * where mix() is the SplitMix64 output function (Steele, Lea, Flood,
+ * "Fast splittable pseudorandom number generators", OOPSLA 2014).
+ *
+ * Normal draws use a variance-matched Irwin-Hall(4) variate: the four 16-bit
+ * fields of h_i are summed (an exact integer), centred, and scaled by one
+ * correctly rounded multiply.  Only integer operations and single IEEE
+ * multiplies/adds are involved, so x86-64 and AArch64 produce identical bits
+ * (build with -ffp-contract=off so no multiply-add is fused).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define GOLDEN 0x9E3779B97F4A7C15ULL
+
+static inline uint64_t mix64(uint64_t z) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+  return z ^ (z >> 31);
+}
+
+uint64_t synth_key(uint64_t seed, uint32_t tensor, uint32_t attempt) {
+  return mix64(mix64(seed + GOLDEN) ^ mix64((((uint64_t)tensor << 32) | attempt) + GOLDEN));
+}
+
+static inline uint64_t draw(uint64_t key, uint64_t i) { return mix64(key + (i + 1) * GOLDEN); }
+
+/* Irwin-Hall(4) of 16-bit uniforms, scaled to unit variance.  The sum of
+ * four uniforms on {0..65535} has mean 131070 and variance (65536^2-1)/3. */
+static inline double unit_normal(uint64_t h) {
+  const double scale = 2.6428997921303018e-05; /* sqrt(3 / (65536^2 - 1)) */
+  int64_t s = (int64_t)(h & 0xFFFFu) + (int64_t)((h >> 16) & 0xFFFFu) +
+              (int64_t)((h >> 32) & 0xFFFFu) + (int64_t)(h >> 48);
+  return (double)(s - 131070) * scale;
+}
+
+static inline uint16_t f32_to_bf16_rne(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+/* out[j] = float(mean + sigma * z) for element indices start .. start+n-1. */
+void synth_normal_f32(uint64_t seed, uint32_t tensor, uint32_t attempt, uint64_t start,
+                      uint64_t n, double mean, double sigma, float *out) {
+  const uint64_t key = synth_key(seed, tensor, attempt);
+#pragma omp parallel for schedule(static)
+  for (int64_t j = 0; j < (int64_t)n; ++j) {
+    double z = unit_normal(draw(key, start + (uint64_t)j));
+    double v = z * sigma;
+    v = v + mean;
+    out[j] = (float)v;
+  }
+}
+
+/* Same draw, multiplied by `gain` (applied before rounding), stored as bf16 (round to nearest even). */
+void synth_normal_bf16(uint64_t seed, uint32_t tensor, uint32_t attempt, uint64_t start,
+                       uint64_t n, double mean, double sigma, double gain, uint16_t *out) {
+  const uint64_t key = synth_key(seed, tensor, attempt);
+#pragma omp parallel for schedule(static)
+  for (int64_t j = 0; j < (int64_t)n; ++j) {
+    double z = unit_normal(draw(key, start + (uint64_t)j));
+    double v = z * sigma;
+    v = v + mean;
+    v = v * gain;
+    out[j] = f32_to_bf16_rne((float)v);
+  }
+}
+
+/* Rows of a matrix whose row r is drawn with attempt attempts[r]:
+ * out[r*row_len + c] = float(sigma * z(key(seed, tensor, attempts[r]), r*row_len + c)). */
+void synth_normal_rows_f32(uint64_t seed, uint32_t tensor, const int32_t *attempts,
+                           uint64_t row0, uint64_t rows, uint64_t row_len, double sigma,
+                           float *out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < (int64_t)rows; ++r) {
+    const uint64_t key = synth_key(seed, tensor, (uint32_t)attempts[r]);
+    const uint64_t base = ((uint64_t)r + row0) * row_len;
+    for (uint64_t c = 0; c < row_len; ++c) {
+      double z = unit_normal(draw(key, base + c));
+      out[(uint64_t)r * row_len + c] = (float)(z * sigma);
+    }
+  }
+}
+
+/* Uniform integers in [lo, hi): lo + floor(u32 * (hi - lo) / 2^32). */
+void synth_uniform_i32(uint64_t seed, uint32_t tensor, uint32_t attempt, uint64_t start,
+                       uint64_t n, int64_t lo, int64_t hi, int32_t *out) {
+  const uint64_t key = synth_key(seed, tensor, attempt);
+  const uint64_t span = (uint64_t)(hi - lo);
+#pragma omp parallel for schedule(static)
+  for (int64_t j = 0; j < (int64_t)n; ++j) {
+    uint64_t u = draw(key, start + (uint64_t)j) >> 32;
+    out[j] = (int32_t)(lo + (int64_t)((u * span) >> 32));
+  }
+}
+
+/* Each row r (row0 <= r < row0+rows) receives k distinct values drawn uniformly
+ * from [0, n_values), in draw order; duplicates are redrawn from the next
+ * counter.  Returns 0, or -1 when k > n_values. */
+int synth_distinct_rows_i32(uint64_t seed, uint32_t tensor, uint64_t row0, uint64_t rows,
+                            int32_t k, int32_t n_values, int32_t *out) {
+  if (k > n_values || k <= 0 || k > 64) return -1;
+  const uint64_t key = synth_key(seed, tensor, 0);
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < (int64_t)rows; ++r) {
+    int32_t *row = out + r * k;
+    uint64_t ctr = ((uint64_t)r + row0) << 20;
+    int have = 0;
+    while (have < k) {
+      uint64_t u = draw(key, ctr++) >> 32;
+      int32_t v = (int32_t)((u * (uint64_t)n_values) >> 32);
+      int dup = 0;
+      for (int q = 0; q < have; ++q) dup |= (row[q] == v);
+      if (!dup) row[have++] = v;
+    }
+  }
+  return 0;
+}
+
+/* Fisher-Yates permutation of 0..n-1. */
+void synth_permutation(uint64_t seed, uint32_t tensor, int32_t n, int32_t *out) {
+  const uint64_t key = synth_key(seed, tensor, 0);
+  for (int32_t i = 0; i < n; ++i) out[i] = i;
+  for (int32_t i = n - 1; i > 0; --i) {
+    uint64_t u = draw(key, (uint64_t)i) >> 32;
+    int32_t j = (int32_t)((u * (uint64_t)(i + 1)) >> 32);
+    int32_t t = out[i];
+    out[i] = out[j];
+    out[j] = t;
+  }
+}
