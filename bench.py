@@ -1,0 +1,405 @@
+"""Throughput of the GB300 MoE-FFN block (tokens/s per layer) on the synthetic workloads.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                    [--extra | --no-extra]
+
+One step = one forward of the whole block (HC prelude, router, experts, reduce, HC post) over one
+batch of the workload, inputs resident in HBM, L2 flushed (a 256 MB write) before every step, each
+step timed with CUDA events on the forward's stream.  Rank 0 prints one JSON line.  With N > 1
+(torchrun) every rank runs its own replica of the workload (rows are independent: no collective
+on the data path), the time is the max over ranks and the value counts every rank's tokens.
+
+--impl reference times the CPU oracle instead (the only other arm: the pages ship no runnable
+implementation), on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+from dataclasses import replace
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE-FFN layer tokens/s (decode B=1/4, prefill 512) + % of HBM/TC roofline"
+DEFAULT_WORKLOAD = "c1_decode_b1"
+EXTRA_WORKLOADS = ["c2_decode_b4_hash", "c3_prefill_512", "c4_prefill_4096"]
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def describe(cfg) -> str:
+    route = "hash" if cfg.is_hash else "score"
+    extra = {"c3_prefill_512": ", Zipf(1.1) expert popularity", "c4_prefill_4096": ", 8 hot experts (router rows x3)"}
+    return (f"{cfg.name}: rows={cfg.rows}, hidden={cfg.hidden}, hc={cfg.hc}, experts={cfg.experts}, "
+            f"top_k={cfg.top_k}, inter={cfg.inter}, shared expert inter={cfg.shared_inter}, {route} routing"
+            f"{extra.get(cfg.name, '')}, seed {cfg.seed}")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---- algorithmic work ----------------------------------------------------------------------------
+
+def work_model(cfg, indices: np.ndarray) -> dict:
+    """Algorithmic bytes and flops of one forward from its routing (indices [rows, top_k])."""
+    R, D, I, E, HC, M = cfg.rows, cfg.hidden, cfg.inter, cfg.experts, cfg.hc, cfg.mix
+    valid = (indices >= 0) & (indices < E)
+    groups = len(np.unique(indices[valid])) + 1          # touched routed experts + shared
+    slots = int(valid.sum()) + R                          # (row, expert) pairs incl. shared
+    w_gateup = groups * 2 * I * D * 2
+    w_down = groups * D * I * 2
+    state = R * HC * D * 4
+    small = M * HC * D * 2 + E * D * 2                    # hc_fn + router
+    flops_experts = slots * 2 * 3 * I * D
+    flops_router = R * (2 * E * D + 2 * M * HC * D)
+    return dict(groups=groups, slots=slots, w_gateup=w_gateup, w_down=w_down, state=state, small=small,
+                bytes_total=w_gateup + w_down + small + 2 * state, flops_total=flops_experts + flops_router,
+                flops_gateup=slots * 2 * 2 * I * D, flops_down=slots * 2 * I * D)
+
+
+def kernel_work(name: str, wm: dict, cfg) -> tuple[str, float]:
+    """(bound, algorithmic bytes or flops) of one launch of a kernel of the forward."""
+    R, D, I, HC, E, K = cfg.rows, cfg.hidden, cfg.inter, cfg.hc, cfg.experts, cfg.top_k
+    if name in ("decode_gateup", "gemm_gateup"):
+        return "hbm", wm["w_gateup"] + (wm["slots"] * (D + I) * (2 if name == "gemm_gateup" else 4))
+    if name in ("decode_down", "gemm_down"):
+        return "hbm", wm["w_down"] + wm["slots"] * (I * 2 + D * 4) * (1 if name == "gemm_down" else 0)
+    if name == "hc_mix":
+        return "hbm", wm["state"] + cfg.mix * HC * D * 2
+    if name == "decode_router":
+        return "hbm", wm["state"] + E * D * 2
+    if name == "prenorm":
+        return "hbm", wm["state"] + 2 * R * D * 4
+    if name == "router_gemm":
+        return "hbm", R * D * 4 + E * D * 2 + R * E * 4
+    if name in ("decode_combine", "post"):
+        return "hbm", 2 * wm["state"] + (wm["slots"] * D * 4 if name == "post" else 0)
+    if name == "scatter":
+        return "hbm", wm["slots"] * D * (4 + 2)
+    return "hbm", R * K * 4
+
+
+# ---- clocks ----------------------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.index), "-lms", "100"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---- our arm --------------------------------------------------------------------------------------
+
+def run_ours(cfg, steps: int, warmup: int, device, rank: int, world: int, dist, peaks, peak_kind,
+             want_e2e: bool, soak_s: float = 1.0) -> dict:
+    import torch
+
+    from deepseek_v4_moe_gb300 import MoeFFN, config_from
+    from synth.device import upload
+
+    case = synth.Case(cfg)
+    dev = upload(case, device)
+    m = MoeFFN(config_from(cfg), {cfg.layer: dev["weights"]})
+    stream = torch.cuda.Stream(device)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    out = torch.empty_like(dev["state"])
+    tok = dev["token_ids"]
+
+    def step():
+        m.forward(dev["state"], tok, cfg.layer, out=out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(warmup, 3)):
+            flush.fill_(1.0)
+            step()
+    torch.cuda.synchronize(device)
+    indices = m.debug("indices")
+    wm = work_model(cfg, indices)
+
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    t_end = time.perf_counter() + soak_s  # load the GPU so the clock samples see this work
+    with torch.cuda.stream(stream):
+        while time.perf_counter() < t_end:
+            flush.fill_(1.0)
+            step()
+            stream.synchronize()
+    # ---- timed region: K steps, each bracketed by events on the forward's stream ----
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+    torch.cuda.synchronize(device)
+    wall1 = time.perf_counter()
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = float(sum(ms))
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    res = dict(total_ms=total_ms, ms_per_step=total_ms / steps, median_ms=statistics.median(ms),
+               value=world * cfg.rows * steps / (total_ms / 1e3), wall_s=wall1 - wall0, clocks=clocks, wm=wm)
+
+    # ---- per-kernel durations: the same steps again with stage events ----
+    m.set_stage_timing(True)
+    per = {}
+    n_kernels = 0
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush.fill_(float(i))
+            step()
+            st = m.stage_times()
+            n_kernels = len(st)
+            for name, t in st:
+                per.setdefault(name, []).append(t)
+    m.set_stage_timing(False)
+    kernels = []
+    tot = sum(statistics.mean(v) for v in per.values())
+    for name, v in per.items():
+        avg = statistics.mean(v)
+        bound, work = kernel_work(name, wm, cfg)
+        gbs = work / (avg * 1e-3) / 1e9
+        kernels.append(dict(name=name, avg_us=round(avg * 1e3, 2), share=round(avg / tot, 4),
+                            alg_bytes=int(work), gbs=round(gbs, 1), frac_hbm=round(gbs / peaks["hbm_gbs"], 4)))
+    kernels.sort(key=lambda k: -k["avg_us"])
+    top = kernels[0]
+    res["kernels"] = kernels
+    res["gpu_launches"] = n_kernels * steps
+    res["roofline"] = {"bound": "hbm", "kernel": top["name"], "achieved": top["gbs"], "peak": peaks["hbm_gbs"],
+                       "unit": "GB/s", "frac": top["frac_hbm"], "traffic": None,
+                       "peak_source": f"{peak_kind} hbm_gbs (copy)"}
+    # whole forward against its binding roofline
+    t_hbm = wm["bytes_total"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = wm["flops_total"] / (peaks["bf16_tflops"] * 1e12)
+    step_s = res["ms_per_step"] / 1e3
+    res["forward_roofline"] = {"alg_bytes": wm["bytes_total"], "alg_flops": wm["flops_total"],
+                               "hbm_frac": round(t_hbm / step_s, 4), "tensor_frac": round(t_tc / step_s, 4),
+                               "binding": "hbm" if t_hbm >= t_tc else "tensor",
+                               "binding_frac": round(max(t_hbm, t_tc) / step_s, 4),
+                               "distinct_experts": wm["groups"] - 1}
+
+    if want_e2e:
+        pin_in = torch.from_numpy(case.state.copy()).pin_memory()
+        pin_tok = torch.from_numpy(case.token_ids.copy()).pin_memory()
+        pin_out = torch.empty_like(pin_in).pin_memory()
+        a_in, a_tok, a_out = pin_in.numpy(), pin_tok.numpy(), pin_out.numpy()
+        for _ in range(max(warmup, 3)):
+            m.forward_host(a_in, a_tok, cfg.layer, a_out, stream=stream)
+        dts = []
+        for i in range(steps):
+            with torch.cuda.stream(stream):
+                flush.fill_(float(i))
+            stream.synchronize()
+            t0 = time.perf_counter()
+            m.forward_host(a_in, a_tok, cfg.layer, a_out, stream=stream)
+            dts.append(time.perf_counter() - t0)
+        e2e_s = sum(dts)
+        if dist is not None:
+            t = torch.tensor([e2e_s], dtype=torch.float64, device=device)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        res["e2e"] = {"value": round(world * cfg.rows * steps / e2e_s, 1), "unit": "tokens/s",
+                      "h2d_bytes_per_step": int(a_in.nbytes + a_tok.nbytes), "d2h_bytes_per_step": int(a_out.nbytes),
+                      "api": "moe_ffn_forward_host (pinned host buffers, synchronous)"}
+    m.close()
+    del dev, flush, out
+    torch.cuda.empty_cache()
+    return res
+
+
+# ---- oracle (CPU baseline and reference arm) ------------------------------------------------------
+
+class _CachedCase:
+    """The workload with its expert matrices drawn up front, so the oracle's timing holds its own
+    arithmetic only (the bf16 -> f64 widening included)."""
+
+    def __init__(self, case, experts):
+        self.__dict__.update(case.__dict__)
+        self._cache = {(w, int(e)): case.expert_matrix(w, int(e)) for e in experts for w in ("gate", "up", "down")}
+
+    def expert_matrix(self, which, e, out=None):
+        return self._cache[(which, int(e))]
+
+
+def oracle_rate(cfg, rows_sample: int, target_s: float):
+    """Oracle tokens/s on `rows_sample` rows of the workload (full block per row)."""
+    import oracle
+    n = max(1, rows_sample)
+    case = synth.Case(replace(cfg, rows=n))
+    st = oracle.prelude_and_route(case)
+    cached = _CachedCase(case, np.unique(st["indices"][(st["indices"] >= 0) & (st["indices"] < cfg.experts)]))
+    t0 = time.perf_counter()
+    oracle.forward_ffn_rows(cached)
+    dt = time.perf_counter() - t0
+    return n / dt, dt, n
+
+
+def run_reference(cfg, steps: int, warmup: int, budget_s: float = 150.0) -> dict:
+    import oracle
+    per_step_rows = 1
+    case = synth.Case(replace(cfg, rows=max(1, steps + warmup)))
+    st_all = oracle.prelude_and_route(case)
+    cached = _CachedCase(case, np.unique(st_all["indices"][(st_all["indices"] >= 0)
+                                                          & (st_all["indices"] < cfg.experts)]))
+    for i in range(warmup):
+        oracle.forward_ffn_rows(cached, rows=[i])
+    times = []
+    t_start = time.perf_counter()
+    for i in range(steps):
+        t0 = time.perf_counter()
+        oracle.forward_ffn_rows(cached, rows=[warmup + i])
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start > budget_s:
+            break
+    total = sum(times)
+    return dict(value=len(times) * per_step_rows / total, ms_per_step=1e3 * total / len(times), timed=len(times))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--extra", dest="extra", action="store_true", default=True)
+    ap.add_argument("--no-extra", dest="extra", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false", default=True)
+    args = ap.parse_args()
+    warmup = max(args.warmup, 3)
+    cfg = synth.CONFIGS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    peaks, peak_kind = load_peaks()
+    config = {"workload": describe(cfg), "rows_per_rank": cfg.rows, "layer": cfg.layer,
+              "l2": "flushed before every step (256 MB write)", "parallelism": f"replicas x{world}"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        ref = run_reference(cfg, args.steps, warmup)
+        cores = os.cpu_count()
+        line = {"impl": "reference", "metric": METRIC, "value": round(ref["value"], 4), "unit": "tokens/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": warmup, "ms_per_step": round(ref["ms_per_step"], 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": round(ref["value"], 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                 "sample": f"{ref['timed']} of {args.steps} steps timed (150 s budget), one row of the "
+                                           f"workload per step, expert weights drawn before timing"},
+                "e2e": {"value": round(ref["value"], 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl")
+        dist = tdist
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+
+    main_res = run_ours(cfg, args.steps, warmup, device, rank, world, dist, peaks, peak_kind, want_e2e=True)
+    workloads = {}
+    if args.extra:
+        for name in EXTRA_WORKLOADS:
+            if name == args.workload:
+                continue
+            c = synth.CONFIGS[name]
+            r = run_ours(c, max(10, args.steps // 5), warmup, device, rank, world, dist, peaks, peak_kind,
+                         want_e2e=False, soak_s=0.5)
+            workloads[name] = {"value": round(r["value"], 1), "unit": "tokens/s", "ms_per_step": round(r["ms_per_step"], 4),
+                               "forward_roofline": r["forward_roofline"], "top_kernel": r["kernels"][0],
+                               "clocks": r["clocks"]}
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_baseline:
+        rate, dt, n = oracle_rate(cfg, 8 if cfg.rows <= 4 else 4, 20.0)
+        cpu = {"value": round(rate, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{n} rows of the workload's distribution (whole block per row, f64 NumPy), {dt:.1f} s; "
+                         f"expert weights drawn before timing"}
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(main_res["value"], 1), "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": warmup, "ms_per_step": round(main_res["ms_per_step"], 5),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32 (bf16 weights)" if cfg.rows <= 4 else "fp16 tensor-core (f32 accumulate)",
+                "data": "synthetic", "config": config, "roofline": main_res["roofline"],
+                "forward_roofline": main_res["forward_roofline"], "kernels": main_res["kernels"],
+                "cpu_baseline": cpu, "e2e": main_res["e2e"], "gpu_launches": main_res["gpu_launches"],
+                "clocks": main_res["clocks"], "median_ms_per_step": round(main_res["median_ms"], 5),
+                "workloads": workloads}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

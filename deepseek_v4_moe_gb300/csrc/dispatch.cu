@@ -1,0 +1,158 @@
+// Token -> expert dispatch of the rows > 4 path, and the slot reduce + hc_post that closes it.
+//
+// The pages' mm_id path (expert_matmul with IdMmScratch in forward_ffn_rows, docs.rs "hf2q 0.1.3
+// .../deepseek4/ffn_forward.rs") groups routed rows by expert; here that is a histogram (counted by
+// the router), an exclusive scan, a tile list for the persistent grouped GEMMs, and a scatter of
+// (row, slot) pairs with their fp16 activation rows into expert-sorted order.  The shared expert is
+// the last group and holds every row.  The order of rows inside a group comes from atomics and
+// does not affect any result: each token's output column is computed alone.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+__global__ void __launch_bounds__(1024) build_tiles_kernel(int *__restrict__ counts, int E, int rows, int mb_gu,
+                                                           int mb_dn, int *__restrict__ offsets,
+                                                           int *__restrict__ cursor, int4 *__restrict__ tiles_gu,
+                                                           int4 *__restrict__ tiles_dn, int *__restrict__ n_tiles) {
+  __shared__ int cnt[kExpertsMax + 1], nb[kExpertsMax + 1], off[kExpertsMax + 2], toff[kExpertsMax + 2];
+  const int G = E + 1;
+  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+    const int c = g < E ? counts[g] : rows;
+    cnt[g] = c;
+    nb[g] = (c + 127) / 128;
+    if (g < E) counts[g] = 0;  // ready for the next forward
+    cursor[g] = 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    off[0] = 0;
+    toff[0] = 0;
+    for (int g = 0; g < G; ++g) {
+      off[g + 1] = off[g] + cnt[g];
+      toff[g + 1] = toff[g] + nb[g];
+    }
+    n_tiles[0] = toff[G] * mb_gu;
+    n_tiles[1] = toff[G] * mb_dn;
+  }
+  __syncthreads();
+  for (int g = threadIdx.x; g <= G; g += blockDim.x) offsets[g] = off[g];
+  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+    const int n = nb[g], c = cnt[g];
+    for (int m = 0; m < mb_gu; ++m)
+      for (int b = 0; b < n; ++b)
+        tiles_gu[toff[g] * mb_gu + m * n + b] = make_int4(g, m, b, min(128, c - b * 128));
+    for (int m = 0; m < mb_dn; ++m)
+      for (int b = 0; b < n; ++b)
+        tiles_dn[toff[g] * mb_dn + m * n + b] = make_int4(g, m, b, min(128, c - b * 128));
+  }
+}
+
+// One warp per (row, slot), slot top_k being the shared expert.
+__global__ void __launch_bounds__(256) scatter_kernel(const int *__restrict__ idx, const float *__restrict__ rw,
+                                                      const float *__restrict__ x, int rows, int K, int E, int D,
+                                                      const int *__restrict__ offsets, int *__restrict__ cursor,
+                                                      int2 *__restrict__ list, float *__restrict__ list_w,
+                                                      __half *__restrict__ x16) {
+  const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (w >= rows * (K + 1)) return;
+  const int r = w / (K + 1), k = w - r * (K + 1);
+  int g;
+  float wt;
+  if (k < K) {
+    const int e = idx[(size_t)r * K + k];
+    if (e < 0 || e >= E) return;
+    g = e;
+    wt = rw[(size_t)r * K + k];
+  } else {
+    g = E;
+    wt = 1.f;
+  }
+  int pos = 0;
+  if (lane == 0) {
+    pos = offsets[g] + atomicAdd(&cursor[g], 1);
+    list[pos] = make_int2(r, k);
+    list_w[pos] = wt;
+  }
+  pos = __shfl_sync(0xffffffffu, pos, 0);
+  const float *src = x + (size_t)r * D;
+  __half *dst = x16 + (size_t)pos * D;
+  for (int c = lane * 8; c < D; c += 256) {
+    const float4 a = *reinterpret_cast<const float4 *>(src + c);
+    const float4 b = *reinterpret_cast<const float4 *>(src + c + 4);
+    __half2 h[4];
+    h[0] = __floats2half2_rn(a.x, a.y);
+    h[1] = __floats2half2_rn(a.z, a.w);
+    h[2] = __floats2half2_rn(b.x, b.y);
+    h[3] = __floats2half2_rn(b.z, b.w);
+    *reinterpret_cast<uint4 *>(dst + c) = *reinterpret_cast<uint4 *>(h);
+  }
+}
+
+void launch_dispatch(const Dims &d, const Scratch &s, int rows, cudaStream_t st, StageTimer *tm) {
+  build_tiles_kernel<<<1, 1024, 0, st>>>(s.counts, d.experts, rows, d.inter / 128, d.hidden / 128, s.offsets,
+                                         s.cursor, s.tiles_gu, s.tiles_dn, s.n_tiles);
+  stage(tm, "build_tiles", st);
+  const int warps = rows * (d.top_k + 1);
+  scatter_kernel<<<(warps + 7) / 8, 256, 0, st>>>(s.idx, s.rw, s.ffn_norm, rows, d.top_k, d.experts, d.hidden,
+                                                  s.offsets, s.cursor, s.list, s.list_w, s.x16);
+  stage(tm, "scatter", st);
+}
+
+// ffn_out[r] = sum of the weighted slot outputs of row r (valid routed slots + shared);
+// out[r, i] = post[r, i] * ffn_out[r] + sum_j comb[r, i, j] * state[r, j].
+__global__ void __launch_bounds__(256) prefill_post_kernel(const float *__restrict__ y_slot,
+                                                           const int *__restrict__ idx, int K, int E,
+                                                           const float *__restrict__ state,
+                                                           const float *__restrict__ post,
+                                                           const float *__restrict__ comb, int D, int hc,
+                                                           float *__restrict__ ffn_out,
+                                                           float *__restrict__ out) {
+  const int r = blockIdx.x;
+  __shared__ int valid[kTopKMax];
+  __shared__ float pc[kHcMax + kHcMax * kHcMax];
+  if (threadIdx.x < K) {
+    const int e = idx[(size_t)r * K + threadIdx.x];
+    valid[threadIdx.x] = e >= 0 && e < E;
+  }
+  if (threadIdx.x < hc) pc[threadIdx.x] = post[(size_t)r * hc + threadIdx.x];
+  if (threadIdx.x < hc * hc) pc[kHcMax + threadIdx.x] = comb[(size_t)r * hc * hc + threadIdx.x];
+  __syncthreads();
+  const float *ys = y_slot + (size_t)r * (K + 1) * D;
+  for (int d = threadIdx.x * 4; d < D; d += blockDim.x * 4) {
+    float4 f = *reinterpret_cast<const float4 *>(ys + (size_t)K * D + d);
+    for (int k = 0; k < K; ++k) {
+      if (!valid[k]) continue;
+      const float4 y = *reinterpret_cast<const float4 *>(ys + (size_t)k * D + d);
+      f.x += y.x;
+      f.y += y.y;
+      f.z += y.z;
+      f.w += y.w;
+    }
+    *reinterpret_cast<float4 *>(ffn_out + (size_t)r * D + d) = f;
+    float4 sv[kHcMax];
+    for (int j = 0; j < hc; ++j) sv[j] = *reinterpret_cast<const float4 *>(state + ((size_t)r * hc + j) * D + d);
+    for (int o = 0; o < hc; ++o) {
+      const float p = pc[o];
+      float4 v = make_float4(p * f.x, p * f.y, p * f.z, p * f.w);
+      for (int j = 0; j < hc; ++j) {
+        const float c = pc[kHcMax + o * hc + j];
+        v.x += c * sv[j].x;
+        v.y += c * sv[j].y;
+        v.z += c * sv[j].z;
+        v.w += c * sv[j].w;
+      }
+      *reinterpret_cast<float4 *>(out + ((size_t)r * hc + o) * D + d) = v;
+    }
+  }
+}
+
+void launch_prefill_post(const Dims &d, const Scratch &s, const float *state, int rows, float *out_state,
+                         cudaStream_t st, StageTimer *tm) {
+  prefill_post_kernel<<<rows, 256, 0, st>>>(s.y_slot, s.idx, d.top_k, d.experts, state, s.post, s.comb, d.hidden,
+                                            d.hc, s.ffn_out, out_state);
+  stage(tm, "post", st);
+}
+
+}  // namespace moe

@@ -1,0 +1,105 @@
+// Host-side launchers of the MoE-FFN kernels, shared between the translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+struct Dims {
+  int hidden, hc, experts, top_k, inter, vocab, iters;
+  float eps;
+  int mix() const { return (2 + hc) * hc; }
+};
+
+// Scratch owned by the handle, sized for max_rows at init.
+struct Scratch {
+  int *status;            // [1] device status bits
+  float *mix_partial;     // [max_rows, mix_chunks, mix+1]
+  unsigned *tickets;      // [max(max_rows/4+1, 1) + 1] zero between launches
+  float *mixes, *pre, *post, *comb;  // [rows, mix] [rows, hc] [rows, hc] [rows, hc, hc]
+  float *ffn_input, *ffn_norm;       // [rows, hidden]
+  float *router_partial;  // [4, router_chunks, experts+1]
+  float *logits;          // [rows, experts]
+  int *idx;               // [rows, top_k]
+  float *rw;              // [rows, top_k]
+  unsigned *safe;         // [rows, top_k]
+  float *ffn_out;         // [rows, hidden]
+  // decode path
+  int *ngroups, *group_e, *group_mask;  // groups of (expert, rows using it); shared expert last
+  float *group_w;         // [groups, 4]
+  float *act_dec;         // [groups, 4, inter]
+  float *y_dec;           // [groups, 4, hidden]
+  // rows > 4 path
+  int *counts;            // [experts] routed slots per expert (zero between launches)
+  int *offsets;           // [experts + 2]
+  int *cursor;            // [experts + 1]
+  int4 *tiles_gu, *tiles_dn;  // (group, m-block, n-block, valid columns)
+  int *n_tiles;           // [2]: gate/up tiles, down tiles
+  int2 *list;             // [positions] (row, slot) in expert-sorted order; slot top_k = shared expert
+  float *list_w;          // [positions] route weight of that slot (1 for the shared expert)
+  __half *x16;            // [positions, hidden] ffn_norm rows in expert-sorted order (fp16)
+  __half *act16;          // [positions, inter] SwiGLU output in the same order (fp16)
+  float *y_slot;          // [rows, top_k + 1, hidden] weighted expert outputs
+  int max_rows, mix_chunks, router_chunks, max_positions, max_tiles_gu, max_tiles_dn;
+};
+
+// Optional per-kernel timing: an event after each kernel launch of a forward.
+struct StageTimer {
+  static constexpr int kMax = 16;
+  cudaEvent_t ev[kMax + 1];
+  const char *name[kMax];
+  int n = 0;
+  bool on = false, created = false;
+  void begin(cudaStream_t st) {
+    n = 0;
+    cudaEventRecord(ev[0], st);
+  }
+  void mark(const char *nm, cudaStream_t st) {
+    if (n < kMax) {
+      name[n] = nm;
+      cudaEventRecord(ev[n + 1], st);
+      ++n;
+    }
+  }
+};
+
+inline void stage(StageTimer *t, const char *nm, cudaStream_t st) {
+  if (t) t->mark(nm, st);
+}
+
+struct LayerDev {
+  const uint16_t *hc_fn;
+  const float *hc_base, *hc_scale, *ffn_norm, *exp_probs_b;
+  const uint16_t *gate;
+  const int32_t *tid2eid;
+  const uint16_t *gate_exps, *up_exps, *down_exps, *gate_sh, *up_sh, *down_sh;
+  __half *gate16, *up16, *down16;  // [(experts+1) * inter, hidden], [(experts+1) * hidden, inter]
+  CUtensorMap tm_gate, tm_up, tm_down;
+  bool has_weights;
+};
+
+// prelude.cu
+void launch_hc_mix(const Dims &d, const Scratch &s, const LayerDev &w, const float *state, int rows,
+                   cudaStream_t st, StageTimer *tm);
+void launch_decode_router(const Dims &d, const Scratch &s, const LayerDev &w, const float *state,
+                          const int32_t *token_ids, int rows, bool hash, cudaStream_t st, StageTimer *tm);
+void launch_prefill_router(const Dims &d, const Scratch &s, const LayerDev &w, const float *state,
+                           const int32_t *token_ids, int rows, bool hash, cudaStream_t st, StageTimer *tm);
+// decode.cu
+void launch_decode_experts(const Dims &d, const Scratch &s, const LayerDev &w, const float *state, int rows,
+                           float *out_state, int num_sms, cudaStream_t st, StageTimer *tm);
+cudaError_t decode_configure(int hidden);
+// dispatch.cu
+void launch_dispatch(const Dims &d, const Scratch &s, int rows, cudaStream_t st, StageTimer *tm);
+void launch_prefill_post(const Dims &d, const Scratch &s, const float *state, int rows, float *out_state,
+                         cudaStream_t st, StageTimer *tm);
+// gemm_tc.cu
+void launch_grouped_gemms(const Dims &d, const Scratch &s, const LayerDev &w, const CUtensorMap &tm_x16,
+                          const CUtensorMap &tm_act16, int num_sms, cudaStream_t st, StageTimer *tm);
+void launch_bf16_to_f16(const uint16_t *src, __half *dst, size_t n, cudaStream_t st);
+size_t gemm_smem_bytes(bool gateup);
+cudaError_t gemm_configure();
+
+}  // namespace moe

@@ -1,0 +1,403 @@
+// C ABI of the MoE-FFN block: validation, scratch ownership, and the order of kernel launches.
+// The argument checks mirror the guards of forward_ffn_rows (docs.rs "hf2q 0.1.3
+// .../deepseek4/ffn_forward.rs"): layer range, at least one row, rows*top_k overflow, routing
+// source present, output distinct from the input state.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "moe_ffn.h"
+
+using moe::Dims;
+using moe::LayerDev;
+using moe::Scratch;
+
+struct moe_ffn_handle {
+  moe_ffn_config cfg;
+  Dims dims;
+  int device = 0, num_sms = 0;
+  std::vector<LayerDev> layers;
+  Scratch s;
+  CUtensorMap tm_x16, tm_act16;
+  float *host_in = nullptr, *host_out = nullptr;  // device staging of moe_ffn_forward_host
+  int32_t *host_tok = nullptr;
+  std::vector<void *> allocs;
+  cudaStream_t last_stream = nullptr;
+  int last_rows = 0;
+  moe::StageTimer timer;
+  std::string err;
+};
+
+static std::string g_init_err;
+
+static int fail(moe_ffn_handle *h, int code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (h)
+    h->err = buf;
+  else
+    g_init_err = buf;
+  return code;
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int check_config(const moe_ffn_config *c) {
+  if (c->hc < 1 || c->hc > moe::kHcMax) return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "hc must be in 1..4");
+  if (c->hidden < 128 || c->hidden % 128 || c->hidden > 8192)
+    return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "hidden must be a multiple of 128 in 128..8192");
+  if (c->inter < 128 || c->inter % 128)
+    return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "inter must be a positive multiple of 128");
+  if (c->shared_inter != c->inter) return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "shared_inter must equal inter");
+  if (c->experts < 16 || c->experts > moe::kExpertsMax || c->experts % 16)
+    return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "experts must be a multiple of 16 in 16..512");
+  if (c->top_k < 1 || c->top_k > moe::kTopKMax || c->top_k > c->experts)
+    return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "top_k must be in 1..min(8, experts)");
+  if (c->n_layers < 1 || c->hash_layer_count < 0 || c->hash_layer_count > c->n_layers)
+    return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "need n_layers >= 1 and 0 <= hash_layer_count <= n_layers");
+  if (c->max_rows < 1 || c->max_rows > 65536) return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "max_rows must be in 1..65536");
+  if (c->vocab < 1) return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "vocab must be positive");
+  if (c->sinkhorn_iters < 0 || c->sinkhorn_iters > 100000)
+    return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "sinkhorn_iters out of range");
+  if (!(c->rms_eps >= 0.f)) return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "rms_eps must be >= 0");
+  return MOE_FFN_OK;
+}
+
+static int check_layer(const moe_ffn_config *c, int l, const moe_ffn_layer_weights *w, bool *has) {
+  const void *req[] = {w->hc_fn, w->hc_base, w->hc_scale, w->ffn_norm, w->gate, w->gate_exps,
+                       w->up_exps, w->down_exps, w->gate_sh, w->up_sh, w->down_sh};
+  int n_set = 0;
+  for (const void *p : req) n_set += p != nullptr;
+  if (n_set == 0 && !w->exp_probs_b && !w->tid2eid) {
+    *has = false;
+    return MOE_FFN_OK;
+  }
+  if (n_set != (int)(sizeof req / sizeof req[0]))
+    return fail(nullptr, MOE_FFN_ERR_NULL_PTR, "layer %d: some weight pointers are NULL", l);
+  const bool hash = l < c->hash_layer_count;
+  if (hash && !w->tid2eid) return fail(nullptr, MOE_FFN_ERR_NO_ROUTING_SOURCE, "layer %d has no routing source (tid2eid)", l);
+  if (!hash && !w->exp_probs_b)
+    return fail(nullptr, MOE_FFN_ERR_NO_ROUTING_SOURCE, "layer %d has no routing source (exp_probs_b)", l);
+  for (const void *p : req)
+    if (!aligned16(p)) return fail(nullptr, MOE_FFN_ERR_ALIGNMENT, "layer %d: weight pointer not 16-byte aligned", l);
+  *has = true;
+  return MOE_FFN_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D fp16 matrix [outer, inner], row-major; boxes of 128 rows x 64 columns, 128-byte swizzle.
+static bool make_tmap(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename T>
+static bool dalloc(moe_ffn_handle *h, T **p, size_t count) {
+  void *q = nullptr;
+  const size_t bytes = count * sizeof(T) > 0 ? count * sizeof(T) : 16;
+  if (cudaMalloc(&q, bytes) != cudaSuccess) return false;
+  h->allocs.push_back(q);
+  *p = static_cast<T *>(q);
+  return true;
+}
+
+static void free_all(moe_ffn_handle *h) {
+  for (void *p : h->allocs) cudaFree(p);
+  h->allocs.clear();
+}
+
+extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weights *layers, moe_ffn_handle **out) {
+  if (!out) return fail(nullptr, MOE_FFN_ERR_NULL_PTR, "out is NULL");
+  *out = nullptr;
+  if (!cfg || !layers) return fail(nullptr, MOE_FFN_ERR_NULL_PTR, "cfg or layers is NULL");
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  std::vector<bool> has(cfg->n_layers);
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    bool hl = false;
+    rc = check_layer(cfg, l, &layers[l], &hl);
+    if (rc) return rc;
+    has[l] = hl;
+  }
+  int dev = 0;
+  cudaDeviceProp prop;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess)
+    return fail(nullptr, MOE_FFN_ERR_CUDA, "no CUDA device");
+  if (prop.major != 10 || prop.minor != 3)
+    return fail(nullptr, MOE_FFN_ERR_UNSUPPORTED, "needs an sm_103 device, found sm_%d%d", prop.major, prop.minor);
+
+  moe_ffn_handle *h = new moe_ffn_handle();
+  h->cfg = *cfg;
+  h->device = dev;
+  h->num_sms = prop.multiProcessorCount;
+  Dims &d = h->dims;
+  d.hidden = cfg->hidden;
+  d.hc = cfg->hc;
+  d.experts = cfg->experts;
+  d.top_k = cfg->top_k;
+  d.inter = cfg->inter;
+  d.vocab = cfg->vocab;
+  d.iters = cfg->sinkhorn_iters;
+  d.eps = cfg->rms_eps;
+  const size_t R = cfg->max_rows, D = d.hidden, E = d.experts, K = d.top_k, I = d.inter, HC = d.hc, M = d.mix();
+  const size_t hcd = HC * D;
+  Scratch &s = h->s;
+  s.max_rows = (int)R;
+  s.mix_chunks = (int)(hcd / 128);
+  s.router_chunks = (int)(D / 128);
+  const size_t mix_part = std::max((size_t)4 * (hcd / 128), R * (hcd % 512 == 0 ? 4 : hcd / 128)) * (M + 1);
+  const size_t G = moe::kDecodeRows * K + 1;
+  bool ok = dalloc(h, &s.status, 1) && dalloc(h, &s.mix_partial, mix_part) && dalloc(h, &s.tickets, R / 4 + 2) &&
+            dalloc(h, &s.mixes, R * M) && dalloc(h, &s.pre, R * HC) && dalloc(h, &s.post, R * HC) &&
+            dalloc(h, &s.comb, R * HC * HC) && dalloc(h, &s.ffn_input, R * D) && dalloc(h, &s.ffn_norm, R * D) &&
+            dalloc(h, &s.router_partial, 4 * (D / 128) * (E + 1)) && dalloc(h, &s.logits, R * E) &&
+            dalloc(h, &s.idx, R * K) && dalloc(h, &s.rw, R * K) && dalloc(h, &s.safe, R * K) &&
+            dalloc(h, &s.ffn_out, R * D) && dalloc(h, &s.ngroups, 1) && dalloc(h, &s.group_e, G) &&
+            dalloc(h, &s.group_mask, G) && dalloc(h, &s.group_w, G * 4) && dalloc(h, &s.act_dec, G * 4 * I) &&
+            dalloc(h, &s.y_dec, G * 4 * D) && dalloc(h, &h->host_in, R * hcd) &&
+            dalloc(h, &h->host_out, R * hcd) && dalloc(h, &h->host_tok, R);
+  const bool prefill = R > (size_t)moe::kDecodeRows;
+  s.max_positions = (int)(R * K + R);
+  const size_t P = prefill ? s.max_positions : 0;
+  s.max_tiles_gu = (int)((P / 128 + E + 1) * (I / 128));
+  s.max_tiles_dn = (int)((P / 128 + E + 1) * (D / 128));
+  if (ok && prefill)
+    ok = dalloc(h, &s.counts, E) && dalloc(h, &s.offsets, E + 2) && dalloc(h, &s.cursor, E + 1) &&
+         dalloc(h, &s.tiles_gu, (size_t)s.max_tiles_gu) && dalloc(h, &s.tiles_dn, (size_t)s.max_tiles_dn) &&
+         dalloc(h, &s.n_tiles, 2) && dalloc(h, &s.list, P) && dalloc(h, &s.list_w, P) &&
+         dalloc(h, &s.x16, P * D) && dalloc(h, &s.act16, P * I) && dalloc(h, &s.y_slot, R * (K + 1) * D);
+  if (!ok) {
+    free_all(h);
+    delete h;
+    return fail(nullptr, MOE_FFN_ERR_NO_MEMORY, "device allocation of the scratch failed");
+  }
+  cudaMemset(s.status, 0, sizeof(int));
+  cudaMemset(s.tickets, 0, (R / 4 + 2) * sizeof(unsigned));
+  if (prefill) {
+    cudaMemset(s.counts, 0, E * sizeof(int));
+    if (!make_tmap(&h->tm_x16, s.x16, D, P) || !make_tmap(&h->tm_act16, s.act16, I, P)) {
+      free_all(h);
+      delete h;
+      return fail(nullptr, MOE_FFN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the activation buffers");
+    }
+  }
+  if (moe::gemm_configure() != cudaSuccess || moe::decode_configure(d.hidden) != cudaSuccess) {
+    free_all(h);
+    delete h;
+    return fail(nullptr, MOE_FFN_ERR_CUDA, "kernel attribute setup failed");
+  }
+  h->layers.resize(cfg->n_layers);
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    LayerDev &L = h->layers[l];
+    std::memset(&L, 0, sizeof L);
+    L.has_weights = has[l];
+    if (!has[l]) continue;
+    const moe_ffn_layer_weights &w = layers[l];
+    L.hc_fn = w.hc_fn;
+    L.hc_base = w.hc_base;
+    L.hc_scale = w.hc_scale;
+    L.ffn_norm = w.ffn_norm;
+    L.gate = w.gate;
+    L.exp_probs_b = w.exp_probs_b;
+    L.tid2eid = w.tid2eid;
+    L.gate_exps = w.gate_exps;
+    L.up_exps = w.up_exps;
+    L.down_exps = w.down_exps;
+    L.gate_sh = w.gate_sh;
+    L.up_sh = w.up_sh;
+    L.down_sh = w.down_sh;
+    if (!prefill) continue;
+    const size_t n_exp = E * I * D, n_sh = I * D;
+    if (!dalloc(h, &L.gate16, n_exp + n_sh) || !dalloc(h, &L.up16, n_exp + n_sh) ||
+        !dalloc(h, &L.down16, n_exp + n_sh)) {
+      free_all(h);
+      delete h;
+      return fail(nullptr, MOE_FFN_ERR_NO_MEMORY, "device allocation of the fp16 expert copies failed");
+    }
+    moe::launch_bf16_to_f16(w.gate_exps, L.gate16, n_exp, 0);
+    moe::launch_bf16_to_f16(w.gate_sh, L.gate16 + n_exp, n_sh, 0);
+    moe::launch_bf16_to_f16(w.up_exps, L.up16, n_exp, 0);
+    moe::launch_bf16_to_f16(w.up_sh, L.up16 + n_exp, n_sh, 0);
+    moe::launch_bf16_to_f16(w.down_exps, L.down16, n_exp, 0);
+    moe::launch_bf16_to_f16(w.down_sh, L.down16 + n_exp, n_sh, 0);
+    if (!make_tmap(&L.tm_gate, L.gate16, D, (E + 1) * I) || !make_tmap(&L.tm_up, L.up16, D, (E + 1) * I) ||
+        !make_tmap(&L.tm_down, L.down16, I, (E + 1) * D)) {
+      free_all(h);
+      delete h;
+      return fail(nullptr, MOE_FFN_ERR_CUDA, "cuTensorMapEncodeTiled failed for layer %d", l);
+    }
+  }
+  const cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    const std::string msg = cudaGetErrorString(e);
+    free_all(h);
+    delete h;
+    return fail(nullptr, MOE_FFN_ERR_CUDA, "init: %s", msg.c_str());
+  }
+  *out = h;
+  return MOE_FFN_OK;
+}
+
+extern "C" int moe_ffn_forward(moe_ffn_handle *h, const float *state, const int32_t *token_ids, int32_t rows,
+                               int32_t layer, float *out_state, void *stream) {
+  if (!h) return fail(nullptr, MOE_FFN_ERR_NULL_PTR, "handle is NULL");
+  const moe_ffn_config &c = h->cfg;
+  if (layer < 0 || layer >= c.n_layers)
+    return fail(h, MOE_FFN_ERR_LAYER_RANGE, "FFN layer index %d is outside 0..%d", layer, c.n_layers);
+  if (rows == 0) return fail(h, MOE_FFN_ERR_ROWS_ZERO, "the FFN requires at least one token row");
+  if (rows < 0 || rows > c.max_rows)
+    return fail(h, MOE_FFN_ERR_ROWS_RANGE, "rows %d outside 1..max_rows (%d)", rows, c.max_rows);
+  if (!state || !out_state) return fail(h, MOE_FFN_ERR_NULL_PTR, "state or out_state is NULL");
+  const LayerDev &L = h->layers[layer];
+  if (!L.has_weights) return fail(h, MOE_FFN_ERR_NO_WEIGHTS, "layer %d has no weights", layer);
+  const bool hash = layer < c.hash_layer_count;
+  if (hash && !token_ids) return fail(h, MOE_FFN_ERR_NULL_PTR, "hash layer %d needs token_ids", layer);
+  if (!aligned16(state) || !aligned16(out_state))
+    return fail(h, MOE_FFN_ERR_ALIGNMENT, "state and out_state must be 16-byte aligned");
+  const size_t bytes = (size_t)rows * c.hc * c.hidden * sizeof(float);
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(state), b0 = reinterpret_cast<uintptr_t>(out_state);
+  if (a0 < b0 + bytes && b0 < a0 + bytes) return fail(h, MOE_FFN_ERR_ALIAS, "out_state overlaps state");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  moe::StageTimer *tm = h->timer.on ? &h->timer : nullptr;
+  if (tm) tm->begin(st);
+  moe::launch_hc_mix(h->dims, h->s, L, state, rows, st, tm);
+  if (rows <= moe::kDecodeRows) {
+    moe::launch_decode_router(h->dims, h->s, L, state, token_ids, rows, hash, st, tm);
+    moe::launch_decode_experts(h->dims, h->s, L, state, rows, out_state, h->num_sms, st, tm);
+  } else {
+    moe::launch_prefill_router(h->dims, h->s, L, state, token_ids, rows, hash, st, tm);
+    moe::launch_dispatch(h->dims, h->s, rows, st, tm);
+    moe::launch_grouped_gemms(h->dims, h->s, L, h->tm_x16, h->tm_act16, h->num_sms, st, tm);
+    moe::launch_prefill_post(h->dims, h->s, state, rows, out_state, st, tm);
+  }
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(h, MOE_FFN_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+  h->last_stream = st;
+  h->last_rows = rows;
+  return MOE_FFN_OK;
+}
+
+extern "C" int moe_ffn_forward_host(moe_ffn_handle *h, const float *state, const int32_t *token_ids, int32_t rows,
+                                    int32_t layer, float *out_state, void *stream) {
+  if (!h) return fail(nullptr, MOE_FFN_ERR_NULL_PTR, "handle is NULL");
+  if (rows <= 0 || rows > h->cfg.max_rows || !state || !out_state)  // the same checks, on the staging buffers
+    return moe_ffn_forward(h, state, token_ids, rows, layer, out_state, stream);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)rows * h->cfg.hc * h->cfg.hidden * sizeof(float);
+  cudaError_t e = cudaMemcpyAsync(h->host_in, state, bytes, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess && token_ids)
+    e = cudaMemcpyAsync(h->host_tok, token_ids, (size_t)rows * sizeof(int32_t), cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return fail(h, MOE_FFN_ERR_CUDA, "host-to-device copy: %s", cudaGetErrorString(e));
+  const int rc = moe_ffn_forward(h, h->host_in, token_ids ? h->host_tok : nullptr, rows, layer, h->host_out, stream);
+  if (rc != MOE_FFN_OK) return rc;
+  e = cudaMemcpyAsync(out_state, h->host_out, bytes, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return fail(h, MOE_FFN_ERR_CUDA, "device-to-host copy: %s", cudaGetErrorString(e));
+  return MOE_FFN_OK;
+}
+
+extern "C" int moe_ffn_status(moe_ffn_handle *h) {
+  if (!h) return fail(nullptr, MOE_FFN_ERR_NULL_PTR, "handle is NULL");
+  int v = 0;
+  cudaError_t e = cudaStreamSynchronize(h->last_stream);
+  if (e == cudaSuccess) e = cudaMemcpy(&v, h->s.status, sizeof v, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(h->s.status, 0, sizeof v);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail(h, MOE_FFN_ERR_CUDA, "status: %s", cudaGetErrorString(e));
+  return v;
+}
+
+extern "C" int moe_ffn_debug_copy(moe_ffn_handle *h, int32_t which, void *host_dst, size_t bytes) {
+  if (!h || !host_dst) return fail(h, MOE_FFN_ERR_NULL_PTR, "handle or destination is NULL");
+  const size_t R = h->last_rows, D = h->dims.hidden, HC = h->dims.hc, E = h->dims.experts, K = h->dims.top_k;
+  const void *src = nullptr;
+  size_t n = 0;
+  switch (which) {
+    case 0: src = h->s.pre; n = R * HC * 4; break;
+    case 1: src = h->s.post; n = R * HC * 4; break;
+    case 2: src = h->s.comb; n = R * HC * HC * 4; break;
+    case 3: src = h->s.ffn_norm; n = R * D * 4; break;
+    case 4: src = h->s.logits; n = R * E * 4; break;
+    case 5: src = h->s.idx; n = R * K * 4; break;
+    case 6: src = h->s.rw; n = R * K * 4; break;
+    case 7: src = h->s.safe; n = R * K * 4; break;
+    case 8: src = h->s.ffn_out; n = R * D * 4; break;
+    default: return fail(h, MOE_FFN_ERR_BAD_CONFIG, "unknown debug buffer %d", which);
+  }
+  if (bytes != n) return fail(h, MOE_FFN_ERR_BAD_CONFIG, "debug buffer %d holds %zu bytes, not %zu", which, n, bytes);
+  cudaError_t e = cudaStreamSynchronize(h->last_stream);
+  if (e == cudaSuccess) e = cudaMemcpy(host_dst, src, n, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(h, MOE_FFN_ERR_CUDA, "debug copy: %s", cudaGetErrorString(e));
+  return MOE_FFN_OK;
+}
+
+extern "C" int moe_ffn_set_stage_timing(moe_ffn_handle *h, int32_t enable) {
+  if (!h) return fail(nullptr, MOE_FFN_ERR_NULL_PTR, "handle is NULL");
+  moe::StageTimer &t = h->timer;
+  if (enable && !t.created) {
+    for (int i = 0; i <= moe::StageTimer::kMax; ++i)
+      if (cudaEventCreate(&t.ev[i]) != cudaSuccess) return fail(h, MOE_FFN_ERR_CUDA, "cudaEventCreate failed");
+    t.created = true;
+  }
+  t.on = enable != 0;
+  t.n = 0;
+  return MOE_FFN_OK;
+}
+
+extern "C" int moe_ffn_stage_times(moe_ffn_handle *h, float *ms, const char **names, int32_t max_stages) {
+  if (!h || !ms) return fail(h, MOE_FFN_ERR_NULL_PTR, "handle or output is NULL");
+  moe::StageTimer &t = h->timer;
+  if (!t.created || t.n == 0) return 0;
+  if (cudaEventSynchronize(t.ev[t.n]) != cudaSuccess) return fail(h, MOE_FFN_ERR_CUDA, "event wait failed");
+  const int n = t.n < max_stages ? t.n : max_stages;
+  for (int i = 0; i < n; ++i) {
+    if (cudaEventElapsedTime(&ms[i], t.ev[i], t.ev[i + 1]) != cudaSuccess)
+      return fail(h, MOE_FFN_ERR_CUDA, "cudaEventElapsedTime failed");
+    if (names) names[i] = t.name[i];
+  }
+  return n;
+}
+
+extern "C" const char *moe_ffn_last_error(const moe_ffn_handle *h) { return h ? h->err.c_str() : g_init_err.c_str(); }
+
+extern "C" void moe_ffn_destroy(moe_ffn_handle *h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  if (h->timer.created)
+    for (int i = 0; i <= moe::StageTimer::kMax; ++i) cudaEventDestroy(h->timer.ev[i]);
+  free_all(h);
+  delete h;
+}

@@ -1,0 +1,168 @@
+/*
+ * moe_ffn.h - C ABI of the GB300 (sm_103a) DeepSeek-V4 routed-MoE FFN block with
+ * hyper-connections.
+ *
+ * The block is the FFN sublayer of docs.rs "hf2q 0.1.3 src/inference/models/deepseek4/
+ * ffn_forward.rs", function forward_ffn_rows: for `rows` tokens of one layer it maps the
+ * hyper-connection state f32 [rows, hc, hidden] to a new state of the same shape through
+ *   hc prelude   rms_norm_no_scale_f32 -> raw_matmul "HC FFN function" -> hc_split_sinkhorn
+ *                -> hc_pre -> rms_norm (ffn_norm)
+ *   router       raw_matmul "MoE gate" -> score route (layer >= hash_layer_count) or hash
+ *                route (layer < hash_layer_count) -> sanitize indices
+ *   experts      routed + shared gate/up projections -> SwiGLU -> down projections
+ *                -> weighted reduce (routed slots weighted, shared added)
+ *   hc post      hc_post (post * ffn_output + comb * state)
+ * Every stage runs in this library's CUDA kernels; there is no host or CPU fallback.
+ *
+ * Conventions where the page leaves the arithmetic open (each fixed here, not by the page):
+ *   - mixes split as [pre (hc) | post (hc) | comb (hc*hc, row-major i*hc+j)]; segment s is
+ *     multiplied by hc_scale[s] and then hc_base is added; pre = sigmoid, post = 2*sigmoid;
+ *     comb = Sinkhorn(exp(a - rowmax)), `sinkhorn_iters` sweeps of row then column
+ *     normalisation, no epsilon;
+ *   - hc_post: out[i] = post[i] * ffn_output + sum_j comb[i][j] * state[j];
+ *   - score route: s = sigmoid(logit); top_k experts by s + exp_probs_b, slots in descending
+ *     order of that value, exact ties to the lower expert index; weights s / sum(s) over the
+ *     chosen experts (no extra scaling factor);
+ *   - hash route: experts = tid2eid[token] in table order; weights sigmoid(logit) normalised
+ *     over the slots whose expert is valid;
+ *   - sanitize: an index outside [0, experts) is replaced by 0 for the projections, and the
+ *     weighted reduce gives that slot no weight;
+ *   - SwiGLU: silu(gate) * up, no clamp, no bias.
+ *
+ * Memory: all tensor arguments are DEVICE pointers owned by the caller, row-major and
+ * contiguous.  bf16 arguments are passed as uint16_t bit patterns.
+ */
+#ifndef MOE_FFN_H
+#define MOE_FFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes (negative = error, the call did nothing on the device). */
+#define MOE_FFN_OK 0
+#define MOE_FFN_ERR_NULL_PTR (-1)          /* a required pointer is NULL */
+#define MOE_FFN_ERR_BAD_CONFIG (-2)        /* config outside the supported shapes (see below) */
+#define MOE_FFN_ERR_LAYER_RANGE (-3)       /* layer >= n_layers (the page's first guard) */
+#define MOE_FFN_ERR_ROWS_ZERO (-4)         /* rows == 0 ("requires at least one token row") */
+#define MOE_FFN_ERR_ROWS_RANGE (-5)        /* rows < 0, rows > max_rows, or rows*top_k overflows */
+#define MOE_FFN_ERR_NO_ROUTING_SOURCE (-6) /* score layer without exp_probs_b, hash layer without tid2eid */
+#define MOE_FFN_ERR_ALIAS (-7)             /* out_state overlaps state */
+#define MOE_FFN_ERR_CUDA (-8)              /* a CUDA runtime/driver call failed; see moe_ffn_last_error */
+#define MOE_FFN_ERR_NO_MEMORY (-9)         /* device or host allocation failed */
+#define MOE_FFN_ERR_UNSUPPORTED (-10)      /* no sm_103 device */
+#define MOE_FFN_ERR_ALIGNMENT (-11)        /* a pointer is not 16-byte aligned */
+#define MOE_FFN_ERR_NO_WEIGHTS (-12)       /* forward on a layer whose weights were not given */
+
+/* Device-side status bits (moe_ffn_status returns their OR since the previous call). */
+#define MOE_FFN_DEV_TOKEN_RANGE 0x1   /* hash layer: token id outside [0, vocab); its slots masked */
+#define MOE_FFN_DEV_ROUTE_RANGE 0x2   /* a routed expert index outside [0, experts); slot masked */
+#define MOE_FFN_DEV_NONFINITE 0x4     /* a router logit was NaN or infinite */
+#define MOE_FFN_DEV_TIMEOUT 0x8       /* a bounded wait inside a kernel gave up (kernel returned) */
+
+/* Shapes and constants of the block (the page's cfg fields).  Supported:
+ *   1 <= hc <= 4;  128 <= hidden <= 8192, hidden % 128 == 0;  inter % 128 == 0;  shared_inter == inter;
+ *   16 <= experts <= 512, experts % 16 == 0;  1 <= top_k <= 8, top_k <= experts;
+ *   hash_layer_count <= n_layers;  1 <= max_rows <= 65536;  vocab >= 1;  sinkhorn_iters >= 0. */
+typedef struct moe_ffn_config {
+  int32_t hidden;            /* hidden_size (4096) */
+  int32_t hc;                /* hyper_connection_count (4) */
+  int32_t experts;           /* num_experts (256) */
+  int32_t top_k;             /* num_experts_per_tok (6) */
+  int32_t inter;             /* expert_intermediate_size (2048) */
+  int32_t shared_inter;      /* shared expert intermediate size (= inter) */
+  int32_t vocab;             /* vocab_size: token ids must lie in [0, vocab) on hash layers */
+  int32_t n_layers;          /* num_hidden_layers */
+  int32_t hash_layer_count;  /* layers below this use hash routing */
+  int32_t max_rows;          /* largest `rows` a forward will be given; sizes the scratch */
+  int32_t sinkhorn_iters;    /* Sinkhorn sweeps (20) */
+  float rms_eps;             /* rms_norm_eps (1e-6) */
+} moe_ffn_config;
+
+/* Weights of one layer: DEVICE pointers, caller-owned, 16-byte aligned, valid for the life of
+ * the handle.  A layer whose pointers are all NULL has no weights; forward on it fails. */
+typedef struct moe_ffn_layer_weights {
+  const uint16_t *hc_fn;       /* bf16 [(2+hc)*hc, hc*hidden]  hc_ffn_fn */
+  const float *hc_base;        /* f32 [(2+hc)*hc]              hc_ffn_base */
+  const float *hc_scale;       /* f32 [3]                      hc_ffn_scale */
+  const float *ffn_norm;       /* f32 [hidden]                 ffn_norm */
+  const uint16_t *gate;        /* bf16 [experts, hidden]       ffn_gate_inp (router) */
+  const float *exp_probs_b;    /* f32 [experts]; required on score layers, else may be NULL */
+  const int32_t *tid2eid;      /* i32 [vocab, top_k]; required on hash layers, else may be NULL */
+  const uint16_t *gate_exps;   /* bf16 [experts, inter, hidden] */
+  const uint16_t *up_exps;     /* bf16 [experts, inter, hidden] */
+  const uint16_t *down_exps;   /* bf16 [experts, hidden, inter] */
+  const uint16_t *gate_sh;     /* bf16 [shared_inter, hidden] */
+  const uint16_t *up_sh;       /* bf16 [shared_inter, hidden] */
+  const uint16_t *down_sh;     /* bf16 [hidden, shared_inter] */
+} moe_ffn_layer_weights;
+
+typedef struct moe_ffn_handle moe_ffn_handle;
+
+/* Creates a handle on the current CUDA device.  Validates the config (BAD_CONFIG) and, for every
+ * layer with weights, the routing source its layer type needs (NO_ROUTING_SOURCE) and pointer
+ * alignment (ALIGNMENT).  Allocates the scratch for max_rows and, per layer with weights, an fp16
+ * copy of the routed and shared expert matrices (the tensor-core operands of the rows > 4 path;
+ * fp16 holds every bf16 value of magnitude >= 2^-14 exactly): 2 * (experts+1) * 3 * inter *
+ * hidden bytes per layer.  Synchronous.  On failure *out is NULL and nothing stays allocated. */
+int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weights *layers, moe_ffn_handle **out);
+
+/* Enqueues the block for `rows` tokens of `layer` on `stream` (a cudaStream_t; NULL = legacy
+ * default stream) and returns without waiting.
+ *   state      f32 [rows, hc, hidden]  input hyper-connection state (read only)
+ *   token_ids  i32 [rows]              token ids (read on hash layers only; may be NULL on score layers)
+ *   out_state  f32 [rows, hc, hidden]  output state; must not overlap state
+ * Returns MOE_FFN_OK or a negative code from the host-side checks (nothing enqueued then).
+ * Rows <= 4 take the weight-streaming decode path; larger batches the tensor-core grouped-GEMM
+ * path.  Forwards on one handle share its scratch: enqueue them on one stream (or order them),
+ * never concurrently.  Data-dependent problems (a token id out of range, an expert index out of
+ * range, a non-finite logit) do not fail the call: they set device status bits, masked slots
+ * contribute nothing, and moe_ffn_status reports them. */
+int moe_ffn_forward(moe_ffn_handle *h, const float *state, const int32_t *token_ids, int32_t rows,
+                    int32_t layer, float *out_state, void *stream);
+
+/* The same block on HOST buffers: copies state [rows, hc, hidden] and token_ids [rows] (may be NULL
+ * on score layers) from host memory into library-owned device buffers, runs moe_ffn_forward on
+ * `stream`, copies the new state back into out_state (host), and waits for the stream.  Pinned
+ * (page-locked) host memory gives the fastest copies.  Same return codes as moe_ffn_forward, plus
+ * MOE_FFN_ERR_CUDA when a copy fails. */
+int moe_ffn_forward_host(moe_ffn_handle *h, const float *state, const int32_t *token_ids, int32_t rows,
+                         int32_t layer, float *out_state, void *stream);
+
+/* Waits for the stream of the last forward and returns the OR of device status bits set since the
+ * previous moe_ffn_status call (>= 0, then cleared), or MOE_FFN_ERR_CUDA. */
+int moe_ffn_status(moe_ffn_handle *h);
+
+/* Copies to host memory an intermediate of the last forward (after waiting for it), for stage-by-
+ * stage checks.  `which` selects the buffer; `bytes` must equal its size for the last `rows`:
+ *   0 pre f32 [rows, hc]      1 post f32 [rows, hc]      2 comb f32 [rows, hc, hc]
+ *   3 ffn_norm f32 [rows, hidden]   4 logits f32 [rows, experts]
+ *   5 indices i32 [rows, top_k]     6 route weights f32 [rows, top_k]
+ *   7 safe indices u32 [rows, top_k] 8 ffn_output f32 [rows, hidden]
+ * Returns MOE_FFN_OK, MOE_FFN_ERR_BAD_CONFIG for an unknown `which` or a size mismatch, or
+ * MOE_FFN_ERR_CUDA. */
+int moe_ffn_debug_copy(moe_ffn_handle *h, int32_t which, void *host_dst, size_t bytes);
+
+/* Per-kernel timing (off by default).  While enabled, each forward records a CUDA event on its
+ * stream before its first kernel and after every kernel; this adds a few microseconds per forward. */
+int moe_ffn_set_stage_timing(moe_ffn_handle *h, int32_t enable);
+
+/* After a forward made with stage timing on: waits for it and writes the duration (ms) of each of
+ * its kernels, in launch order, to ms[i] and the kernel's name (a static string) to names[i] (names
+ * may be NULL).  Returns the number of kernels written (at most max_stages), 0 when nothing was
+ * timed, or a negative code. */
+int moe_ffn_stage_times(moe_ffn_handle *h, float *ms, const char **names, int32_t max_stages);
+
+/* Text of the last error on this handle (or of the last failed init when h is NULL). */
+const char *moe_ffn_last_error(const moe_ffn_handle *h);
+
+/* Waits for outstanding work, frees everything the handle owns.  NULL is ignored. */
+void moe_ffn_destroy(moe_ffn_handle *h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_FFN_H */

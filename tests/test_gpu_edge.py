@@ -1,0 +1,138 @@
+"""Edge cases of the GPU path at tiny shapes (hidden 256, 16 experts, top-2, inter 128) against the
+oracle: ragged row counts on both paths, hash routing with invalid table entries and token ids,
+every row on one expert (and most experts empty), repeated calls, and the host-side error codes."""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth.device import upload
+from tests.inputs import compare_state, tie_free
+
+pytestmark = pytest.mark.gpu
+
+TINY = synth.CONFIGS["c0_tiny"]
+
+
+def _run(case, max_rows=None, layer=None):
+    from deepseek_v4_moe_gb300 import MoeFFN, config_from
+    cfg = case.cfg
+    dev = upload(case)
+    m = MoeFFN(config_from(cfg, max_rows or cfg.rows), {cfg.layer: dev["weights"]})
+    out = m.forward(dev["state"], dev["token_ids"], cfg.layer if layer is None else layer)
+    torch.cuda.synchronize()
+    res = dict(out=out.cpu().numpy(), status=m.status(), indices=m.debug("indices"), weights=m.debug("weights"),
+               ffn_output=m.debug("ffn_output"))
+    return m, dev, res
+
+
+@pytest.mark.parametrize("rows", [1, 3, 5, 17, 129, 300])
+def test_ragged_rows_score(rows, cuda_lib):
+    case, st = tie_free(replace(TINY, rows=rows, name=f"tiny{rows}"))
+    m, dev, res = _run(case)
+    ref = oracle.forward_ffn_rows(case, stages=st)
+    assert res["status"] == 0
+    assert np.array_equal(res["indices"], ref["indices"])
+    compare_state(res["out"], ref["out_state"])
+    m.close()
+
+
+@pytest.mark.parametrize("rows", [3, 9])
+def test_hash_with_invalid_entries(rows, cuda_lib):
+    cfg = replace(TINY, rows=rows, layer=0, name=f"hash{rows}")
+    case = synth.Case(cfg)
+    case.token_ids[0] = 7
+    case.tid2eid[7] = [-1, 5]          # invalid first slot
+    case.token_ids[1] = 9
+    case.tid2eid[9] = [999, 3]         # out of range expert
+    case.token_ids[2] = cfg.vocab + 5  # token outside the vocabulary: both slots masked
+    m, dev, res = _run(case)
+    ref = oracle.forward_ffn_rows(case)
+    assert res["status"] & 0x1 and res["status"] & 0x2
+    assert np.array_equal(res["indices"], ref["indices"])
+    assert np.allclose(res["weights"], ref["weights"], rtol=1e-5, atol=1e-6)
+    compare_state(res["out"], ref["out_state"])
+    m.close()
+
+
+def test_one_expert_takes_every_row(cuda_lib):
+    cfg = replace(TINY, rows=200, name="hot1")
+    case = synth.Case(cfg)
+    case.exp_probs_b = np.zeros(16, np.float32)
+    case.exp_probs_b[11] = 5.0         # expert 11 first in every row; most others get nothing
+    case, st = tie_free_case(case)
+    m, dev, res = _run(case)
+    ref = oracle.forward_ffn_rows(case, stages=st)
+    assert np.all(res["indices"][:, 0] == 11)
+    assert np.array_equal(res["indices"], ref["indices"])
+    compare_state(res["out"], ref["out_state"])
+    m.close()
+
+
+def tie_free_case(case):
+    st = oracle.prelude_and_route(case)
+    for _ in range(20):
+        bad = st["margin"] < 1e-5
+        if not bad.any():
+            return case, st
+        att = case.attempts.copy()
+        att[bad] += 1
+        bias = case.exp_probs_b
+        case = case.with_attempts(att)
+        case.exp_probs_b = bias
+        st = oracle.prelude_and_route(case)
+    raise RuntimeError("ties")
+
+
+def test_repeat_calls_are_identical_and_counters_reset(cuda_lib):
+    case, st = tie_free(replace(TINY, rows=64, name="rep"))
+    from deepseek_v4_moe_gb300 import MoeFFN, config_from
+    dev = upload(case)
+    m = MoeFFN(config_from(case.cfg), {case.cfg.layer: dev["weights"]})
+    outs = [m.forward(dev["state"], None, case.cfg.layer).cpu().numpy() for _ in range(3)]
+    small = m.forward(dev["state"][:3].contiguous(), None, case.cfg.layer).cpu().numpy()
+    again = m.forward(dev["state"], None, case.cfg.layer).cpu().numpy()
+    assert m.status() == 0
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2]) and np.array_equal(outs[0], again)
+    ref = oracle.forward_ffn_rows(case, stages=st)
+    compare_state(outs[0], ref["out_state"])
+    compare_state(small, ref["out_state"][:3])
+    m.close()
+
+
+def test_host_buffer_entry_point(cuda_lib):
+    case, st = tie_free(replace(TINY, rows=6, name="host"))
+    from deepseek_v4_moe_gb300 import MoeFFN, config_from
+    dev = upload(case)
+    m = MoeFFN(config_from(case.cfg), {case.cfg.layer: dev["weights"]})
+    out = np.empty_like(case.state)
+    m.forward_host(case.state, case.token_ids, case.cfg.layer, out)
+    ref = oracle.forward_ffn_rows(case, stages=st)
+    compare_state(out, ref["out_state"])
+    m.close()
+
+
+def test_error_codes(cuda_lib):
+    from deepseek_v4_moe_gb300 import MoeFFN, MoeFFNError, config_from
+    case = synth.Case(replace(TINY, rows=4, layer=0, name="err"))
+    dev = upload(case)
+    m = MoeFFN(config_from(case.cfg), {0: dev["weights"]})
+    s = dev["state"]
+    codes = []
+    for kwargs in (dict(layer=4), dict(layer=3), dict(layer=0, token_ids=None)):
+        try:
+            m.forward(s, kwargs.get("token_ids", dev["token_ids"]), kwargs["layer"])
+        except MoeFFNError as e:
+            codes.append(e.code)
+    assert codes == [-3, -12, -1]
+    lib = m._lib
+    assert lib.moe_ffn_forward(m._h, s.data_ptr(), dev["token_ids"].data_ptr(), 0, 0, s.data_ptr(), None) == -4
+    assert lib.moe_ffn_forward(m._h, s.data_ptr(), dev["token_ids"].data_ptr(), 5, 0, s.data_ptr() + 4096, None) == -5
+    assert lib.moe_ffn_forward(m._h, s.data_ptr(), dev["token_ids"].data_ptr(), 4, 0, s.data_ptr() + 4096, None) == -7
+    assert lib.moe_ffn_forward(m._h, s.data_ptr() + 4, dev["token_ids"].data_ptr(), 1, 0,
+                               torch.empty_like(s).data_ptr(), None) == -11
+    assert m.status() == 0
+    m.close()
