@@ -326,14 +326,16 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.CONFIGS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.ALL_CONFIGS))
+    ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed load before the timed steps")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false", default=True)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--extra", dest="extra", action="store_true", default=True)
     ap.add_argument("--no-extra", dest="extra", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false", default=True)
     args = ap.parse_args()
     warmup = max(args.warmup, 3)
-    cfg = synth.CONFIGS[args.workload]
+    cfg = synth.ALL_CONFIGS[args.workload]
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -367,7 +369,8 @@ def main():
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
 
-    main_res = run_ours(cfg, args.steps, warmup, device, rank, world, dist, peaks, peak_kind, want_e2e=True)
+    main_res = run_ours(cfg, args.steps, warmup, device, rank, world, dist, peaks, peak_kind, want_e2e=args.e2e,
+                        soak_s=args.soak)
     workloads = {}
     if args.extra:
         for name in EXTRA_WORKLOADS:
@@ -375,7 +378,7 @@ def main():
                 continue
             c = synth.CONFIGS[name]
             r = run_ours(c, max(10, args.steps // 5), warmup, device, rank, world, dist, peaks, peak_kind,
-                         want_e2e=False, soak_s=0.5)
+                         want_e2e=False, soak_s=min(0.5, args.soak))
             workloads[name] = {"value": round(r["value"], 1), "unit": "tokens/s", "ms_per_step": round(r["ms_per_step"], 4),
                                "forward_roofline": r["forward_roofline"], "top_kernel": r["kernels"][0],
                                "clocks": r["clocks"]}
@@ -392,7 +395,7 @@ def main():
                 "dtype": "f32 (bf16 weights)" if cfg.rows <= 4 else "fp16 tensor-core (f32 accumulate)",
                 "data": "synthetic", "config": config, "roofline": main_res["roofline"],
                 "forward_roofline": main_res["forward_roofline"], "kernels": main_res["kernels"],
-                "cpu_baseline": cpu, "e2e": main_res["e2e"], "gpu_launches": main_res["gpu_launches"],
+                "cpu_baseline": cpu, "e2e": main_res.get("e2e"), "gpu_launches": main_res["gpu_launches"],
                 "clocks": main_res["clocks"], "median_ms_per_step": round(main_res["median_ms"], 5),
                 "workloads": workloads}
         print(json.dumps(line), flush=True)

@@ -168,6 +168,14 @@ CONFIGS = {
 }
 
 
+# Smaller variants for profiler captures (a few GB on the device): full hidden/inter, 32 experts.
+PROFILE_CONFIGS = {
+    "p_decode_b1_e32": MoeConfig("p_decode_b1_e32", rows=1, experts=32, seed=21),
+    "p_prefill_512_e32": MoeConfig("p_prefill_512_e32", rows=512, experts=32, seed=23),
+}
+ALL_CONFIGS = {**CONFIGS, **PROFILE_CONFIGS}
+
+
 class Case:
     """All inputs of one workload, as host arrays.  Expert weights are drawn on demand.
 
