@@ -76,6 +76,8 @@ def load(build: bool = True):
     lib.moe_ffn_set_stage_timing.restype = ctypes.c_int
     lib.moe_ffn_stage_times.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_char_p), i32]
     lib.moe_ffn_stage_times.restype = ctypes.c_int
+    lib.moe_ffn_hc_split_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, c_f32, vp, vp, vp, vp]
+    lib.moe_ffn_hc_split_noalloc.restype = ctypes.c_int
     lib.moe_ffn_last_error.argtypes = [vp]
     lib.moe_ffn_last_error.restype = ctypes.c_char_p
     lib.moe_ffn_destroy.argtypes = [vp]

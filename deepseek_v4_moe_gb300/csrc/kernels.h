@@ -87,6 +87,12 @@ void launch_decode_router(const Dims &d, const Scratch &s, const LayerDev &w, co
                           const int32_t *token_ids, int rows, bool hash, cudaStream_t st, StageTimer *tm);
 void launch_prefill_router(const Dims &d, const Scratch &s, const LayerDev &w, const float *state,
                            const int32_t *token_ids, int rows, bool hash, cudaStream_t st, StageTimer *tm);
+int hc_mix_chunks(int rows, int hcd);
+void launch_hc_mix_raw(const float *state, const uint16_t *hc_fn, const float *hc_scale, const float *hc_base,
+                       int rows, int hc, int hidden, int iters, float eps, float *partial, unsigned *tickets,
+                       float *mixes, float *pre, float *post, float *comb, cudaStream_t st);
+// moe_ffn.cu
+void set_global_error(const char *msg);
 // decode.cu
 void launch_decode_experts(const Dims &d, const Scratch &s, const LayerDev &w, const float *state, int rows,
                            float *out_state, int num_sms, cudaStream_t st, StageTimer *tm);

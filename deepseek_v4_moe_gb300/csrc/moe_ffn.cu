@@ -37,6 +37,10 @@ struct moe_ffn_handle {
 
 static std::string g_init_err;
 
+namespace moe {
+void set_global_error(const char *msg) { g_init_err = msg; }
+}  // namespace moe
+
 static int fail(moe_ffn_handle *h, int code, const char *fmt, ...) {
   char buf[512];
   va_list ap;

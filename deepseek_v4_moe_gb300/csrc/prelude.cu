@@ -167,6 +167,37 @@ void launch_hc_mix(const Dims &d, const Scratch &s, const LayerDev &w, const flo
   stage(tm, "hc_mix", st);
 }
 
+// Same kernel with caller-chosen scratch (the allocation-free entry point's fixed array).
+int hc_mix_chunks(int rows, int hcd) {
+  return rows <= kDecodeRows ? hcd / 128 : (hcd % 512 == 0 ? 4 : hcd / 128);
+}
+
+void launch_hc_mix_raw(const float *state, const uint16_t *hc_fn, const float *hc_scale, const float *hc_base,
+                       int rows, int hc, int hidden, int iters, float eps, float *partial, unsigned *tickets,
+                       float *mixes, float *pre, float *post, float *comb, cudaStream_t st) {
+  MixArgs a;
+  a.state = state;
+  a.hc_fn = hc_fn;
+  a.hc_scale = hc_scale;
+  a.hc_base = hc_base;
+  a.partial = partial;
+  a.tickets = tickets;
+  a.mixes = mixes;
+  a.pre = pre;
+  a.post = post;
+  a.comb = comb;
+  a.rows = rows;
+  a.hcd = hc * hidden;
+  a.M = (2 + hc) * hc;
+  a.hc = hc;
+  a.iters = iters;
+  a.eps = eps;
+  const int nch = hc_mix_chunks(rows, a.hcd);
+  a.chunk = a.hcd / nch;
+  dim3 grid(nch, (rows + 3) / 4);
+  hc_mix_kernel<4><<<grid, 256, 0, st>>>(a);
+}
+
 // ---------------------------------------------------------------------------------------------
 // Routing of one row by one warp.  Score layers: sigmoid scores, top_k on score + bias in f32
 // (ties to the lower expert index), weights = chosen unbiased scores / their sum.  Hash layers:

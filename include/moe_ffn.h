@@ -156,6 +156,26 @@ int moe_ffn_set_stage_timing(moe_ffn_handle *h, int32_t enable);
  * timed, or a negative code. */
 int moe_ffn_stage_times(moe_ffn_handle *h, float *ms, const char **names, int32_t max_stages);
 
+/* Allocation-free HC split: the first stage of the block (HC RMSNorm, mix GEMV with hc_fn, split
+ * into pre/post and the Sinkhorn comb, the same kernel and conventions as moe_ffn_forward) for
+ * callers that cannot allocate device memory at call time: code running under CUDA graph capture,
+ * serving loops that forbid allocation after start-up, or hosts whose pool owns the whole GPU.
+ * The pages have no counterpart of this entry point; it exists for such callers.
+ *   state    f32 [rows, hc, hidden] (device, 16-byte aligned)    hc_fn bf16 [(2+hc)*hc, hc*hidden]
+ *   hc_scale f32 [3], hc_base f32 [(2+hc)*hc]                    (device)
+ *   pre, post f32 [rows, hc]; comb f32 [rows, hc, hc]            (device outputs)
+ * No handle and no allocation: the scratch is a fixed 1 MiB array inside the library (held by every
+ * GPU that loads the library until exit), shared by all calls.  Limits: 1 <= rows <= 4096 and
+ * rows * (partial sums of the chosen split) must fit the 1 MiB; larger inputs return
+ * MOE_FFN_ERR_ROWS_RANGE with a message in moe_ffn_last_error(NULL).  The first call on each device
+ * looks the array's address up (and may load the module onto that device): make it before any
+ * stream capture.  Calls whose kernels overlap on the GPU race on the shared scratch: order them on
+ * one stream.  Returns MOE_FFN_OK or a negative code (nothing enqueued then). */
+int moe_ffn_hc_split_noalloc(const float *state, const uint16_t *hc_fn, const float *hc_scale,
+                             const float *hc_base, int32_t rows, int32_t hc, int32_t hidden,
+                             int32_t sinkhorn_iters, float rms_eps, float *pre, float *post, float *comb,
+                             void *stream);
+
 /* Text of the last error on this handle (or of the last failed init when h is NULL). */
 const char *moe_ffn_last_error(const moe_ffn_handle *h);
 
