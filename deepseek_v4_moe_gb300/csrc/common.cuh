@@ -44,6 +44,43 @@ __device__ __forceinline__ float dot8(const uint4 w, const float4 a, const float
   return s;
 }
 
+// 16-byte streaming read with an L2 eviction-priority policy (see make_policy_*).
+__device__ __forceinline__ uint4 ld_stream_hint(const void *p, uint64_t policy) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p), "l"(policy));
+  return r;
+}
+
+__device__ __forceinline__ uint64_t make_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t make_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Asynchronous prefetch of [p, p + bytes) into L2 (bytes a multiple of 16, p 16-byte aligned).
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p), "r"(bytes), "l"(policy)
+               : "memory");
+}
+
+// Programmatic dependent launch: wait for the preceding kernel's results / let the next kernel start.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -51,6 +88,48 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+// Comb of one row from its RMS-scaled mixes (split + Sinkhorn, docs.rs "hf2q 0.1.3
+// .../deepseek4/ffn_forward.rs", dispatch_hc_split_sinkhorn): a[i][j] = mix[2hc + i*hc + j] *
+// scale[2] + base[2hc + i*hc + j]; start exp(a - rowmax); `iters` sweeps, each normalising every
+// row then every column (multiplying by the correctly rounded reciprocal of the sum).  One thread,
+// the hc x hc matrix in registers (fixed 4 x 4 arrays; entries beyond hc unused).
+__device__ inline void sinkhorn_comb_row(const float *mix, const float *scale, const float *base, int hc, int iters,
+                                         float *comb) {
+  float c[kHcMax][kHcMax];
+#pragma unroll
+  for (int i = 0; i < kHcMax; ++i) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kHcMax; ++j) {
+      const bool in = i < hc && j < hc;
+      c[i][j] = in ? mix[2 * hc + i * hc + j] * scale[2] + base[2 * hc + i * hc + j] : 0.f;
+      if (in) mx = fmaxf(mx, c[i][j]);
+    }
+#pragma unroll
+    for (int j = 0; j < kHcMax; ++j) c[i][j] = (i < hc && j < hc) ? expf(c[i][j] - mx) : 0.f;
+  }
+#pragma unroll 1
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int i = 0; i < kHcMax; ++i) {
+      const float inv = (i < hc) ? __frcp_rn((c[i][0] + c[i][1]) + (c[i][2] + c[i][3])) : 0.f;
+#pragma unroll
+      for (int j = 0; j < kHcMax; ++j) c[i][j] *= inv;
+    }
+#pragma unroll
+    for (int j = 0; j < kHcMax; ++j) {
+      const float inv = (j < hc) ? __frcp_rn((c[0][j] + c[1][j]) + (c[2][j] + c[3][j])) : 0.f;
+#pragma unroll
+      for (int i = 0; i < kHcMax; ++i) c[i][j] *= inv;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kHcMax; ++i)
+#pragma unroll
+    for (int j = 0; j < kHcMax; ++j)
+      if (i < hc && j < hc) comb[i * hc + j] = c[i][j];
+}
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;

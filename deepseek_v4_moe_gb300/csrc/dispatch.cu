@@ -122,8 +122,9 @@ __global__ void __launch_bounds__(256) prefill_post_kernel(const float *__restri
   const float *ys = y_slot + (size_t)r * (K + 1) * D;
   for (int d = threadIdx.x * 4; d < D; d += blockDim.x * 4) {
     float4 f = *reinterpret_cast<const float4 *>(ys + (size_t)K * D + d);
-    for (int k = 0; k < K; ++k) {
-      if (!valid[k]) continue;
+#pragma unroll
+    for (int k = 0; k < kTopKMax; ++k) {
+      if (k >= K || !valid[k]) continue;
       const float4 y = *reinterpret_cast<const float4 *>(ys + (size_t)k * D + d);
       f.x += y.x;
       f.y += y.y;
@@ -132,11 +133,18 @@ __global__ void __launch_bounds__(256) prefill_post_kernel(const float *__restri
     }
     *reinterpret_cast<float4 *>(ffn_out + (size_t)r * D + d) = f;
     float4 sv[kHcMax];
-    for (int j = 0; j < hc; ++j) sv[j] = *reinterpret_cast<const float4 *>(state + ((size_t)r * hc + j) * D + d);
-    for (int o = 0; o < hc; ++o) {
+#pragma unroll
+    for (int j = 0; j < kHcMax; ++j)
+      sv[j] = j < hc ? *reinterpret_cast<const float4 *>(state + ((size_t)r * hc + j) * D + d)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int o = 0; o < kHcMax; ++o) {
+      if (o >= hc) break;
       const float p = pc[o];
       float4 v = make_float4(p * f.x, p * f.y, p * f.z, p * f.w);
-      for (int j = 0; j < hc; ++j) {
+#pragma unroll
+      for (int j = 0; j < kHcMax; ++j) {
+        if (j >= hc) break;
         const float c = pc[kHcMax + o * hc + j];
         v.x += c * sv[j].x;
         v.y += c * sv[j].y;

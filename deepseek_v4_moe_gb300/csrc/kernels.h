@@ -7,6 +7,24 @@
 
 namespace moe {
 
+// Launch with programmatic stream serialisation: the kernel may start while the previous kernel on
+// the stream finishes; it must call griddepcontrol.wait before reading that kernel's results.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 struct Dims {
   int hidden, hc, experts, top_k, inter, vocab, iters;
   float eps;
@@ -20,6 +38,7 @@ struct Scratch {
   unsigned *tickets;      // [max(max_rows/4+1, 1) + 1] zero between launches
   float *mixes, *pre, *post, *comb;  // [rows, mix] [rows, hc] [rows, hc] [rows, hc, hc]
   float *ffn_input, *ffn_norm;       // [rows, hidden]
+  float *row_rs;          // [rows] rsqrt(mean(ffn_input^2) + eps) (decode)
   float *router_partial;  // [4, router_chunks, experts+1]
   float *logits;          // [rows, experts]
   int *idx;               // [rows, top_k]
@@ -31,6 +50,8 @@ struct Scratch {
   float *group_w;         // [groups, 4]
   float *act_dec;         // [groups, 4, inter]
   float *y_dec;           // [groups, 4, hidden]
+  unsigned *dec_counters; // [groups] gate/up rows done per group, then [hidden/64] d-block arrivals
+  int decode_ctas_by_rows[5];  // co-resident CTAs of the persistent decode kernel, per row count
   // rows > 4 path
   int *counts;            // [experts] routed slots per expert (zero between launches)
   int *offsets;           // [experts + 2]
@@ -94,9 +115,13 @@ void launch_hc_mix_raw(const float *state, const uint16_t *hc_fn, const float *h
 // moe_ffn.cu
 void set_global_error(const char *msg);
 // decode.cu
+constexpr int kDecodeGroupsMax = 4 * 8 + 1;  // rows x top_k distinct experts + the shared one
+constexpr int kDecodeDBlock = 64;            // d-block of the decode reduce + hc_post
+inline int decode_counter_count(const Dims &d) { return kDecodeGroupsMax + d.hidden / kDecodeDBlock + 1; }
 void launch_decode_experts(const Dims &d, const Scratch &s, const LayerDev &w, const float *state, int rows,
                            float *out_state, int num_sms, cudaStream_t st, StageTimer *tm);
 cudaError_t decode_configure(int hidden);
+int decode_resident_ctas(int hidden, int rows, int num_sms);
 // dispatch.cu
 void launch_dispatch(const Dims &d, const Scratch &s, int rows, cudaStream_t st, StageTimer *tm);
 void launch_prefill_post(const Dims &d, const Scratch &s, const float *state, int rows, float *out_state,

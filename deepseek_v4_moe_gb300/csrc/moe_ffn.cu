@@ -187,11 +187,13 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
   bool ok = dalloc(h, &s.status, 1) && dalloc(h, &s.mix_partial, mix_part) && dalloc(h, &s.tickets, R / 4 + 2) &&
             dalloc(h, &s.mixes, R * M) && dalloc(h, &s.pre, R * HC) && dalloc(h, &s.post, R * HC) &&
             dalloc(h, &s.comb, R * HC * HC) && dalloc(h, &s.ffn_input, R * D) && dalloc(h, &s.ffn_norm, R * D) &&
+            dalloc(h, &s.row_rs, R) &&
             dalloc(h, &s.router_partial, 4 * (D / 128) * (E + 1)) && dalloc(h, &s.logits, R * E) &&
             dalloc(h, &s.idx, R * K) && dalloc(h, &s.rw, R * K) && dalloc(h, &s.safe, R * K) &&
             dalloc(h, &s.ffn_out, R * D) && dalloc(h, &s.ngroups, 1) && dalloc(h, &s.group_e, G) &&
             dalloc(h, &s.group_mask, G) && dalloc(h, &s.group_w, G * 4) && dalloc(h, &s.act_dec, G * 4 * I) &&
-            dalloc(h, &s.y_dec, G * 4 * D) && dalloc(h, &h->host_in, R * hcd) &&
+            dalloc(h, &s.y_dec, G * 4 * D) && dalloc(h, &s.dec_counters, (size_t)moe::decode_counter_count(d)) &&
+            dalloc(h, &h->host_in, R * hcd) &&
             dalloc(h, &h->host_out, R * hcd) && dalloc(h, &h->host_tok, R);
   const bool prefill = R > (size_t)moe::kDecodeRows;
   s.max_positions = (int)(R * K + R);
@@ -209,6 +211,7 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
     return fail(nullptr, MOE_FFN_ERR_NO_MEMORY, "device allocation of the scratch failed");
   }
   cudaMemset(s.status, 0, sizeof(int));
+  cudaMemset(s.dec_counters, 0, (size_t)moe::decode_counter_count(d) * sizeof(unsigned));
   cudaMemset(s.tickets, 0, (R / 4 + 2) * sizeof(unsigned));
   if (prefill) {
     cudaMemset(s.counts, 0, E * sizeof(int));
@@ -223,6 +226,15 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
     delete h;
     return fail(nullptr, MOE_FFN_ERR_CUDA, "kernel attribute setup failed");
   }
+  for (int r = 1; r <= moe::kDecodeRows; ++r) {
+    s.decode_ctas_by_rows[r] = moe::decode_resident_ctas(d.hidden, r, h->num_sms);
+    if (s.decode_ctas_by_rows[r] <= 0) {
+      free_all(h);
+      delete h;
+      return fail(nullptr, MOE_FFN_ERR_CUDA, "the decode kernel does not fit on an SM");
+    }
+  }
+  s.decode_ctas_by_rows[0] = 0;
   h->layers.resize(cfg->n_layers);
   for (int l = 0; l < cfg->n_layers; ++l) {
     LayerDev &L = h->layers[l];

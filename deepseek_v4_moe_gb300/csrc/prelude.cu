@@ -22,62 +22,46 @@ namespace moe {
 // and the Sinkhorn-balanced comb.
 // ---------------------------------------------------------------------------------------------
 struct MixArgs {
+  int do_sinkhorn;  // 0: the comb is formed later (decode: inside the expert kernel, off the critical path)
   const float *state;
   const uint16_t *hc_fn;
   const float *hc_scale, *hc_base;
-  float *partial;
+  float *partial;   // [rows, M + 1, chunks]
   unsigned *tickets;
   float *mixes, *pre, *post, *comb;
   int rows, hcd, M, hc, chunk, iters;
   float eps;
 };
 
-__device__ void split_sinkhorn_row(const float *sums, const MixArgs &a, int r) {
+int hc_mix_chunks(int rows, int hcd) {
+  if (rows <= kDecodeRows) return hcd / 128;
+  return hcd % 512 == 0 ? 4 : hcd / 128;
+}
+
+// pre/post of one row from the reduced sums (mixes = sums * rsqrt(mean square + eps)).
+__device__ void split_prepost_row(const float *sums, const float *scale, const float *base, const MixArgs &a, int r) {
   const int hc = a.hc, M = a.M;
   const float rs = rsqrtf(sums[M] / (float)a.hcd + a.eps);
-  float mix[kMixMax];
-  for (int m = 0; m < M; ++m) {
-    mix[m] = sums[m] * rs;
-    a.mixes[(size_t)r * M + m] = mix[m];
-  }
-  const float s0 = a.hc_scale[0], s1 = a.hc_scale[1], s2 = a.hc_scale[2];
+  for (int m = 0; m < M; ++m) a.mixes[(size_t)r * M + m] = sums[m] * rs;
   for (int h = 0; h < hc; ++h) {
-    a.pre[(size_t)r * hc + h] = sigmoidf_(mix[h] * s0 + a.hc_base[h]);
-    a.post[(size_t)r * hc + h] = 2.0f * sigmoidf_(mix[hc + h] * s1 + a.hc_base[hc + h]);
+    a.pre[(size_t)r * hc + h] = sigmoidf_(sums[h] * rs * scale[0] + base[h]);
+    a.post[(size_t)r * hc + h] = 2.0f * sigmoidf_(sums[hc + h] * rs * scale[1] + base[hc + h]);
   }
-  float c[kHcMax][kHcMax];
-  for (int i = 0; i < hc; ++i) {
-    float mx = -INFINITY;
-    for (int j = 0; j < hc; ++j) {
-      c[i][j] = mix[2 * hc + i * hc + j] * s2 + a.hc_base[2 * hc + i * hc + j];
-      mx = fmaxf(mx, c[i][j]);
-    }
-    for (int j = 0; j < hc; ++j) c[i][j] = expf(c[i][j] - mx);
-  }
-  for (int it = 0; it < a.iters; ++it) {
-    for (int i = 0; i < hc; ++i) {
-      float s = 0.f;
-      for (int j = 0; j < hc; ++j) s += c[i][j];
-      for (int j = 0; j < hc; ++j) c[i][j] = c[i][j] / s;
-    }
-    for (int j = 0; j < hc; ++j) {
-      float s = 0.f;
-      for (int i = 0; i < hc; ++i) s += c[i][j];
-      for (int i = 0; i < hc; ++i) c[i][j] = c[i][j] / s;
-    }
-  }
-  for (int i = 0; i < hc; ++i)
-    for (int j = 0; j < hc; ++j) a.comb[((size_t)r * hc + i) * hc + j] = c[i][j];
 }
 
 template <int RB>
 __global__ void __launch_bounds__(256) hc_mix_kernel(MixArgs a) {
+  pdl_trigger();
   const int nch = gridDim.x;
   const int c0 = blockIdx.x * a.chunk;
   const int r0 = blockIdx.y * RB;
   const int nr = min(RB, a.rows - r0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int M = a.M;
+  __shared__ float s_scale[3], s_base[kMixMax];
+  if (threadIdx.x < 3) s_scale[threadIdx.x] = a.hc_scale[threadIdx.x];
+  if (threadIdx.x < M) s_base[threadIdx.x] = a.hc_base[threadIdx.x];
+  pdl_wait();
   float acc[RB][3], ss[RB];
 #pragma unroll
   for (int r = 0; r < RB; ++r) {
@@ -112,11 +96,11 @@ __global__ void __launch_bounds__(256) hc_mix_kernel(MixArgs a) {
   }
   if (lane == 0) {
     for (int r = 0; r < nr; ++r) {
-      float *p = a.partial + ((size_t)(r0 + r) * nch + blockIdx.x) * (M + 1);
+      float *p = a.partial + (size_t)(r0 + r) * (M + 1) * nch + blockIdx.x;
 #pragma unroll
       for (int q = 0; q < 3; ++q)
-        if (warp + 8 * q < M) p[warp + 8 * q] = acc[r][q];
-      if (warp == 0) p[M] = ss[r];
+        if (warp + 8 * q < M) p[(size_t)(warp + 8 * q) * nch] = acc[r][q];
+      if (warp == 0) p[(size_t)M * nch] = ss[r];
     }
   }
   __threadfence();
@@ -126,16 +110,30 @@ __global__ void __launch_bounds__(256) hc_mix_kernel(MixArgs a) {
   __syncthreads();
   if (!is_last) return;
   __threadfence();
+  // Reduce the chunk partials: tpi threads per (row, value), each over a strided share of the
+  // chunks with independent loads, then a shuffle tree; fixed order, so deterministic.
   __shared__ float sums[RB][kMixMax + 1];
-  for (int i = threadIdx.x; i < nr * (M + 1); i += blockDim.x) {
-    const int r = i / (M + 1), v = i - r * (M + 1);
-    const float *p = a.partial + (size_t)(r0 + r) * nch * (M + 1) + v;
+  const int items = nr * (M + 1);
+  int tpi = 32;
+  while (tpi > 1 && items * tpi > (int)blockDim.x) tpi >>= 1;
+  for (int i = threadIdx.x; i < ((items * tpi + 31) / 32) * 32; i += blockDim.x) {
+    const int item = i / tpi, part = i % tpi;
     float s = 0.f;
-    for (int ch = 0; ch < nch; ++ch) s += __ldcg(p + (size_t)ch * (M + 1));
-    sums[r][v] = s;
+    if (item < items) {
+      const float *p = a.partial + (size_t)(r0 * (M + 1) + item) * nch;
+#pragma unroll 8
+      for (int ch = part; ch < nch; ch += tpi) s += __ldcg(p + ch);
+    }
+    for (int o = tpi >> 1; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (part == 0 && item < items) sums[item / (M + 1)][item % (M + 1)] = s;
   }
   __syncthreads();
-  if (threadIdx.x < nr) split_sinkhorn_row(sums[threadIdx.x], a, r0 + threadIdx.x);
+  if (threadIdx.x < nr) {
+    const int r = r0 + threadIdx.x;
+    split_prepost_row(sums[threadIdx.x], s_scale, s_base, a, r);
+    if (a.do_sinkhorn)
+      sinkhorn_comb_row(a.mixes + (size_t)r * M, s_scale, s_base, a.hc, a.iters, a.comb + (size_t)r * a.hc * a.hc);
+  }
   if (threadIdx.x == 0) a.tickets[blockIdx.y] = 0u;
 }
 
@@ -158,20 +156,15 @@ void launch_hc_mix(const Dims &d, const Scratch &s, const LayerDev &w, const flo
   a.hc = d.hc;
   a.iters = d.iters;
   a.eps = d.eps;
-  // Decode: 128-column chunks so that the 0.8 MB hc_fn read spreads over ~128 CTAs.
-  // Prefill: 4 chunks per row group of 4 rows.
-  const int nch = rows <= kDecodeRows ? a.hcd / 128 : (a.hcd % 512 == 0 ? 4 : a.hcd / 128);
+  a.do_sinkhorn = rows > kDecodeRows;
+  const int nch = hc_mix_chunks(rows, a.hcd);
   a.chunk = a.hcd / nch;
   dim3 grid(nch, (rows + 3) / 4);
-  hc_mix_kernel<4><<<grid, 256, 0, st>>>(a);
+  launch_pdl(hc_mix_kernel<4>, grid, dim3(256), 0, st, a);
   stage(tm, "hc_mix", st);
 }
 
 // Same kernel with caller-chosen scratch (the allocation-free entry point's fixed array).
-int hc_mix_chunks(int rows, int hcd) {
-  return rows <= kDecodeRows ? hcd / 128 : (hcd % 512 == 0 ? 4 : hcd / 128);
-}
-
 void launch_hc_mix_raw(const float *state, const uint16_t *hc_fn, const float *hc_scale, const float *hc_base,
                        int rows, int hc, int hidden, int iters, float eps, float *partial, unsigned *tickets,
                        float *mixes, float *pre, float *post, float *comb, cudaStream_t st) {
@@ -192,6 +185,7 @@ void launch_hc_mix_raw(const float *state, const uint16_t *hc_fn, const float *h
   a.hc = hc;
   a.iters = iters;
   a.eps = eps;
+  a.do_sinkhorn = 1;
   const int nch = hc_mix_chunks(rows, a.hcd);
   a.chunk = a.hcd / nch;
   dim3 grid(nch, (rows + 3) / 4);
@@ -216,40 +210,36 @@ struct RouteParams {
   int *counts;  // optional per-expert histogram (rows > 4 path)
 };
 
-__device__ void route_row_warp(const float *logits, int r, const RouteParams &p) {
+// Routes row r with one warp.  `logits` is the row's logits (shared or global memory), `v` a
+// shared buffer of `experts` floats for the row's selection scores.  The code stays compact (the
+// serial tail runs once per forward, mostly out of a cold instruction cache): candidates are
+// scanned with a rolled loop, and slot k of the result lives in lane k.
+__device__ void route_row_warp(const float *logits, int r, const RouteParams &p, float *v, int *s_idx = nullptr,
+                               float *s_w = nullptr) {
   const int lane = threadIdx.x & 31;
   const int E = p.experts, K = p.top_k;
-  int sel[kTopKMax];
-  float sc[kTopKMax];
-  bool valid[kTopKMax];
+  int my_sel = -1;
   if (!p.hash) {
-    constexpr int J = kExpertsMax / 32;
-    float val[J];
     bool bad = false;
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-      const int e = lane + 32 * j;
-      val[j] = -INFINITY;
-      if (e < E) {
-        const float l = logits[e];
-        bad |= !isfinite(l);
-        const float v = sigmoidf_(l) + p.bias[e];
-        val[j] = isnan(v) ? -INFINITY : v;
-      }
+    for (int e = lane; e < E; e += 32) {
+      const float l = logits[e];
+      bad |= !isfinite(l);
+      const float x = sigmoidf_(l) + p.bias[e];
+      v[e] = isnan(x) ? -INFINITY : x;
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, kDevNonFinite);
+    __syncwarp();
     uint32_t taken = 0;
+#pragma unroll 1
     for (int k = 0; k < K; ++k) {
       float bv = -INFINITY;
       int be = 0x7fffffff;
-#pragma unroll
-      for (int j = 0; j < J; ++j) {
-        const int e = lane + 32 * j;
-        if (e < E && !((taken >> j) & 1u)) {
-          if (val[j] > bv || be == 0x7fffffff) {
-            bv = val[j];
-            be = e;
-          }
+#pragma unroll 1
+      for (int j = 0, e = lane; e < E; ++j, e += 32) {
+        const float x = v[e];
+        if (!((taken >> j) & 1u) && (x > bv || be == 0x7fffffff)) {
+          bv = x;
+          be = e;
         }
       }
 #pragma unroll
@@ -262,31 +252,28 @@ __device__ void route_row_warp(const float *logits, int r, const RouteParams &p)
         }
       }
       if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      sel[k] = be;
-      valid[k] = true;
+      if (lane == k) my_sel = be;
     }
   } else {
     const int tok = p.token_ids[r];
     const bool tok_ok = tok >= 0 && tok < p.vocab;
     if (!tok_ok && lane == 0) atomicOr(p.status, kDevTokenRange);
-    for (int k = 0; k < K; ++k) {
-      const int e = tok_ok ? p.tid2eid[(size_t)tok * K + k] : -1;
-      sel[k] = e;
-      valid[k] = e >= 0 && e < E;
-      if (tok_ok && !valid[k] && lane == 0) atomicOr(p.status, kDevRouteRange);
-    }
+    if (lane < K) my_sel = tok_ok ? p.tid2eid[(size_t)tok * K + lane] : -1;
+    const bool bad_entry = tok_ok && lane < K && !(my_sel >= 0 && my_sel < E);
+    if (__any_sync(0xffffffffu, bad_entry) && lane == 0) atomicOr(p.status, kDevRouteRange);
   }
-  float tot = 0.f;
-  for (int k = 0; k < K; ++k) {
-    sc[k] = valid[k] ? sigmoidf_(logits[sel[k]]) : 0.f;
-    tot += sc[k];
-  }
-  if (lane == 0) {
-    for (int k = 0; k < K; ++k) {
-      p.idx[(size_t)r * K + k] = sel[k];
-      p.rw[(size_t)r * K + k] = tot > 0.f ? sc[k] / tot : 0.f;
-      p.safe[(size_t)r * K + k] = valid[k] ? (unsigned)sel[k] : 0u;
-      if (p.counts && valid[k]) atomicAdd(&p.counts[sel[k]], 1);
+  const bool valid = lane < K && my_sel >= 0 && my_sel < E;
+  const float sc = valid ? sigmoidf_(logits[my_sel]) : 0.f;
+  const float tot = warp_sum(sc);
+  if (lane < K) {
+    const float w = tot > 0.f ? sc / tot : 0.f;
+    p.idx[(size_t)r * K + lane] = my_sel;
+    p.rw[(size_t)r * K + lane] = w;
+    p.safe[(size_t)r * K + lane] = valid ? (unsigned)my_sel : 0u;
+    if (p.counts && valid) atomicAdd(&p.counts[my_sel], 1);
+    if (s_idx) {
+      s_idx[lane] = my_sel;
+      s_w[lane] = w;
     }
   }
 }
@@ -301,35 +288,42 @@ __device__ void route_row_warp(const float *logits, int r, const RouteParams &p)
 struct DecodeRouterArgs {
   const float *state, *pre, *norm_w;
   const uint16_t *gate;
-  float *ffn_input, *ffn_norm, *partial, *logits;
+  float *ffn_input, *ffn_norm, *partial, *logits, *row_rs;
   unsigned *ticket;
   int *ngroups, *group_e, *group_mask;
   float *group_w;
-  int rows, hidden, hc;
+  unsigned *counters;  // the expert kernel's completion counters, cleared here
+  int n_counters;
+  int rows, hidden, hc, dchunk;
   float eps;
   RouteParams rp;
 };
 
-constexpr int kRouterChunk = 128;
+constexpr int kRouterChunkMax = 256;
+
+constexpr int kRouterSplit = 4;  // CTAs per d-chunk, each over a quarter of the experts
 
 __global__ void __launch_bounds__(256) decode_router_kernel(DecodeRouterArgs a) {
-  const int nch = gridDim.x;
-  const int d0 = blockIdx.x * kRouterChunk;
+  pdl_trigger();
+  const int nch = gridDim.x, dchunk = a.dchunk;
+  const int d0 = blockIdx.x * dchunk;
   const int E = a.rp.experts, rows = a.rows, tid = threadIdx.x;
-  __shared__ __align__(16) float xw[kDecodeRows][kRouterChunk];
+  const int lane = tid & 31, warp = tid >> 5;
+  __shared__ __align__(16) float xw[kDecodeRows][kRouterChunkMax];
   __shared__ float red[8][kDecodeRows];
   __shared__ float rs_s[kDecodeRows];
   __shared__ int is_last;
+  pdl_wait();
 
   float ssl[kDecodeRows];
 #pragma unroll
   for (int r = 0; r < kDecodeRows; ++r) {
     ssl[r] = 0.f;
-    if (r < rows && tid < kRouterChunk) {
+    if (r < rows && tid < dchunk) {
       const int d = d0 + tid;
       float v = 0.f;
       for (int h = 0; h < a.hc; ++h) v += a.pre[r * a.hc + h] * a.state[((size_t)r * a.hc + h) * a.hidden + d];
-      a.ffn_input[(size_t)r * a.hidden + d] = v;
+      if (blockIdx.y == 0) a.ffn_input[(size_t)r * a.hidden + d] = v;
       xw[r][tid] = v * a.norm_w[d];
       ssl[r] = v * v;
     }
@@ -337,36 +331,59 @@ __global__ void __launch_bounds__(256) decode_router_kernel(DecodeRouterArgs a) 
 #pragma unroll
   for (int r = 0; r < kDecodeRows; ++r) {
     const float v = warp_sum(ssl[r]);
-    if ((tid & 31) == 0) red[tid >> 5][r] = v;
+    if (lane == 0) red[warp][r] = v;
   }
   __syncthreads();
-  for (int e = tid; e < E; e += blockDim.x) {
-    float acc[kDecodeRows] = {0.f, 0.f, 0.f, 0.f};
-    const uint16_t *g = a.gate + (size_t)e * a.hidden + d0;
-#pragma unroll 4
-    for (int dd = 0; dd < kRouterChunk; dd += 8) {
-      const uint4 wv = __ldg(reinterpret_cast<const uint4 *>(g + dd));
+  // Partial logits over this d-chunk for this CTA's quarter of the experts.  A warp reads one
+  // expert's chunk of the router row at a time, 16 bytes per lane (coalesced), eight experts in
+  // flight; lane l owns the elements 8l .. 8l+7 of the chunk.
+  {
+    const int per = (E + kRouterSplit - 1) / kRouterSplit;
+    const int e0 = blockIdx.y * per, e1 = min(E, e0 + per);
+    const bool active = lane * 8 < dchunk;
+    float4 xa[kDecodeRows], xb[kDecodeRows];
 #pragma unroll
-      for (int r = 0; r < kDecodeRows; ++r)
-        if (r < rows)
-          acc[r] += dot8(wv, *reinterpret_cast<const float4 *>(&xw[r][dd]),
-                         *reinterpret_cast<const float4 *>(&xw[r][dd + 4]));
+    for (int r = 0; r < kDecodeRows; ++r) {
+      xa[r] = active ? *reinterpret_cast<const float4 *>(&xw[r][lane * 8]) : make_float4(0.f, 0.f, 0.f, 0.f);
+      xb[r] = active ? *reinterpret_cast<const float4 *>(&xw[r][lane * 8 + 4]) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    for (int r = 0; r < rows; ++r) a.partial[((size_t)r * nch + blockIdx.x) * (E + 1) + e] = acc[r];
+    constexpr int B = 8;
+    for (int eb = e0 + warp; eb < e1; eb += 8 * B) {
+      uint4 wv[B];
+#pragma unroll
+      for (int q = 0; q < B; ++q) {
+        const int e = eb + 8 * q;
+        wv[q] = (e < e1 && active) ? __ldg(reinterpret_cast<const uint4 *>(a.gate + (size_t)e * a.hidden + d0 + lane * 8))
+                                   : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int q = 0; q < B; ++q) {
+        const int e = eb + 8 * q;
+#pragma unroll
+        for (int r = 0; r < kDecodeRows; ++r) {
+          if (r < rows) {
+            const float v = warp_sum(dot8(wv[q], xa[r], xb[r]));
+            if (lane == 0 && e < e1) a.partial[((size_t)r * nch + blockIdx.x) * (E + 1) + e] = v;
+          }
+        }
+      }
+    }
   }
-  if (tid < rows) {
+  if (blockIdx.y == 0 && tid < rows) {
     float s = 0.f;
     for (int w = 0; w < 8; ++w) s += red[w][tid];
     a.partial[((size_t)tid * nch + blockIdx.x) * (E + 1) + E] = s;
   }
   __threadfence();
   __syncthreads();
-  if (tid == 0) is_last = (atomicAdd(a.ticket, 1u) == (unsigned)(nch - 1));
+  if (tid == 0) is_last = (atomicAdd(a.ticket, 1u) == (unsigned)(nch * gridDim.y - 1));
   __syncthreads();
   if (!is_last) return;
   __threadfence();
 
+  for (int i = tid; i < a.n_counters; i += blockDim.x) a.counters[i] = 0u;
   __shared__ float lg[kDecodeRows][kExpertsMax];
+  // Logits: one thread per (row, expert), the chunk partials read with independent loads.
   if (tid < rows) {
     float s = 0.f;
     for (int ch = 0; ch < nch; ++ch) s += __ldcg(a.partial + ((size_t)tid * nch + ch) * (E + 1) + E);
@@ -375,43 +392,54 @@ __global__ void __launch_bounds__(256) decode_router_kernel(DecodeRouterArgs a) 
   __syncthreads();
   for (int i = tid; i < rows * E; i += blockDim.x) {
     const int r = i / E, e = i - r * E;
+    const float *p = a.partial + (size_t)r * nch * (E + 1) + e;
     float s = 0.f;
-    for (int ch = 0; ch < nch; ++ch) s += __ldcg(a.partial + ((size_t)r * nch + ch) * (E + 1) + e);
+#pragma unroll 16
+    for (int ch = 0; ch < nch; ++ch) s += __ldcg(p + (size_t)ch * (E + 1));
     const float l = s * rs_s[r];
     lg[r][e] = l;
     a.logits[(size_t)r * E + e] = l;
   }
-  for (int i = tid; i < rows * a.hidden; i += blockDim.x) {
-    const int r = i / a.hidden, d = i - r * a.hidden;
-    a.ffn_norm[i] = __ldcg(a.ffn_input + i) * rs_s[r] * a.norm_w[d];
-  }
+  if (tid < rows) a.row_rs[tid] = rs_s[tid];
   __syncthreads();
-  const int warp = tid >> 5;
-  if (warp < rows) route_row_warp(lg[warp], warp, a.rp);
+  __shared__ int s_idx[kDecodeRows][kTopKMax];
+  __shared__ float s_w[kDecodeRows][kTopKMax];
+  __shared__ int s_ge[kDecodeGroupsMax], s_gm[kDecodeGroupsMax], s_ng;
+  __shared__ float s_gw[kDecodeGroupsMax][kDecodeRows];
+  __shared__ float sv[kDecodeRows][kExpertsMax];
+  if (warp < rows) route_row_warp(lg[warp], warp, a.rp, sv[warp], s_idx[warp], s_w[warp]);
   __syncthreads();
   if (tid == 0) {
+    // Group 0 is the shared expert (weight 1 for every row), then the distinct routed experts.
     const int K = a.rp.top_k;
-    int ng = 0;
+    s_ge[0] = E;
+    s_gm[0] = (1 << rows) - 1;
+    for (int q = 0; q < kDecodeRows; ++q) s_gw[0][q] = q < rows ? 1.f : 0.f;
+    int ng = 1;
     for (int r = 0; r < rows; ++r)
       for (int k = 0; k < K; ++k) {
-        const int e = a.rp.idx[r * K + k];
+        const int e = s_idx[r][k];
         if (e < 0 || e >= E) continue;
-        int g = 0;
-        while (g < ng && a.group_e[g] != e) ++g;
+        int g = 1;
+        while (g < ng && s_ge[g] != e) ++g;
         if (g == ng) {
-          a.group_e[g] = e;
-          a.group_mask[g] = 0;
-          for (int q = 0; q < kDecodeRows; ++q) a.group_w[g * kDecodeRows + q] = 0.f;
+          s_ge[g] = e;
+          s_gm[g] = 0;
+          for (int q = 0; q < kDecodeRows; ++q) s_gw[g][q] = 0.f;
           ++ng;
         }
-        a.group_mask[g] |= 1 << r;
-        a.group_w[g * kDecodeRows + r] += a.rp.rw[r * K + k];
+        s_gm[g] |= 1 << r;
+        s_gw[g][r] += s_w[r][k];
       }
-    a.group_e[ng] = E;  // shared expert
-    a.group_mask[ng] = (1 << rows) - 1;
-    for (int q = 0; q < kDecodeRows; ++q) a.group_w[ng * kDecodeRows + q] = q < rows ? 1.f : 0.f;
-    *a.ngroups = ng + 1;
+    s_ng = ng;
+    *a.ngroups = ng;
     *a.ticket = 0u;
+  }
+  __syncthreads();
+  for (int g = tid; g < s_ng; g += blockDim.x) {
+    a.group_e[g] = s_ge[g];
+    a.group_mask[g] = s_gm[g];
+    for (int q = 0; q < kDecodeRows; ++q) a.group_w[g * kDecodeRows + q] = s_gw[g][q];
   }
 }
 
@@ -442,6 +470,7 @@ void launch_decode_router(const Dims &d, const Scratch &s, const LayerDev &w, co
   a.gate = w.gate;
   a.ffn_input = s.ffn_input;
   a.ffn_norm = s.ffn_norm;
+  a.row_rs = s.row_rs;
   a.partial = s.router_partial;
   a.logits = s.logits;
   a.ticket = s.tickets + (s.max_rows / 4 + 1);
@@ -449,12 +478,15 @@ void launch_decode_router(const Dims &d, const Scratch &s, const LayerDev &w, co
   a.group_e = s.group_e;
   a.group_mask = s.group_mask;
   a.group_w = s.group_w;
+  a.counters = s.dec_counters;
+  a.n_counters = decode_counter_count(d);
   a.rows = rows;
   a.hidden = d.hidden;
   a.hc = d.hc;
+  a.dchunk = d.hidden % 256 == 0 ? 256 : 128;
   a.eps = d.eps;
   a.rp = make_route(d, s, w, token_ids, hash, nullptr);
-  decode_router_kernel<<<d.hidden / kRouterChunk, 256, 0, st>>>(a);
+  launch_pdl(decode_router_kernel, dim3(d.hidden / a.dchunk, kRouterSplit), dim3(256), 0, st, a);
   stage(tm, "decode_router", st);
 }
 
@@ -471,11 +503,14 @@ __global__ void __launch_bounds__(256) prefill_prenorm_kernel(const float *__res
   __shared__ float red[8];
   const int r = blockIdx.x, tid = threadIdx.x;
   float p[kHcMax];
+#pragma unroll
   for (int h = 0; h < kHcMax; ++h) p[h] = h < hc ? pre[(size_t)r * hc + h] : 0.f;
   float ss = 0.f;
   for (int dd = tid * 4; dd < hidden; dd += blockDim.x * 4) {
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int h = 0; h < hc; ++h) {
+#pragma unroll
+    for (int h = 0; h < kHcMax; ++h) {
+      if (h >= hc) break;
       const float4 x = *reinterpret_cast<const float4 *>(state + ((size_t)r * hc + h) * hidden + dd);
       v.x += p[h] * x.x;
       v.y += p[h] * x.y;
@@ -560,9 +595,10 @@ __global__ void __launch_bounds__(256) router_gemm_kernel(const float *__restric
 }
 
 __global__ void __launch_bounds__(256) route_rows_kernel(const float *__restrict__ logits, int rows, RouteParams p) {
+  __shared__ float sv[8][kExpertsMax];
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (r >= rows) return;
-  route_row_warp(logits + (size_t)r * p.experts, r, p);
+  route_row_warp(logits + (size_t)r * p.experts, r, p, sv[threadIdx.x >> 5]);
 }
 
 void launch_prefill_router(const Dims &d, const Scratch &s, const LayerDev &w, const float *state,
