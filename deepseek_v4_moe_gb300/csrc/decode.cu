@@ -10,16 +10,17 @@
 // expert); each weight row is streamed once by one warp with 16-byte loads, whatever the number of
 // batch rows that use it.  Activations stay f32.
 //
-// One launch covers all of it, so HBM never idles between the gate/up and down projections:
-//   phase A  warps take gate/up rows (group-major, shared expert first) and write
-//            act[g, r, i] = silu(x_r . G[i]) * (x_r . U[i]); each finished row bumps its group's
-//            counter;
-//   phase B  warps take down rows (group-major); a row of group g waits (bounded) until all of
-//            g's gate/up rows are done, then writes y[g, r, d] = act[g, r, :] . Dn[d, :]; the last
-//            writer of a 64-wide d-block (a device-scope counter) forms ffn_out = sum_g w * y and
-//            the hc_post output for that block.
-// The grid is exactly the number of co-resident CTAs, and a phase-B wait only depends on phase-A
-// rows, which never wait; so every wait ends.  Waits still give up after 1 s (device timeout bit).
+// One launch covers all of it, so HBM never idles between the gate/up and down projections.  Work
+// is handed out by device-wide tickets (warps that stream faster take more), in three phases:
+//   phase A  gate/up rows, group-major with the shared expert first, so groups complete in turn:
+//            act[g, r, i] = silu(x_r . G[i]) * (x_r . U[i]); each row bumps its group's counter;
+//   phase B  down rows, group-major; a group's rows wait (bounded) until its gate/up rows are all
+//            published, then y[g, r, d] = act[g, r, :] . Dn[d, :]; each ticket bumps its d-block;
+//   phase C  per 32-wide d-block, once every group's rows of it are in: ffn_out = sum_g w * y and
+//            the hc_post output of that block.
+// The grid is exactly the number of co-resident CTAs, every ticket of a phase is claimed before
+// any warp moves to the next phase, and phase-A work never waits: so every wait ends.  Waits still
+// give up after 1 s (device timeout bit).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -46,47 +47,34 @@ struct DecodeArgs {
 constexpr uint64_t kSpinLimitNs = 1000000000ull;
 
 __device__ __forceinline__ uint4 ld_weight(const uint16_t *p, bool routed, uint64_t pol) {
-  return routed ? ld_stream_hint(p, pol) : ld_stream(p);
+  (void)routed;
+  (void)pol;
+  return ld_stream(p);
 }
 
-// Final reduce + hc_post of d-block `blk` by one warp (after the comb is published).
-__device__ void combine_dblock(const DecodeArgs &a, int blk, int ng, const unsigned *comb_ready) {
+// Final reduce + hc_post of d-block `blk` (32 d, one per lane) by one warp, once its y rows and the
+// comb are published.  y holds zeros for the rows a group does not serve, so the sum over groups
+// is unconditional and its loads are batched.  s_pre holds this lane's state values, loaded before
+// the wait.
+__device__ void combine_dblock(const DecodeArgs &a, int blk, int ng, const float (&s_pre)[kDecodeRows][kHcMax]) {
   const int lane = threadIdx.x & 31, D = a.hidden, hc = a.hc;
-  int ok = 1;
-  if (lane == 0 && ld_acquire_u32(comb_ready) == 0u) {
-    const uint64_t w0 = global_timer_ns();
-    while (ld_acquire_u32(comb_ready) == 0u) {
-      if (global_timer_ns() - w0 > 1000000000ull) {
-        atomicOr(a.status, kDevTimeout);
-        ok = 0;
-        break;
-      }
-      __nanosleep(100);
-    }
-  }
-  if (!__shfl_sync(0xffffffffu, ok, 0)) return;
-  (void)ld_acquire_u32(comb_ready);
-  for (int d = blk * kDecodeDBlock + lane; d < (blk + 1) * kDecodeDBlock; d += 32) {
-    for (int r = 0; r < a.rows; ++r) {
-      float f = 0.f;
+  const int d = blk * kDecodeDBlock + lane;
+#pragma unroll
+  for (int r = 0; r < kDecodeRows; ++r) {
+    if (r >= a.rows) break;
+    float f = 0.f;
 #pragma unroll 8
-      for (int g = 0; g < ng; ++g) {
-        if ((a.group_mask[g] >> r) & 1)
-          f += a.group_w[g * kDecodeRows + r] * __ldcg(a.y + ((size_t)g * kDecodeRows + r) * D + d);
-      }
-      a.ffn_out[(size_t)r * D + d] = f;
-      float s[kHcMax];
+    for (int g = 0; g < ng; ++g)
+      f += __ldcg(a.group_w + g * kDecodeRows + r) * __ldcg(a.y + ((size_t)g * kDecodeRows + r) * D + d);
+    a.ffn_out[(size_t)r * D + d] = f;
 #pragma unroll
-      for (int j = 0; j < kHcMax; ++j) s[j] = j < hc ? a.state[((size_t)r * hc + j) * D + d] : 0.f;
+    for (int o = 0; o < kHcMax; ++o) {
+      if (o < hc) {
+        float v = __ldcg(a.post + r * hc + o) * f;
 #pragma unroll
-      for (int o = 0; o < kHcMax; ++o) {
-        if (o < hc) {
-          float v = a.post[r * hc + o] * f;
-#pragma unroll
-          for (int j = 0; j < kHcMax; ++j)
-            if (j < hc) v += __ldcg(a.comb + (r * hc + o) * hc + j) * s[j];
-          a.out_state[((size_t)r * hc + o) * D + d] = v;
-        }
+        for (int j = 0; j < kHcMax; ++j)
+          if (j < hc) v += __ldcg(a.comb + (r * hc + o) * hc + j) * s_pre[r][j];
+        a.out_state[((size_t)r * hc + o) * D + d] = v;
       }
     }
   }
@@ -103,13 +91,43 @@ __device__ __forceinline__ float4 ld_ca4(const float *p) {
   return v;
 }
 
-// Publishes `n` finished rows on a counter: the writes before it become visible first.
-__device__ __forceinline__ unsigned publish(unsigned *counter, unsigned n) {
-  __threadfence();
-  return atomicAdd(counter, n);
+// Adds n to a completion counter with release semantics: this thread's earlier writes are visible
+// to whoever acquires the new value.  No value is returned, so the warp does not wait for it.
+__device__ __forceinline__ void publish(unsigned *counter, unsigned n) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(counter), "r"(n) : "memory");
 }
 
-__global__ void __launch_bounds__(256, 3) decode_experts_kernel(DecodeArgs a) {
+// Bounded wait (lane 0 polls, the warp follows) until *counter >= target; every lane then acquires
+// the counter so its later reads see what the producers published.  False on timeout.
+__device__ bool wait_at_least(const unsigned *counter, unsigned target, int *status) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0 && ld_acquire_u32(counter) < target) {
+    const uint64_t w0 = global_timer_ns();
+    while (ld_acquire_u32(counter) < target) {
+      if (global_timer_ns() - w0 > kSpinLimitNs) {
+        atomicOr(status, kDevTimeout);
+        ok = 0;
+        break;
+      }
+      __nanosleep(128);
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) (void)ld_acquire_u32(counter);
+  return ok != 0;
+}
+
+// Next work ticket of a phase: lane 0 draws it, the warp shares it.
+__device__ __forceinline__ int draw_ticket(unsigned *tick) {
+  int c = 0;
+  if ((threadIdx.x & 31) == 0) c = (int)atomicAdd(tick, 1u);
+  return __shfl_sync(0xffffffffu, c, 0);
+}
+
+constexpr int kRowsPerTicketA = 2;  // gate/up rows per ticket
+constexpr int kRowsPerTicketB = 4;  // down rows per ticket (a 64-row d-block holds 16 tickets)
+
+__global__ void __launch_bounds__(256, 2) decode_experts_kernel(DecodeArgs a) {
   extern __shared__ __align__(16) float xs[];  // [rows, hidden]
   pdl_wait();
   const int D = a.hidden, I = a.inter, rows = a.rows, E = a.experts;
@@ -126,40 +144,40 @@ __global__ void __launch_bounds__(256, 3) decode_experts_kernel(DecodeArgs a) {
   const uint64_t pol = make_policy_evict_first();
   const int lane = threadIdx.x & 31;
   const int gwarp = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int nwarps = gridDim.x * (blockDim.x >> 5) - 1;  // the grid's last warp forms the comb
+  const int last_warp = gridDim.x * (blockDim.x >> 5) - 1;
   const int ng = *a.ngroups;
+  const int nblk = D / kDecodeDBlock;
   unsigned *group_done = a.counters;
   unsigned *dblock_done = a.counters + kDecodeGroupsMax;
-  unsigned *comb_ready = a.counters + kDecodeGroupsMax + D / kDecodeDBlock;
-  if (gwarp == nwarps) {
+  unsigned *comb_ready = dblock_done + nblk;
+  unsigned *tick = comb_ready + 1;  // [3]
+  if (gwarp == last_warp) {
     // The hc x hc comb (Sinkhorn) is only needed by the final hc_post: form it here, one thread
     // per row, while the other warps stream the expert weights.
     if (lane < rows)
       sinkhorn_comb_row(a.mixes + (size_t)lane * ((2 + a.hc) * a.hc), a.hc_scale, a.hc_base, a.hc, a.iters,
                         a.comb + (size_t)lane * a.hc * a.hc);
     __syncwarp();
-    if (lane == 0) publish(comb_ready, 1u);
+    if (lane == 0) {
+      __threadfence();
+      publish(comb_ready, 1u);
+    }
     return;
   }
 
-  // ---- phase A: a contiguous range of gate/up rows per warp (group-major, shared expert first) ----
-  constexpr int UA = 4;
-  {
-    const long long TA = (long long)ng * I;
-    const int t0 = (int)(TA * gwarp / nwarps), t1 = (int)(TA * (gwarp + 1) / nwarps);
-    int cur = -1, e = 0, mask = 0;
-    bool routed = false;
-    unsigned cnt = 0;
-    for (int t = t0; t < t1; ++t) {
+  // ---- phase A: gate/up rows, tickets in group-major order (the shared expert first) ----
+  // Every row's 2 x hidden bf16 are in flight at once (UA loads per lane per matrix).
+  constexpr int UA = 8;
+  const int TA = ng * I, nA = (TA + kRowsPerTicketA - 1) / kRowsPerTicketA;
+  for (int c = draw_ticket(&tick[0]); c < nA;) {
+    int next = 0;
+    if (lane == 0) next = (int)atomicAdd(&tick[0], 1u);  // consumed after this chunk: latency hidden
+    const int t_end = min(TA, (c + 1) * kRowsPerTicketA);
+    for (int t = c * kRowsPerTicketA; t < t_end; ++t) {
       const int g = t / I, i = t - g * I;
-      if (g != cur) {
-        if (cnt && lane == 0) publish(&group_done[cur], cnt);
-        cur = g;
-        cnt = 0;
-        e = a.group_e[g];
-        mask = a.group_mask[g];
-        routed = e < E;
-      }
+      const int e = a.group_e[g];
+      const int mask = a.group_mask[g];
+      const bool routed = e < E;
       const uint16_t *gw = routed ? a.gate_exps + ((size_t)e * I + i) * D : a.gate_sh + (size_t)i * D;
       const uint16_t *uw = routed ? a.up_exps + ((size_t)e * I + i) * D : a.up_sh + (size_t)i * D;
       float ga[kDecodeRows] = {0.f, 0.f, 0.f, 0.f}, ua[kDecodeRows] = {0.f, 0.f, 0.f, 0.f};
@@ -167,21 +185,21 @@ __global__ void __launch_bounds__(256, 3) decode_experts_kernel(DecodeArgs a) {
         uint4 gv[UA], uv[UA];
 #pragma unroll
         for (int u = 0; u < UA; ++u) {
-          const int c = base + u * 256;
-          if (c < D) {
-            gv[u] = ld_weight(gw + c, routed, pol);
-            uv[u] = ld_weight(uw + c, routed, pol);
+          const int cc = base + u * 256;
+          if (cc < D) {
+            gv[u] = ld_weight(gw + cc, routed, pol);
+            uv[u] = ld_weight(uw + cc, routed, pol);
           }
         }
 #pragma unroll
         for (int u = 0; u < UA; ++u) {
-          const int c = base + u * 256;
-          if (c < D) {
+          const int cc = base + u * 256;
+          if (cc < D) {
 #pragma unroll
             for (int r = 0; r < kDecodeRows; ++r) {
               if (r < rows) {
-                const float4 x0 = *reinterpret_cast<const float4 *>(&xs[r * D + c]);
-                const float4 x1 = *reinterpret_cast<const float4 *>(&xs[r * D + c + 4]);
+                const float4 x0 = *reinterpret_cast<const float4 *>(&xs[r * D + cc]);
+                const float4 x1 = *reinterpret_cast<const float4 *>(&xs[r * D + cc + 4]);
                 ga[r] += dot8(gv[u], x0, x1);
                 ua[r] += dot8(uv[u], x0, x1);
               }
@@ -197,75 +215,58 @@ __global__ void __launch_bounds__(256, 3) decode_experts_kernel(DecodeArgs a) {
           if (lane == 0 && ((mask >> r) & 1)) a.act[((size_t)g * kDecodeRows + r) * I + i] = gs * sigmoidf_(gs) * us;
         }
       }
-      ++cnt;
+      if (lane == 0) publish(&group_done[g], 1u);
     }
-    if (cnt && lane == 0) publish(&group_done[cur], cnt);
+    c = __shfl_sync(0xffffffffu, next, 0);
   }
 
-  // ---- phase B: a contiguous range of down rows per warp; per completed d-block, reduce + hc_post ----
+  // ---- phase B: down rows, tickets in group-major order; a ticket's rows share one group and one
+  // d-block.  A group's rows wait (bounded) until all of its gate/up rows are published.
   constexpr int UB = 8;
-  {
-    const unsigned dblock_total = (unsigned)(ng * kDecodeDBlock);
-    const long long TB = (long long)ng * D;
-    const int t0 = (int)(TB * gwarp / nwarps), t1 = (int)(TB * (gwarp + 1) / nwarps);
-    int cur = -1, e = 0, mask = 0, blk = -1;
-    bool routed = false, ready = false;
-    unsigned cnt = 0;
-    auto flush_block = [&]() {
-      unsigned prev = 0;
-      if (lane == 0) prev = publish(&dblock_done[blk], cnt);
-      prev = __shfl_sync(0xffffffffu, prev, 0);
-      if (prev + cnt == dblock_total) {
-        __threadfence();
-        combine_dblock(a, blk, ng, comb_ready);
-      }
-    };
-    for (int t = t0; t < t1; ++t) {
-      const int g = t / D, dd = t - g * D;
-      if (dd / kDecodeDBlock != blk || g != cur) {
-        if (cnt) flush_block();
-        blk = dd / kDecodeDBlock;
-        cnt = 0;
-      }
-      if (g != cur) {
-        cur = g;
-        e = a.group_e[g];
-        mask = a.group_mask[g];
-        routed = e < E;
-        int ok = 1;
-        if (lane == 0 && ld_acquire_u32(&group_done[g]) < (unsigned)I) {
-          const uint64_t w0 = global_timer_ns();
-          while (ld_acquire_u32(&group_done[g]) < (unsigned)I) {
-            if (global_timer_ns() - w0 > kSpinLimitNs) {
-              atomicOr(a.status, kDevTimeout);
-              ok = 0;
-              break;
-            }
-            __nanosleep(100);
-          }
-        }
-        ready = __shfl_sync(0xffffffffu, ok, 0) != 0;
-        (void)ld_acquire_u32(&group_done[g]);  // each lane orders its act reads after the counter
-      }
-      if (ready) {
-        const uint16_t *dw = routed ? a.down_exps + ((size_t)e * D + dd) * I : a.down_sh + (size_t)dd * I;
-        const float *act = a.act + (size_t)g * kDecodeRows * I;
-        float acc[kDecodeRows] = {0.f, 0.f, 0.f, 0.f};
+  const int TB = ng * D, nB = TB / kRowsPerTicketB;
+  int cur = -1;
+  bool ready = false;
+  for (int c = draw_ticket(&tick[1]); c < nB;) {
+    int next = 0;
+    if (lane == 0) next = (int)atomicAdd(&tick[1], 1u);
+    const int t0 = c * kRowsPerTicketB;
+    const int g = t0 / D, d0 = t0 - g * D;
+    if (g != cur) {
+      cur = g;
+      ready = wait_at_least(&group_done[g], (unsigned)I, a.status);
+    }
+    const int e = a.group_e[g];
+    const int mask = a.group_mask[g];
+    const bool routed = e < E;
+    if (ready) {
+      const float *act = a.act + (size_t)g * kDecodeRows * I;
+#pragma unroll 1
+      for (int q = 0; q < kRowsPerTicketB; q += 2) {
+        // two down rows in flight together
+        const int dd = d0 + q;
+        const uint16_t *dw0 = routed ? a.down_exps + ((size_t)e * D + dd) * I : a.down_sh + (size_t)dd * I;
+        const uint16_t *dw1 = dw0 + I;
+        float acc0[kDecodeRows] = {0.f, 0.f, 0.f, 0.f}, acc1[kDecodeRows] = {0.f, 0.f, 0.f, 0.f};
         for (int base = lane * 8; base < I; base += 256 * UB) {
-          uint4 wv[UB];
-#pragma unroll
-          for (int u = 0; u < UB; ++u)
-            if (base + u * 256 < I) wv[u] = ld_weight(dw + base + u * 256, routed, pol);
+          uint4 w0[UB], w1[UB];
 #pragma unroll
           for (int u = 0; u < UB; ++u) {
-            const int c = base + u * 256;
-            if (c < I) {
+            if (base + u * 256 < I) {
+              w0[u] = ld_weight(dw0 + base + u * 256, routed, pol);
+              w1[u] = ld_weight(dw1 + base + u * 256, routed, pol);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < UB; ++u) {
+            const int cc = base + u * 256;
+            if (cc < I) {
 #pragma unroll
               for (int r = 0; r < kDecodeRows; ++r) {
                 if ((mask >> r) & 1) {
-                  const float4 x0 = ld_ca4(act + (size_t)r * I + c);
-                  const float4 x1 = ld_ca4(act + (size_t)r * I + c + 4);
-                  acc[r] += dot8(wv[u], x0, x1);
+                  const float4 x0 = ld_ca4(act + (size_t)r * I + cc);
+                  const float4 x1 = ld_ca4(act + (size_t)r * I + cc + 4);
+                  acc0[r] += dot8(w0[u], x0, x1);
+                  acc1[r] += dot8(w1[u], x0, x1);
                 }
               }
             }
@@ -274,14 +275,33 @@ __global__ void __launch_bounds__(256, 3) decode_experts_kernel(DecodeArgs a) {
 #pragma unroll
         for (int r = 0; r < kDecodeRows; ++r) {
           if (r < rows) {
-            const float s = warp_sum(acc[r]);
-            if (lane == 0 && ((mask >> r) & 1)) a.y[((size_t)g * kDecodeRows + r) * D + dd] = s;
+            const float s0 = warp_sum(acc0[r]);
+            const float s1 = warp_sum(acc1[r]);
+            if (lane == 0) {  // zeros for rows this group does not serve
+              const bool use = (mask >> r) & 1;
+              a.y[((size_t)g * kDecodeRows + r) * D + dd] = use ? s0 : 0.f;
+              a.y[((size_t)g * kDecodeRows + r) * D + dd + 1] = use ? s1 : 0.f;
+            }
           }
         }
       }
-      ++cnt;
     }
-    if (cnt) flush_block();
+    if (lane == 0) publish(&dblock_done[d0 / kDecodeDBlock], (unsigned)kRowsPerTicketB);
+    c = __shfl_sync(0xffffffffu, next, 0);
+  }
+
+  // ---- phase C: per d-block, once all groups' rows of it are in, ffn_out and hc_post ----
+  for (int c = draw_ticket(&tick[2]); c < nblk; c = draw_ticket(&tick[2])) {
+    float s_pre[kDecodeRows][kHcMax];
+    const int d = c * kDecodeDBlock + lane;
+#pragma unroll
+    for (int r = 0; r < kDecodeRows; ++r)
+#pragma unroll
+      for (int j = 0; j < kHcMax; ++j)
+        s_pre[r][j] = (r < rows && j < a.hc) ? a.state[((size_t)r * a.hc + j) * D + d] : 0.f;
+    if (wait_at_least(&dblock_done[c], (unsigned)(ng * kDecodeDBlock), a.status) &&
+        wait_at_least(comb_ready, 1u, a.status))
+      combine_dblock(a, c, ng, s_pre);
   }
 }
 

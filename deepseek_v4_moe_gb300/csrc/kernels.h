@@ -116,8 +116,9 @@ void launch_hc_mix_raw(const float *state, const uint16_t *hc_fn, const float *h
 void set_global_error(const char *msg);
 // decode.cu
 constexpr int kDecodeGroupsMax = 4 * 8 + 1;  // rows x top_k distinct experts + the shared one
-constexpr int kDecodeDBlock = 64;            // d-block of the decode reduce + hc_post
-inline int decode_counter_count(const Dims &d) { return kDecodeGroupsMax + d.hidden / kDecodeDBlock + 1; }
+constexpr int kDecodeDBlock = 32;            // d-block of the decode reduce + hc_post (one d per lane)
+// counters: rows done per group | arrivals per d-block | comb ready | work tickets of phases A, B, C
+inline int decode_counter_count(const Dims &d) { return kDecodeGroupsMax + d.hidden / kDecodeDBlock + 4; }
 void launch_decode_experts(const Dims &d, const Scratch &s, const LayerDev &w, const float *state, int rows,
                            float *out_state, int num_sms, cudaStream_t st, StageTimer *tm);
 cudaError_t decode_configure(int hidden);
