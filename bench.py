@@ -74,26 +74,63 @@ def work_model(cfg, indices: np.ndarray) -> dict:
                 flops_gateup=slots * 2 * 2 * I * D, flops_down=slots * 2 * I * D)
 
 
-def kernel_work(name: str, wm: dict, cfg) -> tuple[str, float]:
-    """(bound, algorithmic bytes or flops) of one launch of a kernel of the forward."""
+def kernel_work(name: str, wm: dict, cfg) -> tuple[float, float]:
+    """(algorithmic bytes, algorithmic flops) of one launch of a kernel of the forward."""
     R, D, I, HC, E, K = cfg.rows, cfg.hidden, cfg.inter, cfg.hc, cfg.experts, cfg.top_k
-    if name in ("decode_gateup", "gemm_gateup"):
-        return "hbm", wm["w_gateup"] + (wm["slots"] * (D + I) * (2 if name == "gemm_gateup" else 4))
-    if name in ("decode_down", "gemm_down"):
-        return "hbm", wm["w_down"] + wm["slots"] * (I * 2 + D * 4) * (1 if name == "gemm_down" else 0)
+    slots = wm["slots"]
+    if name == "decode_experts":
+        # every touched expert's gate/up/down once, the state read and written by the fused hc_post,
+        # the per-group act / y round trips
+        return (wm["w_gateup"] + wm["w_down"] + 2 * wm["state"] + slots * (I + D) * 4 * 2,
+                wm["flops_gateup"] + wm["flops_down"])
+    if name == "gemm_gateup":
+        return wm["w_gateup"] + slots * (D * 2 + I * 2), wm["flops_gateup"]
+    if name == "gemm_down":
+        return wm["w_down"] + slots * (I * 2 + D * 4), wm["flops_down"]
     if name == "hc_mix":
-        return "hbm", wm["state"] + cfg.mix * HC * D * 2
+        return wm["state"] + cfg.mix * HC * D * 2, 2 * R * cfg.mix * HC * D
     if name == "decode_router":
-        return "hbm", wm["state"] + E * D * 2
+        return R * D * 4 + E * D * 2, 2 * R * E * D
     if name == "prenorm":
-        return "hbm", wm["state"] + 2 * R * D * 4
+        return wm["state"] + 2 * R * D * 4, 0.0
     if name == "router_gemm":
-        return "hbm", R * D * 4 + E * D * 2 + R * E * 4
-    if name in ("decode_combine", "post"):
-        return "hbm", 2 * wm["state"] + (wm["slots"] * D * 4 if name == "post" else 0)
+        return R * D * 4 + E * D * 2 + R * E * 4, 2 * R * E * D
+    if name == "post":
+        return 2 * wm["state"] + slots * D * 4, 0.0
     if name == "scatter":
-        return "hbm", wm["slots"] * D * (4 + 2)
-    return "hbm", R * K * 4
+        return slots * D * (4 + 2), 0.0
+    return R * K * 4, 0.0
+
+
+def roofline_entry(name: str, avg_ms: float, wm: dict, cfg, peaks: dict, peak_kind: str) -> dict:
+    """The kernel's binding roofline: HBM bytes or tensor flops, whichever takes longer at peak."""
+    nbytes, flops = kernel_work(name, wm, cfg)
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    s = avg_ms * 1e-3
+    if t_tc > t_hbm:
+        ach = flops / s / 1e12
+        return dict(bound="tensor", achieved=round(ach, 1), peak=peaks["bf16_tflops"], unit="TFLOP/s",
+                    frac=round(ach / peaks["bf16_tflops"], 4), alg=int(flops),
+                    peak_source=f"{peak_kind} bf16_tflops (cuBLAS; fp16 operands run at the bf16 rate)")
+    ach = nbytes / s / 1e9
+    return dict(bound="hbm", achieved=round(ach, 1), peak=peaks["hbm_gbs"], unit="GB/s",
+                frac=round(ach / peaks["hbm_gbs"], 4), alg=int(nbytes), peak_source=f"{peak_kind} hbm_gbs (copy)")
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest x over all ranks (the job's time is its slowest rank's); x itself with no group."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, rows_per_rank: int, steps: int, seconds: float) -> float:
+    """Whole-job tokens/s: every rank's rows of every step over the slowest rank's time."""
+    return world * rows_per_rank * steps / seconds
 
 
 # ---- clocks ----------------------------------------------------------------------------------------
@@ -198,13 +235,9 @@ def run_ours(cfg, steps: int, warmup: int, device, rank: int, world: int, dist, 
         dist.barrier()
     clocks = sampler.stop()
     ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = float(sum(ms))
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(sum(ms)), dist, device)
     res = dict(total_ms=total_ms, ms_per_step=total_ms / steps, median_ms=statistics.median(ms),
-               value=world * cfg.rows * steps / (total_ms / 1e3), wall_s=wall1 - wall0, clocks=clocks, wm=wm)
+               value=job_rate(world, cfg.rows, steps, total_ms / 1e3), wall_s=wall1 - wall0, clocks=clocks, wm=wm)
 
     # ---- per-kernel durations: the same steps again with stage events ----
     m.set_stage_timing(True)
@@ -223,17 +256,18 @@ def run_ours(cfg, steps: int, warmup: int, device, rank: int, world: int, dist, 
     tot = sum(statistics.mean(v) for v in per.values())
     for name, v in per.items():
         avg = statistics.mean(v)
-        bound, work = kernel_work(name, wm, cfg)
-        gbs = work / (avg * 1e-3) / 1e9
-        kernels.append(dict(name=name, avg_us=round(avg * 1e3, 2), share=round(avg / tot, 4),
-                            alg_bytes=int(work), gbs=round(gbs, 1), frac_hbm=round(gbs / peaks["hbm_gbs"], 4)))
+        rl = roofline_entry(name, avg, wm, cfg, peaks, peak_kind)
+        kernels.append(dict(name=name, avg_us=round(avg * 1e3, 2), share=round(avg / tot, 4), bound=rl["bound"],
+                            achieved=rl["achieved"], unit=rl["unit"], frac=rl["frac"], alg=rl["alg"]))
+        per[name] = (v, rl)
     kernels.sort(key=lambda k: -k["avg_us"])
     top = kernels[0]
     res["kernels"] = kernels
     res["gpu_launches"] = n_kernels * steps
-    res["roofline"] = {"bound": "hbm", "kernel": top["name"], "achieved": top["gbs"], "peak": peaks["hbm_gbs"],
-                       "unit": "GB/s", "frac": top["frac_hbm"], "traffic": None,
-                       "peak_source": f"{peak_kind} hbm_gbs (copy)"}
+    rl = per[top["name"]][1]
+    res["roofline"] = {"bound": rl["bound"], "kernel": top["name"], "achieved": rl["achieved"], "peak": rl["peak"],
+                       "unit": rl["unit"], "frac": rl["frac"], "traffic": None, "peak_source": rl["peak_source"],
+                       "alg_per_launch": rl["alg"]}
     # whole forward against its binding roofline
     t_hbm = wm["bytes_total"] / (peaks["hbm_gbs"] * 1e9)
     t_tc = wm["flops_total"] / (peaks["bf16_tflops"] * 1e12)
@@ -259,12 +293,8 @@ def run_ours(cfg, steps: int, warmup: int, device, rank: int, world: int, dist, 
             t0 = time.perf_counter()
             m.forward_host(a_in, a_tok, cfg.layer, a_out, stream=stream)
             dts.append(time.perf_counter() - t0)
-        e2e_s = sum(dts)
-        if dist is not None:
-            t = torch.tensor([e2e_s], dtype=torch.float64, device=device)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
-        res["e2e"] = {"value": round(world * cfg.rows * steps / e2e_s, 1), "unit": "tokens/s",
+        e2e_s = max_over_ranks(sum(dts), dist, device)
+        res["e2e"] = {"value": round(job_rate(world, cfg.rows, steps, e2e_s), 1), "unit": "tokens/s",
                       "h2d_bytes_per_step": int(a_in.nbytes + a_tok.nbytes), "d2h_bytes_per_step": int(a_out.nbytes),
                       "api": "moe_ffn_forward_host (pinned host buffers, synchronous)"}
     m.close()
@@ -381,7 +411,7 @@ def main():
                          want_e2e=False, soak_s=min(0.5, args.soak))
             workloads[name] = {"value": round(r["value"], 1), "unit": "tokens/s", "ms_per_step": round(r["ms_per_step"], 4),
                                "forward_roofline": r["forward_roofline"], "top_kernel": r["kernels"][0],
-                               "clocks": r["clocks"]}
+                               "kernels": r["kernels"], "clocks": r["clocks"]}
     cpu = None
     if rank == 0 and world == 1 and args.cpu_baseline:
         rate, dt, n = oracle_rate(cfg, 8 if cfg.rows <= 4 else 4, 20.0)

@@ -198,6 +198,40 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *tmap, ui
       : "memory");
 }
 
+// 1-D bulk copy global -> shared memory, completion counted on `bar` (bytes: multiple of 16; both
+// addresses 16-byte aligned).
+__device__ __forceinline__ void tma_bulk_g2s(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(smem_dst)),
+               "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const void *p) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(smem_u32(p)));
+  return r;
+}
+
+// Sum over the warp of 32 values per lane: afterwards lane l holds the sum of every lane's v[l]
+// (a butterfly that halves the live values at each of 5 steps: 31 shuffles for 32 sums).
+__device__ __forceinline__ float transpose_reduce32(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const bool hi = (lane & s) != 0;
+#pragma unroll
+    for (int i = 0; i < s; ++i) {
+      const float send = hi ? v[i] : v[i + s];
+      const float keep = hi ? v[i + s] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+  return v[0];
+}
+
 __device__ __forceinline__ void tmap_prefetch(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

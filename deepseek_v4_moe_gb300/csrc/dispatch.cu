@@ -11,40 +11,79 @@
 
 namespace moe {
 
+// Inclusive scan of one value per thread over a 1024-thread block (warp shuffles, then the warp
+// totals); `tmp` holds 32 floats of scratch.
+__device__ int block_scan_incl(int v, int *tmp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) tmp[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int t = tmp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += n;
+    }
+    tmp[lane] = t;
+  }
+  __syncthreads();
+  const int res = v + (warp > 0 ? tmp[warp - 1] : 0);
+  __syncthreads();
+  return res;
+}
+
+// Groups 0..E-1 are the routed experts (counts from the router), group E the shared expert (every
+// row).  Exclusive scans give each group's first list position and first tile; the gate/up and down
+// tile lists are (group, weight block, token block, valid tokens), group-major then weight-block-major
+// so the token blocks of one weight tile run side by side.  Resets the counts for the next forward.
 __global__ void __launch_bounds__(1024) build_tiles_kernel(int *__restrict__ counts, int E, int rows, int mb_gu,
                                                            int mb_dn, int *__restrict__ offsets,
                                                            int *__restrict__ cursor, int4 *__restrict__ tiles_gu,
                                                            int4 *__restrict__ tiles_dn, int *__restrict__ n_tiles) {
-  __shared__ int cnt[kExpertsMax + 1], nb[kExpertsMax + 1], off[kExpertsMax + 2], toff[kExpertsMax + 2];
-  const int G = E + 1;
-  for (int g = threadIdx.x; g < G; g += blockDim.x) {
-    const int c = g < E ? counts[g] : rows;
+  __shared__ int cnt[kExpertsMax + 1], nb[kExpertsMax + 1], toff[kExpertsMax + 2];
+  __shared__ int tmp[32];
+  const int G = E + 1, g = threadIdx.x;
+  const int c = g < G ? (g < E ? counts[g] : rows) : 0;
+  const int n = (c + 127) / 128;
+  if (g < G) {
     cnt[g] = c;
-    nb[g] = (c + 127) / 128;
-    if (g < E) counts[g] = 0;  // ready for the next forward
+    nb[g] = n;
+    if (g < E) counts[g] = 0;
     cursor[g] = 0;
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    off[0] = 0;
-    toff[0] = 0;
-    for (int g = 0; g < G; ++g) {
-      off[g + 1] = off[g] + cnt[g];
-      toff[g + 1] = toff[g] + nb[g];
-    }
-    n_tiles[0] = toff[G] * mb_gu;
-    n_tiles[1] = toff[G] * mb_dn;
+  const int off_incl = block_scan_incl(c, tmp);
+  const int tb_incl = block_scan_incl(n, tmp);
+  if (g < G) {
+    offsets[g] = off_incl - c;
+    toff[g] = tb_incl - n;
+  }
+  if (g == G - 1) {
+    offsets[G] = off_incl;
+    toff[G] = tb_incl;
+    n_tiles[0] = tb_incl * mb_gu;
+    n_tiles[1] = tb_incl * mb_dn;
   }
   __syncthreads();
-  for (int g = threadIdx.x; g <= G; g += blockDim.x) offsets[g] = off[g];
-  for (int g = threadIdx.x; g < G; g += blockDim.x) {
-    const int n = nb[g], c = cnt[g];
-    for (int m = 0; m < mb_gu; ++m)
-      for (int b = 0; b < n; ++b)
-        tiles_gu[toff[g] * mb_gu + m * n + b] = make_int4(g, m, b, min(128, c - b * 128));
-    for (int m = 0; m < mb_dn; ++m)
-      for (int b = 0; b < n; ++b)
-        tiles_dn[toff[g] * mb_dn + m * n + b] = make_int4(g, m, b, min(128, c - b * 128));
+  const int total_b = toff[G];
+  // every (group, token block) pair, found by binary search over the group tile offsets
+  for (int t = threadIdx.x; t < total_b * (mb_gu > mb_dn ? mb_gu : mb_dn); t += blockDim.x) {
+    const int mb_max = mb_gu > mb_dn ? mb_gu : mb_dn;
+    const int bt = t / mb_max, m = t - bt * mb_max;
+    int lo = 0, hi = G - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (toff[mid] <= bt) lo = mid;
+      else hi = mid - 1;
+    }
+    const int gg = lo, b = bt - toff[gg], nbg = nb[gg];
+    const int4 tile = make_int4(gg, m, b, min(128, cnt[gg] - b * 128));
+    if (m < mb_gu) tiles_gu[toff[gg] * mb_gu + m * nbg + b] = tile;
+    if (m < mb_dn) tiles_dn[toff[gg] * mb_dn + m * nbg + b] = tile;
   }
 }
 

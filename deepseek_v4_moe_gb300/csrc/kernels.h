@@ -41,6 +41,7 @@ struct Scratch {
   float *row_rs;          // [rows] rsqrt(mean(ffn_input^2) + eps) (decode)
   float *router_partial;  // [4, router_chunks, experts+1]
   float *logits;          // [rows, experts]
+  float *router_part;     // [16, rows, experts] split-K partial logits (rows > 4)
   int *idx;               // [rows, top_k]
   float *rw;              // [rows, top_k]
   unsigned *safe;         // [rows, top_k]

@@ -60,8 +60,8 @@ static int check_config(const moe_ffn_config *c) {
   if (c->hc < 1 || c->hc > moe::kHcMax) return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "hc must be in 1..4");
   if (c->hidden < 128 || c->hidden % 128 || c->hidden > 8192)
     return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "hidden must be a multiple of 128 in 128..8192");
-  if (c->inter < 128 || c->inter % 128)
-    return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "inter must be a positive multiple of 128");
+  if (c->inter < 128 || c->inter % 128 || c->inter > 8192)
+    return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "inter must be a multiple of 128 in 128..8192");
   if (c->shared_inter != c->inter) return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "shared_inter must equal inter");
   if (c->experts < 16 || c->experts > moe::kExpertsMax || c->experts % 16)
     return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "experts must be a multiple of 16 in 16..512");
@@ -182,7 +182,7 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
   s.max_rows = (int)R;
   s.mix_chunks = (int)(hcd / 128);
   s.router_chunks = (int)(D / 128);
-  const size_t mix_part = std::max((size_t)4 * (hcd / 128), R * (hcd % 512 == 0 ? 4 : hcd / 128)) * (M + 1);
+  const size_t mix_part = std::max((size_t)4 * (hcd / 128), R * (size_t)moe::hc_mix_chunks((int)R, (int)hcd)) * (M + 1);
   const size_t G = moe::kDecodeRows * K + 1;
   bool ok = dalloc(h, &s.status, 1) && dalloc(h, &s.mix_partial, mix_part) && dalloc(h, &s.tickets, R / 4 + 2) &&
             dalloc(h, &s.mixes, R * M) && dalloc(h, &s.pre, R * HC) && dalloc(h, &s.post, R * HC) &&
@@ -202,6 +202,7 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
   s.max_tiles_dn = (int)((P / 128 + E + 1) * (D / 128));
   if (ok && prefill)
     ok = dalloc(h, &s.counts, E) && dalloc(h, &s.offsets, E + 2) && dalloc(h, &s.cursor, E + 1) &&
+         dalloc(h, &s.router_part, 16 * R * E) &&
          dalloc(h, &s.tiles_gu, (size_t)s.max_tiles_gu) && dalloc(h, &s.tiles_dn, (size_t)s.max_tiles_dn) &&
          dalloc(h, &s.n_tiles, 2) && dalloc(h, &s.list, P) && dalloc(h, &s.list_w, P) &&
          dalloc(h, &s.x16, P * D) && dalloc(h, &s.act16, P * I) && dalloc(h, &s.y_slot, R * (K + 1) * D);

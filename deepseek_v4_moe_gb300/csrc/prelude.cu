@@ -35,7 +35,7 @@ struct MixArgs {
 
 int hc_mix_chunks(int rows, int hcd) {
   if (rows <= kDecodeRows) return hcd / 128;
-  return hcd % 512 == 0 ? 4 : hcd / 128;
+  return hcd % 512 == 0 ? 2 : hcd / 128;
 }
 
 // pre/post of one row from the reduced sums (mixes = sums * rsqrt(mean square + eps)).
@@ -69,23 +69,42 @@ __global__ void __launch_bounds__(256) hc_mix_kernel(MixArgs a) {
 #pragma unroll
     for (int q = 0; q < 3; ++q) acc[r][q] = 0.f;
   }
-  for (int c = c0 + lane * 4; c < c0 + a.chunk; c += 128) {
-    float4 x[RB];
+  // Each lane walks its 4-column slots of the chunk; the next slot's loads are issued before the
+  // current slot's FMAs, so two global round trips are always in flight.
+  auto load_slot = [&](int c, float4 (&x)[RB], uint2 (&w)[3]) {
 #pragma unroll
     for (int r = 0; r < RB; ++r)
       x[r] = (r < nr) ? *reinterpret_cast<const float4 *>(a.state + (size_t)(r0 + r) * a.hcd + c)
                       : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      const int m = warp + 8 * q;
+      w[q] = m < M ? __ldg(reinterpret_cast<const uint2 *>(a.hc_fn + (size_t)m * a.hcd + c)) : make_uint2(0u, 0u);
+    }
+  };
+  auto fma_slot = [&](const float4 (&x)[RB], const uint2 (&w)[3]) {
+#pragma unroll
     for (int r = 0; r < RB; ++r) ss[r] += x[r].x * x[r].x + x[r].y * x[r].y + x[r].z * x[r].z + x[r].w * x[r].w;
 #pragma unroll
     for (int q = 0; q < 3; ++q) {
-      const int m = warp + 8 * q;
-      if (m < M) {
-        const uint2 wv = __ldg(reinterpret_cast<const uint2 *>(a.hc_fn + (size_t)m * a.hcd + c));
-        const float w0 = bf_lo(wv.x), w1 = bf_hi(wv.x), w2 = bf_lo(wv.y), w3 = bf_hi(wv.y);
+      const float w0 = bf_lo(w[q].x), w1 = bf_hi(w[q].x), w2 = bf_lo(w[q].y), w3 = bf_hi(w[q].y);
 #pragma unroll
-        for (int r = 0; r < RB; ++r) acc[r][q] += x[r].x * w0 + x[r].y * w1 + x[r].z * w2 + x[r].w * w3;
-      }
+      for (int r = 0; r < RB; ++r) acc[r][q] += x[r].x * w0 + x[r].y * w1 + x[r].z * w2 + x[r].w * w3;
+    }
+  };
+  {
+    const int slots = a.chunk / 128;
+    float4 xa[RB], xb[RB];
+    uint2 wa[3], wb[3];
+    int c = c0 + lane * 4;
+    load_slot(c, xa, wa);
+    for (int k = 0; k < slots; k += 2) {
+      if (k + 1 < slots) load_slot(c + 128, xb, wb);
+      fma_slot(xa, wa);
+      if (k + 1 >= slots) break;
+      if (k + 2 < slots) load_slot(c + 256, xa, wa);
+      fma_slot(xb, wb);
+      c += 256;
     }
   }
 #pragma unroll
@@ -159,8 +178,7 @@ void launch_hc_mix(const Dims &d, const Scratch &s, const LayerDev &w, const flo
   a.do_sinkhorn = rows > kDecodeRows;
   const int nch = hc_mix_chunks(rows, a.hcd);
   a.chunk = a.hcd / nch;
-  dim3 grid(nch, (rows + 3) / 4);
-  launch_pdl(hc_mix_kernel<4>, grid, dim3(256), 0, st, a);
+  launch_pdl(hc_mix_kernel<4>, dim3(nch, (rows + 3) / 4), dim3(256), 0, st, a);
   stage(tm, "hc_mix", st);
 }
 
@@ -536,14 +554,18 @@ __global__ void __launch_bounds__(256) prefill_prenorm_kernel(const float *__res
 }
 
 // logits[R, E] = X[R, D] . G[E, D]^T, X f32, G bf16; 64x64 tile, 4x4 per thread.
+// Split K: CTA (x, y, z) covers experts 64x.., rows 64y.. and the z-th K slice of kslice columns,
+// writing its partial sums to out + z * R * E (summed in a fixed order by the routing warps).
 __global__ void __launch_bounds__(256) router_gemm_kernel(const float *__restrict__ X, const uint16_t *__restrict__ G,
-                                                          int R, int E, int D, float *__restrict__ out) {
+                                                          int R, int E, int D, int kslice, float *__restrict__ out) {
   __shared__ float Xs[32][68];
   __shared__ float Gs[32][68];
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int r0 = blockIdx.y * 64, e0 = blockIdx.x * 64;
+  const int kb = blockIdx.z * kslice, ke = kb + kslice;
+  out += (size_t)blockIdx.z * R * E;
   float acc[4][4] = {};
-  for (int k0 = 0; k0 < D; k0 += 32) {
+  for (int k0 = kb; k0 < ke; k0 += 32) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int id = tid + i * 256, row = id >> 3, kq = (id & 7) * 4;
@@ -594,11 +616,20 @@ __global__ void __launch_bounds__(256) router_gemm_kernel(const float *__restric
   }
 }
 
-__global__ void __launch_bounds__(256) route_rows_kernel(const float *__restrict__ logits, int rows, RouteParams p) {
+__global__ void __launch_bounds__(256) route_rows_kernel(const float *__restrict__ part, int nsplit, float *logits,
+                                                         int rows, RouteParams p) {
   __shared__ float sv[8][kExpertsMax];
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (r >= rows) return;
-  route_row_warp(logits + (size_t)r * p.experts, r, p, sv[threadIdx.x >> 5]);
+  const int E = p.experts;
+  float *lr = logits + (size_t)r * E;
+  for (int e = threadIdx.x & 31; e < E; e += 32) {
+    float l = 0.f;
+    for (int z = 0; z < nsplit; ++z) l += part[((size_t)z * rows + r) * E + e];
+    lr[e] = l;
+  }
+  __syncwarp();
+  route_row_warp(lr, r, p, sv[threadIdx.x >> 5]);
 }
 
 void launch_prefill_router(const Dims &d, const Scratch &s, const LayerDev &w, const float *state,
@@ -606,11 +637,16 @@ void launch_prefill_router(const Dims &d, const Scratch &s, const LayerDev &w, c
   prefill_prenorm_kernel<<<rows, 256, d.hidden * sizeof(float), st>>>(state, s.pre, w.ffn_norm, d.hidden, d.hc,
                                                                        d.eps, s.ffn_input, s.ffn_norm);
   stage(tm, "prenorm", st);
-  dim3 g((d.experts + 63) / 64, (rows + 63) / 64);
-  router_gemm_kernel<<<g, 256, 0, st>>>(s.ffn_norm, w.gate, rows, d.experts, d.hidden, s.logits);
+  // enough CTAs to fill the GPU: split K into a power of two of slices (at most 16)
+  const int tiles = ((d.experts + 63) / 64) * ((rows + 63) / 64);
+  int nsplit = 1;
+  while (nsplit < 16 && tiles * nsplit < 1024 && d.hidden % (64 * nsplit * 2) == 0) nsplit *= 2;
+  dim3 g((d.experts + 63) / 64, (rows + 63) / 64, nsplit);
+  router_gemm_kernel<<<g, 256, 0, st>>>(s.ffn_norm, w.gate, rows, d.experts, d.hidden, d.hidden / nsplit,
+                                        s.router_part);
   stage(tm, "router_gemm", st);
   RouteParams p = make_route(d, s, w, token_ids, hash, s.counts);
-  route_rows_kernel<<<(rows + 7) / 8, 256, 0, st>>>(s.logits, rows, p);
+  route_rows_kernel<<<(rows + 7) / 8, 256, 0, st>>>(s.router_part, nsplit, s.logits, rows, p);
   stage(tm, "route", st);
 }
 

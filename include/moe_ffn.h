@@ -64,7 +64,7 @@ extern "C" {
 #define MOE_FFN_DEV_TIMEOUT 0x8       /* a bounded wait inside a kernel gave up (kernel returned) */
 
 /* Shapes and constants of the block (the page's cfg fields).  Supported:
- *   1 <= hc <= 4;  128 <= hidden <= 8192, hidden % 128 == 0;  inter % 128 == 0;  shared_inter == inter;
+ *   1 <= hc <= 4;  128 <= hidden <= 8192, hidden % 128 == 0;  128 <= inter <= 8192, inter % 128 == 0;  shared_inter == inter;
  *   16 <= experts <= 512, experts % 16 == 0;  1 <= top_k <= 8, top_k <= experts;
  *   hash_layer_count <= n_layers;  1 <= max_rows <= 65536;  vocab >= 1;  sinkhorn_iters >= 0. */
 typedef struct moe_ffn_config {

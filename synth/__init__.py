@@ -174,6 +174,7 @@ PROFILE_CONFIGS = {
     "p_prefill_512_e32": MoeConfig("p_prefill_512_e32", rows=512, experts=32, seed=23),
     # full router and HC shapes (256 experts, hidden 4096) with inter 128: 0.8 GB of expert weights
     "p_decode_b1_i128": MoeConfig("p_decode_b1_i128", rows=1, inter=128, shared_inter=128, seed=25),
+    "p_prefill_4096_e32": MoeConfig("p_prefill_4096_e32", rows=4096, experts=32, seed=27),
 }
 ALL_CONFIGS = {**CONFIGS, **PROFILE_CONFIGS}
 

@@ -65,3 +65,19 @@ def compare_state(got: np.ndarray, ref: np.ndarray, rel_l2: float = 1e-3, max_fr
     assert rl2 <= rel_l2, f"relative L2 {rl2:.3e} > {rel_l2}"
     assert mx <= max_frac * rms, f"max |delta| {mx:.3e} > {max_frac} * RMS {rms:.3e}"
     return rl2, mx / rms
+
+
+def compare_dot(got: np.ndarray, ref: np.ndarray, x: np.ndarray, w: np.ndarray, tau: float, what: str = ""):
+    """A tolerance for f32 dot products ref = x @ w.T, scaled by each entry's condition.
+
+    An entry's f32 error is bounded by a multiple of sum_d |x_d * w_d| (the rounding of every
+    partial sum and of x itself is relative to that magnitude, not to the result), so the bar is
+    |got - ref| <= tau * (|x| @ |w|.T).  Entries near zero after cancellation get the same absolute
+    slack as their terms deserve.  Returns the largest |delta| / bound ratio seen (<= 1 passes)."""
+    cond = np.abs(x.astype(np.float64)) @ np.abs(w.astype(np.float64)).T
+    diff = np.abs(got.astype(np.float64) - ref)
+    ratio = diff / (tau * cond + 1e-30)
+    worst = np.unravel_index(np.argmax(ratio), ratio.shape)
+    assert ratio[worst] <= 1.0, (f"{what} |delta| {diff[worst]:.3e} at {worst} > {tau:g} x condition "
+                                 f"{cond[worst]:.3e} (ratio {ratio[worst]:.2f})")
+    return float(ratio[worst])

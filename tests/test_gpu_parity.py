@@ -14,10 +14,11 @@ import torch
 import oracle
 import synth
 from synth.device import upload
-from tests.inputs import compare_state, sample_rows, substages, tie_free
+from tests.inputs import compare_dot, compare_state, sample_rows, substages, tie_free
 
 pytestmark = pytest.mark.gpu
 
+LOGIT_TAU = 1e-6
 SAMPLE = {"c0_tiny": 4, "c1_decode_b1": 1, "c2_decode_b4_hash": 4, "c3_prefill_512": 12, "c4_prefill_4096": 12}
 
 
@@ -49,8 +50,10 @@ def test_parity(name, cuda_lib):
     assert np.allclose(res["weights"].sum(axis=1), 1.0, atol=1e-5)
     for k in ("pre", "post", "comb"):
         assert np.allclose(res[k], st[k], rtol=1e-5, atol=1e-6), k
-    assert np.allclose(res["logits"], st["logits"], rtol=1e-4, atol=1e-5)
     assert np.allclose(res["ffn_norm"], st["ffn_norm"], rtol=1e-4, atol=1e-5)
+    # logits: f32 sums over hidden = 4096 products; the bar is relative to sum |x_d * g_ed| (see
+    # compare_dot), with tau = 1e-6 ~ 16 units of f32 rounding over the normalised input
+    compare_dot(res["logits"], st["logits"], st["ffn_norm"], synth.bf16_bits_to_f32(case.gate), LOGIT_TAU, "logits")
     rows = sample_rows(cfg.rows, SAMPLE[name], seed=cfg.seed)
     ref = oracle.forward_ffn_rows(case, stages=substages(st, rows))
     compare_state(res["out"][rows], ref["out_state"])

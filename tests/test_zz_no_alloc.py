@@ -64,12 +64,30 @@ def test_noalloc_split_full_shape_against_oracle(cuda_lib):
         assert np.allclose(comb, st["comb"], rtol=1e-5, atol=1e-6)
 
 
+def _call_with_sized_buffers(lib, rows, hc, hidden):
+    """Calls the split with buffers sized for (rows, hc, hidden), so that even a call the host
+    accepted would stay inside its buffers."""
+    M = (2 + hc) * hc
+    state = torch.zeros(rows * hc * hidden, device="cuda")
+    hc_fn = torch.zeros(M * hc * hidden, dtype=torch.int16, device="cuda")
+    scale = torch.ones(3, device="cuda")
+    base = torch.zeros(M, device="cuda")
+    pre = torch.empty(rows * hc, device="cuda")
+    post = torch.empty(rows * hc, device="cuda")
+    comb = torch.empty(rows * hc * hc, device="cuda")
+    rc = lib.moe_ffn_hc_split_noalloc(state.data_ptr(), hc_fn.data_ptr(), scale.data_ptr(), base.data_ptr(), rows,
+                                      hc, hidden, 20, 1e-6, pre.data_ptr(), post.data_ptr(), comb.data_ptr(),
+                                      torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    return rc
+
+
 def test_noalloc_split_rejects_rows_beyond_the_fixed_scratch(cuda_lib):
     from deepseek_v4_moe_gb300 import _lib
-    t = torch.zeros(16, device="cuda")
-    p = t.data_ptr()
-    rc = cuda_lib.moe_ffn_hc_split_noalloc(p, p, p, p, 5000, 4, 4096, 20, 1e-6, p, p, p, None)
-    assert rc == _lib.ERR_ROWS_RANGE
+    # more rows than the fixed ticket array covers
+    assert _call_with_sized_buffers(cuda_lib, 5000, 4, 4096) == _lib.ERR_ROWS_RANGE
     assert b"fixed scratch" in cuda_lib.moe_ffn_last_error(None)
-    rc = cuda_lib.moe_ffn_hc_split_noalloc(p, p, p, p, 3000, 4, 4096, 20, 1e-6, p, p, p, None)
-    assert rc == _lib.ERR_ROWS_RANGE
+    # within the row cap, but hc*hidden = 24192 is no multiple of 512, so the mix keeps 189 chunk
+    # partials per output and row: 100 rows need about 1.2 MB, above the fixed 1 MiB
+    assert _call_with_sized_buffers(cuda_lib, 100, 3, 8064) == _lib.ERR_ROWS_RANGE
+    assert b"fixed 1 MiB scratch" in cuda_lib.moe_ffn_last_error(None)
