@@ -78,6 +78,11 @@ def kernel_work(name: str, wm: dict, cfg) -> tuple[float, float]:
     """(algorithmic bytes, algorithmic flops) of one launch of a kernel of the forward."""
     R, D, I, HC, E, K = cfg.rows, cfg.hidden, cfg.inter, cfg.hc, cfg.experts, cfg.top_k
     slots = wm["slots"]
+    if name == "decode":
+        # the whole block in one launch: every touched expert once, hc_fn and the router, the state
+        # read and written, the per-group act / y round trips
+        return (wm["w_gateup"] + wm["w_down"] + wm["small"] + 2 * wm["state"] + slots * (I + D) * 4 * 2,
+                wm["flops_gateup"] + wm["flops_down"] + 2 * R * (E + cfg.mix * HC) * D)
     if name == "decode_experts":
         # every touched expert's gate/up/down once, the state read and written by the fused hc_post,
         # the per-group act / y round trips

@@ -25,6 +25,21 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Routing source and outputs of one layer (device pointers): score layers use `bias`
+// (exp_probs_b), hash layers `tid2eid` and the token ids.
+struct RouteParams {
+  int experts, top_k, vocab;
+  bool hash;
+  const float *bias;
+  const int32_t *tid2eid;
+  const int32_t *token_ids;
+  int *idx;
+  float *rw;
+  unsigned *safe;
+  int *status;
+  int *counts;  // optional per-expert histogram (rows > 4 path)
+};
+
 struct Dims {
   int hidden, hc, experts, top_k, inter, vocab, iters;
   float eps;
@@ -39,7 +54,8 @@ struct Scratch {
   float *mixes, *pre, *post, *comb;  // [rows, mix] [rows, hc] [rows, hc] [rows, hc, hc]
   float *ffn_input, *ffn_norm;       // [rows, hidden]
   float *row_rs;          // [rows] rsqrt(mean(ffn_input^2) + eps) (decode)
-  float *router_partial;  // [4, router_chunks, experts+1]
+  float *dec_part;        // decode router partials: [router CTAs, 4] sums of squares, then
+                          // [router CTAs, 4, experts] logits
   float *logits;          // [rows, experts]
   float *router_part;     // [16, rows, experts] split-K partial logits (rows > 4)
   int *idx;               // [rows, top_k]
@@ -51,7 +67,7 @@ struct Scratch {
   float *group_w;         // [groups, 4]
   float *act_dec;         // [groups, 4, inter]
   float *y_dec;           // [groups, 4, hidden]
-  unsigned *dec_counters; // [groups] gate/up rows done per group, then [hidden/64] d-block arrivals
+  unsigned *dec_counters; // the decode kernel's tickets and completion counters (zero between launches)
   int decode_ctas_by_rows[5];  // co-resident CTAs of the persistent decode kernel, per row count
   // rows > 4 path
   int *counts;            // [experts] routed slots per expert (zero between launches)
@@ -105,23 +121,24 @@ struct LayerDev {
 // prelude.cu
 void launch_hc_mix(const Dims &d, const Scratch &s, const LayerDev &w, const float *state, int rows,
                    cudaStream_t st, StageTimer *tm);
-void launch_decode_router(const Dims &d, const Scratch &s, const LayerDev &w, const float *state,
-                          const int32_t *token_ids, int rows, bool hash, cudaStream_t st, StageTimer *tm);
 void launch_prefill_router(const Dims &d, const Scratch &s, const LayerDev &w, const float *state,
                            const int32_t *token_ids, int rows, bool hash, cudaStream_t st, StageTimer *tm);
 int hc_mix_chunks(int rows, int hcd);
 void launch_hc_mix_raw(const float *state, const uint16_t *hc_fn, const float *hc_scale, const float *hc_base,
                        int rows, int hc, int hidden, int iters, float eps, float *partial, unsigned *tickets,
                        float *mixes, float *pre, float *post, float *comb, cudaStream_t st);
+RouteParams make_route(const Dims &d, const Scratch &s, const LayerDev &w, const int32_t *token_ids, bool hash,
+                       int *counts);
 // moe_ffn.cu
 void set_global_error(const char *msg);
 // decode.cu
 constexpr int kDecodeGroupsMax = 4 * 8 + 1;  // rows x top_k distinct experts + the shared one
 constexpr int kDecodeDBlock = 32;            // d-block of the decode reduce + hc_post (one d per lane)
-// counters: rows done per group | arrivals per d-block | comb ready | work tickets of phases A, B, C
-inline int decode_counter_count(const Dims &d) { return kDecodeGroupsMax + d.hidden / kDecodeDBlock + 4; }
-void launch_decode_experts(const Dims &d, const Scratch &s, const LayerDev &w, const float *state, int rows,
-                           float *out_state, int num_sms, cudaStream_t st, StageTimer *tm);
+int decode_counter_count(const Dims &d);
+int decode_mix_ctas(int hc, int hidden);     // CTAs of the decode kernel's mix role
+int decode_router_ctas(int hidden);          // CTAs of its router role
+void launch_decode(const Dims &d, const Scratch &s, const LayerDev &w, const float *state, const int32_t *token_ids,
+                   int rows, bool hash, float *out_state, cudaStream_t st, StageTimer *tm);
 cudaError_t decode_configure(int hidden);
 int decode_resident_ctas(int hidden, int rows, int num_sms);
 // dispatch.cu

@@ -188,7 +188,8 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
             dalloc(h, &s.mixes, R * M) && dalloc(h, &s.pre, R * HC) && dalloc(h, &s.post, R * HC) &&
             dalloc(h, &s.comb, R * HC * HC) && dalloc(h, &s.ffn_input, R * D) && dalloc(h, &s.ffn_norm, R * D) &&
             dalloc(h, &s.row_rs, R) &&
-            dalloc(h, &s.router_partial, 4 * (D / 128) * (E + 1)) && dalloc(h, &s.logits, R * E) &&
+            dalloc(h, &s.dec_part, (size_t)moe::decode_router_ctas((int)D) * 4 * (E + 1)) &&
+            dalloc(h, &s.logits, R * E) &&
             dalloc(h, &s.idx, R * K) && dalloc(h, &s.rw, R * K) && dalloc(h, &s.safe, R * K) &&
             dalloc(h, &s.ffn_out, R * D) && dalloc(h, &s.ngroups, 1) && dalloc(h, &s.group_e, G) &&
             dalloc(h, &s.group_mask, G) && dalloc(h, &s.group_w, G * 4) && dalloc(h, &s.act_dec, G * 4 * I) &&
@@ -233,6 +234,13 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
       free_all(h);
       delete h;
       return fail(nullptr, MOE_FFN_ERR_CUDA, "the decode kernel does not fit on an SM");
+    }
+    // its prelude roles are claimed by the first CTAs to arrive; at least one CTA must be left
+    if (s.decode_ctas_by_rows[r] <= moe::decode_mix_ctas(d.hc, d.hidden) + moe::decode_router_ctas(d.hidden)) {
+      free_all(h);
+      delete h;
+      return fail(nullptr, MOE_FFN_ERR_CUDA, "too few co-resident CTAs (%d) for the decode kernel's roles",
+                  s.decode_ctas_by_rows[r]);
     }
   }
   s.decode_ctas_by_rows[0] = 0;
@@ -310,11 +318,10 @@ extern "C" int moe_ffn_forward(moe_ffn_handle *h, const float *state, const int3
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   moe::StageTimer *tm = h->timer.on ? &h->timer : nullptr;
   if (tm) tm->begin(st);
-  moe::launch_hc_mix(h->dims, h->s, L, state, rows, st, tm);
   if (rows <= moe::kDecodeRows) {
-    moe::launch_decode_router(h->dims, h->s, L, state, token_ids, rows, hash, st, tm);
-    moe::launch_decode_experts(h->dims, h->s, L, state, rows, out_state, h->num_sms, st, tm);
+    moe::launch_decode(h->dims, h->s, L, state, token_ids, rows, hash, out_state, st, tm);
   } else {
+    moe::launch_hc_mix(h->dims, h->s, L, state, rows, st, tm);
     moe::launch_prefill_router(h->dims, h->s, L, state, token_ids, rows, hash, st, tm);
     moe::launch_dispatch(h->dims, h->s, rows, st, tm);
     moe::launch_grouped_gemms(h->dims, h->s, L, h->tm_x16, h->tm_act16, h->num_sms, st, tm);

@@ -215,18 +215,6 @@ void launch_hc_mix_raw(const float *state, const uint16_t *hc_fn, const float *h
 // (ties to the lower expert index), weights = chosen unbiased scores / their sum.  Hash layers:
 // tid2eid[token] in table order, weights = sigmoid(logit) normalised over valid slots.
 // ---------------------------------------------------------------------------------------------
-struct RouteParams {
-  int experts, top_k, vocab;
-  bool hash;
-  const float *bias;
-  const int32_t *tid2eid;
-  const int32_t *token_ids;
-  int *idx;
-  float *rw;
-  unsigned *safe;
-  int *status;
-  int *counts;  // optional per-expert histogram (rows > 4 path)
-};
 
 // Routes row r with one warp.  `logits` is the row's logits (shared or global memory), `v` a
 // shared buffer of `experts` floats for the row's selection scores.  The code stays compact (the
@@ -296,172 +284,7 @@ __device__ void route_row_warp(const float *logits, int r, const RouteParams &p,
   }
 }
 
-// ---------------------------------------------------------------------------------------------
-// Decode router (rows <= 4).  Grid: hidden/128 chunks of d.  Each CTA forms ffn_input =
-// sum_h pre[h] * state[h] on its chunk, partial sum of squares, and partial logits
-// sum_d ffn_input[d] * w[d] * gate[e, d] for every expert (the RMS scale factors out).  The last
-// CTA reduces, writes logits and ffn_norm, routes each row and groups the (row, slot) pairs by
-// expert for the expert kernels (the shared expert is the last group, weight 1).
-// ---------------------------------------------------------------------------------------------
-struct DecodeRouterArgs {
-  const float *state, *pre, *norm_w;
-  const uint16_t *gate;
-  float *ffn_input, *ffn_norm, *partial, *logits, *row_rs;
-  unsigned *ticket;
-  int *ngroups, *group_e, *group_mask;
-  float *group_w;
-  unsigned *counters;  // the expert kernel's completion counters, cleared here
-  int n_counters;
-  int rows, hidden, hc, dchunk;
-  float eps;
-  RouteParams rp;
-};
-
-constexpr int kRouterChunkMax = 256;
-
-constexpr int kRouterSplit = 4;  // CTAs per d-chunk, each over a quarter of the experts
-
-__global__ void __launch_bounds__(256) decode_router_kernel(DecodeRouterArgs a) {
-  pdl_trigger();
-  const int nch = gridDim.x, dchunk = a.dchunk;
-  const int d0 = blockIdx.x * dchunk;
-  const int E = a.rp.experts, rows = a.rows, tid = threadIdx.x;
-  const int lane = tid & 31, warp = tid >> 5;
-  __shared__ __align__(16) float xw[kDecodeRows][kRouterChunkMax];
-  __shared__ float red[8][kDecodeRows];
-  __shared__ float rs_s[kDecodeRows];
-  __shared__ int is_last;
-  pdl_wait();
-
-  float ssl[kDecodeRows];
-#pragma unroll
-  for (int r = 0; r < kDecodeRows; ++r) {
-    ssl[r] = 0.f;
-    if (r < rows && tid < dchunk) {
-      const int d = d0 + tid;
-      float v = 0.f;
-      for (int h = 0; h < a.hc; ++h) v += a.pre[r * a.hc + h] * a.state[((size_t)r * a.hc + h) * a.hidden + d];
-      if (blockIdx.y == 0) a.ffn_input[(size_t)r * a.hidden + d] = v;
-      xw[r][tid] = v * a.norm_w[d];
-      ssl[r] = v * v;
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < kDecodeRows; ++r) {
-    const float v = warp_sum(ssl[r]);
-    if (lane == 0) red[warp][r] = v;
-  }
-  __syncthreads();
-  // Partial logits over this d-chunk for this CTA's quarter of the experts.  A warp reads one
-  // expert's chunk of the router row at a time, 16 bytes per lane (coalesced), eight experts in
-  // flight; lane l owns the elements 8l .. 8l+7 of the chunk.
-  {
-    const int per = (E + kRouterSplit - 1) / kRouterSplit;
-    const int e0 = blockIdx.y * per, e1 = min(E, e0 + per);
-    const bool active = lane * 8 < dchunk;
-    float4 xa[kDecodeRows], xb[kDecodeRows];
-#pragma unroll
-    for (int r = 0; r < kDecodeRows; ++r) {
-      xa[r] = active ? *reinterpret_cast<const float4 *>(&xw[r][lane * 8]) : make_float4(0.f, 0.f, 0.f, 0.f);
-      xb[r] = active ? *reinterpret_cast<const float4 *>(&xw[r][lane * 8 + 4]) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    constexpr int B = 8;
-    for (int eb = e0 + warp; eb < e1; eb += 8 * B) {
-      uint4 wv[B];
-#pragma unroll
-      for (int q = 0; q < B; ++q) {
-        const int e = eb + 8 * q;
-        wv[q] = (e < e1 && active) ? __ldg(reinterpret_cast<const uint4 *>(a.gate + (size_t)e * a.hidden + d0 + lane * 8))
-                                   : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int q = 0; q < B; ++q) {
-        const int e = eb + 8 * q;
-#pragma unroll
-        for (int r = 0; r < kDecodeRows; ++r) {
-          if (r < rows) {
-            const float v = warp_sum(dot8(wv[q], xa[r], xb[r]));
-            if (lane == 0 && e < e1) a.partial[((size_t)r * nch + blockIdx.x) * (E + 1) + e] = v;
-          }
-        }
-      }
-    }
-  }
-  if (blockIdx.y == 0 && tid < rows) {
-    float s = 0.f;
-    for (int w = 0; w < 8; ++w) s += red[w][tid];
-    a.partial[((size_t)tid * nch + blockIdx.x) * (E + 1) + E] = s;
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) is_last = (atomicAdd(a.ticket, 1u) == (unsigned)(nch * gridDim.y - 1));
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-
-  for (int i = tid; i < a.n_counters; i += blockDim.x) a.counters[i] = 0u;
-  __shared__ float lg[kDecodeRows][kExpertsMax];
-  // Logits: one thread per (row, expert), the chunk partials read with independent loads.
-  if (tid < rows) {
-    float s = 0.f;
-    for (int ch = 0; ch < nch; ++ch) s += __ldcg(a.partial + ((size_t)tid * nch + ch) * (E + 1) + E);
-    rs_s[tid] = rsqrtf(s / (float)a.hidden + a.eps);
-  }
-  __syncthreads();
-  for (int i = tid; i < rows * E; i += blockDim.x) {
-    const int r = i / E, e = i - r * E;
-    const float *p = a.partial + (size_t)r * nch * (E + 1) + e;
-    float s = 0.f;
-#pragma unroll 16
-    for (int ch = 0; ch < nch; ++ch) s += __ldcg(p + (size_t)ch * (E + 1));
-    const float l = s * rs_s[r];
-    lg[r][e] = l;
-    a.logits[(size_t)r * E + e] = l;
-  }
-  if (tid < rows) a.row_rs[tid] = rs_s[tid];
-  __syncthreads();
-  __shared__ int s_idx[kDecodeRows][kTopKMax];
-  __shared__ float s_w[kDecodeRows][kTopKMax];
-  __shared__ int s_ge[kDecodeGroupsMax], s_gm[kDecodeGroupsMax], s_ng;
-  __shared__ float s_gw[kDecodeGroupsMax][kDecodeRows];
-  __shared__ float sv[kDecodeRows][kExpertsMax];
-  if (warp < rows) route_row_warp(lg[warp], warp, a.rp, sv[warp], s_idx[warp], s_w[warp]);
-  __syncthreads();
-  if (tid == 0) {
-    // Group 0 is the shared expert (weight 1 for every row), then the distinct routed experts.
-    const int K = a.rp.top_k;
-    s_ge[0] = E;
-    s_gm[0] = (1 << rows) - 1;
-    for (int q = 0; q < kDecodeRows; ++q) s_gw[0][q] = q < rows ? 1.f : 0.f;
-    int ng = 1;
-    for (int r = 0; r < rows; ++r)
-      for (int k = 0; k < K; ++k) {
-        const int e = s_idx[r][k];
-        if (e < 0 || e >= E) continue;
-        int g = 1;
-        while (g < ng && s_ge[g] != e) ++g;
-        if (g == ng) {
-          s_ge[g] = e;
-          s_gm[g] = 0;
-          for (int q = 0; q < kDecodeRows; ++q) s_gw[g][q] = 0.f;
-          ++ng;
-        }
-        s_gm[g] |= 1 << r;
-        s_gw[g][r] += s_w[r][k];
-      }
-    s_ng = ng;
-    *a.ngroups = ng;
-    *a.ticket = 0u;
-  }
-  __syncthreads();
-  for (int g = tid; g < s_ng; g += blockDim.x) {
-    a.group_e[g] = s_ge[g];
-    a.group_mask[g] = s_gm[g];
-    for (int q = 0; q < kDecodeRows; ++q) a.group_w[g * kDecodeRows + q] = s_gw[g][q];
-  }
-}
-
-static RouteParams make_route(const Dims &d, const Scratch &s, const LayerDev &w, const int32_t *token_ids,
+RouteParams make_route(const Dims &d, const Scratch &s, const LayerDev &w, const int32_t *token_ids,
                               bool hash, int *counts) {
   RouteParams p;
   p.experts = d.experts;
@@ -477,35 +300,6 @@ static RouteParams make_route(const Dims &d, const Scratch &s, const LayerDev &w
   p.status = s.status;
   p.counts = counts;
   return p;
-}
-
-void launch_decode_router(const Dims &d, const Scratch &s, const LayerDev &w, const float *state,
-                          const int32_t *token_ids, int rows, bool hash, cudaStream_t st, StageTimer *tm) {
-  DecodeRouterArgs a;
-  a.state = state;
-  a.pre = s.pre;
-  a.norm_w = w.ffn_norm;
-  a.gate = w.gate;
-  a.ffn_input = s.ffn_input;
-  a.ffn_norm = s.ffn_norm;
-  a.row_rs = s.row_rs;
-  a.partial = s.router_partial;
-  a.logits = s.logits;
-  a.ticket = s.tickets + (s.max_rows / 4 + 1);
-  a.ngroups = s.ngroups;
-  a.group_e = s.group_e;
-  a.group_mask = s.group_mask;
-  a.group_w = s.group_w;
-  a.counters = s.dec_counters;
-  a.n_counters = decode_counter_count(d);
-  a.rows = rows;
-  a.hidden = d.hidden;
-  a.hc = d.hc;
-  a.dchunk = d.hidden % 256 == 0 ? 256 : 128;
-  a.eps = d.eps;
-  a.rp = make_route(d, s, w, token_ids, hash, nullptr);
-  launch_pdl(decode_router_kernel, dim3(d.hidden / a.dchunk, kRouterSplit), dim3(256), 0, st, a);
-  stage(tm, "decode_router", st);
 }
 
 // ---------------------------------------------------------------------------------------------
