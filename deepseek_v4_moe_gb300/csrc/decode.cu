@@ -73,7 +73,7 @@ struct DecodeArgs {
 // counter slots.  The prelude flags share one 128-byte line; each work-ticket counter, the group
 // counters and the d-block counters get lines of their own, so that the atomics of one phase do
 // not queue behind another's at the same L2 line.
-constexpr int kCntRole = 0, kCntMixDone = 1, kCntRtDone = 3, kCntX = 4, kCntRoute = 5,
+constexpr int kCntRole = 0, kCntMixDone = 1, kCntRtDone = 3, kCntRoute = 5,
               kCntComb = 6, kCntExit = 7, kCntAbort = 8;
 constexpr int kCntTickA = 32, kCntTickB = 64, kCntTickC = 96, kCntGroups = 128;
 constexpr int kCntDBlocks = kCntGroups + 64;  // after the group counters, on a fresh line
@@ -340,6 +340,17 @@ __device__ void mix_role(const DecodeArgs &a, int j, PreludeSmem &sm, unsigned *
 // CTA works on its own chunk of hidden and only the last one needs the whole row.
 // ---------------------------------------------------------------------------------------------
 
+// RMS scale of row r from the router CTAs' partial sums of squares, by one warp (lane l: router
+// CTAs l, l + 32, ...; then a warp sum).  The router tail and every streaming CTA form it this
+// way, so all of them get the same bits.
+__device__ __forceinline__ float row_rs_from_partials(const DecodeArgs &a, int rows, int r, int nsum) {
+  const int lane = threadIdx.x & 31;
+  float x = 0.f;
+  for (int c = lane; c < nsum; c += 32) x += __ldcg(a.ss_part + c * rows + r);
+  x = warp_sum(x);
+  return rsqrtf(x / (float)a.hidden + a.eps);
+}
+
 // Routing of row r by one warp.  Score layers: top_k on the selection scores sigmoid(logit) + bias
 // (formed beforehand in sm.sc, in f32; ties to the lower expert index), weights = the chosen
 // unbiased scores / their sum.  Hash layers: the tid2eid row in table order, weights =
@@ -436,8 +447,8 @@ __device__ void group_rows(const DecodeArgs &a, PreludeSmem &sm, bool live) {
   }
 }
 
-// Tail of the router role, run by the last router CTA: the RMS scale of every row (x published),
-// the logits reduced in a fixed order, the selection scores (every thread a share), routing (one
+// Tail of the router role, run by the last router CTA: the RMS scale of every row, the logits
+// reduced in a fixed order, the selection scores (every thread a share), routing (one
 // warp per row) and grouping (published).  `live` false: the same code
 // with one partial and no global write or publication, run by idle CTAs to bring it into L2.
 template <int ROWS>
@@ -446,22 +457,15 @@ __device__ __noinline__ void router_tail(const DecodeArgs &a, PreludeSmem &sm, u
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.experts;
   const int nsum = live ? a.nr : 1;
-  // RMS scales: warp r sums row r's partials (lane l: router CTAs l, l + 32, ...)
+  // RMS scales (the streaming CTAs form the same values themselves)
   if (warp < rows) {
-    float x = 0.f;
-    for (int c = lane; c < nsum; c += 32) x += __ldcg(a.ss_part + c * rows + warp);
-    x = warp_sum(x);
-    const float rs = rsqrtf(x / (float)a.hidden + a.eps);
+    const float rs = row_rs_from_partials(a, rows, warp, nsum);
     if (lane == 0) {
       sm.rs[warp] = rs;
       if (live) a.row_rs[warp] = rs;
     }
   }
-  if (live) __threadfence();
   __syncthreads();
-  // x = xw * rs is complete (the router CTAs wrote xw before arriving): the shared expert, which
-  // needs no routing, streams from here on while the routing below completes
-  if (tid == 0 && live) publish(&cnt[kCntX], 1u);
   // logits: four quarters of the router CTAs per (row, 4 experts); each thread issues its quarter's
   // loads back to back, then the quarters are added in a fixed order
   const int E4 = E / 4, units = rows * E4, q4 = (nsum + 3) / 4;
@@ -640,11 +644,18 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
   }
   pdl_wait();  // the state (read by phase C) comes from the previous kernel
 
-  // ---- x = (ffn_input * norm weight) * rs, once the router roles have published rs ----
-  (void)cta_wait_at_least(&cnt[kCntX], 1u, a.status, &cnt[kCntAbort], &sm.flag);
+  // ---- x = (ffn_input * norm weight) * rs, once every router CTA has written its share of xw and
+  // of the sums of squares: each CTA forms rs itself, so the shared expert, which needs no
+  // routing, streams while the router tail still routes ----
+  (void)cta_wait_at_least(&cnt[kCntRtDone], (unsigned)a.nr, a.status, &cnt[kCntAbort], &sm.flag);
+  if ((tid >> 5) < rows) {
+    const float rs = row_rs_from_partials(a, rows, tid >> 5, a.nr);
+    if (lane == 0) sm.rs[tid >> 5] = rs;
+  }
+  __syncthreads();
   for (int i = tid * 4; i < rows * D; i += blockDim.x * 4) {
     const int r = i / D;
-    const float rs = __ldcg(a.row_rs + r);
+    const float rs = sm.rs[r];
     const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.xw + i));
     const float4 x = make_float4(v.x * rs, v.y * rs, v.z * rs, v.w * rs);
     *reinterpret_cast<float4 *>(&xs[i]) = x;
