@@ -57,7 +57,7 @@ struct Scratch {
   float *dec_part;        // decode router partials: [router CTAs, 4] sums of squares, then
                           // [router CTAs, 4, experts] logits
   float *logits;          // [rows, experts]
-  float *router_part;     // [16, rows, experts] split-K partial logits (rows > 4)
+  float *router_part;     // [splits, rows, experts] split-K partial logits (rows > 4)
   int *idx;               // [rows, top_k]
   float *rw;              // [rows, top_k]
   unsigned *safe;         // [rows, top_k]
@@ -80,6 +80,7 @@ struct Scratch {
   __half *x16;            // [positions, hidden] ffn_norm rows in expert-sorted order (fp16)
   __half *act16;          // [positions, inter] SwiGLU output in the same order (fp16)
   float *y_slot;          // [rows, top_k + 1, hidden] weighted expert outputs
+  float *mix_tc_part;     // [splits, rows, 32] mix partials, then [splits, rows] sums of squares
   int max_rows, mix_chunks, router_chunks, max_positions, max_tiles_gu, max_tiles_dn;
 };
 
@@ -114,7 +115,9 @@ struct LayerDev {
   const int32_t *tid2eid;
   const uint16_t *gate_exps, *up_exps, *down_exps, *gate_sh, *up_sh, *down_sh;
   __half *gate16, *up16, *down16;  // [(experts+1) * inter, hidden], [(experts+1) * hidden, inter]
-  CUtensorMap tm_gate, tm_up, tm_down;
+  __half *hcfn16;                  // [32, hc * hidden]: hc_fn in fp16, rows past the mix width zero
+  __half *router16;                // [experts rounded up to 256, hidden]: the router in fp16, padded
+  CUtensorMap tm_gate, tm_up, tm_down, tm_hcfn, tm_router;
   bool has_weights;
 };
 
@@ -145,6 +148,13 @@ int decode_resident_ctas(int hidden, int rows, int num_sms);
 void launch_dispatch(const Dims &d, const Scratch &s, int rows, cudaStream_t st, StageTimer *tm);
 void launch_prefill_post(const Dims &d, const Scratch &s, const float *state, int rows, float *out_state,
                          cudaStream_t st, StageTimer *tm);
+// splitgemm.cu
+void launch_prefill_mix(const Dims &d, const Scratch &s, const LayerDev &w, const float *state, int rows,
+                        cudaStream_t st, StageTimer *tm);
+int launch_router_tc(const Dims &d, const Scratch &s, const LayerDev &w, int rows, cudaStream_t st);
+int mix_tc_part_floats(int max_rows, int hcd);
+int splitgemm_splits(int k);  // K splits of the tensor-core mix / router GEMMs
+cudaError_t splitgemm_configure();
 // gemm_tc.cu
 void launch_grouped_gemms(const Dims &d, const Scratch &s, const LayerDev &w, const CUtensorMap &tm_x16,
                           const CUtensorMap &tm_act16, int num_sms, cudaStream_t st, StageTimer *tm);

@@ -115,13 +115,13 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D fp16 matrix [outer, inner], row-major; boxes of 128 rows x 64 columns, 128-byte swizzle.
-static bool make_tmap(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer) {
+// 2-D fp16 matrix [outer, inner], row-major; boxes of `box_rows` rows x 64 columns, 128-byte swizzle.
+static bool make_tmap(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_rows = 128) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -203,10 +203,11 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
   s.max_tiles_dn = (int)((P / 128 + E + 1) * (D / 128));
   if (ok && prefill)
     ok = dalloc(h, &s.counts, E) && dalloc(h, &s.offsets, E + 2) && dalloc(h, &s.cursor, E + 1) &&
-         dalloc(h, &s.router_part, 16 * R * E) &&
+         dalloc(h, &s.router_part, (size_t)moe::splitgemm_splits((int)D) * R * E) &&
          dalloc(h, &s.tiles_gu, (size_t)s.max_tiles_gu) && dalloc(h, &s.tiles_dn, (size_t)s.max_tiles_dn) &&
          dalloc(h, &s.n_tiles, 2) && dalloc(h, &s.list, P) && dalloc(h, &s.list_w, P) &&
-         dalloc(h, &s.x16, P * D) && dalloc(h, &s.act16, P * I) && dalloc(h, &s.y_slot, R * (K + 1) * D);
+         dalloc(h, &s.x16, P * D) && dalloc(h, &s.act16, P * I) && dalloc(h, &s.y_slot, R * (K + 1) * D) &&
+         dalloc(h, &s.mix_tc_part, (size_t)moe::mix_tc_part_floats((int)R, (int)hcd));
   if (!ok) {
     free_all(h);
     delete h;
@@ -223,7 +224,8 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
       return fail(nullptr, MOE_FFN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the activation buffers");
     }
   }
-  if (moe::gemm_configure() != cudaSuccess || moe::decode_configure(d.hidden) != cudaSuccess) {
+  if (moe::gemm_configure() != cudaSuccess || moe::decode_configure(d.hidden) != cudaSuccess ||
+      moe::splitgemm_configure() != cudaSuccess) {
     free_all(h);
     delete h;
     return fail(nullptr, MOE_FFN_ERR_CUDA, "kernel attribute setup failed");
@@ -278,8 +280,21 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
     moe::launch_bf16_to_f16(w.up_sh, L.up16 + n_exp, n_sh, 0);
     moe::launch_bf16_to_f16(w.down_exps, L.down16, n_exp, 0);
     moe::launch_bf16_to_f16(w.down_sh, L.down16 + n_exp, n_sh, 0);
+    // hc_fn and the router in fp16 for the tensor-core mix and router GEMMs, zero-padded to whole
+    // TMA boxes (32 mix rows; the experts to a multiple of 256)
+    const size_t e_pad = (E + 255) / 256 * 256;
+    if (!dalloc(h, &L.hcfn16, 32 * hcd) || !dalloc(h, &L.router16, e_pad * D)) {
+      free_all(h);
+      delete h;
+      return fail(nullptr, MOE_FFN_ERR_NO_MEMORY, "device allocation of the fp16 mix/router copies failed");
+    }
+    cudaMemset(L.hcfn16, 0, 32 * hcd * sizeof(__half));
+    cudaMemset(L.router16, 0, e_pad * D * sizeof(__half));
+    moe::launch_bf16_to_f16(w.hc_fn, L.hcfn16, M * hcd, 0);
+    moe::launch_bf16_to_f16(w.gate, L.router16, E * D, 0);
     if (!make_tmap(&L.tm_gate, L.gate16, D, (E + 1) * I) || !make_tmap(&L.tm_up, L.up16, D, (E + 1) * I) ||
-        !make_tmap(&L.tm_down, L.down16, I, (E + 1) * D)) {
+        !make_tmap(&L.tm_down, L.down16, I, (E + 1) * D) || !make_tmap(&L.tm_hcfn, L.hcfn16, hcd, 32, 32) ||
+        !make_tmap(&L.tm_router, L.router16, D, e_pad, 256)) {
       free_all(h);
       delete h;
       return fail(nullptr, MOE_FFN_ERR_CUDA, "cuTensorMapEncodeTiled failed for layer %d", l);
@@ -321,7 +336,7 @@ extern "C" int moe_ffn_forward(moe_ffn_handle *h, const float *state, const int3
   if (rows <= moe::kDecodeRows) {
     moe::launch_decode(h->dims, h->s, L, state, token_ids, rows, hash, out_state, st, tm);
   } else {
-    moe::launch_hc_mix(h->dims, h->s, L, state, rows, st, tm);
+    moe::launch_prefill_mix(h->dims, h->s, L, state, rows, st, tm);
     moe::launch_prefill_router(h->dims, h->s, L, state, token_ids, rows, hash, st, tm);
     moe::launch_dispatch(h->dims, h->s, rows, st, tm);
     moe::launch_grouped_gemms(h->dims, h->s, L, h->tm_x16, h->tm_act16, h->num_sms, st, tm);

@@ -347,69 +347,6 @@ __global__ void __launch_bounds__(256) prefill_prenorm_kernel(const float *__res
   }
 }
 
-// logits[R, E] = X[R, D] . G[E, D]^T, X f32, G bf16; 64x64 tile, 4x4 per thread.
-// Split K: CTA (x, y, z) covers experts 64x.., rows 64y.. and the z-th K slice of kslice columns,
-// writing its partial sums to out + z * R * E (summed in a fixed order by the routing warps).
-__global__ void __launch_bounds__(256) router_gemm_kernel(const float *__restrict__ X, const uint16_t *__restrict__ G,
-                                                          int R, int E, int D, int kslice, float *__restrict__ out) {
-  __shared__ float Xs[32][68];
-  __shared__ float Gs[32][68];
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  const int r0 = blockIdx.y * 64, e0 = blockIdx.x * 64;
-  const int kb = blockIdx.z * kslice, ke = kb + kslice;
-  out += (size_t)blockIdx.z * R * E;
-  float acc[4][4] = {};
-  for (int k0 = kb; k0 < ke; k0 += 32) {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int id = tid + i * 256, row = id >> 3, kq = (id & 7) * 4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (r0 + row < R) v = *reinterpret_cast<const float4 *>(X + (size_t)(r0 + row) * D + k0 + kq);
-      Xs[kq + 0][row] = v.x;
-      Xs[kq + 1][row] = v.y;
-      Xs[kq + 2][row] = v.z;
-      Xs[kq + 3][row] = v.w;
-    }
-    {
-      const int e = tid >> 2, kq = (tid & 3) * 8;
-      uint4 w = make_uint4(0u, 0u, 0u, 0u);
-      if (e0 + e < E) w = __ldg(reinterpret_cast<const uint4 *>(G + (size_t)(e0 + e) * D + k0 + kq));
-      Gs[kq + 0][e] = bf_lo(w.x);
-      Gs[kq + 1][e] = bf_hi(w.x);
-      Gs[kq + 2][e] = bf_lo(w.y);
-      Gs[kq + 3][e] = bf_hi(w.y);
-      Gs[kq + 4][e] = bf_lo(w.z);
-      Gs[kq + 5][e] = bf_hi(w.z);
-      Gs[kq + 6][e] = bf_lo(w.w);
-      Gs[kq + 7][e] = bf_hi(w.w);
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int k = 0; k < 32; ++k) {
-      float av[4], bv[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) av[i] = Xs[k][ty * 4 + i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) bv[j] = Gs[k][tx * 4 + j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = r0 + ty * 4 + i;
-    if (r >= R) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + tx * 4 + j;
-      if (e < E) out[(size_t)r * E + e] = acc[i][j];
-    }
-  }
-}
-
 __global__ void __launch_bounds__(256) route_rows_kernel(const float *__restrict__ part, int nsplit, float *logits,
                                                          int rows, RouteParams p) {
   __shared__ float sv[8][kExpertsMax];
@@ -431,13 +368,8 @@ void launch_prefill_router(const Dims &d, const Scratch &s, const LayerDev &w, c
   prefill_prenorm_kernel<<<rows, 256, d.hidden * sizeof(float), st>>>(state, s.pre, w.ffn_norm, d.hidden, d.hc,
                                                                        d.eps, s.ffn_input, s.ffn_norm);
   stage(tm, "prenorm", st);
-  // enough CTAs to fill the GPU: split K into a power of two of slices (at most 16)
-  const int tiles = ((d.experts + 63) / 64) * ((rows + 63) / 64);
-  int nsplit = 1;
-  while (nsplit < 16 && tiles * nsplit < 1024 && d.hidden % (64 * nsplit * 2) == 0) nsplit *= 2;
-  dim3 g((d.experts + 63) / 64, (rows + 63) / 64, nsplit);
-  router_gemm_kernel<<<g, 256, 0, st>>>(s.ffn_norm, w.gate, rows, d.experts, d.hidden, d.hidden / nsplit,
-                                        s.router_part);
+  // logits on the tensor cores (splitgemm.cu), split over K so that the grid fills the GPU
+  const int nsplit = launch_router_tc(d, s, w, rows, st);
   stage(tm, "router_gemm", st);
   RouteParams p = make_route(d, s, w, token_ids, hash, s.counts);
   route_rows_kernel<<<(rows + 7) / 8, 256, 0, st>>>(s.router_part, nsplit, s.logits, rows, p);
