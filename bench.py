@@ -92,8 +92,10 @@ def kernel_work(name: str, wm: dict, cfg) -> tuple[float, float]:
         return wm["w_gateup"] + slots * (D * 2 + I * 2), wm["flops_gateup"]
     if name == "gemm_down":
         return wm["w_down"] + slots * (I * 2 + D * 4), wm["flops_down"]
-    if name == "hc_mix":
+    if name in ("hc_mix", "mix_gemm"):
         return wm["state"] + cfg.mix * HC * D * 2, 2 * R * cfg.mix * HC * D
+    if name == "mix_finish":
+        return R * (cfg.mix + HC * (2 + HC)) * 4, 0.0
     if name == "decode_router":
         return R * D * 4 + E * D * 2, 2 * R * E * D
     if name == "prenorm":

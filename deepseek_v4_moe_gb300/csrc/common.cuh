@@ -131,6 +131,32 @@ __device__ inline void sinkhorn_comb_row(const float *mix, const float *scale, c
       if (i < hc && j < hc) comb[i * hc + j] = c[i][j];
 }
 
+// The same comb by a whole warp: lane 4i + j (lanes 0-15; 16-31 mirror them) holds entry (i, j).
+// Row sums pair entries as (c0 + c1) + (c2 + c3) through xor shuffles 1 and 2, column sums through
+// xor 4 and 8, and every lane takes the correctly rounded reciprocal of its own sum: the same
+// operations in the same order as sinkhorn_comb_row, so the same bits.  Lanes 0..hc*hc-1 by
+// (i, j) < hc store.  Every lane of the warp must call it.
+__device__ inline void sinkhorn_comb_warp(const float *mix, const float *scale, const float *base, int hc, int iters,
+                                          float *comb) {
+  const int lane = threadIdx.x & 31, i = (lane >> 2) & 3, j = lane & 3;
+  const bool in = i < hc && j < hc;
+  float c = in ? mix[2 * hc + i * hc + j] * scale[2] + base[2 * hc + i * hc + j] : 0.f;
+  float mx = in ? c : -INFINITY;
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  c = in ? expf(c - mx) : 0.f;
+#pragma unroll 1
+  for (int it = 0; it < iters; ++it) {
+    const float r1 = c + __shfl_xor_sync(0xffffffffu, c, 1);
+    const float rsum = r1 + __shfl_xor_sync(0xffffffffu, r1, 2);
+    c *= i < hc ? __frcp_rn(rsum) : 0.f;
+    const float c1 = c + __shfl_xor_sync(0xffffffffu, c, 4);
+    const float csum = c1 + __shfl_xor_sync(0xffffffffu, c1, 8);
+    c *= j < hc ? __frcp_rn(csum) : 0.f;
+  }
+  if (lane < 16 && in) comb[i * hc + j] = c;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -245,8 +245,9 @@ __device__ __noinline__ void mix_tail(const DecodeArgs &a, PreludeSmem &sm, unsi
       a.post[tid * hc + h] = 2.0f * hc_gate(sm.sums[tid][hc + h], rs, sm.hc_scale[1], sm.hc_base[hc + h]);
     }
     for (int m = 0; m < M; ++m) a.mixes[tid * M + m] = sm.sums[tid][m] * rs;
-    sinkhorn_comb_row(a.mixes + tid * M, sm.hc_scale, sm.hc_base, hc, a.iters, a.comb + tid * hc * hc);
   }
+  __syncthreads();
+  if (warp < rows) sinkhorn_comb_warp(a.mixes + warp * M, sm.hc_scale, sm.hc_base, hc, a.iters, a.comb + warp * hc * hc);
   __threadfence();
   __syncthreads();
   if (tid == 0) publish(&cnt[kCntComb], 1u);

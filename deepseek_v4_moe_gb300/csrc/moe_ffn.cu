@@ -336,8 +336,8 @@ extern "C" int moe_ffn_forward(moe_ffn_handle *h, const float *state, const int3
   if (rows <= moe::kDecodeRows) {
     moe::launch_decode(h->dims, h->s, L, state, token_ids, rows, hash, out_state, st, tm);
   } else {
-    moe::launch_prefill_mix(h->dims, h->s, L, state, rows, st, tm);
-    moe::launch_prefill_router(h->dims, h->s, L, state, token_ids, rows, hash, st, tm);
+    moe::launch_prefill_mix(h->dims, h->s, L, state, rows, h->num_sms, st, tm);
+    moe::launch_prefill_router(h->dims, h->s, L, state, token_ids, rows, hash, h->num_sms, st, tm);
     moe::launch_dispatch(h->dims, h->s, rows, st, tm);
     moe::launch_grouped_gemms(h->dims, h->s, L, h->tm_x16, h->tm_act16, h->num_sms, st, tm);
     moe::launch_prefill_post(h->dims, h->s, state, rows, out_state, st, tm);

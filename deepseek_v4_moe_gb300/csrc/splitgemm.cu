@@ -41,7 +41,7 @@ struct Cfg {
   static constexpr int kBBytes = BN * BK * 2;
   static constexpr int kStageBytes = 2 * kPlaneBytes + kBBytes;
   static constexpr size_t kSmem = (size_t)STAGES * kStageBytes + 1024;
-  static constexpr int kTmemCols = BN < 32 ? 32 : BN;
+  static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;  // two accumulators
 };
 }  // namespace sg
 
@@ -50,7 +50,7 @@ struct SplitGemmArgs {
   float *c_part;      // [splits, R, ldc]
   float *ss_part;     // [splits, R] or nullptr
   int *status;
-  int R, K, N, ldc, kb_per_split;
+  int R, K, N, ldc, kb_per_split, splits, n_tiles;
 };
 
 // The 16-byte chunk `c` (0..7) of row `r` of a 128 x 64 fp16 K-major tile in the 128-byte
@@ -70,18 +70,29 @@ __global__ void __launch_bounds__(sg::kThreads, 1)
   using namespace sg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES], done_bar;
+  __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES], tfull_bar[2], tempty_bar[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r0 = blockIdx.x * BM, split = blockIdx.y, n0 = blockIdx.z * BN;
-  const int kb0 = split * a.kb_per_split, nkb = a.kb_per_split;
+  // work items (row tile, K split, weight tile), this CTA's items b, b + grid, ...
+  const int m_tiles = (a.R + BM - 1) / BM, nkb = a.kb_per_split;
+  const int n_items = m_tiles * a.splits * a.n_tiles;
+  const int my_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  auto item_of = [&](int i, int &r0, int &split, int &n0) {
+    const int it = blockIdx.x + i * gridDim.x;
+    r0 = (it % m_tiles) * BM;
+    split = (it / m_tiles) % a.splits;
+    n0 = (it / (m_tiles * a.splits)) * BN;
+  };
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full_bar[s], kConvWarps + 1);  // eight converter warps + the producer's expect_tx
       mbar_init(&empty_bar[s], 1);
     }
-    mbar_init(&done_bar, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], kConvWarps);
+    }
     abort_flag = 0;
     fence_mbar_init();
     tmap_prefetch(&tmW);
@@ -94,28 +105,66 @@ __global__ void __launch_bounds__(sg::kThreads, 1)
   volatile int *abort_p = &abort_flag;
 
   if (warp < kConvWarps) {
-    // ---------------- converters ----------------
+    // ---------------- converters, and the epilogue of the previous item ----------------
     // thread t: row t / 2 of the tile, k half t % 2 (32 values = 8 float4 = 4 chunks per plane)
     const int t = threadIdx.x, row = t >> 1, half = t & 1;
-    const bool row_ok = r0 + row < a.R;
-    const float *xrow = a.X + (size_t)(r0 + row) * a.K + (size_t)kb0 * BK + half * 32;
+    const int total = my_items * nkb;  // k-blocks this CTA converts, over all of its items
+    auto x_at = [&](int g) -> const float * {
+      int r0, split, n0;
+      item_of(g / nkb, r0, split, n0);
+      if (r0 + row >= a.R) return nullptr;
+      return a.X + (size_t)(r0 + row) * a.K + (size_t)(split * nkb + g % nkb) * BK + half * 32;
+    };
+    // drains the accumulator of item i to the global partials
+    auto drain = [&](int i) -> bool {
+      int ready = 0;
+      if (lane == 0) ready = mbar_wait_bounded(&tfull_bar[i & 1], (uint32_t)(i >> 1) & 1u, abort_p, a.status, kWaitNs) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, ready, 0)) return false;
+      tc_fence_after();
+      int r0, split, n0;
+      item_of(i, r0, split, n0);
+      static_assert(BN % 32 == 0, "each epilogue warp of a lane quarter takes half the columns");
+      const int q = warp & 3, er = q * 32 + lane;
+      const int cbeg = (warp >> 2) * (BN / 2), cend = cbeg + BN / 2;
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)((i & 1) * BN);
+      float *dst = a.c_part + ((size_t)split * a.R + r0 + er) * a.ldc + n0;
+      for (int c0 = cbeg; c0 < cend; c0 += 16) {
+        float v[16];
+        tmem_ld16(tbase + c0, v);
+        if (r0 + er < a.R) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (n0 + c0 + j < a.N) dst[c0 + j] = v[j];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty_bar[i & 1]);
+      return true;
+    };
     float ss = 0.f;
     float4 cur[8], nxt[8];
+    {
+      const float *x0 = total > 0 ? x_at(0) : nullptr;
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      cur[j] = row_ok ? __ldcs(reinterpret_cast<const float4 *>(xrow) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < 8; ++j) cur[j] = x0 ? __ldcs(reinterpret_cast<const float4 *>(x0) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     int stage = 0;
     uint32_t phase = 0;
-    for (int kb = 0; kb < nkb; ++kb) {
-      if (kb + 1 < nkb) {
+    bool ok = true;
+    for (int g = 0; g < total && ok; ++g) {
+      if (g + 1 < total) {
+        const float *xn = x_at(g + 1);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          nxt[j] = row_ok ? __ldcs(reinterpret_cast<const float4 *>(xrow + (size_t)(kb + 1) * BK) + j)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
+          nxt[j] = xn ? __ldcs(reinterpret_cast<const float4 *>(xn) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_p, a.status, kWaitNs) ? 1 : 0;
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      int w_ok = 1;
+      if (lane == 0) w_ok = mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_p, a.status, kWaitNs) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+        ok = false;
+        break;
+      }
       uint8_t *hi_p = smem + (size_t)stage * C::kStageBytes;
       uint8_t *lo_p = hi_p + kPlaneBytes;
 #pragma unroll
@@ -146,71 +195,68 @@ __global__ void __launch_bounds__(sg::kThreads, 1)
         stage = 0;
         phase ^= 1u;
       }
-    }
-    if (a.ss_part) {
-      ss += __shfl_xor_sync(0xffffffffu, ss, 1);  // the two halves of the row
-      if (half == 0 && row_ok) a.ss_part[(size_t)split * a.R + r0 + row] = ss;
-    }
-    // ---------------- epilogue: warps w and w + 4 share TMEM lane quarter w % 4 ----------------
-    int ready = 0;
-    if (lane == 0) ready = mbar_wait_bounded(&done_bar, 0u, abort_p, a.status, kWaitNs) ? 1 : 0;
-    if (__shfl_sync(0xffffffffu, ready, 0)) {
-      tc_fence_after();
-      static_assert(BN % 32 == 0, "each epilogue warp of a lane quarter takes half the columns");
-      const int q = warp & 3, er = q * 32 + lane;
-      const int cbeg = (warp >> 2) * (BN / 2), cend = cbeg + BN / 2;
-      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
-      float *dst = a.c_part + ((size_t)split * a.R + r0 + er) * a.ldc + n0;
-      for (int c0 = cbeg; c0 < cend; c0 += 16) {
-        float v[16];
-        tmem_ld16(tbase + c0, v);
-        if (r0 + er < a.R) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (n0 + c0 + j < a.N) dst[c0 + j] = v[j];
+      if (g % nkb == nkb - 1) {  // the last k-block of item i: its sums of squares, then drain item i - 1
+        const int i = g / nkb;
+        if (a.ss_part) {
+          const float s2 = ss + __shfl_xor_sync(0xffffffffu, ss, 1);  // the two halves of the row
+          int r0, split, n0;
+          item_of(i, r0, split, n0);
+          if (half == 0 && r0 + row < a.R && n0 == 0) a.ss_part[(size_t)split * a.R + r0 + row] = s2;
         }
+        ss = 0.f;
+        if (i > 0 && !drain(i - 1)) ok = false;
       }
     }
+    if (ok && my_items > 0) (void)drain(my_items - 1);
   } else if (warp == kConvWarps && lane == 0) {
     // ---------------- TMA producer of the weights ----------------
     int stage = 0;
     uint32_t phase = 0;
-    for (int kb = 0; kb < nkb; ++kb) {
+    for (int g = 0; g < my_items * nkb && !*abort_p; ++g) {
+      int r0, split, n0;
+      item_of(g / nkb, r0, split, n0);
       if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_p, a.status, kWaitNs)) break;
       mbar_arrive_expect_tx(&full_bar[stage], C::kBBytes);
-      tma_load_2d(smem + (size_t)stage * C::kStageBytes + 2 * kPlaneBytes, &tmW, &full_bar[stage], (kb0 + kb) * BK, n0);
+      tma_load_2d(smem + (size_t)stage * C::kStageBytes + 2 * kPlaneBytes, &tmW, &full_bar[stage],
+                  (split * nkb + g % nkb) * BK, n0);
       if (++stage == STAGES) {
         stage = 0;
         phase ^= 1u;
       }
     }
   } else if (warp == kConvWarps + 1 && lane == 0) {
-    // ---------------- MMA issuer ----------------
+    // ---------------- MMA issuer: item i accumulates in TMEM buffer i % 2 ----------------
     const uint32_t idesc = idesc_f16_f32(BM, BN);
     int stage = 0;
     uint32_t phase = 0;
-    bool ok = true;
-    for (int kb = 0; kb < nkb; ++kb) {
-      if (!mbar_wait_bounded(&full_bar[stage], phase, abort_p, a.status, kWaitNs)) {
-        ok = false;
-        break;
-      }
+    for (int i = 0; i < my_items && !*abort_p; ++i) {
+      if (!mbar_wait_bounded(&tempty_bar[i & 1], ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_p, a.status, kWaitNs)) break;
       tc_fence_after();
-      const uint32_t shi = smem_u32(smem + (size_t)stage * C::kStageBytes);
-      const uint32_t slo = shi + kPlaneBytes, sb = shi + 2 * kPlaneBytes;
+      const uint32_t acc = tmem + (uint32_t)((i & 1) * BN);
+      bool ok = true;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!mbar_wait_bounded(&full_bar[stage], phase, abort_p, a.status, kWaitNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t shi = smem_u32(smem + (size_t)stage * C::kStageBytes);
+        const uint32_t slo = shi + kPlaneBytes, sb = shi + 2 * kPlaneBytes;
 #pragma unroll
-      for (int k = 0; k < BK / UMMA_K; ++k) {
-        const uint64_t bdesc = smem_desc_sw128(sb + k * UMMA_K * 2);
-        tc_mma_f16(tmem, smem_desc_sw128(shi + k * UMMA_K * 2), bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
-        tc_mma_f16(tmem, smem_desc_sw128(slo + k * UMMA_K * 2), bdesc, idesc, 1u);
+        for (int k = 0; k < BK / UMMA_K; ++k) {
+          const uint64_t bdesc = smem_desc_sw128(sb + k * UMMA_K * 2);
+          tc_mma_f16(acc, smem_desc_sw128(shi + k * UMMA_K * 2), bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          tc_mma_f16(acc, smem_desc_sw128(slo + k * UMMA_K * 2), bdesc, idesc, 1u);
+        }
+        tc_commit(&empty_bar[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
-      tc_commit(&empty_bar[stage]);
-      if (++stage == STAGES) {
-        stage = 0;
-        phase ^= 1u;
-      }
+      if (!ok) break;
+      tc_commit(&tfull_bar[i & 1]);
     }
-    if (ok) tc_commit(&done_bar);
   }
   tc_fence_before();
   __syncthreads();
@@ -247,12 +293,19 @@ int splitgemm_splits(int k) {
   return kb / per;
 }
 
+// One CTA per SM at most, each with the same number of work items (the last ones possibly one less).
+static int persistent_grid(int rows, int splits, int n_tiles, int num_sms) {
+  const int items = (rows + sg::BM - 1) / sg::BM * splits * n_tiles;
+  const int per = (items + num_sms - 1) / num_sms;
+  return (items + per - 1) / per;
+}
+
 int mix_tc_part_floats(int max_rows, int hcd) { return splitgemm_splits(hcd) * max_rows * (kMixBN + 1); }
 
 // Per row (one warp): the split partials summed in a fixed order (lane l takes splits l, l + 32,
 // ..., then a transpose reduction over the warp gives lane m the sum of output m), then
 // mixes = dot * rsqrt(ss / (hc*hidden) + eps), pre = sigmoid, post = 2 sigmoid, and the comb
-// (Sinkhorn) of the row.
+// (Sinkhorn, the warp-parallel form) of the row.
 __global__ void __launch_bounds__(256) mix_finish_kernel(const float *__restrict__ part, const float *__restrict__ ss_part,
                                                          int splits, int rows, int hcd, int M, int hc,
                                                          const float *__restrict__ scale, const float *__restrict__ base,
@@ -286,10 +339,10 @@ __global__ void __launch_bounds__(256) mix_finish_kernel(const float *__restrict
   const float mpost = __shfl_sync(0xffffffffu, mix, (hc + lane) & 31);
   if (lane < hc) post[(size_t)r * hc + lane] = 2.0f * sigmoidf_(mpost * scale[1] + base[hc + lane]);
   __syncwarp();
-  if (lane == 0) sinkhorn_comb_row(mixes + (size_t)r * M, scale, base, hc, iters, comb + (size_t)r * hc * hc);
+  sinkhorn_comb_warp(mixes + (size_t)r * M, scale, base, hc, iters, comb + (size_t)r * hc * hc);
 }
 
-void launch_prefill_mix(const Dims &d, const Scratch &s, const LayerDev &w, const float *state, int rows,
+void launch_prefill_mix(const Dims &d, const Scratch &s, const LayerDev &w, const float *state, int rows, int num_sms,
                         cudaStream_t st, StageTimer *tm) {
   const int hcd = d.hc * d.hidden;
   const int splits = splitgemm_splits(hcd);
@@ -303,8 +356,10 @@ void launch_prefill_mix(const Dims &d, const Scratch &s, const LayerDev &w, cons
   a.N = d.mix();
   a.ldc = kMixBN;
   a.kb_per_split = hcd / sg::BK / splits;
-  dim3 grid((rows + sg::BM - 1) / sg::BM, splits, 1);
-  splitgemm_kernel<kMixBN, kMixStages><<<grid, sg::kThreads, sg::Cfg<kMixBN, kMixStages>::kSmem, st>>>(w.tm_hcfn, a);
+  a.splits = splits;
+  a.n_tiles = 1;
+  splitgemm_kernel<kMixBN, kMixStages>
+      <<<persistent_grid(rows, splits, 1, num_sms), sg::kThreads, sg::Cfg<kMixBN, kMixStages>::kSmem, st>>>(w.tm_hcfn, a);
   stage(tm, "mix_gemm", st);
   mix_finish_kernel<<<(rows + 7) / 8, 256, 0, st>>>(s.mix_tc_part, a.ss_part, splits, rows, hcd, d.mix(), d.hc,
                                                         w.hc_scale, w.hc_base, d.iters, d.eps, s.mixes, s.pre, s.post,
@@ -314,7 +369,7 @@ void launch_prefill_mix(const Dims &d, const Scratch &s, const LayerDev &w, cons
 
 // Router logits of the rows > 4 path: partials [splits, rows, experts] for route_rows_kernel, which
 // sums them in a fixed order.  Returns the number of splits.
-int launch_router_tc(const Dims &d, const Scratch &s, const LayerDev &w, int rows, cudaStream_t st) {
+int launch_router_tc(const Dims &d, const Scratch &s, const LayerDev &w, int rows, int num_sms, cudaStream_t st) {
   const int n_tiles = (d.experts + kRouterBN - 1) / kRouterBN;
   const int splits = splitgemm_splits(d.hidden);  // at most 16 for hidden <= 8192
   SplitGemmArgs a;
@@ -327,9 +382,11 @@ int launch_router_tc(const Dims &d, const Scratch &s, const LayerDev &w, int row
   a.N = d.experts;
   a.ldc = d.experts;
   a.kb_per_split = d.hidden / sg::BK / splits;
-  dim3 grid((rows + sg::BM - 1) / sg::BM, splits, n_tiles);
+  a.splits = splits;
+  a.n_tiles = n_tiles;
   splitgemm_kernel<kRouterBN, kRouterStages>
-      <<<grid, sg::kThreads, sg::Cfg<kRouterBN, kRouterStages>::kSmem, st>>>(w.tm_router, a);
+      <<<persistent_grid(rows, splits, n_tiles, num_sms), sg::kThreads, sg::Cfg<kRouterBN, kRouterStages>::kSmem, st>>>(
+          w.tm_router, a);
   return splits;
 }
 
