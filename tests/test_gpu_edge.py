@@ -29,7 +29,7 @@ def _run(case, max_rows=None, layer=None):
     return m, dev, res
 
 
-@pytest.mark.parametrize("rows", [1, 3, 5, 17, 129, 300])
+@pytest.mark.parametrize("rows", [1, 2, 3, 5, 17, 129, 300])
 def test_ragged_rows_score(rows, cuda_lib):
     case, st = tie_free(replace(TINY, rows=rows, name=f"tiny{rows}"))
     m, dev, res = _run(case)
@@ -100,6 +100,27 @@ def test_repeat_calls_are_identical_and_counters_reset(cuda_lib):
     ref = oracle.forward_ffn_rows(case, stages=st)
     compare_state(outs[0], ref["out_state"])
     compare_state(small, ref["out_state"][:3])
+    m.close()
+
+
+def test_decode_row_counts_interleaved(cuda_lib):
+    # One handle, decode calls of 4, 1, 2, 3, 4 and 2 rows in turn: each row count runs its own
+    # instance of the persistent decode kernel, and every launch must leave its tickets and counters
+    # at zero for the next one (the last CTA out resets them).
+    case, st = tie_free(replace(TINY, rows=4, name="dec_interleave"))
+    from deepseek_v4_moe_gb300 import MoeFFN, config_from
+    dev = upload(case)
+    m = MoeFFN(config_from(case.cfg), {case.cfg.layer: dev["weights"]})
+    ref = oracle.forward_ffn_rows(case, stages=st)["out_state"]
+    seen = {}
+    for r in (4, 1, 2, 3, 4, 2):
+        out = m.forward(dev["state"][:r].contiguous(), dev["token_ids"][:r].contiguous(), case.cfg.layer)
+        got = out.cpu().numpy()
+        assert m.status() == 0
+        compare_state(got, ref[:r])
+        if r in seen:
+            assert np.array_equal(got, seen[r])  # same inputs, same bits
+        seen[r] = got
     m.close()
 
 
