@@ -83,7 +83,7 @@ constexpr uint64_t kSpinLimitNs = 1000000000ull;
 constexpr int kRouterChunk = 64;  // hidden columns per router CTA
 constexpr int kMixCols = 512;     // flattened-state columns per mix CTA (a multiple of 128)
 constexpr int kWarmCtas = 16;     // streaming-only CTAs that pre-run the prelude tails' code
-constexpr int kRowsPerTicketA = 2;  // gate/up rows per ticket
+constexpr int kRowsPerTicketA = 1;  // gate/up rows per ticket
 constexpr int kRowsPerTicketB = 4;  // down rows per ticket (a 32-row d-block holds 8 tickets)
 
 // Shared memory of the prelude roles (static; the streaming phases use the dynamic x buffer).
@@ -671,7 +671,7 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
   // ---- phase A: gate/up rows, tickets in group-major order (the shared expert first) ----
   // Every row's 2 x hidden bf16 are in flight at once (UA loads per lane per matrix).  Group 0
   // (the shared expert) needs no routing; the first ticket past it waits for the routing.
-  constexpr int UA = 8;
+  constexpr int UA = ROWS >= 3 ? 4 : 8;  // loads in flight per lane and matrix (fewer for 3-4 rows, whose FMAs are longer)
   const int perg = I / kRowsPerTicketA;
   int ng = -1;
   // the group table, once routed, in registers: lane l holds groups l and l + 32 (group 0, the
@@ -760,7 +760,7 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
 
   // ---- phase B: down rows, tickets in group-major order; a ticket's rows share one group and one
   // d-block.  A group's rows wait (bounded) until all of its gate/up rows are published.
-  constexpr int UB = 8;
+  constexpr int UB = ROWS >= 3 ? 4 : 8;
   const int nB = ng * D / kRowsPerTicketB;
   int cur = -1;
   bool ready = false;
