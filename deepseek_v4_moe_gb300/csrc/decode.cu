@@ -669,9 +669,10 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
   const int all_rows = (1 << rows) - 1;
 
   // ---- phase A: gate/up rows, tickets in group-major order (the shared expert first) ----
-  // Every row's 2 x hidden bf16 are in flight at once (UA loads per lane per matrix).  Group 0
-  // (the shared expert) needs no routing; the first ticket past it waits for the routing.
-  constexpr int UA = ROWS >= 3 ? 4 : 8;  // loads in flight per lane and matrix (fewer for 3-4 rows, whose FMAs are longer)
+  // A row's gate and up elements stream in batches of UA 16-byte loads per lane and matrix, all
+  // of a batch in flight at once (fewer for 3-4 rows, whose FMAs take longer).  Group 0 (the
+  // shared expert) needs no routing; the first ticket past it waits for the routing.
+  constexpr int UA = ROWS >= 3 ? 4 : 8;
   const int perg = I / kRowsPerTicketA;
   int ng = -1;
   // the group table, once routed, in registers: lane l holds groups l and l + 32 (group 0, the
