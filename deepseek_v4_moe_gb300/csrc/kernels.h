@@ -125,8 +125,8 @@ struct LayerDev {
 void launch_hc_mix(const Dims &d, const Scratch &s, const LayerDev &w, const float *state, int rows,
                    cudaStream_t st, StageTimer *tm);
 void launch_prefill_router(const Dims &d, const Scratch &s, const LayerDev &w, const float *state,
-                           const int32_t *token_ids, int rows, bool hash, int num_sms, cudaStream_t st,
-                           StageTimer *tm);
+                           const int32_t *token_ids, const CUtensorMap &tm_ffn_norm, int rows, bool hash, int num_sms,
+                           cudaStream_t st, StageTimer *tm);
 int hc_mix_chunks(int rows, int hcd);
 void launch_hc_mix_raw(const float *state, const uint16_t *hc_fn, const float *hc_scale, const float *hc_base,
                        int rows, int hc, int hidden, int iters, float eps, float *partial, unsigned *tickets,
@@ -150,9 +150,10 @@ void launch_dispatch(const Dims &d, const Scratch &s, int rows, cudaStream_t st,
 void launch_prefill_post(const Dims &d, const Scratch &s, const float *state, int rows, float *out_state,
                          cudaStream_t st, StageTimer *tm);
 // splitgemm.cu
-void launch_prefill_mix(const Dims &d, const Scratch &s, const LayerDev &w, const float *state, int rows, int num_sms,
-                        cudaStream_t st, StageTimer *tm);
-int launch_router_tc(const Dims &d, const Scratch &s, const LayerDev &w, int rows, int num_sms, cudaStream_t st);
+void launch_prefill_mix(const Dims &d, const Scratch &s, const LayerDev &w, const float *state,
+                        const CUtensorMap &tm_state, int rows, int num_sms, cudaStream_t st, StageTimer *tm);
+int launch_router_tc(const Dims &d, const Scratch &s, const LayerDev &w, const CUtensorMap &tm_x, int rows, int num_sms,
+                     cudaStream_t st);
 int mix_tc_part_floats(int max_rows, int hcd);
 int splitgemm_splits(int k);  // K splits of the tensor-core mix / router GEMMs
 cudaError_t splitgemm_configure();

@@ -25,7 +25,7 @@ struct moe_ffn_handle {
   int device = 0, num_sms = 0;
   std::vector<LayerDev> layers;
   Scratch s;
-  CUtensorMap tm_x16, tm_act16;
+  CUtensorMap tm_x16, tm_act16, tm_ffn_norm;
   float *host_in = nullptr, *host_out = nullptr;  // device staging of moe_ffn_forward_host
   int32_t *host_tok = nullptr;
   std::vector<void *> allocs;
@@ -113,6 +113,20 @@ static EncodeTiledFn encode_fn() {
       fn = reinterpret_cast<EncodeTiledFn>(p);
   }
   return fn;
+}
+
+// 2-D f32 matrix [outer, inner], row-major; boxes of 128 rows x 64 columns, unswizzled (the
+// tensor-core mix/router GEMMs convert them in shared memory); rows past `outer` read as zeros.
+static bool make_tmap_f32(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 4};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 2-D fp16 matrix [outer, inner], row-major; boxes of `box_rows` rows x 64 columns, 128-byte swizzle.
@@ -218,7 +232,8 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
   cudaMemset(s.tickets, 0, (R / 4 + 2) * sizeof(unsigned));
   if (prefill) {
     cudaMemset(s.counts, 0, E * sizeof(int));
-    if (!make_tmap(&h->tm_x16, s.x16, D, P) || !make_tmap(&h->tm_act16, s.act16, I, P)) {
+    if (!make_tmap(&h->tm_x16, s.x16, D, P) || !make_tmap(&h->tm_act16, s.act16, I, P) ||
+        !make_tmap_f32(&h->tm_ffn_norm, s.ffn_norm, D, R)) {
       free_all(h);
       delete h;
       return fail(nullptr, MOE_FFN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the activation buffers");
@@ -336,8 +351,12 @@ extern "C" int moe_ffn_forward(moe_ffn_handle *h, const float *state, const int3
   if (rows <= moe::kDecodeRows) {
     moe::launch_decode(h->dims, h->s, L, state, token_ids, rows, hash, out_state, st, tm);
   } else {
-    moe::launch_prefill_mix(h->dims, h->s, L, state, rows, h->num_sms, st, tm);
-    moe::launch_prefill_router(h->dims, h->s, L, state, token_ids, rows, hash, h->num_sms, st, tm);
+    // the state changes with every call: its tensor map is encoded here (host only, no GPU work)
+    CUtensorMap tm_state;
+    if (!make_tmap_f32(&tm_state, state, (uint64_t)c.hc * c.hidden, (uint64_t)rows))
+      return fail(h, MOE_FFN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the state");
+    moe::launch_prefill_mix(h->dims, h->s, L, state, tm_state, rows, h->num_sms, st, tm);
+    moe::launch_prefill_router(h->dims, h->s, L, state, token_ids, h->tm_ffn_norm, rows, hash, h->num_sms, st, tm);
     moe::launch_dispatch(h->dims, h->s, rows, st, tm);
     moe::launch_grouped_gemms(h->dims, h->s, L, h->tm_x16, h->tm_act16, h->num_sms, st, tm);
     moe::launch_prefill_post(h->dims, h->s, state, rows, out_state, st, tm);

@@ -364,13 +364,13 @@ __global__ void __launch_bounds__(256) route_rows_kernel(const float *__restrict
 }
 
 void launch_prefill_router(const Dims &d, const Scratch &s, const LayerDev &w, const float *state,
-                           const int32_t *token_ids, int rows, bool hash, int num_sms, cudaStream_t st,
-                           StageTimer *tm) {
+                           const int32_t *token_ids, const CUtensorMap &tm_ffn_norm, int rows, bool hash, int num_sms,
+                           cudaStream_t st, StageTimer *tm) {
   prefill_prenorm_kernel<<<rows, 256, d.hidden * sizeof(float), st>>>(state, s.pre, w.ffn_norm, d.hidden, d.hc,
                                                                        d.eps, s.ffn_input, s.ffn_norm);
   stage(tm, "prenorm", st);
   // logits on the tensor cores (splitgemm.cu), split over K so that the grid fills the GPU
-  const int nsplit = launch_router_tc(d, s, w, rows, num_sms, st);
+  const int nsplit = launch_router_tc(d, s, w, tm_ffn_norm, rows, num_sms, st);
   stage(tm, "router_gemm", st);
   RouteParams p = make_route(d, s, w, token_ids, hash, s.counts);
   route_rows_kernel<<<(rows + 7) / 8, 256, 0, st>>>(s.router_part, nsplit, s.logits, rows, p);

@@ -6,7 +6,8 @@
 //
 // Both are f32 GEMMs whose results decide integers later (the top-k) or feed a Sinkhorn, so they
 // must be about as exact as f32 arithmetic.  Each activation is split x = hi + lo into two fp16
-// values (hi = rn(x), lo = rn(x - hi), so |x - hi - lo| <= 2^-22 |x|), the weights are fp16
+// values (hi = rn(x), lo = rn(x - hi), so |x - hi - lo| <= 2^-22 |x| where fp16 is normal; inputs
+// must stay below fp16's largest value, 65504), the weights are fp16
 // copies of the bf16 ones (exact above 2^-14), fp16 x fp16 products are exact in the f32
 // accumulator, and two MMAs per k-step (hi and lo) give f32-level dot products at tensor-core
 // rate.
@@ -14,15 +15,17 @@
 //   C_part[s, r, n] = sum over k in split s of X[r, k] * W[n, k]
 //   ss_part[s, r]   = sum over k in split s of X[r, k]^2           (when asked for)
 //
-// Layout: A = the 128 activation rows of the tile (M = 128), converted in shared memory by eight
-// warps into two 128 x 64 fp16 planes per k-stage in the 128-byte-swizzled K-major layout the MMA
-// reads; B = BN weight rows (N = BN), loaded by TMA.  Roles (320 threads, one CTA per SM):
-//   warps 0-7  converters: f32 loads (next stage in flight while this one converts), split,
-//              swizzled shared stores, sums of squares; then the epilogue (TMEM -> global)
-//   warp 8     TMEM allocator and TMA producer of B (one thread)
-//   warp 9     MMA issuer (one thread)
-// Every mbarrier wait is bounded (2 s); on expiry the device timeout bit is raised, every role
-// leaves its loop and TMEM is freed before the kernel returns.
+// Layout: A = the 128 activation rows of a tile (M = 128), converted in shared memory into two
+// 128 x 64 fp16 planes per k-stage in the 128-byte-swizzled K-major layout the MMA reads; B = BN
+// weight rows (N = BN), loaded by TMA.  Persistent: one CTA per SM walks (row tile, K split,
+// weight tile) items.  Roles:
+//   next warp  TMEM allocator and activation producer: one 128 x 64 f32 TMA box per k-stage into
+//              a ring of f32 slots (the bytes in flight cost no registers)
+//   converters (kConvWarps): f32 from shared memory, split, swizzled stores, sums of squares; then
+//              the epilogue of the previous item (TMEM -> global), so that it overlaps the next
+//              item's MMAs (two TMEM accumulators)
+//   next warp  MMA issuer (one thread)
+//   last warp  weight producer (one thread, TMA)
 #include <cuda.h>
 
 #include "common.cuh"
@@ -33,15 +36,23 @@ namespace moe {
 namespace sg {
 constexpr int BM = 128, BK = 64, UMMA_K = 16;
 constexpr int kPlaneBytes = BM * BK * 2;  // one 128 x 64 fp16 plane: 16 KB
-constexpr int kConvWarps = 8, kThreads = 32 * (kConvWarps + 2);
+constexpr int kXBytes = BM * BK * 4;      // one 128 x 64 f32 activation tile: 32 KB
+constexpr int kConvWarps = 8, kThreads = 32 * (kConvWarps + 3);
+constexpr int kConvSteps = BM / kConvWarps / 2;  // two tile rows per converter-warp step
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-template <int BN, int STAGES>
+// XS slots of staged f32 activations (bulk copies, so the bytes in flight cost no registers) and
+// CS slots of converted fp16 planes with their weight tile
+template <int BN, int XS, int CS>
 struct Cfg {
   static constexpr int kBBytes = BN * BK * 2;
-  static constexpr int kStageBytes = 2 * kPlaneBytes + kBBytes;
-  static constexpr size_t kSmem = (size_t)STAGES * kStageBytes + 1024;
+  static constexpr int kCBytes = 2 * kPlaneBytes + kBBytes;
+  static constexpr size_t kSmem = (size_t)XS * kXBytes + (size_t)CS * kCBytes + 1024;
   static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;  // two accumulators
+  // converter warps draining an accumulator: groups of four (one per TMEM lane quarter), each
+  // group a share of the columns in whole 16-column loads
+  static constexpr int kDrainGroups = kConvWarps / 4 < BN / 16 ? kConvWarps / 4 : BN / 16;
+  static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
 };
 }  // namespace sg
 
@@ -59,18 +70,36 @@ __device__ __forceinline__ uint32_t sw128_chunk(int r, int c) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-__device__ __forceinline__ uint32_t pack_half2(__half a, __half b) {
-  return (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
+// x rounded to fp16's 11-bit significand (round to nearest even on the 13 dropped bits), still in
+// f32: integer operations only, so that the conversion pipe (a quarter of the ALU rate) is spent
+// on the two packed conversions below alone.  Equal to fp16(x) wherever fp16 is normal; below
+// 2^-14 the fp16 conversion rounds once more, by at most 2^-25 in absolute terms.
+__device__ __forceinline__ float round_to_f16_precision(float x) {
+  uint32_t u = __float_as_uint(x);
+  u += 0x00000FFFu + ((u >> 13) & 1u);
+  return __uint_as_float(u & 0xFFFFE000u);
 }
 
-template <int BN, int STAGES>
+// Four activations as fp16 pairs: hi = rn(x) and lo = rn(x - hi), two packed conversions each.
+__device__ __forceinline__ void split4(const float4 v, uint2 &hi, uint2 &lo) {
+  const float hx = round_to_f16_precision(v.x), hy = round_to_f16_precision(v.y);
+  const float hz = round_to_f16_precision(v.z), hw = round_to_f16_precision(v.w);
+  const __half2 h01 = __floats2half2_rn(hx, hy), h23 = __floats2half2_rn(hz, hw);
+  const __half2 l01 = __floats2half2_rn(v.x - hx, v.y - hy), l23 = __floats2half2_rn(v.z - hz, v.w - hw);
+  hi = make_uint2(*reinterpret_cast<const uint32_t *>(&h01), *reinterpret_cast<const uint32_t *>(&h23));
+  lo = make_uint2(*reinterpret_cast<const uint32_t *>(&l01), *reinterpret_cast<const uint32_t *>(&l23));
+}
+
+template <int BN, int XS, int CS>
 __global__ void __launch_bounds__(sg::kThreads, 1)
-    splitgemm_kernel(const __grid_constant__ CUtensorMap tmW, SplitGemmArgs a) {
-  using C = sg::Cfg<BN, STAGES>;
+    splitgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                     SplitGemmArgs a) {
+  using C = sg::Cfg<BN, XS, CS>;
   using namespace sg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES], tfull_bar[2], tempty_bar[2];
+  uint8_t *xring = smem, *cring = smem + (size_t)XS * kXBytes;
+  __shared__ __align__(8) uint64_t xfull[XS], xempty[XS], cfull[CS], cempty[CS], tfull[2], tempty[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -78,6 +107,7 @@ __global__ void __launch_bounds__(sg::kThreads, 1)
   const int m_tiles = (a.R + BM - 1) / BM, nkb = a.kb_per_split;
   const int n_items = m_tiles * a.splits * a.n_tiles;
   const int my_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const int total = my_items * nkb;  // k-blocks of this CTA over all of its items
   auto item_of = [&](int i, int &r0, int &split, int &n0) {
     const int it = blockIdx.x + i * gridDim.x;
     r0 = (it % m_tiles) * BM;
@@ -85,17 +115,22 @@ __global__ void __launch_bounds__(sg::kThreads, 1)
     n0 = (it / (m_tiles * a.splits)) * BN;
   };
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full_bar[s], kConvWarps + 1);  // eight converter warps + the producer's expect_tx
-      mbar_init(&empty_bar[s], 1);
+    for (int s = 0; s < XS; ++s) {
+      mbar_init(&xfull[s], 1);            // the producer's expect_tx
+      mbar_init(&xempty[s], kConvWarps);  // every converter warp has read the slot
+    }
+    for (int s = 0; s < CS; ++s) {
+      mbar_init(&cfull[s], kConvWarps + 1);  // the converter warps + the weight producer's expect_tx
+      mbar_init(&cempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&tfull_bar[b], 1);
-      mbar_init(&tempty_bar[b], kConvWarps);
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4 * C::kDrainGroups);
     }
     abort_flag = 0;
     fence_mbar_init();
     tmap_prefetch(&tmW);
+    tmap_prefetch(&tmX);
   }
   if (warp == kConvWarps) tmem_alloc(&tmem_base, C::kTmemCols);
   tc_fence_before();
@@ -103,29 +138,27 @@ __global__ void __launch_bounds__(sg::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base;
   volatile int *abort_p = &abort_flag;
+  // warp-wide bounded wait: lane 0 waits, the warp follows its verdict
+  auto warp_wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+    int ok = 0;
+    if (lane == 0) ok = mbar_wait_bounded(bar, parity, abort_p, a.status, kWaitNs) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  };
 
   if (warp < kConvWarps) {
     // ---------------- converters, and the epilogue of the previous item ----------------
-    // thread t: row t / 2 of the tile, k half t % 2 (32 values = 8 float4 = 4 chunks per plane)
-    const int t = threadIdx.x, row = t >> 1, half = t & 1;
-    const int total = my_items * nkb;  // k-blocks this CTA converts, over all of its items
-    auto x_at = [&](int g) -> const float * {
-      int r0, split, n0;
-      item_of(g / nkb, r0, split, n0);
-      if (r0 + row >= a.R) return nullptr;
-      return a.X + (size_t)(r0 + row) * a.K + (size_t)(split * nkb + g % nkb) * BK + half * 32;
-    };
-    // drains the accumulator of item i to the global partials
+    // Warp w converts 2 kConvSteps rows of each tile, two rows per step: lane l takes float4
+    // l % 16 of row 2 kConvSteps w + 2j + l / 16 (a conflict-free 512-byte read) and writes its
+    // 4 fp16 of each plane as 8 bytes of the row's swizzled 128-byte line.
     auto drain = [&](int i) -> bool {
-      int ready = 0;
-      if (lane == 0) ready = mbar_wait_bounded(&tfull_bar[i & 1], (uint32_t)(i >> 1) & 1u, abort_p, a.status, kWaitNs) ? 1 : 0;
-      if (!__shfl_sync(0xffffffffu, ready, 0)) return false;
+      if ((warp >> 2) >= C::kDrainGroups) return true;  // not a draining warp
+      if (!warp_wait(&tfull[i & 1], (uint32_t)(i >> 1) & 1u)) return false;
       tc_fence_after();
       int r0, split, n0;
       item_of(i, r0, split, n0);
-      static_assert(BN % 32 == 0, "each epilogue warp of a lane quarter takes half the columns");
+      static_assert(BN % (16 * C::kDrainGroups) == 0, "whole 16-column loads per drain group");
       const int q = warp & 3, er = q * 32 + lane;
-      const int cbeg = (warp >> 2) * (BN / 2), cend = cbeg + BN / 2;
+      const int cbeg = (warp >> 2) * (BN / C::kDrainGroups), cend = cbeg + BN / C::kDrainGroups;
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)((i & 1) * BN);
       float *dst = a.c_part + ((size_t)split * a.R + r0 + er) * a.ldc + n0;
       for (int c0 = cbeg; c0 < cend; c0 += 16) {
@@ -139,108 +172,92 @@ __global__ void __launch_bounds__(sg::kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty_bar[i & 1]);
+      if (lane == 0) mbar_arrive(&tempty[i & 1]);
       return true;
     };
-    float ss = 0.f;
-    float4 cur[8], nxt[8];
-    {
-      const float *x0 = total > 0 ? x_at(0) : nullptr;
+    const int f4 = lane & 15, sub = lane >> 4;
+    float ss[kConvSteps];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) cur[j] = x0 ? __ldcs(reinterpret_cast<const float4 *>(x0) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    int stage = 0;
-    uint32_t phase = 0;
+    for (int j = 0; j < kConvSteps; ++j) ss[j] = 0.f;
     bool ok = true;
     for (int g = 0; g < total && ok; ++g) {
-      if (g + 1 < total) {
-        const float *xn = x_at(g + 1);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          nxt[j] = xn ? __ldcs(reinterpret_cast<const float4 *>(xn) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      int w_ok = 1;
-      if (lane == 0) w_ok = mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_p, a.status, kWaitNs) ? 1 : 0;
-      if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+      const int xs = g % XS, cs = g % CS;
+      const int i = g / nkb;
+      int r0, split, n0;
+      item_of(i, r0, split, n0);
+      if (!warp_wait(&xfull[xs], (uint32_t)(g / XS) & 1u) || !warp_wait(&cempty[cs], ((uint32_t)(g / CS) & 1u) ^ 1u)) {
         ok = false;
         break;
       }
-      uint8_t *hi_p = smem + (size_t)stage * C::kStageBytes;
+      const uint8_t *xp = xring + (size_t)xs * kXBytes;
+      uint8_t *hi_p = cring + (size_t)cs * C::kCBytes;
       uint8_t *lo_p = hi_p + kPlaneBytes;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {  // chunk c of this half: float4 2c and 2c + 1
-        uint32_t h[4], l[4];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const float4 v = cur[2 * c + q];
-          ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-          const __half hx = __float2half_rn(v.x), hy = __float2half_rn(v.y), hz = __float2half_rn(v.z),
-                       hw = __float2half_rn(v.w);
-          h[2 * q] = pack_half2(hx, hy);
-          h[2 * q + 1] = pack_half2(hz, hw);
-          l[2 * q] = pack_half2(__float2half_rn(v.x - __half2float(hx)), __float2half_rn(v.y - __half2float(hy)));
-          l[2 * q + 1] = pack_half2(__float2half_rn(v.z - __half2float(hz)), __float2half_rn(v.w - __half2float(hw)));
-        }
-        const uint32_t off = sw128_chunk(row, half * 4 + c);
-        *reinterpret_cast<uint4 *>(hi_p + off) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4 *>(lo_p + off) = make_uint4(l[0], l[1], l[2], l[3]);
+      for (int j = 0; j < kConvSteps; ++j) {
+        const int row = warp * 2 * kConvSteps + 2 * j + sub;
+        float4 v = *reinterpret_cast<const float4 *>(xp + row * 256 + f4 * 16);
+        if (r0 + row >= a.R) v = make_float4(0.f, 0.f, 0.f, 0.f);  // past this call's rows
+        ss[j] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        uint2 hi, lo;
+        split4(v, hi, lo);
+        const uint32_t off = sw128_chunk(row, f4 >> 1) + (uint32_t)((f4 & 1) * 8);
+        *reinterpret_cast<uint2 *>(hi_p + off) = hi;
+        *reinterpret_cast<uint2 *>(lo_p + off) = lo;
       }
       // the generic-proxy stores must be visible to the tensor core's async proxy
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(&full_bar[stage]);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
-      if (++stage == STAGES) {
-        stage = 0;
-        phase ^= 1u;
+      if (lane == 0) {
+        mbar_arrive(&cfull[cs]);
+        mbar_arrive(&xempty[xs]);
       }
       if (g % nkb == nkb - 1) {  // the last k-block of item i: its sums of squares, then drain item i - 1
-        const int i = g / nkb;
         if (a.ss_part) {
-          const float s2 = ss + __shfl_xor_sync(0xffffffffu, ss, 1);  // the two halves of the row
-          int r0, split, n0;
-          item_of(i, r0, split, n0);
-          if (half == 0 && r0 + row < a.R && n0 == 0) a.ss_part[(size_t)split * a.R + r0 + row] = s2;
+#pragma unroll
+          for (int j = 0; j < kConvSteps; ++j) {
+            float t = ss[j];
+            t += __shfl_xor_sync(0xffffffffu, t, 1);
+            t += __shfl_xor_sync(0xffffffffu, t, 2);
+            t += __shfl_xor_sync(0xffffffffu, t, 4);
+            t += __shfl_xor_sync(0xffffffffu, t, 8);
+            const int row = warp * 2 * kConvSteps + 2 * j + sub;
+            if (f4 == 0 && r0 + row < a.R && n0 == 0) a.ss_part[(size_t)split * a.R + r0 + row] = t;
+          }
         }
-        ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < kConvSteps; ++j) ss[j] = 0.f;
         if (i > 0 && !drain(i - 1)) ok = false;
       }
     }
     if (ok && my_items > 0) (void)drain(my_items - 1);
   } else if (warp == kConvWarps && lane == 0) {
-    // ---------------- TMA producer of the weights ----------------
-    int stage = 0;
-    uint32_t phase = 0;
-    for (int g = 0; g < my_items * nkb && !*abort_p; ++g) {
+    // ---------------- activation producer: one 128 x 64 f32 TMA box per k-stage ----------------
+    // (rows past the end of X arrive as zeros)
+    for (int g = 0; g < total && !*abort_p; ++g) {
+      const int xs = g % XS;
       int r0, split, n0;
       item_of(g / nkb, r0, split, n0);
-      if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_p, a.status, kWaitNs)) break;
-      mbar_arrive_expect_tx(&full_bar[stage], C::kBBytes);
-      tma_load_2d(smem + (size_t)stage * C::kStageBytes + 2 * kPlaneBytes, &tmW, &full_bar[stage],
-                  (split * nkb + g % nkb) * BK, n0);
-      if (++stage == STAGES) {
-        stage = 0;
-        phase ^= 1u;
-      }
+      if (!mbar_wait_bounded(&xempty[xs], ((uint32_t)(g / XS) & 1u) ^ 1u, abort_p, a.status, kWaitNs)) break;
+      mbar_arrive_expect_tx(&xfull[xs], kXBytes);
+      tma_load_2d(xring + (size_t)xs * kXBytes, &tmX, &xfull[xs], (split * nkb + g % nkb) * BK, r0);
     }
   } else if (warp == kConvWarps + 1 && lane == 0) {
     // ---------------- MMA issuer: item i accumulates in TMEM buffer i % 2 ----------------
     const uint32_t idesc = idesc_f16_f32(BM, BN);
-    int stage = 0;
-    uint32_t phase = 0;
+    int g = 0;
     for (int i = 0; i < my_items && !*abort_p; ++i) {
-      if (!mbar_wait_bounded(&tempty_bar[i & 1], ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_p, a.status, kWaitNs)) break;
+      if (!mbar_wait_bounded(&tempty[i & 1], ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_p, a.status, kWaitNs)) break;
       tc_fence_after();
       const uint32_t acc = tmem + (uint32_t)((i & 1) * BN);
       bool ok = true;
-      for (int kb = 0; kb < nkb; ++kb) {
-        if (!mbar_wait_bounded(&full_bar[stage], phase, abort_p, a.status, kWaitNs)) {
+      for (int kb = 0; kb < nkb; ++kb, ++g) {
+        const int cs = g % CS;
+        if (!mbar_wait_bounded(&cfull[cs], (uint32_t)(g / CS) & 1u, abort_p, a.status, kWaitNs)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t shi = smem_u32(smem + (size_t)stage * C::kStageBytes);
+        const uint32_t shi = smem_u32(cring + (size_t)cs * C::kCBytes);
         const uint32_t slo = shi + kPlaneBytes, sb = shi + 2 * kPlaneBytes;
 #pragma unroll
         for (int k = 0; k < BK / UMMA_K; ++k) {
@@ -248,14 +265,20 @@ __global__ void __launch_bounds__(sg::kThreads, 1)
           tc_mma_f16(acc, smem_desc_sw128(shi + k * UMMA_K * 2), bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
           tc_mma_f16(acc, smem_desc_sw128(slo + k * UMMA_K * 2), bdesc, idesc, 1u);
         }
-        tc_commit(&empty_bar[stage]);
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        tc_commit(&cempty[cs]);
       }
       if (!ok) break;
-      tc_commit(&tfull_bar[i & 1]);
+      tc_commit(&tfull[i & 1]);
+    }
+  } else if (warp == kConvWarps + 2 && lane == 0) {
+    // ---------------- weight producer ----------------
+    for (int g = 0; g < total && !*abort_p; ++g) {
+      const int cs = g % CS;
+      int r0, split, n0;
+      item_of(g / nkb, r0, split, n0);
+      if (!mbar_wait_bounded(&cempty[cs], ((uint32_t)(g / CS) & 1u) ^ 1u, abort_p, a.status, kWaitNs)) break;
+      mbar_arrive_expect_tx(&cfull[cs], C::kBBytes);
+      tma_load_2d(cring + (size_t)cs * C::kCBytes + 2 * kPlaneBytes, &tmW, &cfull[cs], (split * nkb + g % nkb) * BK, n0);
     }
   }
   tc_fence_before();
@@ -270,15 +293,15 @@ __global__ void __launch_bounds__(sg::kThreads, 1)
 // Host side and the mix finish
 // ---------------------------------------------------------------------------------------------
 
-constexpr int kMixBN = 32, kMixStages = 5;       // mix: up to 24 outputs, a light B tile
-constexpr int kRouterBN = 256, kRouterStages = 3;
+constexpr int kMixBN = 32, kMixXS = 3, kMixCS = 3;           // mix: up to 24 outputs, a light B tile
+constexpr int kRouterBN = 256, kRouterXS = 3, kRouterCS = 2;
 
 cudaError_t splitgemm_configure() {
-  cudaError_t e = cudaFuncSetAttribute(splitgemm_kernel<kMixBN, kMixStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)sg::Cfg<kMixBN, kMixStages>::kSmem);
+  cudaError_t e = cudaFuncSetAttribute(splitgemm_kernel<kMixBN, kMixXS, kMixCS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)sg::Cfg<kMixBN, kMixXS, kMixCS>::kSmem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(splitgemm_kernel<kRouterBN, kRouterStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)sg::Cfg<kRouterBN, kRouterStages>::kSmem);
+  return cudaFuncSetAttribute(splitgemm_kernel<kRouterBN, kRouterXS, kRouterCS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sg::Cfg<kRouterBN, kRouterXS, kRouterCS>::kSmem);
 }
 
 // Splits of K.  The tensor cores' f32 accumulation does not round every addition to nearest, so
@@ -342,8 +365,8 @@ __global__ void __launch_bounds__(256) mix_finish_kernel(const float *__restrict
   sinkhorn_comb_warp(mixes + (size_t)r * M, scale, base, hc, iters, comb + (size_t)r * hc * hc);
 }
 
-void launch_prefill_mix(const Dims &d, const Scratch &s, const LayerDev &w, const float *state, int rows, int num_sms,
-                        cudaStream_t st, StageTimer *tm) {
+void launch_prefill_mix(const Dims &d, const Scratch &s, const LayerDev &w, const float *state,
+                        const CUtensorMap &tm_state, int rows, int num_sms, cudaStream_t st, StageTimer *tm) {
   const int hcd = d.hc * d.hidden;
   const int splits = splitgemm_splits(hcd);
   SplitGemmArgs a;
@@ -358,8 +381,8 @@ void launch_prefill_mix(const Dims &d, const Scratch &s, const LayerDev &w, cons
   a.kb_per_split = hcd / sg::BK / splits;
   a.splits = splits;
   a.n_tiles = 1;
-  splitgemm_kernel<kMixBN, kMixStages>
-      <<<persistent_grid(rows, splits, 1, num_sms), sg::kThreads, sg::Cfg<kMixBN, kMixStages>::kSmem, st>>>(w.tm_hcfn, a);
+  splitgemm_kernel<kMixBN, kMixXS, kMixCS>
+      <<<persistent_grid(rows, splits, 1, num_sms), sg::kThreads, sg::Cfg<kMixBN, kMixXS, kMixCS>::kSmem, st>>>(w.tm_hcfn, tm_state, a);
   stage(tm, "mix_gemm", st);
   mix_finish_kernel<<<(rows + 7) / 8, 256, 0, st>>>(s.mix_tc_part, a.ss_part, splits, rows, hcd, d.mix(), d.hc,
                                                         w.hc_scale, w.hc_base, d.iters, d.eps, s.mixes, s.pre, s.post,
@@ -369,7 +392,8 @@ void launch_prefill_mix(const Dims &d, const Scratch &s, const LayerDev &w, cons
 
 // Router logits of the rows > 4 path: partials [splits, rows, experts] for route_rows_kernel, which
 // sums them in a fixed order.  Returns the number of splits.
-int launch_router_tc(const Dims &d, const Scratch &s, const LayerDev &w, int rows, int num_sms, cudaStream_t st) {
+int launch_router_tc(const Dims &d, const Scratch &s, const LayerDev &w, const CUtensorMap &tm_x, int rows, int num_sms,
+                     cudaStream_t st) {
   const int n_tiles = (d.experts + kRouterBN - 1) / kRouterBN;
   const int splits = splitgemm_splits(d.hidden);  // at most 16 for hidden <= 8192
   SplitGemmArgs a;
@@ -384,9 +408,9 @@ int launch_router_tc(const Dims &d, const Scratch &s, const LayerDev &w, int row
   a.kb_per_split = d.hidden / sg::BK / splits;
   a.splits = splits;
   a.n_tiles = n_tiles;
-  splitgemm_kernel<kRouterBN, kRouterStages>
-      <<<persistent_grid(rows, splits, n_tiles, num_sms), sg::kThreads, sg::Cfg<kRouterBN, kRouterStages>::kSmem, st>>>(
-          w.tm_router, a);
+  splitgemm_kernel<kRouterBN, kRouterXS, kRouterCS>
+      <<<persistent_grid(rows, splits, n_tiles, num_sms), sg::kThreads, sg::Cfg<kRouterBN, kRouterXS, kRouterCS>::kSmem, st>>>(
+          w.tm_router, tm_x, a);
   return splits;
 }
 
