@@ -14,11 +14,13 @@
 // are exact in fp16 above 2^-14; activations get an 11-bit significand), accumulation is f32 in
 // TMEM.
 //
-// Roles per CTA (192 threads, one CTA per SM, persistent over a device-built tile list):
+// Roles per CTA (320 threads, one CTA per SM, persistent over a device-built tile list):
 //   warp 0     TMA producer: A (gate and up, or down) and B tiles into a multi-stage smem ring
 //   warp 1     TMEM allocator and MMA issuer (one thread), commits free smem stages / TMEM
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator (double buffered in TMEM, so the next
-//              tile's MMAs run under this tile's epilogue), SwiGLU or route-weight scaling
+//   warps 2-9  epilogue: tcgen05.ld of the accumulator (double buffered in TMEM, so the next
+//              tile's MMAs run under this tile's epilogue), SwiGLU or route-weight scaling; two
+//              warps per TMEM lane quarter, each every other 16-column chunk, so that the
+//              epilogue keeps up with the MMAs
 // Every mbarrier wait is bounded (2 s); on expiry the CTA raises the device timeout bit, all roles
 // leave their loops, and TMEM is freed before the kernel returns.
 #include <cuda.h>
@@ -54,8 +56,10 @@ struct GemmArgs {
   int inter, hidden, top_k, k_blocks, a_rows_per_group, which;
 };
 
+constexpr int kEpiWarps = 8, kGemmThreads = 32 * (2 + kEpiWarps);
+
 template <bool GATEUP>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                         const __grid_constant__ CUtensorMap tmB, GemmArgs a) {
   using C = GemmCfg<GATEUP>;
@@ -73,7 +77,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull_bar[b], 1);
-      mbar_init(&tempty_bar[b], 4);
+      mbar_init(&tempty_bar[b], kEpiWarps);
     }
     abort_flag = 0;
     fence_mbar_init();
@@ -152,6 +156,7 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp >= 2) {
     // ---------------- epilogue ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;  // which 16-column chunks of the quarter's rows
     const int row = q * 32 + lane;
     const int K1 = a.top_k + 1;
     int it = 0;
@@ -169,7 +174,7 @@ __global__ void __launch_bounds__(192, 1)
       const int pos0 = a.offsets[tl.x] + tl.z * BN;
       const int n_valid = tl.w;
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
-      for (int c0 = 0; c0 < n_valid; c0 += 16) {
+      for (int c0 = half * 16; c0 < n_valid; c0 += 32) {
         if (GATEUP) {
           float gv[16], uv[16];
           tmem_ld16(tbase + c0, gv);
@@ -237,14 +242,14 @@ void launch_grouped_gemms(const Dims &d, const Scratch &s, const LayerDev &w, co
   a.a_rows_per_group = d.inter;
   a.which = 0;
   const int grid_gu = num_sms < s.max_tiles_gu ? num_sms : s.max_tiles_gu;
-  grouped_gemm_kernel<true><<<grid_gu, 192, GemmCfg<true>::kSmem, st>>>(w.tm_gate, w.tm_up, tm_x16, a);
+  grouped_gemm_kernel<true><<<grid_gu, kGemmThreads, GemmCfg<true>::kSmem, st>>>(w.tm_gate, w.tm_up, tm_x16, a);
   stage(tm, "gemm_gateup", st);
   a.tiles = s.tiles_dn;
   a.k_blocks = d.inter / BK;
   a.a_rows_per_group = d.hidden;
   a.which = 1;
   const int grid_dn = num_sms < s.max_tiles_dn ? num_sms : s.max_tiles_dn;
-  grouped_gemm_kernel<false><<<grid_dn, 192, GemmCfg<false>::kSmem, st>>>(w.tm_down, w.tm_down, tm_act16, a);
+  grouped_gemm_kernel<false><<<grid_dn, kGemmThreads, GemmCfg<false>::kSmem, st>>>(w.tm_down, w.tm_down, tm_act16, a);
   stage(tm, "gemm_down", st);
 }
 
