@@ -99,7 +99,7 @@ def kernel_work(name: str, wm: dict, cfg) -> tuple[float, float]:
     if name == "decode_router":
         return R * D * 4 + E * D * 2, 2 * R * E * D
     if name == "prenorm":
-        return wm["state"] + 2 * R * D * 4, 0.0
+        return wm["state"] + R * D * 4, 0.0
     if name == "router_gemm":
         return R * D * 4 + E * D * 2 + R * E * 4, 2 * R * E * D
     if name == "post":

@@ -309,8 +309,7 @@ RouteParams make_route(const Dims &d, const Scratch &s, const LayerDev &w, const
 __global__ void __launch_bounds__(256) prefill_prenorm_kernel(const float *__restrict__ state,
                                                               const float *__restrict__ pre,
                                                               const float *__restrict__ norm_w, int hidden, int hc,
-                                                              float eps, float *__restrict__ ffn_input,
-                                                              float *__restrict__ ffn_norm) {
+                                                              float eps, float *__restrict__ ffn_norm) {
   extern __shared__ __align__(16) float xin[];
   __shared__ float red[8];
   const int r = blockIdx.x, tid = threadIdx.x;
@@ -330,7 +329,6 @@ __global__ void __launch_bounds__(256) prefill_prenorm_kernel(const float *__res
       v.w += p[h] * x.w;
     }
     *reinterpret_cast<float4 *>(&xin[dd]) = v;
-    *reinterpret_cast<float4 *>(ffn_input + (size_t)r * hidden + dd) = v;
     ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
   }
   ss = warp_sum(ss);
@@ -367,7 +365,7 @@ void launch_prefill_router(const Dims &d, const Scratch &s, const LayerDev &w, c
                            const int32_t *token_ids, const CUtensorMap &tm_ffn_norm, int rows, bool hash, int num_sms,
                            cudaStream_t st, StageTimer *tm) {
   prefill_prenorm_kernel<<<rows, 256, d.hidden * sizeof(float), st>>>(state, s.pre, w.ffn_norm, d.hidden, d.hc,
-                                                                       d.eps, s.ffn_input, s.ffn_norm);
+                                                                       d.eps, s.ffn_norm);
   stage(tm, "prenorm", st);
   // logits on the tensor cores (splitgemm.cu), split over K so that the grid fills the GPU
   const int nsplit = launch_router_tc(d, s, w, tm_ffn_norm, rows, num_sms, st);
