@@ -83,21 +83,14 @@ def kernel_work(name: str, wm: dict, cfg) -> tuple[float, float]:
         # read and written, the per-group act / y round trips
         return (wm["w_gateup"] + wm["w_down"] + wm["small"] + 2 * wm["state"] + slots * (I + D) * 4 * 2,
                 wm["flops_gateup"] + wm["flops_down"] + 2 * R * (E + cfg.mix * HC) * D)
-    if name == "decode_experts":
-        # every touched expert's gate/up/down once, the state read and written by the fused hc_post,
-        # the per-group act / y round trips
-        return (wm["w_gateup"] + wm["w_down"] + 2 * wm["state"] + slots * (I + D) * 4 * 2,
-                wm["flops_gateup"] + wm["flops_down"])
     if name == "gemm_gateup":
         return wm["w_gateup"] + slots * (D * 2 + I * 2), wm["flops_gateup"]
     if name == "gemm_down":
         return wm["w_down"] + slots * (I * 2 + D * 4), wm["flops_down"]
-    if name in ("hc_mix", "mix_gemm"):
+    if name == "mix_gemm":
         return wm["state"] + cfg.mix * HC * D * 2, 2 * R * cfg.mix * HC * D
     if name == "mix_finish":
         return R * (cfg.mix + HC * (2 + HC)) * 4, 0.0
-    if name == "decode_router":
-        return R * D * 4 + E * D * 2, 2 * R * E * D
     if name == "prenorm":
         return wm["state"] + R * D * 4, 0.0
     if name == "router_gemm":
@@ -105,7 +98,7 @@ def kernel_work(name: str, wm: dict, cfg) -> tuple[float, float]:
     if name == "post":
         return 2 * wm["state"] + slots * D * 4, 0.0
     if name == "scatter":
-        return slots * D * (4 + 2), 0.0
+        return R * D * 4 + slots * D * 2, 0.0  # each normalised row read once, written as fp16 per slot
     return R * K * 4, 0.0
 
 
@@ -114,7 +107,7 @@ def kernel_work(name: str, wm: dict, cfg) -> tuple[float, float]:
 # every touched expert once, so a capture on the 32-expert profiling workload with the same
 # routing width (6 routed + shared) carries the same bytes as the full workload.  A kernel change
 # removes its entry until it is captured again.
-NCU_TRAFFIC = {("decode", 1, 7): 356_791_808}
+NCU_TRAFFIC = {}
 
 
 def roofline_entry(name: str, avg_ms: float, wm: dict, cfg, peaks: dict, peak_kind: str) -> dict:

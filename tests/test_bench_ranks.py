@@ -71,6 +71,6 @@ def test_work_model_counts_groups_and_slots():
     assert wm["slots"] == valid.size + cfg.rows
     one = 3 * cfg.inter * cfg.hidden * 2
     assert wm["w_gateup"] + wm["w_down"] == wm["groups"] * one
-    # the binding roofline of a decode expert kernel is HBM; a big prefill GEMM's may be the tensor pipe
-    rl = bench.roofline_entry("decode_experts", 0.1, wm, cfg, bench.FALLBACK_PEAKS, "fallback")
+    # the binding roofline of the decode kernel is HBM; a big prefill GEMM's may be the tensor pipe
+    rl = bench.roofline_entry("decode", 0.1, wm, cfg, bench.FALLBACK_PEAKS, "fallback")
     assert rl["bound"] == "hbm" and rl["unit"] == "GB/s" and rl["alg"] > wm["w_gateup"] + wm["w_down"]
