@@ -186,6 +186,28 @@ def hc_post(f: np.ndarray, state: np.ndarray, post: np.ndarray, comb: np.ndarray
     return post[:, :, None] * f[:, None, :] + np.einsum("rij,rjd->rid", comb, state)
 
 
+# ---- the hyper-connection prelude of any sublayer -------------------------------------------------
+
+def hc_sublayer_pre(state: np.ndarray, hc_fn: np.ndarray, hc_scale: np.ndarray, hc_base: np.ndarray,
+                    norm_w: np.ndarray, hc: int, iters: int, eps: float, dtype=F64):
+    """The HC prelude a sublayer runs on the state before its body, for the attention sublayer
+    (docs.rs "hf2q 0.1.3 src/inference/models/deepseek4/attention_forward.rs": rms_norm_no_scale_f32,
+    raw_matmul "HC attention function", dispatch_hc_split_sinkhorn, dispatch_hc_pre, then rms_norm
+    with attn_norm) and the same five stages of the FFN sublayer (ffn_forward.rs, with the HC FFN
+    function and ffn_norm).  state [rows, hc, hidden]; hc_fn bf16 bits [(2+hc)*hc, hc*hidden].
+    Returns the pre, post and comb of the sublayer, its input x = hc_pre(state, pre) and the
+    normalised input x_norm its body consumes.  The sublayer's output f is folded back by
+    ``hc_post`` (the attention page's last stage, dispatch_hc_post on the output projection)."""
+    state = state.astype(dtype)
+    rows = state.shape[0]
+    flat = state.reshape(rows, -1)
+    mixes = hc_mixes(rms_norm_no_scale(flat, eps), bf16_to_float(hc_fn, dtype))
+    pre, post, comb = hc_split_sinkhorn(mixes, hc_scale.astype(dtype), hc_base.astype(dtype), hc, iters)
+    x = hc_pre(state, pre)
+    x_norm = rms_norm(x, norm_w.astype(dtype), eps)
+    return dict(mixes=mixes, pre=pre, post=post, comb=comb, x=x, x_norm=x_norm)
+
+
 # ---- whole block --------------------------------------------------------------------------------
 
 def prelude_and_route(case, dtype=F64, rows=None):

@@ -32,6 +32,7 @@ _lib = None
 T_STATE, T_HC_FN, T_HC_BASE, T_FFN_NORM, T_GATE, T_BIAS, T_TID2EID = 1, 2, 3, 4, 5, 6, 7
 T_GATE_EXPS, T_UP_EXPS, T_DOWN_EXPS, T_GATE_SH, T_UP_SH, T_DOWN_SH = 8, 9, 10, 11, 12, 13
 T_TOKENS, T_HOT, T_ZIPF_PERM = 14, 15, 16
+T_HC_ATTN_FN, T_HC_ATTN_BASE, T_ATTN_NORM, T_ATTN_OUT = 17, 18, 19, 20
 
 ZIPF_BIAS_FILE = os.path.join(os.path.dirname(_HERE), "tests", "golden", "zipf_exp_probs_b_seed3.txt")
 
@@ -238,6 +239,21 @@ class Case:
         tensor = {"gate": T_GATE_EXPS, "up": T_UP_EXPS, "down": T_DOWN_EXPS}[which]
         n = c.inter * c.hidden
         return normal_bf16(c.seed, tensor, n * n_experts, c.weight_sigma, start=e0 * n, out=out)
+
+    def attn_hc(self) -> dict:
+        """The attention sublayer's hyper-connection weights, drawn like the FFN's: hc_attn_fn bf16
+        [(2+hc)*hc, hc*hidden] N(0, weight_sigma), hc_attn_base f32 N(0, 0.1), hc_attn_scale ones,
+        attn_norm f32 1 + N(0, 0.05); and attn_out f32 [rows, hidden] N(0, 1), a stand-in for the
+        attention body's output that hc_post folds back into the state."""
+        if getattr(self, "_attn", None) is None:
+            c, s = self.cfg, self.cfg.seed
+            self._attn = dict(
+                hc_fn=normal_bf16(s, T_HC_ATTN_FN, c.mix * c.hc * c.hidden, c.weight_sigma).reshape(c.mix, c.hc * c.hidden),
+                hc_base=normal_f32(s, T_HC_ATTN_BASE, c.mix, 0.0, 0.1),
+                hc_scale=np.ones(3, np.float32),
+                norm=normal_f32(s, T_ATTN_NORM, c.hidden, 1.0, 0.05),
+                attn_out=normal_f32(s, T_ATTN_OUT, c.rows * c.hidden).reshape(c.rows, c.hidden))
+        return self._attn
 
     def with_attempts(self, attempts: np.ndarray) -> "Case":
         return Case(self.cfg, attempts)

@@ -285,3 +285,68 @@ def test_row_subset_equals_full(rows):
     full = oracle.forward_ffn_rows(case)
     part = oracle.forward_ffn_rows(case, rows=rows)
     assert np.allclose(full["out_state"][rows], part["out_state"], rtol=1e-14, atol=1e-15)
+
+
+# ---- HC prelude of a sublayer (attention_forward.rs and ffn_forward.rs, the same five stages) ----
+
+def _bf16_bits(x):
+    # exact for values representable in bf16 (0, +-1, powers of two)
+    return (np.asarray(x, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def test_hc_sublayer_pre_hand_worked_hc1():
+    # hc = 1, hidden = 2, state [3, 4] (mean square 12.5), eps 0; the mix rows pick the two state
+    # columns for pre and post and give comb zero: pre = s(3/sqrt(12.5)), post = 2 s(4/sqrt(12.5)),
+    # comb = [[1]], x = pre * [3, 4], x_norm = [3, 4] / sqrt(12.5) * w
+    state = np.array([[[3.0, 4.0]]])
+    fn = _bf16_bits([[1.0, 0.0], [0.0, 1.0], [0.0, 0.0]])
+    w = np.array([2.0, -0.5])
+    got = O.hc_sublayer_pre(state, fn, np.ones(3), np.zeros(3), w, hc=1, iters=20, eps=0.0)
+    a, b = 3 / math.sqrt(12.5), 4 / math.sqrt(12.5)
+    pre = 1 / (1 + math.exp(-a))
+    assert abs(got["pre"][0, 0] - pre) < 1e-15
+    assert abs(got["post"][0, 0] - 2 / (1 + math.exp(-b))) < 1e-15
+    assert got["comb"].shape == (1, 1, 1) and got["comb"][0, 0, 0] == 1.0
+    assert np.allclose(got["x"], [[3 * pre, 4 * pre]], rtol=1e-15)
+    assert np.allclose(got["x_norm"], [[a * 2.0, b * -0.5]], rtol=1e-14)
+
+
+def test_hc_sublayer_pre_equal_streams_closed_form():
+    # every stream equal to s: x = P s with P = sum_h pre_h, so x_norm = P s / sqrt(P^2 ms + eps) * w
+    hc, hidden, eps = 4, 64, 1e-3
+    s = RNG.standard_normal((3, hidden))
+    state = np.repeat(s[:, None, :], hc, axis=1)
+    fn = _bf16_bits(np.where(RNG.random(((2 + hc) * hc, hc * hidden)) < 0.5, 0.0, 0.0625))
+    base = RNG.standard_normal((2 + hc) * hc) * 0.1
+    w = 1 + 0.05 * RNG.standard_normal(hidden)
+    got = O.hc_sublayer_pre(state, fn, np.ones(3), base, w, hc=hc, iters=20, eps=eps)
+    P = got["pre"].sum(axis=1, keepdims=True)
+    ms = (s * s).mean(axis=1, keepdims=True)
+    assert np.allclose(got["x_norm"], P * s / np.sqrt(P * P * ms + eps) * w, rtol=1e-13)
+    # and the mixes are the dots of the flat row scaled by its RMS over hc*hidden (= RMS of s)
+    m_ref = np.array([[sum(s[r, d] * O.bf16_to_float(fn)[m, h * hidden + d] for h in range(hc) for d in range(hidden))
+                       for m in range((2 + hc) * hc)] for r in range(3)]) / np.sqrt(ms + eps)
+    assert np.allclose(got["mixes"], m_ref, rtol=1e-12)
+
+
+def test_hc_sublayer_pre_zero_weights_give_half_sum():
+    case = synth.Case(synth.CONFIGS["c0_tiny"])
+    a = case.attn_hc()
+    st = case.state.astype(np.float64)
+    got = O.hc_sublayer_pre(st, np.zeros_like(a["hc_fn"]), a["hc_scale"], np.zeros_like(a["hc_base"]), a["norm"],
+                            hc=4, iters=20, eps=1e-6)
+    assert np.all(got["pre"] == 0.5) and np.all(got["post"] == 1.0)
+    assert np.allclose(got["comb"], 0.25, atol=1e-15)
+    assert np.allclose(got["x"], 0.5 * st.sum(axis=1), rtol=1e-15)
+
+
+def test_hc_sublayer_pre_with_ffn_weights_is_the_ffn_prelude():
+    # the FFN sublayer runs the same stages: with its weights the sublayer prelude gives the
+    # block's own pre, post, comb, ffn_input and ffn_norm
+    case = synth.Case(synth.CONFIGS["c0_tiny"])
+    c = case.cfg
+    st = oracle.prelude_and_route(case)
+    got = O.hc_sublayer_pre(case.state, case.hc_fn, case.hc_scale, case.hc_base, case.ffn_norm, c.hc,
+                            c.sinkhorn_iters, c.rms_eps)
+    for k, ref in (("pre", "pre"), ("post", "post"), ("comb", "comb"), ("x", "ffn_input"), ("x_norm", "ffn_norm")):
+        assert np.array_equal(got[k], st[ref]), k
