@@ -313,6 +313,131 @@ def run_ours(cfg, steps: int, warmup: int, device, rank: int, world: int, dist, 
     return res
 
 
+# ---- the hyper-connection prelude and post of a sublayer (attention), timed on their own ----------
+
+HC_SUBLAYER_WORKLOADS = ["c1_decode_b1", "c4_prefill_4096"]
+
+
+def hc_sublayer_bytes(cfg) -> tuple[int, int]:
+    """Algorithmic bytes of hc_pre (state once, hc_fn, norm weight, x_norm and pre/post/comb out)
+    and of hc_post (f and state in, the new state out, post/comb in)."""
+    R, D, HC, M = cfg.rows, cfg.hidden, cfg.hc, cfg.mix
+    small = R * (2 * HC + HC * HC) * 4
+    pre = R * HC * D * 4 + M * HC * D * 2 + D * 4 + R * D * 4 + small
+    post = R * D * 4 + 2 * R * HC * D * 4 + R * (HC + HC * HC) * 4
+    return pre, post
+
+
+def run_hc_sublayer(cfg, steps: int, warmup: int, device, peaks) -> dict:
+    """The attention sublayer's HC prelude (moe_ffn_hc_pre) and post (moe_ffn_hc_post) on the
+    workload's state, L2 flushed before each, timed with CUDA events on their stream."""
+    import torch
+
+    from deepseek_v4_moe_gb300 import MoeFFN, config_from
+
+    case = synth.Case(cfg)
+    a = case.attn_hc()
+    w = {k: torch.from_numpy(a[k].view(np.int16) if a[k].dtype == np.uint16 else a[k]).to(device)
+         for k in ("hc_fn", "hc_base", "hc_scale", "norm")}
+    m = MoeFFN(config_from(cfg), {})
+    m.set_attn_hc(cfg.layer, w)
+    state = torch.from_numpy(case.state).to(device)
+    f = torch.from_numpy(a["attn_out"]).to(device)
+    out = torch.empty_like(state)
+    stream = torch.cuda.Stream(device)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 3) + steps):
+            flush.fill_(float(i))
+            timed = i >= max(warmup, 3)
+            e = ev[i - max(warmup, 3)] if timed else None
+            if timed:
+                e[0].record(stream)
+            p = m.hc_pre(state, cfg.layer, "attn", stream=stream)
+            if timed:
+                e[1].record(stream)
+                # the post reads f and the state again: flush between, so it meets them in HBM
+                flush.fill_(0.5)
+                e[2].record(stream)
+            m.hc_post(f, state, p["post"], p["comb"], out=out, stream=stream)
+            if timed:
+                e[3].record(stream)
+    torch.cuda.synchronize(device)
+    assert m.status() == 0
+    pre_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    post_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+    m.close()
+    b_pre, b_post = hc_sublayer_bytes(cfg)
+    peak = peaks["hbm_gbs"]
+    res = {}
+    for name, ms, b in (("hc_pre", pre_ms, b_pre), ("hc_post", post_ms, b_post)):
+        gbs = b / (ms * 1e-3) / 1e9
+        res[name] = {"avg_us": round(ms * 1e3, 2), "alg_bytes": b, "achieved": round(gbs, 1), "unit": "GB/s",
+                     "peak": peak, "frac": round(gbs / peak, 4),
+                     "bound": "hbm" if cfg.rows > 4 else "latency (under 1 MB moved)"}
+    res["rows"] = cfg.rows
+    return res
+
+
+# ---- several layers in one submission (moe_ffn_forward_layers) --------------------------------------
+
+CHAIN_WORKLOADS = ["c1_decode_b1", "c2_decode_b4_hash"]
+CHAIN_LAYERS = 4
+
+
+def run_layer_chain(cfg, steps: int, warmup: int, device) -> dict:
+    """CHAIN_LAYERS consecutive FFN blocks on the workload's rows, each on the previous one's
+    output: launched one by one (eager) and as one captured chain (moe_ffn_forward_layers).  Every
+    layer has weights of its own (the workload's generator with the seed offset per layer) and
+    routes the way the workload's layer does; the L2 is flushed before each chain."""
+    import torch
+
+    from deepseek_v4_moe_gb300 import MoeFFN, config_from
+    from synth.device import upload
+
+    n = CHAIN_LAYERS
+    ccfg = replace(cfg, n_layers=n, hash_layer_count=n if cfg.is_hash else 0)
+    devs = [upload(synth.Case(replace(ccfg, seed=ccfg.seed + 1000 * l)), device) for l in range(n)]
+    m = MoeFFN(config_from(ccfg), {l: d["weights"] for l, d in enumerate(devs)})
+    state, tok = devs[0]["state"], devs[0]["token_ids"]
+    bufs = [torch.empty_like(state), torch.empty_like(state)]
+    out = torch.empty_like(state)
+    stream = torch.cuda.Stream(device)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def eager():
+        x = state
+        for l in range(n):
+            x = m.forward(x, tok, l, out=bufs[l % 2], stream=stream)
+
+    def chained():
+        m.forward_layers(state, tok, 0, n, out=out, stream=stream)
+
+    res = {}
+    for name, fn in (("eager", eager), ("graph", chained)):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        with torch.cuda.stream(stream):
+            for i in range(max(warmup, 3) + steps):
+                flush.fill_(float(i))
+                k = i - max(warmup, 3)
+                if k >= 0:
+                    ev[k][0].record(stream)
+                fn()
+                if k >= 0:
+                    ev[k][1].record(stream)
+        torch.cuda.synchronize(device)
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        res[name] = {"us_per_layer": round(ms * 1e3 / n, 2), "tokens_per_s_per_layer": round(cfg.rows * n / (ms / 1e3), 1)}
+    assert torch.equal(out, bufs[(n - 1) % 2]), "the chain differs from the layers launched one by one"
+    assert m.status() == 0
+    m.close()
+    res.update(layers=n, rows=cfg.rows, weights="distinct per layer")
+    del devs
+    torch.cuda.empty_cache()
+    return res
+
+
 # ---- oracle (CPU baseline and reference arm) ------------------------------------------------------
 
 class _CachedCase:
@@ -426,6 +551,14 @@ def main():
             workloads[name] = {"value": round(r["value"], 1), "unit": "tokens/s", "ms_per_step": round(r["ms_per_step"], 4),
                                "forward_roofline": r["forward_roofline"], "top_kernel": r["kernels"][0],
                                "kernels": r["kernels"], "clocks": r["clocks"]}
+    hc_sub = {}
+    if args.extra:
+        for name in HC_SUBLAYER_WORKLOADS:
+            hc_sub[name] = run_hc_sublayer(synth.CONFIGS[name], 20, warmup, device, peaks)
+    chain = {}
+    if args.extra:
+        for name in CHAIN_WORKLOADS:
+            chain[name] = run_layer_chain(synth.CONFIGS[name], 20, warmup, device)
     cpu = None
     if rank == 0 and world == 1 and args.cpu_baseline:
         rate, dt, n, passes = oracle_rate(cfg, 8 if cfg.rows <= 4 else 4, 10.0)
@@ -441,7 +574,7 @@ def main():
                 "forward_roofline": main_res["forward_roofline"], "kernels": main_res["kernels"],
                 "cpu_baseline": cpu, "e2e": main_res.get("e2e"), "gpu_launches": main_res["gpu_launches"],
                 "clocks": main_res["clocks"], "median_ms_per_step": round(main_res["median_ms"], 5),
-                "workloads": workloads}
+                "workloads": workloads, "hc_sublayer_attn": hc_sub, "layer_chain": chain}
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()

@@ -30,6 +30,12 @@ class MoeFfnLayerWeights(ctypes.Structure):
     _fields_ = [(n, c_vp) for n in WEIGHT_FIELDS]
 
 
+class MoeFfnHcWeights(ctypes.Structure):
+    _fields_ = [("hc_fn", c_vp), ("hc_base", c_vp), ("hc_scale", c_vp), ("norm", c_vp)]
+
+
+SUBLAYER_ATTN, SUBLAYER_FFN = 0, 1
+
 # return codes and device status bits (include/moe_ffn.h)
 OK, ERR_NULL_PTR, ERR_BAD_CONFIG, ERR_LAYER_RANGE, ERR_ROWS_ZERO, ERR_ROWS_RANGE = 0, -1, -2, -3, -4, -5
 ERR_NO_ROUTING_SOURCE, ERR_ALIAS, ERR_CUDA, ERR_NO_MEMORY, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_NO_WEIGHTS = (
@@ -66,6 +72,8 @@ def load(build: bool = True):
     lib.moe_ffn_init.restype = ctypes.c_int
     lib.moe_ffn_forward.argtypes = [vp, vp, vp, i32, i32, vp, vp]
     lib.moe_ffn_forward.restype = ctypes.c_int
+    lib.moe_ffn_forward_layers.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
+    lib.moe_ffn_forward_layers.restype = ctypes.c_int
     lib.moe_ffn_forward_host.argtypes = [vp, vp, vp, i32, i32, vp, vp]
     lib.moe_ffn_forward_host.restype = ctypes.c_int
     lib.moe_ffn_status.argtypes = [vp]
@@ -78,6 +86,12 @@ def load(build: bool = True):
     lib.moe_ffn_stage_times.restype = ctypes.c_int
     lib.moe_ffn_hc_split_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, c_f32, vp, vp, vp, vp]
     lib.moe_ffn_hc_split_noalloc.restype = ctypes.c_int
+    lib.moe_ffn_set_attn_hc.argtypes = [vp, i32, ctypes.POINTER(MoeFfnHcWeights)]
+    lib.moe_ffn_set_attn_hc.restype = ctypes.c_int
+    lib.moe_ffn_hc_pre.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, vp, vp]
+    lib.moe_ffn_hc_pre.restype = ctypes.c_int
+    lib.moe_ffn_hc_post.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp]
+    lib.moe_ffn_hc_post.restype = ctypes.c_int
     lib.moe_ffn_last_error.argtypes = [vp]
     lib.moe_ffn_last_error.restype = ctypes.c_char_p
     lib.moe_ffn_destroy.argtypes = [vp]

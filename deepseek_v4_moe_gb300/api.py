@@ -8,7 +8,7 @@ import numpy as np
 import torch
 
 from . import _lib
-from ._lib import MoeFfnConfig, MoeFfnLayerWeights, WEIGHT_FIELDS
+from ._lib import SUBLAYER_ATTN, SUBLAYER_FFN, MoeFfnConfig, MoeFfnHcWeights, MoeFfnLayerWeights, WEIGHT_FIELDS
 
 DEBUG_BUFFERS = {"pre": 0, "post": 1, "comb": 2, "ffn_norm": 3, "logits": 4, "indices": 5, "weights": 6,
                  "safe_indices": 7, "ffn_output": 8}
@@ -94,6 +94,26 @@ class MoeFFN:
         self.last_rows = state.shape[0]
         return out
 
+    def forward_layers(self, state: torch.Tensor, token_ids: Optional[torch.Tensor], first_layer: int, n_layers: int,
+                       out: Optional[torch.Tensor] = None,
+                       stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+        """Enqueues the blocks of n_layers consecutive layers, each on the previous one's output
+        (one CUDA graph per argument set, captured by the first call); returns the final state."""
+        self._check_state(state)
+        if token_ids is not None and (token_ids.dtype != torch.int32 or not token_ids.is_cuda
+                                      or token_ids.numel() != state.shape[0]):
+            raise ValueError("token_ids must be a CUDA int32 tensor with one id per row")
+        if out is None:
+            out = torch.empty_like(state)
+        s = stream if stream is not None else torch.cuda.current_stream(state.device)
+        rc = self._lib.moe_ffn_forward_layers(self._h, state.data_ptr(),
+                                              token_ids.data_ptr() if token_ids is not None else None,
+                                              state.shape[0], first_layer, n_layers, out.data_ptr(), s.cuda_stream)
+        if rc != 0:
+            self._err(rc)
+        self.last_rows = state.shape[0]
+        return out
+
     def forward_host(self, state: np.ndarray, token_ids: Optional[np.ndarray], layer: int,
                      out: np.ndarray, stream: Optional[torch.cuda.Stream] = None) -> np.ndarray:
         """The block on host arrays (or pinned host tensors' numpy views); waits for completion."""
@@ -106,6 +126,69 @@ class MoeFFN:
             self._err(rc)
         self.last_rows = rows
         return out
+
+    # ---- the hyper-connection prelude and post of a sublayer ----
+
+    def set_attn_hc(self, layer: int, weights: Mapping[str, torch.Tensor]):
+        """Registers the attention sublayer's HC weights of ``layer``: a dict with ``hc_fn`` (bf16
+        [(2+hc)*hc, hc*hidden]), ``hc_base``, ``hc_scale`` and ``norm`` (f32) device tensors."""
+        for name in ("hc_fn", "hc_base", "hc_scale", "norm"):
+            t = weights[name]
+            want = (torch.bfloat16, torch.int16, torch.uint16) if name == "hc_fn" else (torch.float32,)
+            if not t.is_cuda or not t.is_contiguous() or t.dtype not in want:
+                raise ValueError(f"attention {name} must be a contiguous CUDA tensor of "
+                                 f"{'bf16 values' if name == 'hc_fn' else 'float32'}")
+        self._keep.setdefault(("attn", int(layer)), {}).update(weights)
+        w = MoeFfnHcWeights(hc_fn=weights["hc_fn"].data_ptr(), hc_base=weights["hc_base"].data_ptr(),
+                            hc_scale=weights["hc_scale"].data_ptr(), norm=weights["norm"].data_ptr())
+        rc = self._lib.moe_ffn_set_attn_hc(self._h, layer, ctypes.byref(w))
+        if rc != 0:
+            self._err(rc)
+
+    def hc_pre(self, state: torch.Tensor, layer: int, sublayer: str = "attn",
+               stream: Optional[torch.cuda.Stream] = None) -> dict:
+        """Enqueues the HC prelude of ``sublayer`` ("attn" or "ffn"); returns device tensors
+        x_norm [rows, hidden], pre, post [rows, hc] and comb [rows, hc, hc]."""
+        c = self.config
+        self._check_state(state)
+        rows = state.shape[0]
+        out = {"x_norm": torch.empty((rows, c.hidden), dtype=torch.float32, device=state.device),
+               "pre": torch.empty((rows, c.hc), dtype=torch.float32, device=state.device),
+               "post": torch.empty((rows, c.hc), dtype=torch.float32, device=state.device),
+               "comb": torch.empty((rows, c.hc, c.hc), dtype=torch.float32, device=state.device)}
+        sub = {"attn": SUBLAYER_ATTN, "ffn": SUBLAYER_FFN}[sublayer]
+        s = stream if stream is not None else torch.cuda.current_stream(state.device)
+        rc = self._lib.moe_ffn_hc_pre(self._h, layer, sub, state.data_ptr(), rows, out["x_norm"].data_ptr(),
+                                      out["pre"].data_ptr(), out["post"].data_ptr(), out["comb"].data_ptr(),
+                                      s.cuda_stream)
+        if rc != 0:
+            self._err(rc)
+        return out
+
+    def hc_post(self, f: torch.Tensor, state: torch.Tensor, post: torch.Tensor, comb: torch.Tensor,
+                out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+        """Enqueues hc_post of a sublayer body's output f [rows, hidden]; returns the new state."""
+        c = self.config
+        self._check_state(state)
+        rows = state.shape[0]
+        for name, t, shape in (("f", f, (rows, c.hidden)), ("post", post, (rows, c.hc)),
+                               ("comb", comb, (rows, c.hc, c.hc))):
+            if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != shape:
+                raise ValueError(f"{name} must be a contiguous CUDA float32 {list(shape)} tensor")
+        if out is None:
+            out = torch.empty_like(state)
+        s = stream if stream is not None else torch.cuda.current_stream(state.device)
+        rc = self._lib.moe_ffn_hc_post(self._h, f.data_ptr(), state.data_ptr(), post.data_ptr(), comb.data_ptr(),
+                                       rows, out.data_ptr(), s.cuda_stream)
+        if rc != 0:
+            self._err(rc)
+        return out
+
+    def _check_state(self, state: torch.Tensor):
+        c = self.config
+        if state.dtype != torch.float32 or not state.is_cuda or not state.is_contiguous() or state.dim() != 3 \
+                or state.shape[1:] != (c.hc, c.hidden):
+            raise ValueError(f"state must be a contiguous CUDA float32 [rows, {c.hc}, {c.hidden}] tensor")
 
     def status(self) -> int:
         rc = self._lib.moe_ffn_status(self._h)

@@ -90,52 +90,13 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
 
 // Comb of one row from its RMS-scaled mixes (split + Sinkhorn, docs.rs "hf2q 0.1.3
-// .../deepseek4/ffn_forward.rs", dispatch_hc_split_sinkhorn): a[i][j] = mix[2hc + i*hc + j] *
-// scale[2] + base[2hc + i*hc + j]; start exp(a - rowmax); `iters` sweeps, each normalising every
-// row then every column (multiplying by the correctly rounded reciprocal of the sum).  One thread,
-// the hc x hc matrix in registers (fixed 4 x 4 arrays; entries beyond hc unused).
-__device__ inline void sinkhorn_comb_row(const float *mix, const float *scale, const float *base, int hc, int iters,
-                                         float *comb) {
-  float c[kHcMax][kHcMax];
-#pragma unroll
-  for (int i = 0; i < kHcMax; ++i) {
-    float mx = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kHcMax; ++j) {
-      const bool in = i < hc && j < hc;
-      c[i][j] = in ? mix[2 * hc + i * hc + j] * scale[2] + base[2 * hc + i * hc + j] : 0.f;
-      if (in) mx = fmaxf(mx, c[i][j]);
-    }
-#pragma unroll
-    for (int j = 0; j < kHcMax; ++j) c[i][j] = (i < hc && j < hc) ? expf(c[i][j] - mx) : 0.f;
-  }
-#pragma unroll 1
-  for (int it = 0; it < iters; ++it) {
-#pragma unroll
-    for (int i = 0; i < kHcMax; ++i) {
-      const float inv = (i < hc) ? __frcp_rn((c[i][0] + c[i][1]) + (c[i][2] + c[i][3])) : 0.f;
-#pragma unroll
-      for (int j = 0; j < kHcMax; ++j) c[i][j] *= inv;
-    }
-#pragma unroll
-    for (int j = 0; j < kHcMax; ++j) {
-      const float inv = (j < hc) ? __frcp_rn((c[0][j] + c[1][j]) + (c[2][j] + c[3][j])) : 0.f;
-#pragma unroll
-      for (int i = 0; i < kHcMax; ++i) c[i][j] *= inv;
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < kHcMax; ++i)
-#pragma unroll
-    for (int j = 0; j < kHcMax; ++j)
-      if (i < hc && j < hc) comb[i * hc + j] = c[i][j];
-}
-
-// The same comb by a whole warp: lane 4i + j (lanes 0-15; 16-31 mirror them) holds entry (i, j).
-// Row sums pair entries as (c0 + c1) + (c2 + c3) through xor shuffles 1 and 2, column sums through
-// xor 4 and 8, and every lane takes the correctly rounded reciprocal of its own sum: the same
-// operations in the same order as sinkhorn_comb_row, so the same bits.  Lanes 0..hc*hc-1 by
-// (i, j) < hc store.  Every lane of the warp must call it.
+// .../deepseek4/ffn_forward.rs", dispatch_hc_split_sinkhorn), by a whole warp: a[i][j] =
+// mix[2hc + i*hc + j] * scale[2] + base[2hc + i*hc + j]; start exp(a - rowmax); `iters` sweeps,
+// each normalising every row then every column (multiplying by the correctly rounded reciprocal
+// of the sum).  Lane 4i + j (lanes 0-15; 16-31 mirror them) holds entry (i, j).  Row sums pair
+// entries as (c0 + c1) + (c2 + c3) through xor shuffles 1 and 2, column sums through xor 4 and 8,
+// so every kernel that forms a comb with it gets the same bits.  Lanes 0..hc*hc-1 by (i, j) < hc
+// store.  Every lane of the warp must call it.
 __device__ inline void sinkhorn_comb_warp(const float *mix, const float *scale, const float *base, int hc, int iters,
                                           float *comb) {
   const int lane = threadIdx.x & 31, i = (lane >> 2) & 3, j = lane & 3;

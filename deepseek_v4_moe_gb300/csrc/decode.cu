@@ -884,6 +884,9 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
   if (sm.flag) {
     __threadfence();
     for (int i = tid; i < a.n_counters; i += blockDim.x) cnt[i] = 0u;
+    // performed before this CTA retires: a decode launch that follows directly (programmatic
+    // dependent launch) draws its role ticket before its griddepcontrol.wait
+    __threadfence();
   }
 }
 

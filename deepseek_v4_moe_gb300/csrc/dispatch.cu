@@ -202,4 +202,53 @@ void launch_prefill_post(const Dims &d, const Scratch &s, const float *state, in
   stage(tm, "post", st);
 }
 
+// hc_post of a sublayer whose output f is given (the attention sublayer's output projection, or
+// any body): out[r, i, d] = post[r, i] * f[r, d] + sum_j comb[r, i, j] * state[r, j, d].  One
+// thread per (row, 4 columns), a row's post and comb staged once per CTA.  Every byte is read or
+// written once, so loads and stores take the streaming (evict-first) path.
+constexpr int kHcPostThreads = 128;
+
+__global__ void __launch_bounds__(kHcPostThreads) hc_post_kernel(const float *__restrict__ f,
+                                                                  const float *__restrict__ state,
+                                                                  const float *__restrict__ post,
+                                                                  const float *__restrict__ comb, int D, int hc,
+                                                                  int blocks_per_row, float *__restrict__ out) {
+  const int r = blockIdx.x / blocks_per_row;
+  const int d = ((blockIdx.x - r * blocks_per_row) * kHcPostThreads + threadIdx.x) * 4;
+  __shared__ float pc[kHcMax + kHcMax * kHcMax];
+  if (threadIdx.x < hc) pc[threadIdx.x] = post[(size_t)r * hc + threadIdx.x];
+  if (threadIdx.x < hc * hc) pc[kHcMax + threadIdx.x] = comb[(size_t)r * hc * hc + threadIdx.x];
+  __syncthreads();
+  if (d >= D) return;
+  const float4 fv = __ldcs(reinterpret_cast<const float4 *>(f + (size_t)r * D + d));
+  float4 sv[kHcMax];
+#pragma unroll
+  for (int j = 0; j < kHcMax; ++j)
+    sv[j] = j < hc ? __ldcs(reinterpret_cast<const float4 *>(state + ((size_t)r * hc + j) * D + d))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int o = 0; o < kHcMax; ++o) {
+    if (o >= hc) break;
+    const float p = pc[o];
+    float4 v = make_float4(p * fv.x, p * fv.y, p * fv.z, p * fv.w);
+#pragma unroll
+    for (int j = 0; j < kHcMax; ++j) {
+      if (j >= hc) break;
+      const float c = pc[kHcMax + o * hc + j];
+      v.x += c * sv[j].x;
+      v.y += c * sv[j].y;
+      v.z += c * sv[j].z;
+      v.w += c * sv[j].w;
+    }
+    __stcs(reinterpret_cast<float4 *>(out + ((size_t)r * hc + o) * D + d), v);
+  }
+}
+
+void launch_hc_post(const Dims &d, const float *f, const float *state, const float *post, const float *comb,
+                    int rows, float *out_state, cudaStream_t st) {
+  const int per_row = (d.hidden / 4 + kHcPostThreads - 1) / kHcPostThreads;
+  hc_post_kernel<<<(unsigned)rows * per_row, kHcPostThreads, 0, st>>>(f, state, post, comb, d.hidden, d.hc, per_row,
+                                                                     out_state);
+}
+
 }  // namespace moe

@@ -122,15 +122,16 @@ struct LayerDev {
 };
 
 // prelude.cu
-void launch_hc_mix(const Dims &d, const Scratch &s, const LayerDev &w, const float *state, int rows,
-                   cudaStream_t st, StageTimer *tm);
 void launch_prefill_router(const Dims &d, const Scratch &s, const LayerDev &w, const float *state,
                            const int32_t *token_ids, const CUtensorMap &tm_ffn_norm, int rows, bool hash, int num_sms,
                            cudaStream_t st, StageTimer *tm);
 int hc_mix_chunks(int rows, int hcd);
+void launch_hc_pre(const Dims &d, const Scratch &s, const LayerDev &w, const float *state, const CUtensorMap *tm_state,
+                   int rows, int num_sms, float *x_norm, float *pre, float *post, float *comb, cudaStream_t st);
 void launch_hc_mix_raw(const float *state, const uint16_t *hc_fn, const float *hc_scale, const float *hc_base,
                        int rows, int hc, int hidden, int iters, float eps, float *partial, unsigned *tickets,
-                       float *mixes, float *pre, float *post, float *comb, cudaStream_t st);
+                       float *mixes, float *pre, float *post, float *comb, cudaStream_t st,
+                       const float *norm_w = nullptr, float *x_norm = nullptr);
 RouteParams make_route(const Dims &d, const Scratch &s, const LayerDev &w, const int32_t *token_ids, bool hash,
                        int *counts);
 // moe_ffn.cu
@@ -149,6 +150,8 @@ int decode_resident_ctas(int hidden, int rows, int num_sms);
 void launch_dispatch(const Dims &d, const Scratch &s, int rows, cudaStream_t st, StageTimer *tm);
 void launch_prefill_post(const Dims &d, const Scratch &s, const float *state, int rows, float *out_state,
                          cudaStream_t st, StageTimer *tm);
+void launch_hc_post(const Dims &d, const float *f, const float *state, const float *post, const float *comb,
+                    int rows, float *out_state, cudaStream_t st);
 // splitgemm.cu
 void launch_prefill_mix(const Dims &d, const Scratch &s, const LayerDev &w, const float *state,
                         const CUtensorMap &tm_state, int rows, int num_sms, cudaStream_t st, StageTimer *tm);

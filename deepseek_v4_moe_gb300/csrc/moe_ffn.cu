@@ -24,6 +24,7 @@ struct moe_ffn_handle {
   Dims dims;
   int device = 0, num_sms = 0;
   std::vector<LayerDev> layers;
+  std::vector<LayerDev> attn;  // the attention sublayer's HC weights (hc fields and ffn_norm = attn_norm only)
   Scratch s;
   CUtensorMap tm_x16, tm_act16, tm_ffn_norm;
   float *host_in = nullptr, *host_out = nullptr;  // device staging of moe_ffn_forward_host
@@ -33,7 +34,18 @@ struct moe_ffn_handle {
   int last_rows = 0;
   moe::StageTimer timer;
   std::string err;
+  // moe_ffn_forward_layers: captured chains (most recent use last) and the intermediate state
+  struct Chain {
+    const void *state, *tok, *out;
+    int rows, first, n;
+    cudaGraphExec_t exec;
+  };
+  std::vector<Chain> chains;
+  cudaStream_t capture = nullptr;
+  float *chain_state = nullptr;  // [max_rows, hc, hidden]
 };
+
+static constexpr size_t kMaxChains = 8;
 
 static std::string g_init_err;
 
@@ -262,6 +274,8 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
   }
   s.decode_ctas_by_rows[0] = 0;
   h->layers.resize(cfg->n_layers);
+  h->attn.resize(cfg->n_layers);
+  for (LayerDev &A : h->attn) std::memset(&A, 0, sizeof A);
   for (int l = 0; l < cfg->n_layers; ++l) {
     LayerDev &L = h->layers[l];
     std::memset(&L, 0, sizeof L);
@@ -326,9 +340,9 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
   return MOE_FFN_OK;
 }
 
-extern "C" int moe_ffn_forward(moe_ffn_handle *h, const float *state, const int32_t *token_ids, int32_t rows,
-                               int32_t layer, float *out_state, void *stream) {
-  if (!h) return fail(nullptr, MOE_FFN_ERR_NULL_PTR, "handle is NULL");
+// The forward's host-side checks (the guards of forward_ffn_rows, plus pointers and alignment).
+static int check_forward(moe_ffn_handle *h, const float *state, const int32_t *token_ids, int32_t rows, int32_t layer,
+                         const float *out_state) {
   const moe_ffn_config &c = h->cfg;
   if (layer < 0 || layer >= c.n_layers)
     return fail(h, MOE_FFN_ERR_LAYER_RANGE, "FFN layer index %d is outside 0..%d", layer, c.n_layers);
@@ -336,18 +350,23 @@ extern "C" int moe_ffn_forward(moe_ffn_handle *h, const float *state, const int3
   if (rows < 0 || rows > c.max_rows)
     return fail(h, MOE_FFN_ERR_ROWS_RANGE, "rows %d outside 1..max_rows (%d)", rows, c.max_rows);
   if (!state || !out_state) return fail(h, MOE_FFN_ERR_NULL_PTR, "state or out_state is NULL");
-  const LayerDev &L = h->layers[layer];
-  if (!L.has_weights) return fail(h, MOE_FFN_ERR_NO_WEIGHTS, "layer %d has no weights", layer);
-  const bool hash = layer < c.hash_layer_count;
-  if (hash && !token_ids) return fail(h, MOE_FFN_ERR_NULL_PTR, "hash layer %d needs token_ids", layer);
+  if (!h->layers[layer].has_weights) return fail(h, MOE_FFN_ERR_NO_WEIGHTS, "layer %d has no weights", layer);
+  if (layer < c.hash_layer_count && !token_ids)
+    return fail(h, MOE_FFN_ERR_NULL_PTR, "hash layer %d needs token_ids", layer);
   if (!aligned16(state) || !aligned16(out_state))
     return fail(h, MOE_FFN_ERR_ALIGNMENT, "state and out_state must be 16-byte aligned");
   const size_t bytes = (size_t)rows * c.hc * c.hidden * sizeof(float);
   const uintptr_t a0 = reinterpret_cast<uintptr_t>(state), b0 = reinterpret_cast<uintptr_t>(out_state);
   if (a0 < b0 + bytes && b0 < a0 + bytes) return fail(h, MOE_FFN_ERR_ALIAS, "out_state overlaps state");
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  moe::StageTimer *tm = h->timer.on ? &h->timer : nullptr;
-  if (tm) tm->begin(st);
+  return MOE_FFN_OK;
+}
+
+// Enqueues one layer's block (arguments already checked).
+static int enqueue_forward(moe_ffn_handle *h, const float *state, const int32_t *token_ids, int32_t rows,
+                           int32_t layer, float *out_state, cudaStream_t st, moe::StageTimer *tm) {
+  const moe_ffn_config &c = h->cfg;
+  const LayerDev &L = h->layers[layer];
+  const bool hash = layer < c.hash_layer_count;
   if (rows <= moe::kDecodeRows) {
     moe::launch_decode(h->dims, h->s, L, state, token_ids, rows, hash, out_state, st, tm);
   } else {
@@ -363,6 +382,85 @@ extern "C" int moe_ffn_forward(moe_ffn_handle *h, const float *state, const int3
   }
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(h, MOE_FFN_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+  return MOE_FFN_OK;
+}
+
+extern "C" int moe_ffn_forward(moe_ffn_handle *h, const float *state, const int32_t *token_ids, int32_t rows,
+                               int32_t layer, float *out_state, void *stream) {
+  if (!h) return fail(nullptr, MOE_FFN_ERR_NULL_PTR, "handle is NULL");
+  int rc = check_forward(h, state, token_ids, rows, layer, out_state);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  moe::StageTimer *tm = h->timer.on ? &h->timer : nullptr;
+  if (tm) tm->begin(st);
+  rc = enqueue_forward(h, state, token_ids, rows, layer, out_state, st, tm);
+  if (rc) return rc;
+  h->last_stream = st;
+  h->last_rows = rows;
+  return MOE_FFN_OK;
+}
+
+extern "C" int moe_ffn_forward_layers(moe_ffn_handle *h, const float *state, const int32_t *token_ids, int32_t rows,
+                                      int32_t first_layer, int32_t n_layers, float *out_state, void *stream) {
+  if (!h) return fail(nullptr, MOE_FFN_ERR_NULL_PTR, "handle is NULL");
+  const moe_ffn_config &c = h->cfg;
+  if (n_layers < 1 || first_layer < 0 || first_layer > c.n_layers - n_layers)
+    return fail(h, MOE_FFN_ERR_LAYER_RANGE, "layers %d..%d are outside 0..%d", first_layer, first_layer + n_layers - 1,
+                c.n_layers - 1);
+  for (int l = first_layer; l < first_layer + n_layers; ++l) {
+    const int rc = check_forward(h, state, token_ids, rows, l, out_state);
+    if (rc) return rc;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (n_layers == 1) return moe_ffn_forward(h, state, token_ids, rows, first_layer, out_state, stream);
+  if (!h->chain_state && !dalloc(h, &h->chain_state, (size_t)c.max_rows * c.hc * c.hidden))
+    return fail(h, MOE_FFN_ERR_NO_MEMORY, "device allocation of the chain's intermediate state failed");
+  size_t k = 0;
+  for (; k < h->chains.size(); ++k) {
+    const moe_ffn_handle::Chain &ch = h->chains[k];
+    if (ch.state == state && ch.tok == token_ids && ch.out == out_state && ch.rows == rows &&
+        ch.first == first_layer && ch.n == n_layers)
+      break;
+  }
+  if (k == h->chains.size()) {
+    // capture the chain on the handle's own stream: layer i writes out_state when n_layers - 1 - i
+    // is even, else the intermediate buffer, so the last layer lands in out_state and no layer
+    // reads the buffer it writes
+    if (!h->capture && cudaStreamCreateWithFlags(&h->capture, cudaStreamNonBlocking) != cudaSuccess)
+      return fail(h, MOE_FFN_ERR_CUDA, "cudaStreamCreate failed");
+    cudaError_t e = cudaStreamBeginCapture(h->capture, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return fail(h, MOE_FFN_ERR_CUDA, "begin capture: %s", cudaGetErrorString(e));
+    int rc = MOE_FFN_OK;
+    const float *in = state;
+    for (int i = 0; i < n_layers && rc == MOE_FFN_OK; ++i) {
+      float *o = (n_layers - 1 - i) % 2 == 0 ? out_state : h->chain_state;
+      rc = enqueue_forward(h, in, token_ids, rows, first_layer + i, o, h->capture, nullptr);
+      in = o;
+    }
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(h->capture, &g);
+    if (rc != MOE_FFN_OK || e != cudaSuccess) {
+      if (g) cudaGraphDestroy(g);
+      return rc != MOE_FFN_OK ? rc : fail(h, MOE_FFN_ERR_CUDA, "end capture: %s", cudaGetErrorString(e));
+    }
+    cudaGraphExec_t exec = nullptr;
+    e = cudaGraphInstantiate(&exec, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) return fail(h, MOE_FFN_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e));
+    if (h->chains.size() == kMaxChains) {  // the least recently used goes (freed once it has run)
+      cudaGraphExecDestroy(h->chains.front().exec);
+      h->chains.erase(h->chains.begin());
+    }
+    h->chains.push_back({state, token_ids, out_state, rows, first_layer, n_layers, exec});
+    k = h->chains.size() - 1;
+  } else if (k + 1 != h->chains.size()) {
+    const moe_ffn_handle::Chain ch = h->chains[k];
+    h->chains.erase(h->chains.begin() + (long)k);
+    h->chains.push_back(ch);
+    k = h->chains.size() - 1;
+  }
+  const cudaError_t e = cudaGraphLaunch(h->chains[k].exec, st);
+  if (e != cudaSuccess) return fail(h, MOE_FFN_ERR_CUDA, "graph launch: %s", cudaGetErrorString(e));
   h->last_stream = st;
   h->last_rows = rows;
   return MOE_FFN_OK;
@@ -384,6 +482,110 @@ extern "C" int moe_ffn_forward_host(moe_ffn_handle *h, const float *state, const
   e = cudaMemcpyAsync(out_state, h->host_out, bytes, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return fail(h, MOE_FFN_ERR_CUDA, "device-to-host copy: %s", cudaGetErrorString(e));
+  return MOE_FFN_OK;
+}
+
+static bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return a && b && x < y + nb && y < x + na;
+}
+
+static int check_rows(moe_ffn_handle *h, int32_t rows) {
+  if (rows == 0) return fail(h, MOE_FFN_ERR_ROWS_ZERO, "at least one token row is required");
+  if (rows < 0 || rows > h->cfg.max_rows)
+    return fail(h, MOE_FFN_ERR_ROWS_RANGE, "rows %d outside 1..max_rows (%d)", rows, h->cfg.max_rows);
+  return MOE_FFN_OK;
+}
+
+extern "C" int moe_ffn_set_attn_hc(moe_ffn_handle *h, int32_t layer, const moe_ffn_hc_weights *w) {
+  if (!h) return fail(nullptr, MOE_FFN_ERR_NULL_PTR, "handle is NULL");
+  const moe_ffn_config &c = h->cfg;
+  if (layer < 0 || layer >= c.n_layers)
+    return fail(h, MOE_FFN_ERR_LAYER_RANGE, "layer index %d is outside 0..%d", layer, c.n_layers);
+  if (!w || !w->hc_fn || !w->hc_base || !w->hc_scale || !w->norm)
+    return fail(h, MOE_FFN_ERR_NULL_PTR, "attention HC weights of layer %d: a pointer is NULL", layer);
+  if (!aligned16(w->hc_fn) || !aligned16(w->hc_base) || !aligned16(w->hc_scale) || !aligned16(w->norm))
+    return fail(h, MOE_FFN_ERR_ALIGNMENT, "attention HC weights of layer %d must be 16-byte aligned", layer);
+  LayerDev &A = h->attn[layer];
+  A.hc_fn = w->hc_fn;
+  A.hc_base = w->hc_base;
+  A.hc_scale = w->hc_scale;
+  A.ffn_norm = w->norm;
+  if (c.max_rows > moe::kDecodeRows) {
+    const size_t hcd = (size_t)c.hc * c.hidden, M = h->dims.mix();
+    if (!A.hcfn16) {
+      if (!dalloc(h, &A.hcfn16, 32 * hcd)) {
+        A.has_weights = false;
+        return fail(h, MOE_FFN_ERR_NO_MEMORY, "device allocation of the fp16 attention hc_fn failed");
+      }
+      cudaMemset(A.hcfn16, 0, 32 * hcd * sizeof(__half));
+    }
+    moe::launch_bf16_to_f16(w->hc_fn, A.hcfn16, M * hcd, 0);
+    if (!make_tmap(&A.tm_hcfn, A.hcfn16, hcd, 32, 32)) {
+      A.has_weights = false;
+      return fail(h, MOE_FFN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the attention hc_fn of layer %d", layer);
+    }
+  }
+  const cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    A.has_weights = false;
+    return fail(h, MOE_FFN_ERR_CUDA, "set_attn_hc: %s", cudaGetErrorString(e));
+  }
+  A.has_weights = true;
+  return MOE_FFN_OK;
+}
+
+extern "C" int moe_ffn_hc_pre(moe_ffn_handle *h, int32_t layer, int32_t sublayer, const float *state, int32_t rows,
+                              float *x_norm, float *pre, float *post, float *comb, void *stream) {
+  if (!h) return fail(nullptr, MOE_FFN_ERR_NULL_PTR, "handle is NULL");
+  const moe_ffn_config &c = h->cfg;
+  if (layer < 0 || layer >= c.n_layers)
+    return fail(h, MOE_FFN_ERR_LAYER_RANGE, "layer index %d is outside 0..%d", layer, c.n_layers);
+  if (sublayer != MOE_FFN_SUBLAYER_ATTN && sublayer != MOE_FFN_SUBLAYER_FFN)
+    return fail(h, MOE_FFN_ERR_BAD_CONFIG, "unknown sublayer %d", sublayer);
+  int rc = check_rows(h, rows);
+  if (rc) return rc;
+  if (!state || !x_norm || !post || !comb) return fail(h, MOE_FFN_ERR_NULL_PTR, "state, x_norm, post or comb is NULL");
+  if (!aligned16(state) || !aligned16(x_norm))
+    return fail(h, MOE_FFN_ERR_ALIGNMENT, "state and x_norm must be 16-byte aligned");
+  const LayerDev &L = sublayer == MOE_FFN_SUBLAYER_ATTN ? h->attn[layer] : h->layers[layer];
+  if (!L.has_weights)
+    return fail(h, MOE_FFN_ERR_NO_WEIGHTS, "layer %d has no %s HC weights", layer,
+                sublayer == MOE_FFN_SUBLAYER_ATTN ? "attention" : "FFN");
+  const size_t R = rows, HC = c.hc, D = c.hidden, sb = R * HC * D * 4;
+  if (overlaps(state, sb, x_norm, R * D * 4) || overlaps(state, sb, pre, R * HC * 4) ||
+      overlaps(state, sb, post, R * HC * 4) || overlaps(state, sb, comb, R * HC * HC * 4))
+    return fail(h, MOE_FFN_ERR_ALIAS, "an output overlaps state");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CUtensorMap tm_state;
+  if (rows > moe::kDecodeRows && !make_tmap_f32(&tm_state, state, (uint64_t)HC * D, (uint64_t)rows))
+    return fail(h, MOE_FFN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the state");
+  moe::launch_hc_pre(h->dims, h->s, L, state, &tm_state, rows, h->num_sms, x_norm, pre ? pre : h->s.pre, post, comb,
+                     st);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(h, MOE_FFN_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+  h->last_stream = st;
+  return MOE_FFN_OK;
+}
+
+extern "C" int moe_ffn_hc_post(moe_ffn_handle *h, const float *f, const float *state, const float *post,
+                               const float *comb, int32_t rows, float *out_state, void *stream) {
+  if (!h) return fail(nullptr, MOE_FFN_ERR_NULL_PTR, "handle is NULL");
+  int rc = check_rows(h, rows);
+  if (rc) return rc;
+  if (!f || !state || !post || !comb || !out_state)
+    return fail(h, MOE_FFN_ERR_NULL_PTR, "f, state, post, comb or out_state is NULL");
+  if (!aligned16(f) || !aligned16(state) || !aligned16(out_state))
+    return fail(h, MOE_FFN_ERR_ALIGNMENT, "f, state and out_state must be 16-byte aligned");
+  const size_t R = rows, HC = h->cfg.hc, D = h->cfg.hidden, sb = R * HC * D * 4;
+  if (overlaps(out_state, sb, state, sb) || overlaps(out_state, sb, f, R * D * 4) ||
+      overlaps(out_state, sb, post, R * HC * 4) || overlaps(out_state, sb, comb, R * HC * HC * 4))
+    return fail(h, MOE_FFN_ERR_ALIAS, "out_state overlaps an input");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  moe::launch_hc_post(h->dims, f, state, post, comb, rows, out_state, st);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(h, MOE_FFN_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+  h->last_stream = st;
   return MOE_FFN_OK;
 }
 
@@ -456,6 +658,8 @@ extern "C" void moe_ffn_destroy(moe_ffn_handle *h) {
   cudaDeviceSynchronize();
   if (h->timer.created)
     for (int i = 0; i <= moe::StageTimer::kMax; ++i) cudaEventDestroy(h->timer.ev[i]);
+  for (const moe_ffn_handle::Chain &ch : h->chains) cudaGraphExecDestroy(ch.exec);
+  if (h->capture) cudaStreamDestroy(h->capture);
   free_all(h);
   delete h;
 }

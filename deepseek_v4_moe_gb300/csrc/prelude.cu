@@ -22,16 +22,68 @@ namespace moe {
 // and the Sinkhorn-balanced comb.
 // ---------------------------------------------------------------------------------------------
 struct MixArgs {
-  int do_sinkhorn;  // 0: the comb is formed later (decode: inside the expert kernel, off the critical path)
   const float *state;
   const uint16_t *hc_fn;
   const float *hc_scale, *hc_base;
   float *partial;   // [rows, M + 1, chunks]
   unsigned *tickets;
   float *mixes, *pre, *post, *comb;
+  const float *norm_w;  // with x_norm: the last CTA also forms x_norm = RMSNorm(hc_pre(state, pre)) * norm_w
+  float *x_norm;        // [rows, hidden], or null
   int rows, hcd, M, hc, chunk, iters;
   float eps;
 };
+
+// hc_pre and the sublayer's RMSNorm for rows r0..r0+nr-1, by the whole CTA (the last one of the
+// mix): a row's x stays in registers (hidden <= 8192 = kPrenormSlots x 256 threads x 4), its sum
+// of squares is reduced across the CTA, then x * rs * norm_w is stored.  The state was just read
+// by the mix CTAs, so it comes from L2.
+constexpr int kPrenormSlots = 8;
+__device__ void prenorm_rows(const MixArgs &a, int r0, int nr) {
+  __shared__ float red[8];
+  const int hc = a.hc, hidden = a.hcd / hc;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = r0; r < r0 + nr; ++r) {
+    float p[kHcMax];
+#pragma unroll
+    for (int h = 0; h < kHcMax; ++h) p[h] = h < hc ? a.pre[(size_t)r * hc + h] : 0.f;
+    float4 x[kPrenormSlots];
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < kPrenormSlots; ++k) {
+      const int d = (k * (int)blockDim.x + (int)threadIdx.x) * 4;
+      x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (d < hidden) {
+#pragma unroll
+        for (int h = 0; h < kHcMax; ++h) {
+          if (h >= hc) break;
+          const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.state + ((size_t)r * hc + h) * hidden + d));
+          x[k].x += p[h] * v.x;
+          x[k].y += p[h] * v.y;
+          x[k].z += p[h] * v.z;
+          x[k].w += p[h] * v.w;
+        }
+        ss += x[k].x * x[k].x + x[k].y * x[k].y + x[k].z * x[k].z + x[k].w * x[k].w;
+      }
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
+    const float rs = rsqrtf(tot / (float)hidden + a.eps);
+#pragma unroll
+    for (int k = 0; k < kPrenormSlots; ++k) {
+      const int d = (k * (int)blockDim.x + (int)threadIdx.x) * 4;
+      if (d < hidden) {
+        const float4 g = *reinterpret_cast<const float4 *>(a.norm_w + d);
+        *reinterpret_cast<float4 *>(a.x_norm + (size_t)r * hidden + d) =
+            make_float4(x[k].x * rs * g.x, x[k].y * rs * g.y, x[k].z * rs * g.z, x[k].w * rs * g.w);
+      }
+    }
+    __syncthreads();  // red is reused by the next row
+  }
+}
 
 int hc_mix_chunks(int rows, int hcd) {
   if (rows <= kDecodeRows) return hcd / 128;
@@ -147,45 +199,21 @@ __global__ void __launch_bounds__(256) hc_mix_kernel(MixArgs a) {
     if (part == 0 && item < items) sums[item / (M + 1)][item % (M + 1)] = s;
   }
   __syncthreads();
-  if (threadIdx.x < nr) {
-    const int r = r0 + threadIdx.x;
-    split_prepost_row(sums[threadIdx.x], s_scale, s_base, a, r);
-    if (a.do_sinkhorn)
-      sinkhorn_comb_row(a.mixes + (size_t)r * M, s_scale, s_base, a.hc, a.iters, a.comb + (size_t)r * a.hc * a.hc);
+  if (threadIdx.x < nr) split_prepost_row(sums[threadIdx.x], s_scale, s_base, a, r0 + threadIdx.x);
+  __syncthreads();  // mixes and pre of this CTA's rows are written (global, visible to the CTA)
+  if (warp < nr) {
+    const int r = r0 + warp;
+    sinkhorn_comb_warp(a.mixes + (size_t)r * M, s_scale, s_base, a.hc, a.iters, a.comb + (size_t)r * a.hc * a.hc);
   }
+  if (a.x_norm) prenorm_rows(a, r0, nr);
   if (threadIdx.x == 0) a.tickets[blockIdx.y] = 0u;
-}
-
-void launch_hc_mix(const Dims &d, const Scratch &s, const LayerDev &w, const float *state, int rows,
-                   cudaStream_t st, StageTimer *tm) {
-  MixArgs a;
-  a.state = state;
-  a.hc_fn = w.hc_fn;
-  a.hc_scale = w.hc_scale;
-  a.hc_base = w.hc_base;
-  a.partial = s.mix_partial;
-  a.tickets = s.tickets;
-  a.mixes = s.mixes;
-  a.pre = s.pre;
-  a.post = s.post;
-  a.comb = s.comb;
-  a.rows = rows;
-  a.hcd = d.hc * d.hidden;
-  a.M = d.mix();
-  a.hc = d.hc;
-  a.iters = d.iters;
-  a.eps = d.eps;
-  a.do_sinkhorn = rows > kDecodeRows;
-  const int nch = hc_mix_chunks(rows, a.hcd);
-  a.chunk = a.hcd / nch;
-  launch_pdl(hc_mix_kernel<4>, dim3(nch, (rows + 3) / 4), dim3(256), 0, st, a);
-  stage(tm, "hc_mix", st);
 }
 
 // Same kernel with caller-chosen scratch (the allocation-free entry point's fixed array).
 void launch_hc_mix_raw(const float *state, const uint16_t *hc_fn, const float *hc_scale, const float *hc_base,
                        int rows, int hc, int hidden, int iters, float eps, float *partial, unsigned *tickets,
-                       float *mixes, float *pre, float *post, float *comb, cudaStream_t st) {
+                       float *mixes, float *pre, float *post, float *comb, cudaStream_t st, const float *norm_w,
+                       float *x_norm) {
   MixArgs a;
   a.state = state;
   a.hc_fn = hc_fn;
@@ -203,7 +231,8 @@ void launch_hc_mix_raw(const float *state, const uint16_t *hc_fn, const float *h
   a.hc = hc;
   a.iters = iters;
   a.eps = eps;
-  a.do_sinkhorn = 1;
+  a.norm_w = norm_w;
+  a.x_norm = x_norm;
   const int nch = hc_mix_chunks(rows, a.hcd);
   a.chunk = a.hcd / nch;
   dim3 grid(nch, (rows + 3) / 4);
@@ -373,6 +402,25 @@ void launch_prefill_router(const Dims &d, const Scratch &s, const LayerDev &w, c
   RouteParams p = make_route(d, s, w, token_ids, hash, s.counts);
   route_rows_kernel<<<(rows + 7) / 8, 256, 0, st>>>(s.router_part, nsplit, s.logits, rows, p);
   stage(tm, "route", st);
+}
+
+// The HC prelude of a sublayer on its own (the attention sublayer, or the FFN's without its
+// body): pre/post/comb into the caller's buffers, then hc_pre + the sublayer's RMSNorm into x_norm.
+// Rows <= 4 take the split-K CUDA-core mix; more rows the tensor-core split GEMM (tm_state set).
+void launch_hc_pre(const Dims &d, const Scratch &s, const LayerDev &w, const float *state, const CUtensorMap *tm_state,
+                   int rows, int num_sms, float *x_norm, float *pre, float *post, float *comb, cudaStream_t st) {
+  if (rows <= kDecodeRows) {  // one launch: the mix's last CTA also forms x_norm
+    launch_hc_mix_raw(state, w.hc_fn, w.hc_scale, w.hc_base, rows, d.hc, d.hidden, d.iters, d.eps, s.mix_partial,
+                      s.tickets, s.mixes, pre, post, comb, st, w.ffn_norm, x_norm);
+    return;
+  }
+  Scratch s2 = s;
+  s2.pre = pre;
+  s2.post = post;
+  s2.comb = comb;
+  launch_prefill_mix(d, s2, w, state, *tm_state, rows, num_sms, st, nullptr);
+  prefill_prenorm_kernel<<<rows, 256, d.hidden * sizeof(float), st>>>(state, pre, w.ffn_norm, d.hidden, d.hc, d.eps,
+                                                                       x_norm);
 }
 
 }  // namespace moe

@@ -124,6 +124,27 @@ int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weights *layers,
 int moe_ffn_forward(moe_ffn_handle *h, const float *state, const int32_t *token_ids, int32_t rows,
                     int32_t layer, float *out_state, void *stream);
 
+/* Several layers in one submission: enqueues the blocks of layers first_layer .. first_layer +
+ * n_layers - 1 for the same `rows` tokens on `stream`, each taking the state the previous one made:
+ * state -> layer first_layer -> ... -> out_state.  A decode step's loop over layers is its unit of
+ * submission (docs.rs "hf2q 0.1.10 .../deepseek4/decode_cohort.rs", forward_verifier_decode_cohort:
+ * two layers per command buffer, a B=4 step encoded as four rows=1 passes per layer); here each
+ * layer is one launch for all rows and the whole chain is one CUDA graph.  The chain runs FFN
+ * blocks back to back; the attention sublayer a model puts between them is the caller's (every
+ * entry point of this library can be captured into the caller's own graph, which is how a step
+ * with attention is batched).
+ * The first call for a given (state, token_ids, rows, first_layer, n_layers, out_state) captures
+ * the chain into a CUDA graph that the handle owns (the 8 most recently used are kept); later calls
+ * with the same arguments launch it, reading whatever the buffers then hold.  The intermediate
+ * states live in a handle-owned f32 [max_rows, hc, hidden] buffer, allocated by the first call with
+ * n_layers > 1.  So make the first call of each argument set outside any stream capture, and not
+ * while another thread captures in global mode.  Per-kernel stage timing does not apply.
+ * Returns the codes of moe_ffn_forward, checked for every layer of the chain (LAYER_RANGE also when
+ * n_layers < 1 or the chain passes the last layer), NO_MEMORY or CUDA; nothing is enqueued on an
+ * error. */
+int moe_ffn_forward_layers(moe_ffn_handle *h, const float *state, const int32_t *token_ids, int32_t rows,
+                           int32_t first_layer, int32_t n_layers, float *out_state, void *stream);
+
 /* The same block on HOST buffers: copies state [rows, hc, hidden] and token_ids [rows] (may be NULL
  * on score layers) from host memory into library-owned device buffers, runs moe_ffn_forward on
  * `stream`, copies the new state back into out_state (host), and waits for the stream.  Pinned
@@ -175,6 +196,57 @@ int moe_ffn_hc_split_noalloc(const float *state, const uint16_t *hc_fn, const fl
                              const float *hc_base, int32_t rows, int32_t hc, int32_t hidden,
                              int32_t sinkhorn_iters, float rms_eps, float *pre, float *post, float *comb,
                              void *stream);
+
+/* ---- The hyper-connection prelude and post of a sublayer ------------------------------------
+ * Every sublayer of a layer wraps its body in the same hyper-connection stages: the attention
+ * sublayer (docs.rs "hf2q 0.1.3 src/inference/models/deepseek4/attention_forward.rs", with the "HC
+ * attention function" and attn_norm) as the FFN sublayer (ffn_forward.rs, with the "HC FFN
+ * function" and ffn_norm).  Before the body: RMSNorm of the flattened state (no weight), the mix
+ * GEMV with the sublayer's hc_fn, split + Sinkhorn into pre/post/comb (the conventions above),
+ * hc_pre (x = sum_h pre[h] * state[h]) and the sublayer's RMSNorm of x.  After the body: hc_post
+ * folds the body's output f back into the state.  The FFN sublayer's HC weights come with
+ * moe_ffn_init; the attention sublayer's are registered with moe_ffn_set_attn_hc. */
+#define MOE_FFN_SUBLAYER_ATTN 0
+#define MOE_FFN_SUBLAYER_FFN 1
+
+/* HC weights of one sublayer: DEVICE pointers, caller-owned, 16-byte aligned. */
+typedef struct moe_ffn_hc_weights {
+  const uint16_t *hc_fn;   /* bf16 [(2+hc)*hc, hc*hidden]  hc_attn_fn */
+  const float *hc_base;    /* f32 [(2+hc)*hc]              hc_attn_base */
+  const float *hc_scale;   /* f32 [3]                      hc_attn_scale */
+  const float *norm;       /* f32 [hidden]                 attn_norm */
+} moe_ffn_hc_weights;
+
+/* Registers the attention sublayer's HC weights for `layer`; they must stay valid for the life of
+ * the handle, and a later call for the same layer replaces them.  On a handle with max_rows > 4
+ * this also makes an fp16 copy of hc_fn (the tensor-core operand of the many-row path,
+ * 32 * hc * hidden * 2 bytes, owned by the handle).  Synchronous.  Returns MOE_FFN_OK,
+ * LAYER_RANGE, NULL_PTR, ALIGNMENT, NO_MEMORY or CUDA. */
+int moe_ffn_set_attn_hc(moe_ffn_handle *h, int32_t layer, const moe_ffn_hc_weights *w);
+
+/* Enqueues the HC prelude of `sublayer` (MOE_FFN_SUBLAYER_ATTN or _FFN) of `layer` for `rows`
+ * tokens on `stream` and returns without waiting.
+ *   state   f32 [rows, hc, hidden]  the state entering the sublayer (read only)
+ *   x_norm  f32 [rows, hidden]      out: the body's input, RMSNorm(hc_pre(state, pre)) * norm
+ *   pre     f32 [rows, hc]          out; may be NULL
+ *   post    f32 [rows, hc]          out, for moe_ffn_hc_post
+ *   comb    f32 [rows, hc, hc]      out, for moe_ffn_hc_post (row-major i*hc + j)
+ * state and x_norm must be 16-byte aligned; no output may overlap state.  Uses the handle's scratch
+ * like moe_ffn_forward (order the calls on one stream).  Returns MOE_FFN_OK, LAYER_RANGE, ROWS_ZERO,
+ * ROWS_RANGE, NULL_PTR, ALIGNMENT, ALIAS, BAD_CONFIG (unknown sublayer), NO_WEIGHTS (the sublayer's
+ * HC weights are not there) or CUDA; nothing is enqueued on an error. */
+int moe_ffn_hc_pre(moe_ffn_handle *h, int32_t layer, int32_t sublayer, const float *state, int32_t rows,
+                   float *x_norm, float *pre, float *post, float *comb, void *stream);
+
+/* Enqueues hc_post: out_state[r, i, d] = post[r, i] * f[r, d] + sum_j comb[r, i, j] * state[r, j, d].
+ *   f          f32 [rows, hidden]      the sublayer body's output
+ *   state      f32 [rows, hc, hidden]  the state given to moe_ffn_hc_pre
+ *   post, comb f32 [rows, hc], [rows, hc, hc] from moe_ffn_hc_pre
+ *   out_state  f32 [rows, hc, hidden]  must not overlap any input
+ * f, state and out_state must be 16-byte aligned.  Needs no scratch.  Returns MOE_FFN_OK,
+ * ROWS_ZERO, ROWS_RANGE, NULL_PTR, ALIGNMENT, ALIAS or CUDA. */
+int moe_ffn_hc_post(moe_ffn_handle *h, const float *f, const float *state, const float *post, const float *comb,
+                    int32_t rows, float *out_state, void *stream);
 
 /* Text of the last error on this handle (or of the last failed init when h is NULL). */
 const char *moe_ffn_last_error(const moe_ffn_handle *h);
