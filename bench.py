@@ -502,6 +502,8 @@ def main():
     ap.add_argument("--extra", dest="extra", action="store_true", default=True)
     ap.add_argument("--no-extra", dest="extra", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false", default=True)
+    ap.add_argument("--section", choices=["hc_sublayer", "layer_chain"], default=None,
+                    help="time only this extra section on --workload and print its JSON (for profiling)")
     args = ap.parse_args()
     warmup = max(args.warmup, 3)
     cfg = synth.ALL_CONFIGS[args.workload]
@@ -538,6 +540,14 @@ def main():
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
 
+    if args.section is not None:
+        if args.section == "hc_sublayer":
+            res = run_hc_sublayer(cfg, args.steps, warmup, device, peaks)
+        else:
+            res = run_layer_chain(cfg, args.steps, warmup, device)
+        if rank == 0:
+            print(json.dumps({"section": args.section, "workload": args.workload, **res}), flush=True)
+        return
     main_res = run_ours(cfg, args.steps, warmup, device, rank, world, dist, peaks, peak_kind, want_e2e=args.e2e,
                         soak_s=args.soak)
     workloads = {}

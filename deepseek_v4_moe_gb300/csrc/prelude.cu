@@ -34,54 +34,75 @@ struct MixArgs {
   float eps;
 };
 
-// hc_pre and the sublayer's RMSNorm for rows r0..r0+nr-1, by the whole CTA (the last one of the
-// mix): a row's x stays in registers (hidden <= 8192 = kPrenormSlots x 256 threads x 4), its sum
-// of squares is reduced across the CTA, then x * rs * norm_w is stored.  The state was just read
-// by the mix CTAs, so it comes from L2.
-constexpr int kPrenormSlots = 8;
-__device__ void prenorm_rows(const MixArgs &a, int r0, int nr) {
-  __shared__ float red[8];
+// hc_pre and the sublayer's RMSNorm for rows r0..r0+nr-1 by the last 128 threads of the mix's
+// last CTA (warps 4-7; the first four run the Sinkhorn meanwhile), synchronised by named barrier 1.
+// A row's x waits in shared memory (hidden <= 8192 = kPrenormSlots x 128 threads x 4 columns)
+// for its RMS; the state loads go out four slots (16 float4) at a time, so a row of hidden 4096
+// costs two round trips to L2, where the mix CTAs just left the state.  The loops stay rolled:
+// this code runs once per call, mostly out of a cold instruction cache.
+constexpr int kPrenormThreads = 128, kPrenormSlots = 16, kPrenormBatch = 4;
+__device__ __forceinline__ void prenorm_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ void prenorm_rows(const MixArgs &a, int r0, int nr, int t, const float *sums, const float *scale,
+                             const float *base) {
+  __shared__ float red[kPrenormThreads / 32];
+  __shared__ float4 xs[kPrenormSlots * kPrenormThreads];  // slot k of thread t at k * 128 + t
   const int hc = a.hc, hidden = a.hcd / hc;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = t >> 5, lane = t & 31;
   for (int r = r0; r < r0 + nr; ++r) {
+    // pre of row r from its reduced sums (row r - r0 of sums, stride kMixMax + 1), exactly as the
+    // split forms it
+    const float *sm = sums + (size_t)(r - r0) * (kMixMax + 1);
+    const float rs = rsqrtf(sm[a.M] / (float)a.hcd + a.eps);
     float p[kHcMax];
 #pragma unroll
-    for (int h = 0; h < kHcMax; ++h) p[h] = h < hc ? a.pre[(size_t)r * hc + h] : 0.f;
-    float4 x[kPrenormSlots];
+    for (int h = 0; h < kHcMax; ++h) p[h] = h < hc ? sigmoidf_(sm[h] * rs * scale[0] + base[h]) : 0.f;
     float ss = 0.f;
+#pragma unroll 1
+    for (int k0 = 0; k0 < kPrenormSlots; k0 += kPrenormBatch) {
+      if (k0 * kPrenormThreads * 4 >= hidden) break;  // uniform: no slot of this batch is in range
+      float4 v[kPrenormBatch][kHcMax];
 #pragma unroll
-    for (int k = 0; k < kPrenormSlots; ++k) {
-      const int d = (k * (int)blockDim.x + (int)threadIdx.x) * 4;
-      x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (d < hidden) {
+      for (int k = 0; k < kPrenormBatch; ++k) {
+        const int d = ((k0 + k) * kPrenormThreads + t) * 4;
+#pragma unroll
+        for (int h = 0; h < kHcMax; ++h)
+          v[k][h] = (d < hidden && h < hc)
+                        ? __ldcg(reinterpret_cast<const float4 *>(a.state + ((size_t)r * hc + h) * hidden + d))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < kPrenormBatch; ++k) {
+        float4 xv = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int h = 0; h < kHcMax; ++h) {
-          if (h >= hc) break;
-          const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.state + ((size_t)r * hc + h) * hidden + d));
-          x[k].x += p[h] * v.x;
-          x[k].y += p[h] * v.y;
-          x[k].z += p[h] * v.z;
-          x[k].w += p[h] * v.w;
+          xv.x += p[h] * v[k][h].x;
+          xv.y += p[h] * v[k][h].y;
+          xv.z += p[h] * v[k][h].z;
+          xv.w += p[h] * v[k][h].w;
         }
-        ss += x[k].x * x[k].x + x[k].y * x[k].y + x[k].z * x[k].z + x[k].w * x[k].w;
+        xs[(k0 + k) * kPrenormThreads + t] = xv;
+        ss += xv.x * xv.x + xv.y * xv.y + xv.z * xv.z + xv.w * xv.w;
       }
     }
     ss = warp_sum(ss);
-    if (lane == 0) red[warp] = ss;
-    __syncthreads();
+    if (lane == 0) red[w] = ss;
+    prenorm_barrier();
     float tot = 0.f;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
-    const float rs = rsqrtf(tot / (float)hidden + a.eps);
 #pragma unroll
+    for (int q = 0; q < kPrenormThreads / 32; ++q) tot += red[q];
+    const float xrs = rsqrtf(tot / (float)hidden + a.eps);
+#pragma unroll 4
     for (int k = 0; k < kPrenormSlots; ++k) {
-      const int d = (k * (int)blockDim.x + (int)threadIdx.x) * 4;
+      const int d = (k * kPrenormThreads + t) * 4;
       if (d < hidden) {
         const float4 g = *reinterpret_cast<const float4 *>(a.norm_w + d);
+        const float4 x = xs[k * kPrenormThreads + t];
         *reinterpret_cast<float4 *>(a.x_norm + (size_t)r * hidden + d) =
-            make_float4(x[k].x * rs * g.x, x[k].y * rs * g.y, x[k].z * rs * g.z, x[k].w * rs * g.w);
+            make_float4(x.x * xrs * g.x, x.y * xrs * g.y, x.z * xrs * g.z, x.w * xrs * g.w);
       }
     }
-    __syncthreads();  // red is reused by the next row
+    prenorm_barrier();  // red is reused by the next row
   }
 }
 
@@ -90,19 +111,8 @@ int hc_mix_chunks(int rows, int hcd) {
   return hcd % 512 == 0 ? 2 : hcd / 128;
 }
 
-// pre/post of one row from the reduced sums (mixes = sums * rsqrt(mean square + eps)).
-__device__ void split_prepost_row(const float *sums, const float *scale, const float *base, const MixArgs &a, int r) {
-  const int hc = a.hc, M = a.M;
-  const float rs = rsqrtf(sums[M] / (float)a.hcd + a.eps);
-  for (int m = 0; m < M; ++m) a.mixes[(size_t)r * M + m] = sums[m] * rs;
-  for (int h = 0; h < hc; ++h) {
-    a.pre[(size_t)r * hc + h] = sigmoidf_(sums[h] * rs * scale[0] + base[h]);
-    a.post[(size_t)r * hc + h] = 2.0f * sigmoidf_(sums[hc + h] * rs * scale[1] + base[hc + h]);
-  }
-}
-
 template <int RB>
-__global__ void __launch_bounds__(256) hc_mix_kernel(MixArgs a) {
+__global__ void __launch_bounds__(256, 2) hc_mix_kernel(MixArgs a) {
   pdl_trigger();
   const int nch = gridDim.x;
   const int c0 = blockIdx.x * a.chunk;
@@ -192,20 +202,34 @@ __global__ void __launch_bounds__(256) hc_mix_kernel(MixArgs a) {
     float s = 0.f;
     if (item < items) {
       const float *p = a.partial + (size_t)(r0 * (M + 1) + item) * nch;
-#pragma unroll 8
+#pragma unroll 16
       for (int ch = part; ch < nch; ch += tpi) s += __ldcg(p + ch);
     }
     for (int o = tpi >> 1; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (part == 0 && item < items) sums[item / (M + 1)][item % (M + 1)] = s;
   }
   __syncthreads();
-  if (threadIdx.x < nr) split_prepost_row(sums[threadIdx.x], s_scale, s_base, a, r0 + threadIdx.x);
-  __syncthreads();  // mixes and pre of this CTA's rows are written (global, visible to the CTA)
+  // warps 0-3, one row each: the split, lane-parallel (mixes = sums * rs; pre and post from the
+  // first 2hc), then the comb (warp Sinkhorn).  Warps 4-7 meanwhile: x_norm, forming pre
+  // themselves from the same sums by the same expression (x_norm needs pre, not the comb).
+  __shared__ float s_mix[RB][kMixMax];
   if (warp < nr) {
-    const int r = r0 + warp;
-    sinkhorn_comb_warp(a.mixes + (size_t)r * M, s_scale, s_base, a.hc, a.iters, a.comb + (size_t)r * a.hc * a.hc);
+    const int r = r0 + warp, hc = a.hc;
+    const float rs = rsqrtf(sums[warp][M] / (float)a.hcd + a.eps);
+    if (lane < M) {
+      const float mx = sums[warp][lane] * rs;
+      s_mix[warp][lane] = mx;
+      a.mixes[(size_t)r * M + lane] = mx;
+      if (lane < hc)
+        a.pre[(size_t)r * hc + lane] = sigmoidf_(mx * s_scale[0] + s_base[lane]);
+      else if (lane < 2 * hc)
+        a.post[(size_t)r * hc + lane - hc] = 2.0f * sigmoidf_(mx * s_scale[1] + s_base[lane]);
+    }
+    __syncwarp();
+    sinkhorn_comb_warp(s_mix[warp], s_scale, s_base, hc, a.iters, a.comb + (size_t)r * hc * hc);
+  } else if (a.x_norm && threadIdx.x >= 256 - kPrenormThreads) {
+    prenorm_rows(a, r0, nr, threadIdx.x - (256 - kPrenormThreads), &sums[0][0], s_scale, s_base);
   }
-  if (a.x_norm) prenorm_rows(a, r0, nr);
   if (threadIdx.x == 0) a.tickets[blockIdx.y] = 0u;
 }
 
