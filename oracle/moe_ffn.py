@@ -13,6 +13,11 @@ stage it follows and, where the page leaves the arithmetic open, the reading
 taken.  All arithmetic is float64 (``dtype`` can be set to float32 to measure the
 effect of precision); bf16 weights are widened exactly.
 
+Quantised experts: the page consumes the expert matrices as raw GGUF types without naming one.
+The quantised mode here reads them as MXFP8 (OCP Microscaling: E4M3 codes, one E8M0 power-of-two
+scale per 32 consecutive elements of a row); ``mxfp8_to_float`` decodes that format by its
+definition, and the rest of the block is unchanged.
+
 Parity unpinned (fixed by reading, not by the page): the orientation of the comb
 matrix in hc_post (out_i = sum_j comb[i, j] * state_j), the Sinkhorn start, order and
 iteration count (exp(a - rowmax); rows then columns; 20), the absence of any eps in
@@ -29,6 +34,40 @@ F64 = np.float64
 def bf16_to_float(u16: np.ndarray, dtype=F64) -> np.ndarray:
     """Widen bf16 bit patterns (uint16) exactly: the bf16 value is the top half of an f32."""
     return (np.asarray(u16).astype(np.uint32) << 16).view(np.float32).astype(dtype)
+
+
+def e4m3_to_float(q: np.ndarray, dtype=F64) -> np.ndarray:
+    """OCP 8-bit floating point E4M3 codes (uint8) to values: sign bit 7; exponent field bits 3-6
+    with bias 7; mantissa bits 0-2.  Exponent field 0: subnormal (m / 8) * 2^-6; else
+    (1 + m / 8) * 2^(e - 7); exponent 15 with mantissa 7 is NaN (the format has no infinities)."""
+    q = np.asarray(q).astype(np.int64)
+    e, m = (q >> 3) & 0xF, q & 0x7
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2((e - 7).astype(np.float64)))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return np.where(q & 0x80, -mag, mag).astype(dtype)
+
+
+def e8m0_to_float(s: np.ndarray, dtype=F64) -> np.ndarray:
+    """OCP MX E8M0 scale codes to values 2^(s - 127); code 255 is NaN."""
+    s = np.asarray(s).astype(np.int64)
+    return np.where(s == 255, np.nan, np.exp2((s - 127).astype(np.float64))).astype(dtype)
+
+
+def mxfp8_to_float(q: np.ndarray, s: np.ndarray, dtype=F64) -> np.ndarray:
+    """MXFP8 matrix [rows, K] (E4M3 codes) with scales [rows, K / 32]: element k of a row is its
+    code's value times the scale of block k // 32.  Exact in float64."""
+    v = e4m3_to_float(q, dtype).reshape(*q.shape[:-1], q.shape[-1] // 32, 32)
+    return (v * e8m0_to_float(s, dtype)[..., None]).reshape(q.shape)
+
+
+def expert_weights(case, which: str, e, dtype=F64) -> np.ndarray:
+    """Matrix `which` (gate, up, down) of routed expert e, or of the shared expert when e is None,
+    widened from the workload's storage (bf16, or MXFP8 when cfg.weights is "mxfp8")."""
+    if getattr(case.cfg, "weights", "bf16") == "mxfp8":
+        return mxfp8_to_float(*(case.shared_mx(which) if e is None else case.expert_matrix_mx(which, int(e))), dtype)
+    if e is None:
+        return bf16_to_float({"gate": case.gate_sh, "up": case.up_sh, "down": case.down_sh}[which], dtype)
+    return bf16_to_float(case.expert_matrix(which, int(e)), dtype)
 
 
 def sigmoid(x):
@@ -246,13 +285,13 @@ def forward_ffn_rows(case, dtype=F64, rows=None, stages=None):
     routed = np.zeros((n, c.top_k, c.hidden), dtype)
     for e in np.unique(st["safe_indices"][st["valid"]]):
         r_k = np.argwhere((st["indices"] == e))
-        G = bf16_to_float(case.expert_matrix("gate", int(e)), dtype)
-        U = bf16_to_float(case.expert_matrix("up", int(e)), dtype)
-        Dn = bf16_to_float(case.expert_matrix("down", int(e)), dtype)
+        G = expert_weights(case, "gate", e, dtype)
+        U = expert_weights(case, "up", e, dtype)
+        Dn = expert_weights(case, "down", e, dtype)
         y = expert_ffn(xf[r_k[:, 0]], G, U, Dn)
         routed[r_k[:, 0], r_k[:, 1]] = y
-    shared = expert_ffn(xf, bf16_to_float(case.gate_sh, dtype), bf16_to_float(case.up_sh, dtype),
-                        bf16_to_float(case.down_sh, dtype))
+    shared = expert_ffn(xf, expert_weights(case, "gate", None, dtype), expert_weights(case, "up", None, dtype),
+                        expert_weights(case, "down", None, dtype))
     f = weighted_reduce(st["indices"], st["weights"], routed, shared, c.experts)
     out = hc_post(f, st["state"], st["post"], st["comb"])
     st.update(routed_down=routed, shared_down=shared, ffn_output=f, out_state=out)

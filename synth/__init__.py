@@ -61,6 +61,8 @@ def _load():
         lib.synth_distinct_rows_i32.argtypes = [u64, u32, u64, u64, i32, i32, vp]
         lib.synth_distinct_rows_i32.restype = ctypes.c_int
         lib.synth_permutation.argtypes = [u64, u32, i32, vp]
+        lib.synth_quantize_mxfp8.argtypes = [vp, u64, vp, vp]
+        lib.synth_normal_mxfp8.argtypes = [u64, u32, u64, u64, f64, vp, vp]
         lib.synth_key.argtypes = [u64, u32, u32]
         lib.synth_key.restype = u64
         _lib = lib
@@ -87,6 +89,27 @@ def normal_bf16(seed, tensor, n, sigma, start=0, gain=1.0, out: Optional[np.ndar
     assert out.dtype == np.uint16 and out.size == n
     _load().synth_normal_bf16(seed, tensor, 0, start, n, 0.0, sigma, gain, _ptr(out))
     return out
+
+
+def quantize_mxfp8(v: np.ndarray):
+    """MXFP8 (OCP MX, E4M3 elements, one E8M0 scale per 32 consecutive values) of float32 values,
+    n a multiple of 32: (codes uint8 [n], scales uint8 [n / 32])."""
+    v = np.ascontiguousarray(v, np.float32).ravel()
+    assert v.size % 32 == 0
+    q, s = np.empty(v.size, np.uint8), np.empty(v.size // 32, np.uint8)
+    _load().synth_quantize_mxfp8(_ptr(v), v.size, _ptr(q), _ptr(s))
+    return q, s
+
+
+def normal_mxfp8(seed, tensor, n, sigma, start=0, out_q: Optional[np.ndarray] = None,
+                 out_s: Optional[np.ndarray] = None):
+    """MXFP8 of the N(0, sigma) draws that normal_bf16 rounds to bf16 (start, n multiples of 32)."""
+    assert start % 32 == 0 and n % 32 == 0
+    q = np.empty(n, np.uint8) if out_q is None else out_q
+    s = np.empty(n // 32, np.uint8) if out_s is None else out_s
+    assert q.dtype == np.uint8 and q.size == n and s.dtype == np.uint8 and s.size == n // 32
+    _load().synth_normal_mxfp8(seed, tensor, start, n, sigma, _ptr(q), _ptr(s))
+    return q, s
 
 
 def normal_rows_f32(seed, tensor, attempts: np.ndarray, row_len, sigma=1.0) -> np.ndarray:
@@ -145,6 +168,7 @@ class MoeConfig:
     sinkhorn_iters: int = 20
     rms_eps: float = 1e-6
     weight_sigma: float = 0.02
+    weights: str = "bf16"         # expert matrices: "bf16", or "mxfp8" (the same draws in MXFP8)
 
     @property
     def mix(self) -> int:
@@ -239,6 +263,30 @@ class Case:
         tensor = {"gate": T_GATE_EXPS, "up": T_UP_EXPS, "down": T_DOWN_EXPS}[which]
         n = c.inter * c.hidden
         return normal_bf16(c.seed, tensor, n * n_experts, c.weight_sigma, start=e0 * n, out=out)
+
+    # The expert matrices in MXFP8 (workloads with weights="mxfp8"): the same draws as the bf16
+    # matrices, stored as E4M3 codes [rows, K] and E8M0 scales [rows, K / 32], K the contiguous axis.
+    def expert_matrix_mx(self, which: str, e: int):
+        c = self.cfg
+        tensor = {"gate": T_GATE_EXPS, "up": T_UP_EXPS, "down": T_DOWN_EXPS}[which]
+        n = c.inter * c.hidden
+        q, s = normal_mxfp8(c.seed, tensor, n, c.weight_sigma, start=e * n)
+        shape = (c.hidden, c.inter) if which == "down" else (c.inter, c.hidden)
+        return q.reshape(shape), s.reshape(shape[0], shape[1] // 32)
+
+    def expert_block_mx(self, which: str, e0: int, n_experts: int, out_q: np.ndarray, out_s: np.ndarray):
+        """Fill out_q (n_experts * inter * hidden codes) and out_s (1/32 as many scales)."""
+        c = self.cfg
+        tensor = {"gate": T_GATE_EXPS, "up": T_UP_EXPS, "down": T_DOWN_EXPS}[which]
+        n = c.inter * c.hidden
+        return normal_mxfp8(c.seed, tensor, n * n_experts, c.weight_sigma, start=e0 * n, out_q=out_q, out_s=out_s)
+
+    def shared_mx(self, which: str):
+        c = self.cfg
+        tensor = {"gate": T_GATE_SH, "up": T_UP_SH, "down": T_DOWN_SH}[which]
+        q, s = normal_mxfp8(c.seed, tensor, c.shared_inter * c.hidden, c.weight_sigma)
+        shape = (c.hidden, c.shared_inter) if which == "down" else (c.shared_inter, c.hidden)
+        return q.reshape(shape), s.reshape(shape[0], shape[1] // 32)
 
     def attn_hc(self) -> dict:
         """The attention sublayer's hyper-connection weights, drawn like the FFN's: hc_attn_fn bf16

@@ -140,3 +140,69 @@ void synth_permutation(uint64_t seed, uint32_t tensor, int32_t n, int32_t *out) 
     out[j] = t;
   }
 }
+
+/* ---- MXFP8 storage of the same draws (input preparation, not the block's arithmetic) ----------
+ * OCP Microscaling (MX) format, E4M3 elements: every 32 consecutive elements share one E8M0 scale
+ * X = 2^(shared_exp), shared_exp = floor(log2(max |v|)) - 8 (8: the largest exponent of an E4M3
+ * value), stored as shared_exp + 127; each element is v / X rounded to the nearest E4M3 value (ties
+ * to even), saturating at +-448.  E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits;
+ * exponent field 0 holds the subnormals m/8 * 2^-6; no infinities. */
+static uint8_t e4m3_encode(double x) {
+  const uint8_t sign = x < 0 ? 0x80u : 0u;
+  double a = fabs(x);
+  if (!(a < 448.0)) return sign | 0x7Eu; /* saturate (also catches the rounding to 448 below) */
+  if (a < 0.015625) {                    /* below 2^-6: subnormal grid of 2^-9 */
+    const double q = nearbyint(a * 512.0); /* exact scaling; ties to even */
+    return sign | (uint8_t)q;            /* q == 8 is 2^-6, the smallest normal (code 0x08) */
+  }
+  int e;
+  const double f = frexp(a, &e); /* a = f * 2^e, f in [0.5, 1): the E4M3 exponent is e - 1 */
+  double mq = nearbyint((f * 2.0 - 1.0) * 8.0);
+  int ex = e - 1;
+  if (mq == 8.0) {
+    mq = 0.0;
+    ex += 1;
+  }
+  const int code = ((ex + 7) << 3) | (int)mq;
+  return sign | (uint8_t)(code > 0x7E ? 0x7E : code);
+}
+
+static void mx_block(const float *v, uint8_t *q, uint8_t *s) {
+  double amax = 0.0;
+  for (int k = 0; k < 32; ++k) amax = fmax(amax, fabs((double)v[k]));
+  int shared = 0;
+  if (amax > 0.0) {
+    int e;
+    (void)frexp(amax, &e);
+    shared = (e - 1) - 8;
+    if (shared < -127) shared = -127;
+    if (shared > 127) shared = 127;
+  }
+  *s = (uint8_t)(shared + 127);
+  const double inv = ldexp(1.0, -shared);
+  for (int k = 0; k < 32; ++k) q[k] = e4m3_encode((double)v[k] * inv);
+}
+
+/* MXFP8 of n given values (n a multiple of 32): q[n] E4M3 codes, s[n/32] E8M0 scales. */
+void synth_quantize_mxfp8(const float *v, uint64_t n, uint8_t *q, uint8_t *s) {
+#pragma omp parallel for schedule(static)
+  for (int64_t b = 0; b < (int64_t)(n / 32); ++b) mx_block(v + 32 * b, q + 32 * b, s + b);
+}
+
+/* MXFP8 of the draws float(sigma * z) of elements start .. start+n-1 (start and n multiples of 32):
+ * the same numbers synth_normal_bf16 rounds to bf16 (gain 1). */
+void synth_normal_mxfp8(uint64_t seed, uint32_t tensor, uint64_t start, uint64_t n, double sigma, uint8_t *q,
+                        uint8_t *s) {
+  const uint64_t key = synth_key(seed, tensor, 0);
+#pragma omp parallel for schedule(static)
+  for (int64_t b = 0; b < (int64_t)(n / 32); ++b) {
+    float v[32];
+    for (int k = 0; k < 32; ++k) {
+      double z = unit_normal(draw(key, start + (uint64_t)(32 * b + k)));
+      double x = z * sigma;
+      x = x + 0.0;
+      v[k] = (float)x;
+    }
+    mx_block(v, q + 32 * b, s + b);
+  }
+}
