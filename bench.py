@@ -63,8 +63,9 @@ def work_model(cfg, indices: np.ndarray) -> dict:
     valid = (indices >= 0) & (indices < E)
     groups = len(np.unique(indices[valid])) + 1          # touched routed experts + shared
     slots = int(valid.sum()) + R                          # (row, expert) pairs incl. shared
-    w_gateup = groups * 2 * I * D * 2
-    w_down = groups * D * I * 2
+    wb = 1 + 1 / 32 if cfg.weights == "mxfp8" else 2    # bytes per expert weight: MXFP8 codes + scales, or bf16
+    w_gateup = int(groups * 2 * I * D * wb)
+    w_down = int(groups * D * I * wb)
     state = R * HC * D * 4
     small = M * HC * D * 2 + E * D * 2                    # hc_fn + router
     flops_experts = slots * 2 * 3 * I * D
@@ -198,8 +199,12 @@ def run_ours(cfg, steps: int, warmup: int, device, rank: int, world: int, dist, 
     from synth.device import upload
 
     case = synth.Case(cfg)
-    dev = upload(case, device)
+    mx = cfg.weights == "mxfp8"
+    dev = upload(case, device, experts=not mx)
     m = MoeFFN(config_from(cfg), {cfg.layer: dev["weights"]})
+    if mx:
+        from synth.device import upload_mx
+        m.set_mxfp8_experts(cfg.layer, upload_mx(case, device))
     stream = torch.cuda.Stream(device)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     out = torch.empty_like(dev["state"])
@@ -316,6 +321,7 @@ def run_ours(cfg, steps: int, warmup: int, device, rank: int, world: int, dist, 
 # ---- the hyper-connection prelude and post of a sublayer (attention), timed on their own ----------
 
 HC_SUBLAYER_WORKLOADS = ["c1_decode_b1", "c4_prefill_4096"]
+MX_WORKLOADS = ["c1_decode_b1", "c2_decode_b4_hash"]   # the same workloads on MXFP8 experts
 
 
 def hc_sublayer_bytes(cfg) -> tuple[int, int]:
@@ -561,6 +567,15 @@ def main():
             workloads[name] = {"value": round(r["value"], 1), "unit": "tokens/s", "ms_per_step": round(r["ms_per_step"], 4),
                                "forward_roofline": r["forward_roofline"], "top_kernel": r["kernels"][0],
                                "kernels": r["kernels"], "clocks": r["clocks"]}
+    mx = {}
+    if args.extra:
+        for name in MX_WORKLOADS:
+            c = replace(synth.CONFIGS[name], weights="mxfp8")
+            r = run_ours(c, max(10, args.steps // 5), warmup, device, rank, world, dist, peaks, peak_kind,
+                         want_e2e=False, soak_s=min(0.5, args.soak))
+            mx[name] = {"value": round(r["value"], 1), "unit": "tokens/s", "ms_per_step": round(r["ms_per_step"], 4),
+                        "forward_roofline": r["forward_roofline"], "top_kernel": r["kernels"][0],
+                        "clocks": r["clocks"], "weights": "MXFP8 (E4M3 + E8M0 per 32), 1.03 B per weight"}
     hc_sub = {}
     if args.extra:
         for name in HC_SUBLAYER_WORKLOADS:
@@ -584,7 +599,7 @@ def main():
                 "forward_roofline": main_res["forward_roofline"], "kernels": main_res["kernels"],
                 "cpu_baseline": cpu, "e2e": main_res.get("e2e"), "gpu_launches": main_res["gpu_launches"],
                 "clocks": main_res["clocks"], "median_ms_per_step": round(main_res["median_ms"], 5),
-                "workloads": workloads, "hc_sublayer_attn": hc_sub, "layer_chain": chain}
+                "workloads": workloads, "mxfp8_experts": mx, "hc_sublayer_attn": hc_sub, "layer_chain": chain}
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()

@@ -36,6 +36,13 @@ class MoeFfnHcWeights(ctypes.Structure):
 
 SUBLAYER_ATTN, SUBLAYER_FFN = 0, 1
 
+MXFP8_FIELDS = ["gate_exps", "gate_exps_scale", "up_exps", "up_exps_scale", "down_exps", "down_exps_scale",
+                "gate_sh", "gate_sh_scale", "up_sh", "up_sh_scale", "down_sh", "down_sh_scale"]
+
+
+class MoeFfnMxfp8Experts(ctypes.Structure):
+    _fields_ = [(n, c_vp) for n in MXFP8_FIELDS]
+
 # return codes and device status bits (include/moe_ffn.h)
 OK, ERR_NULL_PTR, ERR_BAD_CONFIG, ERR_LAYER_RANGE, ERR_ROWS_ZERO, ERR_ROWS_RANGE = 0, -1, -2, -3, -4, -5
 ERR_NO_ROUTING_SOURCE, ERR_ALIAS, ERR_CUDA, ERR_NO_MEMORY, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_NO_WEIGHTS = (
@@ -86,6 +93,8 @@ def load(build: bool = True):
     lib.moe_ffn_stage_times.restype = ctypes.c_int
     lib.moe_ffn_hc_split_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, c_f32, vp, vp, vp, vp]
     lib.moe_ffn_hc_split_noalloc.restype = ctypes.c_int
+    lib.moe_ffn_set_mxfp8_experts.argtypes = [vp, i32, ctypes.POINTER(MoeFfnMxfp8Experts)]
+    lib.moe_ffn_set_mxfp8_experts.restype = ctypes.c_int
     lib.moe_ffn_set_attn_hc.argtypes = [vp, i32, ctypes.POINTER(MoeFfnHcWeights)]
     lib.moe_ffn_set_attn_hc.restype = ctypes.c_int
     lib.moe_ffn_hc_pre.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, vp, vp]

@@ -8,7 +8,8 @@ import numpy as np
 import torch
 
 from . import _lib
-from ._lib import SUBLAYER_ATTN, SUBLAYER_FFN, MoeFfnConfig, MoeFfnHcWeights, MoeFfnLayerWeights, WEIGHT_FIELDS
+from ._lib import (MXFP8_FIELDS, SUBLAYER_ATTN, SUBLAYER_FFN, MoeFfnConfig, MoeFfnHcWeights, MoeFfnLayerWeights,
+                   MoeFfnMxfp8Experts, WEIGHT_FIELDS)
 
 DEBUG_BUFFERS = {"pre": 0, "post": 1, "comb": 2, "ffn_norm": 3, "logits": 4, "indices": 5, "weights": 6,
                  "safe_indices": 7, "ffn_output": 8}
@@ -126,6 +127,20 @@ class MoeFFN:
             self._err(rc)
         self.last_rows = rows
         return out
+
+    def set_mxfp8_experts(self, layer: int, experts: Mapping[str, torch.Tensor]):
+        """Makes ``layer`` run on MXFP8 experts: uint8 device tensors named like the fields of
+        ``moe_ffn_mxfp8_experts`` (E4M3 codes in the bf16 layouts, E8M0 scales per 32 elements)."""
+        w = MoeFfnMxfp8Experts()
+        for name in MXFP8_FIELDS:
+            t = experts[name]
+            if not t.is_cuda or not t.is_contiguous() or t.dtype != torch.uint8:
+                raise ValueError(f"{name} must be a contiguous CUDA uint8 tensor")
+            setattr(w, name, t.data_ptr())
+        self._keep.setdefault(("mxfp8", int(layer)), {}).update(experts)
+        rc = self._lib.moe_ffn_set_mxfp8_experts(self._h, layer, ctypes.byref(w))
+        if rc != 0:
+            self._err(rc)
 
     # ---- the hyper-connection prelude and post of a sublayer ----
 

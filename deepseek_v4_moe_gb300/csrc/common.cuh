@@ -45,6 +45,54 @@ __device__ __forceinline__ float dot8(const uint4 w, const float4 a, const float
 }
 
 // 16-byte streaming read with an L2 eviction-priority policy (see make_policy_*).
+// ---- MXFP8 (OCP Microscaling, E4M3 elements, one E8M0 scale per 32 elements) -----------------
+// E8M0 scale code -> 2^(s - 127): the code is the float's exponent field (0: 2^-127, a subnormal;
+// 255: NaN).
+__device__ __forceinline__ float e8m0_value(unsigned s) {
+  return __uint_as_float(s == 0u ? 0x00400000u : s == 255u ? 0x7FC00000u : s << 23);
+}
+
+// The 16 E4M3 codes of w (element k in byte k) as floats: the hardware converts pairs to f16
+// (exact: every E4M3 value is an f16 value), then to f32.
+__device__ __forceinline__ void e4m3x16_to_float(const uint4 w, float (&f)[16]) {
+  const unsigned words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    unsigned h0, h1;
+    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n cvt.rn.f16x2.e4m3x2 %1, hi;\n}"
+        : "=r"(h0), "=r"(h1)
+        : "r"(words[q]));
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&h0));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&h1));
+    f[4 * q] = a.x;
+    f[4 * q + 1] = a.y;
+    f[4 * q + 2] = b.x;
+    f[4 * q + 3] = b.y;
+  }
+}
+
+// sum_k f[k] * x[k] over 16 elements, x as four float4
+__device__ __forceinline__ float dot16(const float (&f)[16], const float4 x0, const float4 x1, const float4 x2,
+                                       const float4 x3) {
+  float s = f[0] * x0.x;
+  s = fmaf(f[1], x0.y, s);
+  s = fmaf(f[2], x0.z, s);
+  s = fmaf(f[3], x0.w, s);
+  s = fmaf(f[4], x1.x, s);
+  s = fmaf(f[5], x1.y, s);
+  s = fmaf(f[6], x1.z, s);
+  s = fmaf(f[7], x1.w, s);
+  s = fmaf(f[8], x2.x, s);
+  s = fmaf(f[9], x2.y, s);
+  s = fmaf(f[10], x2.z, s);
+  s = fmaf(f[11], x2.w, s);
+  s = fmaf(f[12], x3.x, s);
+  s = fmaf(f[13], x3.y, s);
+  s = fmaf(f[14], x3.z, s);
+  s = fmaf(f[15], x3.w, s);
+  return s;
+}
+
 __device__ __forceinline__ uint4 ld_stream_hint(const void *p, uint64_t policy) {
   uint4 r;
   asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"

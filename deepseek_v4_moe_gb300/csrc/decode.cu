@@ -49,6 +49,10 @@ struct DecodeArgs {
   const uint16_t *gate;            // [experts, hidden] router, bf16
   RouteParams rp;                  // routing source and the idx / rw / safe outputs
   const uint16_t *gate_exps, *up_exps, *down_exps, *gate_sh, *up_sh, *down_sh;
+  // MXFP8 experts (the MX instances): E4M3 codes in the bf16 matrices' layouts, and E8M0 scales,
+  // one per 32 consecutive elements of a row
+  const uint8_t *gate_q, *up_q, *down_q, *gate_sh_q, *up_sh_q, *down_sh_q;
+  const uint8_t *gate_s, *up_s, *down_s, *gate_sh_s, *up_sh_s, *down_sh_s;
   // scratch
   float *mix_part;   // [nm, rows, M + 1] mix partial sums (the last entry: sum of squares)
   float *mixes, *pre, *post, *comb;
@@ -622,7 +626,7 @@ __device__ void router_role(const DecodeArgs &a, int j, PreludeSmem &sm, unsigne
 // Streaming phases
 // ---------------------------------------------------------------------------------------------
 
-template <int ROWS>
+template <int ROWS, bool MX>
 __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
   extern __shared__ __align__(16) float xs[];  // [rows, hidden]: x = ffn_norm(ffn_input)
   __shared__ __align__(16) PreludeSmem sm;
@@ -673,6 +677,7 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
   // of a batch in flight at once (fewer for 3-4 rows, whose FMAs take longer).  Group 0 (the
   // shared expert) needs no routing; the first ticket past it waits for the routing.
   constexpr int UA = ROWS >= 3 ? 4 : 8;
+  constexpr int UQA = 4;  // MX: 16-byte loads per lane and matrix in flight (2048 codes a trip)
   const int perg = I / kRowsPerTicketA;
   int ng = -1;
   // the group table, once routed, in registers: lane l holds groups l and l + 32 (group 0, the
@@ -716,9 +721,66 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
     group_of(g, e, mask);
     const bool routed = e < E;
     for (int i = i0; i < i0 + kRowsPerTicketA; ++i) {
+      float ga[kDecodeRows] = {0.f, 0.f, 0.f, 0.f}, ua[kDecodeRows] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (MX) {
+        // 16 codes per lane and 16-byte load, all of a batch in flight; each 16-code piece lies in
+        // one 32-element scale block, so its partial dot takes the block's scale once
+        const size_t ro = routed ? (size_t)e * I + i : (size_t)i;
+        const uint8_t *gq = (routed ? a.gate_q : a.gate_sh_q) + ro * D;
+        const uint8_t *uq = (routed ? a.up_q : a.up_sh_q) + ro * D;
+        const uint8_t *gsc = (routed ? a.gate_s : a.gate_sh_s) + ro * (D / 32);
+        const uint8_t *usc = (routed ? a.up_s : a.up_sh_s) + ro * (D / 32);
+        // the loop runs the same trips on every lane (its shuffles need the whole warp); lanes past
+        // the row's end only skip the loads and the arithmetic.  Each trip covers 512 * UQA codes
+        // (up to 128 scale blocks); lane l loads scale word k0 / 128 + l of the row (four blocks)
+        // with the codes, and a code piece takes its block's byte from the lane that holds it.
+        const unsigned *gsw = reinterpret_cast<const unsigned *>(gsc), *usw = reinterpret_cast<const unsigned *>(usc);
+        for (int k0 = 0; k0 < D; k0 += 512 * UQA) {
+          uint4 gv[UQA], uv[UQA];
+          const bool wl = k0 / 128 + lane < D / 128;
+          const unsigned gword = wl ? __ldg(gsw + k0 / 128 + lane) : 0u, uword = wl ? __ldg(usw + k0 / 128 + lane) : 0u;
+#pragma unroll
+          for (int u = 0; u < UQA; ++u) {
+            const int cc = k0 + u * 512 + lane * 16;
+            if (cc < D) {
+              gv[u] = ld_stream(gq + cc);
+              uv[u] = ld_stream(uq + cc);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < UQA; ++u) {
+            const int cc = k0 + u * 512 + lane * 16;
+            // block cc / 32 is block 16u + lane / 2 of this trip: byte (lane / 2) % 4 of the trip's
+            // word 4u + lane / 8
+            const int src = 4 * u + lane / 8, sh = ((lane >> 1) & 3) * 8;
+            const unsigned gw = __shfl_sync(0xffffffffu, gword, src);
+            const unsigned uw = __shfl_sync(0xffffffffu, uword, src);
+            if (cc < D) {
+              float f[16];
+              e4m3x16_to_float(gv[u], f);
+              const float sg = e8m0_value((gw >> sh) & 0xFFu);
+#pragma unroll
+              for (int r = 0; r < kDecodeRows; ++r) {
+                if ((mask >> r) & 1) {
+                  const float4 *xp = reinterpret_cast<const float4 *>(&xs[r * D + cc]);
+                  ga[r] = fmaf(sg, dot16(f, xp[0], xp[1], xp[2], xp[3]), ga[r]);
+                }
+              }
+              e4m3x16_to_float(uv[u], f);
+              const float su = e8m0_value((uw >> sh) & 0xFFu);
+#pragma unroll
+              for (int r = 0; r < kDecodeRows; ++r) {
+                if ((mask >> r) & 1) {
+                  const float4 *xp = reinterpret_cast<const float4 *>(&xs[r * D + cc]);
+                  ua[r] = fmaf(su, dot16(f, xp[0], xp[1], xp[2], xp[3]), ua[r]);
+                }
+              }
+            }
+          }
+        }
+      } else {
       const uint16_t *gw = routed ? a.gate_exps + ((size_t)e * I + i) * D : a.gate_sh + (size_t)i * D;
       const uint16_t *uw = routed ? a.up_exps + ((size_t)e * I + i) * D : a.up_sh + (size_t)i * D;
-      float ga[kDecodeRows] = {0.f, 0.f, 0.f, 0.f}, ua[kDecodeRows] = {0.f, 0.f, 0.f, 0.f};
       for (int base = lane * 8; base < D; base += 256 * UA) {
         uint4 gv[UA], uv[UA];
 #pragma unroll
@@ -745,6 +807,7 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
           }
         }
       }
+      }
 #pragma unroll
       for (int r = 0; r < kDecodeRows; ++r) {
         if ((mask >> r) & 1) {
@@ -762,6 +825,7 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
   // ---- phase B: down rows, tickets in group-major order; a ticket's rows share one group and one
   // d-block.  A group's rows wait (bounded) until all of its gate/up rows are published.
   constexpr int UB = ROWS >= 3 ? 4 : 8;
+  constexpr int UQB = 4;  // MX: 16-byte loads per lane and down row in flight (4 x 512 codes: inter 2048)
   const int nB = ng * D / kRowsPerTicketB;
   int cur = -1;
   bool ready = false;
@@ -783,9 +847,57 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
       for (int q = 0; q < kRowsPerTicketB; q += 2) {
         // two down rows in flight together
         const int dd = d0 + q;
+        float acc0[kDecodeRows] = {0.f, 0.f, 0.f, 0.f}, acc1[kDecodeRows] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (MX) {
+          const size_t ro = routed ? (size_t)e * D + dd : (size_t)dd;
+          const uint8_t *dq0 = (routed ? a.down_q : a.down_sh_q) + ro * I, *dq1 = dq0 + I;
+          const uint8_t *ds0 = (routed ? a.down_s : a.down_sh_s) + ro * (I / 32), *ds1 = ds0 + I / 32;
+          // scale words as in phase A: lane l loads word k0 / 128 + l of each row with the codes
+          const unsigned *d0w = reinterpret_cast<const unsigned *>(ds0), *d1w = reinterpret_cast<const unsigned *>(ds1);
+          for (int k0 = 0; k0 < I; k0 += 512 * UQB) {  // warp-uniform trips, as in phase A
+            uint4 w0[UQB], w1[UQB];
+            const bool wl = k0 / 128 + lane < I / 128;
+            const unsigned word0 = wl ? __ldg(d0w + k0 / 128 + lane) : 0u, word1 = wl ? __ldg(d1w + k0 / 128 + lane) : 0u;
+#pragma unroll
+            for (int u = 0; u < UQB; ++u) {
+              const int cc = k0 + u * 512 + lane * 16;
+              if (cc < I) {
+                w0[u] = ld_stream(dq0 + cc);
+                w1[u] = ld_stream(dq1 + cc);
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < UQB; ++u) {
+              const int cc = k0 + u * 512 + lane * 16;
+              const int src = 4 * u + lane / 8, sh = ((lane >> 1) & 3) * 8;
+              const unsigned sw0 = __shfl_sync(0xffffffffu, word0, src);
+              const unsigned sw1 = __shfl_sync(0xffffffffu, word1, src);
+              if (cc < I) {
+                float f[16];
+                e4m3x16_to_float(w0[u], f);
+                const float sc0 = e8m0_value((sw0 >> sh) & 0xFFu);
+#pragma unroll
+                for (int r = 0; r < kDecodeRows; ++r) {
+                  if ((mask >> r) & 1) {
+                    const float *ar = act + (size_t)r * I + cc;
+                    acc0[r] = fmaf(sc0, dot16(f, ld_ca4(ar), ld_ca4(ar + 4), ld_ca4(ar + 8), ld_ca4(ar + 12)), acc0[r]);
+                  }
+                }
+                e4m3x16_to_float(w1[u], f);
+                const float sc1 = e8m0_value((sw1 >> sh) & 0xFFu);
+#pragma unroll
+                for (int r = 0; r < kDecodeRows; ++r) {
+                  if ((mask >> r) & 1) {
+                    const float *ar = act + (size_t)r * I + cc;
+                    acc1[r] = fmaf(sc1, dot16(f, ld_ca4(ar), ld_ca4(ar + 4), ld_ca4(ar + 8), ld_ca4(ar + 12)), acc1[r]);
+                  }
+                }
+              }
+            }
+          }
+        } else {
         const uint16_t *dw0 = routed ? a.down_exps + ((size_t)e * D + dd) * I : a.down_sh + (size_t)dd * I;
         const uint16_t *dw1 = dw0 + I;
-        float acc0[kDecodeRows] = {0.f, 0.f, 0.f, 0.f}, acc1[kDecodeRows] = {0.f, 0.f, 0.f, 0.f};
         for (int base = lane * 8; base < I; base += 256 * UB) {
           uint4 w0[UB], w1[UB];
 #pragma unroll
@@ -810,6 +922,7 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
               }
             }
           }
+        }
         }
 #pragma unroll
         for (int r = 0; r < kDecodeRows; ++r) {
@@ -899,22 +1012,32 @@ int decode_router_ctas(int hidden) { return hidden / kRouterChunk; }
 int decode_counter_count(const Dims &d) { return kCntDBlocks + d.hidden / kDecodeDBlock; }
 
 using DecodeKernel = void (*)(DecodeArgs);
-static DecodeKernel decode_kernel_for(int rows) {
-  return rows == 1 ? decode_kernel<1> : rows == 2 ? decode_kernel<2> : rows == 3 ? decode_kernel<3> : decode_kernel<4>;
+static DecodeKernel decode_kernel_for(int rows, bool mx) {
+  if (mx)
+    return rows == 1   ? decode_kernel<1, true>
+           : rows == 2 ? decode_kernel<2, true>
+           : rows == 3 ? decode_kernel<3, true>
+                       : decode_kernel<4, true>;
+  return rows == 1   ? decode_kernel<1, false>
+         : rows == 2 ? decode_kernel<2, false>
+         : rows == 3 ? decode_kernel<3, false>
+                     : decode_kernel<4, false>;
 }
 
 cudaError_t decode_configure(int hidden) {
-  for (int r = 1; r <= kDecodeRows; ++r) {
-    const cudaError_t e = cudaFuncSetAttribute(decode_kernel_for(r), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               r * hidden * (int)sizeof(float));
-    if (e != cudaSuccess) return e;
-  }
+  for (int mx = 0; mx < 2; ++mx)
+    for (int r = 1; r <= kDecodeRows; ++r) {
+      const cudaError_t e = cudaFuncSetAttribute(decode_kernel_for(r, mx != 0),
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 r * hidden * (int)sizeof(float));
+      if (e != cudaSuccess) return e;
+    }
   return cudaSuccess;
 }
 
-int decode_resident_ctas(int hidden, int rows, int num_sms) {
+int decode_resident_ctas(int hidden, int rows, int num_sms, bool mx) {
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel_for(rows), 256,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel_for(rows, mx), 256,
                                                     (size_t)rows * hidden * sizeof(float)) != cudaSuccess)
     return 0;
   return per_sm * num_sms;
@@ -936,6 +1059,18 @@ void launch_decode(const Dims &d, const Scratch &s, const LayerDev &w, const flo
   a.gate_sh = w.gate_sh;
   a.up_sh = w.up_sh;
   a.down_sh = w.down_sh;
+  a.gate_q = w.gate_q;
+  a.up_q = w.up_q;
+  a.down_q = w.down_q;
+  a.gate_sh_q = w.gate_sh_q;
+  a.up_sh_q = w.up_sh_q;
+  a.down_sh_q = w.down_sh_q;
+  a.gate_s = w.gate_s;
+  a.up_s = w.up_s;
+  a.down_s = w.down_s;
+  a.gate_sh_s = w.gate_sh_s;
+  a.up_sh_s = w.up_sh_s;
+  a.down_sh_s = w.down_sh_s;
   a.nm = decode_mix_ctas(d.hc, d.hidden);
   a.nr = decode_router_ctas(d.hidden);
   a.mix_part = s.mix_partial;
@@ -970,7 +1105,8 @@ void launch_decode(const Dims &d, const Scratch &s, const LayerDev &w, const flo
   a.mix_chunk = kMixCols;
   a.eps = d.eps;
   const size_t xs_bytes = (size_t)rows * d.hidden * sizeof(float);
-  launch_pdl(decode_kernel_for(rows), dim3(s.decode_ctas_by_rows[rows]), dim3(256), xs_bytes, st, a);
+  launch_pdl(decode_kernel_for(rows, w.mx), dim3(w.mx ? s.decode_ctas_mx[rows] : s.decode_ctas_by_rows[rows]), dim3(256),
+             xs_bytes, st, a);
   stage(tm, "decode", st);
 }
 

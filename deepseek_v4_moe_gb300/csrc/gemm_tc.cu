@@ -271,4 +271,25 @@ void launch_bf16_to_f16(const uint16_t *src, __half *dst, size_t n, cudaStream_t
   bf16_to_f16_kernel<<<1024, 256, 0, st>>>(src, dst, n);
 }
 
+// MXFP8 (E4M3 codes q[n], E8M0 scales s[n / 32]) to fp16 for the tensor-core operands: each 16-code
+// piece of a 32-element block decoded exactly in f32 (code value times 2^(s - 127)), then rounded to
+// f16, which is exact whenever the product is an f16 value (scales 2^-15 .. 2^7).
+__global__ void mxfp8_to_f16_kernel(const uint8_t *__restrict__ q, const uint8_t *__restrict__ sc,
+                                    __half *__restrict__ dst, size_t n) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x * 16;
+  for (size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 16; i < n; i += stride) {
+    float f[16];
+    e4m3x16_to_float(*reinterpret_cast<const uint4 *>(q + i), f);
+    const float x = e8m0_value(sc[i / 32]);
+    __half2 h[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) h[k] = __floats2half2_rn(f[2 * k] * x, f[2 * k + 1] * x);
+    *reinterpret_cast<uint4 *>(dst + i) = *reinterpret_cast<uint4 *>(h);
+    *reinterpret_cast<uint4 *>(dst + i + 8) = *reinterpret_cast<uint4 *>(h + 4);
+  }
+}
+void launch_mxfp8_to_f16(const uint8_t *q, const uint8_t *s, __half *dst, size_t n, cudaStream_t st) {
+  mxfp8_to_f16_kernel<<<1024, 256, 0, st>>>(q, s, dst, n);
+}
+
 }  // namespace moe

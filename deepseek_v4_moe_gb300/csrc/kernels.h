@@ -69,6 +69,7 @@ struct Scratch {
   float *y_dec;           // [groups, 4, hidden]
   unsigned *dec_counters; // the decode kernel's tickets and completion counters (zero between launches)
   int decode_ctas_by_rows[5];  // co-resident CTAs of the persistent decode kernel, per row count
+  int decode_ctas_mx[5];       // the same for its MXFP8-expert instances
   // rows > 4 path
   int *counts;            // [experts] routed slots per expert (zero between launches)
   int *offsets;           // [experts + 2]
@@ -118,6 +119,11 @@ struct LayerDev {
   __half *hcfn16;                  // [32, hc * hidden]: hc_fn in fp16, rows past the mix width zero
   __half *router16;                // [experts rounded up to 256, hidden]: the router in fp16, padded
   CUtensorMap tm_gate, tm_up, tm_down, tm_hcfn, tm_router;
+  // MXFP8 experts (moe_ffn_set_mxfp8_experts): E4M3 codes in the bf16 layouts, E8M0 scales [rows, K/32]
+  const uint8_t *gate_q, *up_q, *down_q, *gate_sh_q, *up_sh_q, *down_sh_q;
+  const uint8_t *gate_s, *up_s, *down_s, *gate_sh_s, *up_sh_s, *down_sh_s;
+  bool mx;            // the experts are the MXFP8 ones (decode streams them; prefill uses their fp16 copies)
+  bool has_experts;   // some expert weights are registered (bf16 at init, or MXFP8 later)
   bool has_weights;
 };
 
@@ -145,7 +151,8 @@ int decode_router_ctas(int hidden);          // CTAs of its router role
 void launch_decode(const Dims &d, const Scratch &s, const LayerDev &w, const float *state, const int32_t *token_ids,
                    int rows, bool hash, float *out_state, cudaStream_t st, StageTimer *tm);
 cudaError_t decode_configure(int hidden);
-int decode_resident_ctas(int hidden, int rows, int num_sms);
+int decode_resident_ctas(int hidden, int rows, int num_sms, bool mx);
+void launch_mxfp8_to_f16(const uint8_t *q, const uint8_t *s, __half *dst, size_t n, cudaStream_t st);
 // dispatch.cu
 void launch_dispatch(const Dims &d, const Scratch &s, int rows, cudaStream_t st, StageTimer *tm);
 void launch_prefill_post(const Dims &d, const Scratch &s, const float *state, int rows, float *out_state,

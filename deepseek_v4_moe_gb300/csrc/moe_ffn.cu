@@ -89,24 +89,29 @@ static int check_config(const moe_ffn_config *c) {
   return MOE_FFN_OK;
 }
 
-static int check_layer(const moe_ffn_config *c, int l, const moe_ffn_layer_weights *w, bool *has) {
-  const void *req[] = {w->hc_fn, w->hc_base, w->hc_scale, w->ffn_norm, w->gate, w->gate_exps,
-                       w->up_exps, w->down_exps, w->gate_sh, w->up_sh, w->down_sh};
-  int n_set = 0;
-  for (const void *p : req) n_set += p != nullptr;
-  if (n_set == 0 && !w->exp_probs_b && !w->tid2eid) {
-    *has = false;
-    return MOE_FFN_OK;
-  }
-  if (n_set != (int)(sizeof req / sizeof req[0]))
+static int check_layer(const moe_ffn_config *c, int l, const moe_ffn_layer_weights *w, bool *has, bool *experts) {
+  const void *core[] = {w->hc_fn, w->hc_base, w->hc_scale, w->ffn_norm, w->gate};
+  const void *exps[] = {w->gate_exps, w->up_exps, w->down_exps, w->gate_sh, w->up_sh, w->down_sh};
+  int n_core = 0, n_exps = 0;
+  for (const void *p : core) n_core += p != nullptr;
+  for (const void *p : exps) n_exps += p != nullptr;
+  *has = *experts = false;
+  if (n_core == 0 && n_exps == 0 && !w->exp_probs_b && !w->tid2eid) return MOE_FFN_OK;
+  if (n_core != (int)(sizeof core / sizeof core[0]))
     return fail(nullptr, MOE_FFN_ERR_NULL_PTR, "layer %d: some weight pointers are NULL", l);
+  if (n_exps != 0 && n_exps != (int)(sizeof exps / sizeof exps[0]))
+    return fail(nullptr, MOE_FFN_ERR_NULL_PTR,
+                "layer %d: some expert pointers are NULL (give all six, or none and register MXFP8 experts)", l);
   const bool hash = l < c->hash_layer_count;
   if (hash && !w->tid2eid) return fail(nullptr, MOE_FFN_ERR_NO_ROUTING_SOURCE, "layer %d has no routing source (tid2eid)", l);
   if (!hash && !w->exp_probs_b)
     return fail(nullptr, MOE_FFN_ERR_NO_ROUTING_SOURCE, "layer %d has no routing source (exp_probs_b)", l);
-  for (const void *p : req)
+  for (const void *p : core)
     if (!aligned16(p)) return fail(nullptr, MOE_FFN_ERR_ALIGNMENT, "layer %d: weight pointer not 16-byte aligned", l);
+  for (const void *p : exps)
+    if (p && !aligned16(p)) return fail(nullptr, MOE_FFN_ERR_ALIGNMENT, "layer %d: weight pointer not 16-byte aligned", l);
   *has = true;
+  *experts = n_exps != 0;
   return MOE_FFN_OK;
 }
 
@@ -169,18 +174,37 @@ static void free_all(moe_ffn_handle *h) {
   h->allocs.clear();
 }
 
+// The fp16 copies of a layer's experts (routed, then the shared one as expert `experts`) that the
+// tensor-core GEMMs of the rows > 4 path read, and their tensor maps; allocated once per layer.
+static int alloc_f16_experts(moe_ffn_handle *h, LayerDev &L) {
+  if (L.gate16) return MOE_FFN_OK;
+  const size_t E = h->dims.experts, I = h->dims.inter, D = h->dims.hidden;
+  const size_t n = (E + 1) * I * D;
+  if (!dalloc(h, &L.gate16, n) || !dalloc(h, &L.up16, n) || !dalloc(h, &L.down16, n)) {
+    h->err = "device allocation of the fp16 expert copies failed";
+    return MOE_FFN_ERR_NO_MEMORY;
+  }
+  if (!make_tmap(&L.tm_gate, L.gate16, D, (E + 1) * I) || !make_tmap(&L.tm_up, L.up16, D, (E + 1) * I) ||
+      !make_tmap(&L.tm_down, L.down16, I, (E + 1) * D)) {
+    h->err = "cuTensorMapEncodeTiled failed for the fp16 expert copies";
+    return MOE_FFN_ERR_CUDA;
+  }
+  return MOE_FFN_OK;
+}
+
 extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weights *layers, moe_ffn_handle **out) {
   if (!out) return fail(nullptr, MOE_FFN_ERR_NULL_PTR, "out is NULL");
   *out = nullptr;
   if (!cfg || !layers) return fail(nullptr, MOE_FFN_ERR_NULL_PTR, "cfg or layers is NULL");
   int rc = check_config(cfg);
   if (rc) return rc;
-  std::vector<bool> has(cfg->n_layers);
+  std::vector<bool> has(cfg->n_layers), has_exps(cfg->n_layers);
   for (int l = 0; l < cfg->n_layers; ++l) {
-    bool hl = false;
-    rc = check_layer(cfg, l, &layers[l], &hl);
+    bool hl = false, he = false;
+    rc = check_layer(cfg, l, &layers[l], &hl, &he);
     if (rc) return rc;
     has[l] = hl;
+    has_exps[l] = he;
   }
   int dev = 0;
   cudaDeviceProp prop;
@@ -257,22 +281,23 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
     delete h;
     return fail(nullptr, MOE_FFN_ERR_CUDA, "kernel attribute setup failed");
   }
-  for (int r = 1; r <= moe::kDecodeRows; ++r) {
-    s.decode_ctas_by_rows[r] = moe::decode_resident_ctas(d.hidden, r, h->num_sms);
-    if (s.decode_ctas_by_rows[r] <= 0) {
-      free_all(h);
-      delete h;
-      return fail(nullptr, MOE_FFN_ERR_CUDA, "the decode kernel does not fit on an SM");
+  for (int mx = 0; mx < 2; ++mx)
+    for (int r = 1; r <= moe::kDecodeRows; ++r) {
+      int &n = mx ? s.decode_ctas_mx[r] : s.decode_ctas_by_rows[r];
+      n = moe::decode_resident_ctas(d.hidden, r, h->num_sms, mx != 0);
+      if (n <= 0) {
+        free_all(h);
+        delete h;
+        return fail(nullptr, MOE_FFN_ERR_CUDA, "the decode kernel does not fit on an SM");
+      }
+      // its prelude roles are claimed by the first CTAs to arrive; at least one CTA must be left
+      if (n <= moe::decode_mix_ctas(d.hc, d.hidden) + moe::decode_router_ctas(d.hidden)) {
+        free_all(h);
+        delete h;
+        return fail(nullptr, MOE_FFN_ERR_CUDA, "too few co-resident CTAs (%d) for the decode kernel's roles", n);
+      }
     }
-    // its prelude roles are claimed by the first CTAs to arrive; at least one CTA must be left
-    if (s.decode_ctas_by_rows[r] <= moe::decode_mix_ctas(d.hc, d.hidden) + moe::decode_router_ctas(d.hidden)) {
-      free_all(h);
-      delete h;
-      return fail(nullptr, MOE_FFN_ERR_CUDA, "too few co-resident CTAs (%d) for the decode kernel's roles",
-                  s.decode_ctas_by_rows[r]);
-    }
-  }
-  s.decode_ctas_by_rows[0] = 0;
+  s.decode_ctas_by_rows[0] = s.decode_ctas_mx[0] = 0;
   h->layers.resize(cfg->n_layers);
   h->attn.resize(cfg->n_layers);
   for (LayerDev &A : h->attn) std::memset(&A, 0, sizeof A);
@@ -280,6 +305,7 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
     LayerDev &L = h->layers[l];
     std::memset(&L, 0, sizeof L);
     L.has_weights = has[l];
+    L.has_experts = has_exps[l];
     if (!has[l]) continue;
     const moe_ffn_layer_weights &w = layers[l];
     L.hc_fn = w.hc_fn;
@@ -297,18 +323,21 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
     L.down_sh = w.down_sh;
     if (!prefill) continue;
     const size_t n_exp = E * I * D, n_sh = I * D;
-    if (!dalloc(h, &L.gate16, n_exp + n_sh) || !dalloc(h, &L.up16, n_exp + n_sh) ||
-        !dalloc(h, &L.down16, n_exp + n_sh)) {
-      free_all(h);
-      delete h;
-      return fail(nullptr, MOE_FFN_ERR_NO_MEMORY, "device allocation of the fp16 expert copies failed");
+    if (L.has_experts) {
+      rc = alloc_f16_experts(h, L);
+      if (rc) {
+        const std::string msg = h->err;
+        free_all(h);
+        delete h;
+        return fail(nullptr, rc, "%s", msg.c_str());
+      }
+      moe::launch_bf16_to_f16(w.gate_exps, L.gate16, n_exp, 0);
+      moe::launch_bf16_to_f16(w.gate_sh, L.gate16 + n_exp, n_sh, 0);
+      moe::launch_bf16_to_f16(w.up_exps, L.up16, n_exp, 0);
+      moe::launch_bf16_to_f16(w.up_sh, L.up16 + n_exp, n_sh, 0);
+      moe::launch_bf16_to_f16(w.down_exps, L.down16, n_exp, 0);
+      moe::launch_bf16_to_f16(w.down_sh, L.down16 + n_exp, n_sh, 0);
     }
-    moe::launch_bf16_to_f16(w.gate_exps, L.gate16, n_exp, 0);
-    moe::launch_bf16_to_f16(w.gate_sh, L.gate16 + n_exp, n_sh, 0);
-    moe::launch_bf16_to_f16(w.up_exps, L.up16, n_exp, 0);
-    moe::launch_bf16_to_f16(w.up_sh, L.up16 + n_exp, n_sh, 0);
-    moe::launch_bf16_to_f16(w.down_exps, L.down16, n_exp, 0);
-    moe::launch_bf16_to_f16(w.down_sh, L.down16 + n_exp, n_sh, 0);
     // hc_fn and the router in fp16 for the tensor-core mix and router GEMMs, zero-padded to whole
     // TMA boxes (32 mix rows; the experts to a multiple of 256)
     const size_t e_pad = (E + 255) / 256 * 256;
@@ -321,9 +350,7 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
     cudaMemset(L.router16, 0, e_pad * D * sizeof(__half));
     moe::launch_bf16_to_f16(w.hc_fn, L.hcfn16, M * hcd, 0);
     moe::launch_bf16_to_f16(w.gate, L.router16, E * D, 0);
-    if (!make_tmap(&L.tm_gate, L.gate16, D, (E + 1) * I) || !make_tmap(&L.tm_up, L.up16, D, (E + 1) * I) ||
-        !make_tmap(&L.tm_down, L.down16, I, (E + 1) * D) || !make_tmap(&L.tm_hcfn, L.hcfn16, hcd, 32, 32) ||
-        !make_tmap(&L.tm_router, L.router16, D, e_pad, 256)) {
+    if (!make_tmap(&L.tm_hcfn, L.hcfn16, hcd, 32, 32) || !make_tmap(&L.tm_router, L.router16, D, e_pad, 256)) {
       free_all(h);
       delete h;
       return fail(nullptr, MOE_FFN_ERR_CUDA, "cuTensorMapEncodeTiled failed for layer %d", l);
@@ -351,6 +378,8 @@ static int check_forward(moe_ffn_handle *h, const float *state, const int32_t *t
     return fail(h, MOE_FFN_ERR_ROWS_RANGE, "rows %d outside 1..max_rows (%d)", rows, c.max_rows);
   if (!state || !out_state) return fail(h, MOE_FFN_ERR_NULL_PTR, "state or out_state is NULL");
   if (!h->layers[layer].has_weights) return fail(h, MOE_FFN_ERR_NO_WEIGHTS, "layer %d has no weights", layer);
+  if (!h->layers[layer].has_experts)
+    return fail(h, MOE_FFN_ERR_NO_WEIGHTS, "layer %d has no expert weights (bf16 at init, or MXFP8)", layer);
   if (layer < c.hash_layer_count && !token_ids)
     return fail(h, MOE_FFN_ERR_NULL_PTR, "hash layer %d needs token_ids", layer);
   if (!aligned16(state) || !aligned16(out_state))
@@ -586,6 +615,51 @@ extern "C" int moe_ffn_hc_post(moe_ffn_handle *h, const float *f, const float *s
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(h, MOE_FFN_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
   h->last_stream = st;
+  return MOE_FFN_OK;
+}
+
+extern "C" int moe_ffn_set_mxfp8_experts(moe_ffn_handle *h, int32_t layer, const moe_ffn_mxfp8_experts *w) {
+  if (!h) return fail(nullptr, MOE_FFN_ERR_NULL_PTR, "handle is NULL");
+  const moe_ffn_config &c = h->cfg;
+  if (layer < 0 || layer >= c.n_layers)
+    return fail(h, MOE_FFN_ERR_LAYER_RANGE, "layer index %d is outside 0..%d", layer, c.n_layers);
+  LayerDev &L = h->layers[layer];
+  if (!L.has_weights) return fail(h, MOE_FFN_ERR_NO_WEIGHTS, "layer %d has no weights (moe_ffn_init)", layer);
+  if (!w) return fail(h, MOE_FFN_ERR_NULL_PTR, "MXFP8 experts of layer %d: NULL", layer);
+  const uint8_t *p[] = {w->gate_exps, w->gate_exps_scale, w->up_exps, w->up_exps_scale, w->down_exps,
+                        w->down_exps_scale, w->gate_sh, w->gate_sh_scale, w->up_sh, w->up_sh_scale,
+                        w->down_sh, w->down_sh_scale};
+  for (const uint8_t *q : p) {
+    if (!q) return fail(h, MOE_FFN_ERR_NULL_PTR, "MXFP8 experts of layer %d: a pointer is NULL", layer);
+    if (!aligned16(q)) return fail(h, MOE_FFN_ERR_ALIGNMENT, "MXFP8 experts of layer %d must be 16-byte aligned", layer);
+  }
+  L.gate_q = w->gate_exps;
+  L.gate_s = w->gate_exps_scale;
+  L.up_q = w->up_exps;
+  L.up_s = w->up_exps_scale;
+  L.down_q = w->down_exps;
+  L.down_s = w->down_exps_scale;
+  L.gate_sh_q = w->gate_sh;
+  L.gate_sh_s = w->gate_sh_scale;
+  L.up_sh_q = w->up_sh;
+  L.up_sh_s = w->up_sh_scale;
+  L.down_sh_q = w->down_sh;
+  L.down_sh_s = w->down_sh_scale;
+  if (c.max_rows > moe::kDecodeRows) {  // the tensor-core path reads fp16 copies
+    const int rc = alloc_f16_experts(h, L);
+    if (rc) return fail(h, rc, "%s", h->err.c_str());
+    const size_t E = c.experts, I = c.inter, D = c.hidden, n_exp = E * I * D, n_sh = I * D;
+    moe::launch_mxfp8_to_f16(L.gate_q, L.gate_s, L.gate16, n_exp, 0);
+    moe::launch_mxfp8_to_f16(L.gate_sh_q, L.gate_sh_s, L.gate16 + n_exp, n_sh, 0);
+    moe::launch_mxfp8_to_f16(L.up_q, L.up_s, L.up16, n_exp, 0);
+    moe::launch_mxfp8_to_f16(L.up_sh_q, L.up_sh_s, L.up16 + n_exp, n_sh, 0);
+    moe::launch_mxfp8_to_f16(L.down_q, L.down_s, L.down16, n_exp, 0);
+    moe::launch_mxfp8_to_f16(L.down_sh_q, L.down_sh_s, L.down16 + n_exp, n_sh, 0);
+  }
+  const cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail(h, MOE_FFN_ERR_CUDA, "set_mxfp8_experts: %s", cudaGetErrorString(e));
+  L.mx = true;
+  L.has_experts = true;
   return MOE_FFN_OK;
 }
 

@@ -83,7 +83,9 @@ typedef struct moe_ffn_config {
 } moe_ffn_config;
 
 /* Weights of one layer: DEVICE pointers, caller-owned, 16-byte aligned, valid for the life of
- * the handle.  A layer whose pointers are all NULL has no weights; forward on it fails. */
+ * the handle.  A layer whose pointers are all NULL has no weights; forward on it fails.  The six
+ * expert matrices may be NULL together (and only together): the layer's experts then come later
+ * in MXFP8 (moe_ffn_set_mxfp8_experts), and a forward before that fails with NO_WEIGHTS. */
 typedef struct moe_ffn_layer_weights {
   const uint16_t *hc_fn;       /* bf16 [(2+hc)*hc, hc*hidden]  hc_ffn_fn */
   const float *hc_base;        /* f32 [(2+hc)*hc]              hc_ffn_base */
@@ -247,6 +249,30 @@ int moe_ffn_hc_pre(moe_ffn_handle *h, int32_t layer, int32_t sublayer, const flo
  * ROWS_ZERO, ROWS_RANGE, NULL_PTR, ALIGNMENT, ALIAS or CUDA. */
 int moe_ffn_hc_post(moe_ffn_handle *h, const float *f, const float *state, const float *post, const float *comb,
                     int32_t rows, float *out_state, void *stream);
+
+/* ---- Quantised expert weights -----------------------------------------------------------------
+ * The page consumes the expert matrices as raw GGUF types without naming a format; the quantised
+ * mode here reads them as MXFP8 (OCP Microscaling): E4M3 codes (1 sign, 4 exponent bits with bias
+ * 7, 3 mantissa bits; no infinities) in the bf16 matrices' layouts, and one E8M0 scale (2^(s-127))
+ * per 32 consecutive elements of a row, so element k of a row is value(code) * 2^(scale[k/32] - 127).
+ * The rest of the block is unchanged.  Rows <= 4 stream the codes and scales (half the bytes of
+ * bf16); larger batches run the tensor-core path on fp16 copies made at registration, exact when
+ * every element is an f16 value (scales 2^-15 .. 2^7). */
+typedef struct moe_ffn_mxfp8_experts {
+  const uint8_t *gate_exps, *gate_exps_scale;  /* E4M3 [experts, inter, hidden], E8M0 [experts, inter, hidden/32] */
+  const uint8_t *up_exps, *up_exps_scale;      /* the same layouts */
+  const uint8_t *down_exps, *down_exps_scale;  /* E4M3 [experts, hidden, inter], E8M0 [experts, hidden, inter/32] */
+  const uint8_t *gate_sh, *gate_sh_scale;      /* E4M3 [shared_inter, hidden], E8M0 [shared_inter, hidden/32] */
+  const uint8_t *up_sh, *up_sh_scale;          /* the same layouts */
+  const uint8_t *down_sh, *down_sh_scale;      /* E4M3 [hidden, shared_inter], E8M0 [hidden, shared_inter/32] */
+} moe_ffn_mxfp8_experts;
+
+/* Makes `layer` run on these MXFP8 experts (DEVICE pointers, caller-owned, 16-byte aligned, valid
+ * for the life of the handle), in place of any bf16 experts given at init; a later call replaces
+ * them.  The layer must have its other weights from moe_ffn_init.  On a handle with max_rows > 4
+ * this fills the fp16 copies the tensor-core path reads (allocating them if init did not).
+ * Synchronous.  Returns MOE_FFN_OK, LAYER_RANGE, NO_WEIGHTS, NULL_PTR, ALIGNMENT, NO_MEMORY or CUDA. */
+int moe_ffn_set_mxfp8_experts(moe_ffn_handle *h, int32_t layer, const moe_ffn_mxfp8_experts *w);
 
 /* Text of the last error on this handle (or of the last failed init when h is NULL). */
 const char *moe_ffn_last_error(const moe_ffn_handle *h);
