@@ -43,7 +43,8 @@ def describe(cfg) -> str:
     extra = {"c3_prefill_512": ", Zipf(1.1) expert popularity", "c4_prefill_4096": ", 8 hot experts (router rows x3)"}
     return (f"{cfg.name}: rows={cfg.rows}, hidden={cfg.hidden}, hc={cfg.hc}, experts={cfg.experts}, "
             f"top_k={cfg.top_k}, inter={cfg.inter}, shared expert inter={cfg.shared_inter}, {route} routing"
-            f"{extra.get(cfg.name, '')}, seed {cfg.seed}")
+            f"{extra.get(cfg.name, '')}, seed {cfg.seed}"
+            f"{', MXFP8 experts (E4M3, E8M0 scale per 32)' if cfg.weights == 'mxfp8' else ''}")
 
 
 def load_peaks():
@@ -508,11 +509,13 @@ def main():
     ap.add_argument("--extra", dest="extra", action="store_true", default=True)
     ap.add_argument("--no-extra", dest="extra", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false", default=True)
+    ap.add_argument("--weights", choices=["bf16", "mxfp8"], default="bf16",
+                    help="expert weight format of the workload (mxfp8: a profiling and comparison mode)")
     ap.add_argument("--section", choices=["hc_sublayer", "layer_chain"], default=None,
                     help="time only this extra section on --workload and print its JSON (for profiling)")
     args = ap.parse_args()
     warmup = max(args.warmup, 3)
-    cfg = synth.ALL_CONFIGS[args.workload]
+    cfg = replace(synth.ALL_CONFIGS[args.workload], weights=args.weights)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

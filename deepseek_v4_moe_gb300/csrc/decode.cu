@@ -756,23 +756,18 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
             const unsigned gw = __shfl_sync(0xffffffffu, gword, src);
             const unsigned uw = __shfl_sync(0xffffffffu, uword, src);
             if (cc < D) {
-              float f[16];
-              e4m3x16_to_float(gv[u], f);
-              const float sg = e8m0_value((gw >> sh) & 0xFFu);
+              // both matrices decoded, so each row's x is read from shared memory once for both
+              float fg[16], fu[16];
+              e4m3x16_to_float_scaled(gv[u], fg);
+              e4m3x16_to_float_scaled(uv[u], fu);
+              const float sg = e8m0_value((gw >> sh) & 0xFFu), su = e8m0_value((uw >> sh) & 0xFFu);
 #pragma unroll
               for (int r = 0; r < kDecodeRows; ++r) {
                 if ((mask >> r) & 1) {
                   const float4 *xp = reinterpret_cast<const float4 *>(&xs[r * D + cc]);
-                  ga[r] = fmaf(sg, dot16(f, xp[0], xp[1], xp[2], xp[3]), ga[r]);
-                }
-              }
-              e4m3x16_to_float(uv[u], f);
-              const float su = e8m0_value((uw >> sh) & 0xFFu);
-#pragma unroll
-              for (int r = 0; r < kDecodeRows; ++r) {
-                if ((mask >> r) & 1) {
-                  const float4 *xp = reinterpret_cast<const float4 *>(&xs[r * D + cc]);
-                  ua[r] = fmaf(su, dot16(f, xp[0], xp[1], xp[2], xp[3]), ua[r]);
+                  const float4 x0 = xp[0], x1 = xp[1], x2 = xp[2], x3 = xp[3];
+                  ga[r] = fmaf(sg, dot16(fg, x0, x1, x2, x3) * kE4m3Unscale, ga[r]);
+                  ua[r] = fmaf(su, dot16(fu, x0, x1, x2, x3) * kE4m3Unscale, ua[r]);
                 }
               }
             }
@@ -873,23 +868,17 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
               const unsigned sw0 = __shfl_sync(0xffffffffu, word0, src);
               const unsigned sw1 = __shfl_sync(0xffffffffu, word1, src);
               if (cc < I) {
-                float f[16];
-                e4m3x16_to_float(w0[u], f);
-                const float sc0 = e8m0_value((sw0 >> sh) & 0xFFu);
+                float f0[16], f1[16];
+                e4m3x16_to_float_scaled(w0[u], f0);
+                e4m3x16_to_float_scaled(w1[u], f1);
+                const float sc0 = e8m0_value((sw0 >> sh) & 0xFFu), sc1 = e8m0_value((sw1 >> sh) & 0xFFu);
 #pragma unroll
                 for (int r = 0; r < kDecodeRows; ++r) {
                   if ((mask >> r) & 1) {
                     const float *ar = act + (size_t)r * I + cc;
-                    acc0[r] = fmaf(sc0, dot16(f, ld_ca4(ar), ld_ca4(ar + 4), ld_ca4(ar + 8), ld_ca4(ar + 12)), acc0[r]);
-                  }
-                }
-                e4m3x16_to_float(w1[u], f);
-                const float sc1 = e8m0_value((sw1 >> sh) & 0xFFu);
-#pragma unroll
-                for (int r = 0; r < kDecodeRows; ++r) {
-                  if ((mask >> r) & 1) {
-                    const float *ar = act + (size_t)r * I + cc;
-                    acc1[r] = fmaf(sc1, dot16(f, ld_ca4(ar), ld_ca4(ar + 4), ld_ca4(ar + 8), ld_ca4(ar + 12)), acc1[r]);
+                    const float4 x0 = ld_ca4(ar), x1 = ld_ca4(ar + 4), x2 = ld_ca4(ar + 8), x3 = ld_ca4(ar + 12);
+                    acc0[r] = fmaf(sc0, dot16(f0, x0, x1, x2, x3) * kE4m3Unscale, acc0[r]);
+                    acc1[r] = fmaf(sc1, dot16(f1, x0, x1, x2, x3) * kE4m3Unscale, acc1[r]);
                   }
                 }
               }
