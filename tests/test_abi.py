@@ -73,3 +73,23 @@ def test_null_arguments(lib):
     assert lib.moe_ffn_forward(None, None, None, 1, 0, None, None) == _lib.ERR_NULL_PTR
     assert lib.moe_ffn_status(None) == _lib.ERR_NULL_PTR
     lib.moe_ffn_destroy(None)
+
+
+def test_experts_may_all_be_left_for_mxfp8(lib):
+    # the six bf16 expert matrices NULL together pass the layer checks (the experts come later in
+    # MXFP8); init then stops at the device query, which has no GPU here
+    exps = dict(gate_exps=None, up_exps=None, down_exps=None, gate_sh=None, up_sh=None, down_sh=None)
+    rc, msg = _init(lib, _cfg(), {3: _fake_layer(**exps)})
+    assert rc in (_lib.ERR_CUDA, _lib.ERR_UNSUPPORTED), msg
+    rc, _ = _init(lib, _cfg(), {3: _fake_layer(gate_exps=None, up_exps=None)})   # some, not all
+    assert rc == _lib.ERR_NULL_PTR
+    rc, _ = _init(lib, _cfg(), {3: _fake_layer(down_sh=0x10008)})                # present, misaligned
+    assert rc == _lib.ERR_ALIGNMENT
+
+
+def test_new_entry_points_reject_a_null_handle(lib):
+    assert lib.moe_ffn_set_attn_hc(None, 0, None) == _lib.ERR_NULL_PTR
+    assert lib.moe_ffn_set_mxfp8_experts(None, 0, None) == _lib.ERR_NULL_PTR
+    assert lib.moe_ffn_hc_pre(None, 0, 0, None, 1, None, None, None, None, None) == _lib.ERR_NULL_PTR
+    assert lib.moe_ffn_hc_post(None, None, None, None, None, 1, None, None) == _lib.ERR_NULL_PTR
+    assert lib.moe_ffn_forward_layers(None, None, None, 1, 0, 2, None, None) == _lib.ERR_NULL_PTR
