@@ -8,9 +8,15 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+@pytest.hookimpl(tryfirst=True)
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: full-shape case (minutes of CPU oracle work)")
+    # every test is bounded (pytest-timeout, where installed; an explicit --timeout wins): a test
+    # stuck on a kernel that does not return ends, dumping its stack, instead of holding the GPU
+    if config.pluginmanager.hasplugin("timeout") and not getattr(config.option, "timeout", None):
+        config.option.timeout = 900
+        config.option.timeout_method = "thread"
 
 
 @pytest.fixture(scope="session")
