@@ -106,3 +106,23 @@ def test_zipf_targets_capped_and_normalised():
     order = np.sort(p)[::-1]
     # below the cap the shares follow rank^-1.1
     assert abs(order[5] / order[10] - (11 / 6) ** 1.1) < 1e-9
+
+
+def test_mx_experts_chunked_equal_per_expert_and_deterministic():
+    # upload_mx draws experts in chunks; each chunk must equal the per-expert matrices
+    from dataclasses import replace
+    cfg = replace(synth.CONFIGS["c0_tiny"], weights="mxfp8")
+    c = synth.Case(cfg)
+    per = cfg.inter * cfg.hidden
+    q = np.empty(3 * per, np.uint8)
+    s = np.empty(3 * per // 32, np.uint8)
+    c.expert_block_mx("down", 4, 3, q, s)
+    for k in range(3):
+        eq, es = c.expert_matrix_mx("down", 4 + k)
+        assert eq.shape == (cfg.hidden, cfg.inter) and es.shape == (cfg.hidden, cfg.inter // 32)
+        assert np.array_equal(q[k * per:(k + 1) * per], eq.ravel())
+        assert np.array_equal(s[k * per // 32:(k + 1) * per // 32], es.ravel())
+    q2, s2 = synth.Case(cfg).expert_matrix_mx("down", 5)
+    assert np.array_equal(q2, c.expert_matrix_mx("down", 5)[0]) and np.array_equal(s2, c.expert_matrix_mx("down", 5)[1])
+    sq, ss = c.shared_mx("gate")
+    assert sq.shape == (cfg.shared_inter, cfg.hidden) and ss.shape == (cfg.shared_inter, cfg.hidden // 32)
