@@ -47,7 +47,9 @@ struct moe_ffn_handle {
 
 static constexpr size_t kMaxChains = 8;
 
-static std::string g_init_err;
+// Message of the last failure without a handle, one per host thread: several threads may fail
+// validation at the same time, and each reads back its own text.
+static thread_local std::string g_init_err;
 
 namespace moe {
 void set_global_error(const char *msg) { g_init_err = msg; }

@@ -1,10 +1,10 @@
 // Allocation-free variant of the hyper-connection split (HC mix + split + Sinkhorn).
 //
-// Some callers cannot allocate device memory when they call in: code running while a CUDA graph
-// is being captured (cudaMalloc is not a capturable operation and synchronises the device),
-// real-time or serving loops that forbid allocation after start-up, and hosts whose memory pool
-// already owns all of the GPU's memory.  This entry point takes its scratch from a fixed array
-// compiled into the library instead of a handle, so it allocates nothing per call.
+// Some callers cannot allocate device memory when they call in: serving or real-time loops that
+// forbid allocation after start-up (cudaMalloc may synchronise the whole device and its latency is
+// unbounded), and hosts whose memory pool already owns all of the GPU's memory, where cudaMalloc
+// fails.  This entry point takes its scratch from a fixed array compiled into the library instead
+// of a handle, so it allocates nothing per call.
 //
 // The array is file-scope device memory: every GPU that loads the library holds its 1 MiB until
 // the process exits.  Host code cannot use the array's name as a device address (on the host the
@@ -42,6 +42,10 @@ extern "C" int moe_ffn_hc_split_noalloc(const float *state, const uint16_t *hc_f
                                         const float *hc_base, int32_t rows, int32_t hc, int32_t hidden,
                                         int32_t sinkhorn_iters, float rms_eps, float *pre, float *post,
                                         float *comb, void *stream) {
+  // an error left by earlier, unrelated work would otherwise surface after this call's work was
+  // enqueued; report it first, with nothing enqueued
+  if (cudaPeekAtLastError() != cudaSuccess)
+    return reject(MOE_FFN_ERR_CUDA, "hc_split_noalloc: a CUDA error is pending from earlier work");
   if (!state || !hc_fn || !hc_scale || !hc_base || !pre || !post || !comb)
     return reject(MOE_FFN_ERR_NULL_PTR, "hc_split_noalloc: a pointer argument is NULL");
   if (hc < 1 || hc > moe::kHcMax || hidden < 128 || hidden % 128 || hidden > 8192 || sinkhorn_iters < 0 ||
@@ -81,6 +85,7 @@ extern "C" int moe_ffn_hc_split_noalloc(const float *state, const uint16_t *hc_f
     return reject(MOE_FFN_ERR_CUDA, "hc_split_noalloc: clearing the tickets failed");
   moe::launch_hc_mix_raw(state, hc_fn, hc_scale, hc_base, rows, hc, hidden, sinkhorn_iters, rms_eps, part, tickets,
                          mixes, pre, post, comb, st);
+  // a failure here comes after the memset was enqueued (the header says so)
   if (cudaGetLastError() != cudaSuccess) return reject(MOE_FFN_ERR_CUDA, "hc_split_noalloc: launch failed");
   return MOE_FFN_OK;
 }

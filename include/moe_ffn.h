@@ -181,19 +181,24 @@ int moe_ffn_stage_times(moe_ffn_handle *h, float *ms, const char **names, int32_
 
 /* Allocation-free HC split: the first stage of the block (HC RMSNorm, mix GEMV with hc_fn, split
  * into pre/post and the Sinkhorn comb, the same kernel and conventions as moe_ffn_forward) for
- * callers that cannot allocate device memory at call time: code running under CUDA graph capture,
- * serving loops that forbid allocation after start-up, or hosts whose pool owns the whole GPU.
- * The pages have no counterpart of this entry point; it exists for such callers.
+ * callers that cannot allocate device memory at call time: serving or real-time loops that forbid
+ * allocation after start-up (cudaMalloc may synchronise the device), or hosts whose memory pool
+ * owns the whole GPU, where cudaMalloc fails.  The pages have no counterpart of this entry point;
+ * it exists for such callers.
  *   state    f32 [rows, hc, hidden] (device, 16-byte aligned)    hc_fn bf16 [(2+hc)*hc, hc*hidden]
  *   hc_scale f32 [3], hc_base f32 [(2+hc)*hc]                    (device)
  *   pre, post f32 [rows, hc]; comb f32 [rows, hc, hc]            (device outputs)
  * No handle and no allocation: the scratch is a fixed 1 MiB array inside the library (held by every
- * GPU that loads the library until exit), shared by all calls.  Limits: 1 <= rows <= 4096 and
- * rows * (partial sums of the chosen split) must fit the 1 MiB; larger inputs return
+ * GPU that loads the library until exit), shared by all calls; each call clears the part that
+ * must start at zero (one cudaMemsetAsync on the array) before its kernel.  Limits: 1 <= rows <=
+ * 4096 and rows * (partial sums of the chosen split) must fit the 1 MiB; larger inputs return
  * MOE_FFN_ERR_ROWS_RANGE with a message in moe_ffn_last_error(NULL).  The first call on each device
  * looks the array's address up (and may load the module onto that device): make it before any
  * stream capture.  Calls whose kernels overlap on the GPU race on the shared scratch: order them on
- * one stream.  Returns MOE_FFN_OK or a negative code (nothing enqueued then). */
+ * one stream.  Returns MOE_FFN_OK or a negative code.  A CUDA error already pending from earlier
+ * work is reported as MOE_FFN_ERR_CUDA before anything is enqueued; every other negative code
+ * except a failed kernel launch also means nothing was enqueued (a failed launch comes after the
+ * memset). */
 int moe_ffn_hc_split_noalloc(const float *state, const uint16_t *hc_fn, const float *hc_scale,
                              const float *hc_base, int32_t rows, int32_t hc, int32_t hidden,
                              int32_t sinkhorn_iters, float rms_eps, float *pre, float *post, float *comb,
@@ -274,7 +279,10 @@ typedef struct moe_ffn_mxfp8_experts {
  * Synchronous.  Returns MOE_FFN_OK, LAYER_RANGE, NO_WEIGHTS, NULL_PTR, ALIGNMENT, NO_MEMORY or CUDA. */
 int moe_ffn_set_mxfp8_experts(moe_ffn_handle *h, int32_t layer, const moe_ffn_mxfp8_experts *w);
 
-/* Text of the last error on this handle (or of the last failed init when h is NULL). */
+/* Text of the last error on this handle, or, when h is NULL, of the last failed call made without
+ * a handle (init, the allocation-free split, a NULL handle) on the calling thread: that message
+ * is kept per thread, so threads that fail at the same time do not overwrite each other's text.
+ * The pointer stays valid until the same handle (or, for NULL, the same thread) fails again. */
 const char *moe_ffn_last_error(const moe_ffn_handle *h);
 
 /* Waits for outstanding work, frees everything the handle owns.  NULL is ignored. */

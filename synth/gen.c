@@ -10,11 +10,16 @@
  * where mix() is the SplitMix64 output function (Steele, Lea, Flood,
  * "Fast splittable pseudorandom number generators", OOPSLA 2014).
  *
- * Normal draws use a variance-matched Irwin-Hall(4) variate: the four 16-bit
- * fields of h_i are summed (an exact integer), centred, and scaled by one
- * correctly rounded multiply.  Only integer operations and single IEEE
- * multiplies/adds are involved, so x86-64 and AArch64 produce identical bits
- * (build with -ffp-contract=off so no multiply-add is fused).
+ * Normal draws use Marsaglia's polar method (G. Marsaglia, T. A. Bray, "A
+ * convenient method for generating normal variables", SIAM Review 6, 1964):
+ * pair j takes two signed 32-bit uniforms u, v in [-1, 1) from h_j, redraws
+ * them from a second stream while s = u^2 + v^2 is 0 or >= 1, and gives the
+ * normals u f and v f, f = sqrt(-2 ln(s) / s); element i is member i % 2 of
+ * pair i / 2.  The tails are those of a true normal (out to about 9.4 sigma
+ * with 32-bit uniforms).  ln is evaluated here from its series (exact range
+ * reduction, then 2 atanh) with IEEE +, -, *, / and sqrt only, so x86-64 and
+ * AArch64 produce identical bits (build with -ffp-contract=off so that no
+ * multiply-add is fused).
  */
 #include <math.h>
 #include <stdint.h>
@@ -34,13 +39,63 @@ uint64_t synth_key(uint64_t seed, uint32_t tensor, uint32_t attempt) {
 
 static inline uint64_t draw(uint64_t key, uint64_t i) { return mix64(key + (i + 1) * GOLDEN); }
 
-/* Irwin-Hall(4) of 16-bit uniforms, scaled to unit variance.  The sum of
- * four uniforms on {0..65535} has mean 131070 and variance (65536^2-1)/3. */
-static inline double unit_normal(uint64_t h) {
-  const double scale = 2.6428997921303018e-05; /* sqrt(3 / (65536^2 - 1)) */
-  int64_t s = (int64_t)(h & 0xFFFFu) + (int64_t)((h >> 16) & 0xFFFFu) +
-              (int64_t)((h >> 32) & 0xFFFFu) + (int64_t)(h >> 48);
-  return (double)(s - 131070) * scale;
+/* ln(s) for a normal double s > 0: s = m 2^e with m in [sqrt(1/2), sqrt(2)) by exact bit
+ * operations, then ln m = 2 atanh(t) = 2 (t + t^3/3 + t^5/5 + ...), t = (m - 1) / (m + 1),
+ * |t| <= 0.1716; fourteen terms leave a remainder below 1e-19. */
+static double ln_pos(double s) {
+  uint64_t u;
+  memcpy(&u, &s, 8);
+  int e = (int)((u >> 52) & 0x7FFu) - 1023;
+  u = (u & 0x000FFFFFFFFFFFFFULL) | 0x3FF0000000000000ULL; /* m in [1, 2) */
+  double m;
+  memcpy(&m, &u, 8);
+  if (m > 1.4142135623730951) {
+    m = m * 0.5;
+    e += 1;
+  }
+  const double t = (m - 1.0) / (m + 1.0);
+  const double t2 = t * t;
+  double p = 1.0 / 27.0;
+  for (int k = 12; k >= 0; --k) p = p * t2 + 1.0 / (double)(2 * k + 1);
+  return (double)e * 0.6931471805599453 + 2.0 * t * p;
+}
+
+/* The two normals of pair j of the stream `key` (polar method, see the file header). */
+static inline void normal_pair(uint64_t key, uint64_t j, double *z0, double *z1) {
+  const uint64_t key2 = mix64(key ^ 0x5851F42D4C957F2DULL);
+  uint64_t h = draw(key, j);
+  for (uint64_t a = 1; a <= 256; ++a) {
+    const double u = (double)((int64_t)(h >> 32) - 2147483648LL) * 4.656612873077393e-10; /* 2^-31 */
+    const double v = (double)((int64_t)(h & 0xFFFFFFFFu) - 2147483648LL) * 4.656612873077393e-10;
+    const double s = u * u + v * v;
+    if (s > 0.0 && s < 1.0) {
+      const double f = sqrt(-2.0 * ln_pos(s) / s);
+      *z0 = u * f;
+      *z1 = v * f;
+      return;
+    }
+    h = draw(key2, (j << 8) + a); /* rejected (probability 1 - pi/4): a fresh pair of uniforms */
+  }
+  *z0 = *z1 = 0.0; /* 256 rejections in a row: never seen (probability below 1e-170) */
+}
+
+/* Element i of the standard normal stream `key`. */
+static inline double unit_normal(uint64_t key, uint64_t i) {
+  double z0, z1;
+  normal_pair(key, i >> 1, &z0, &z1);
+  return (i & 1) ? z1 : z0;
+}
+
+/* Standard normals of elements start .. start+n-1 of the stream `key` into z (pairs drawn once). */
+static void normal_run(uint64_t key, uint64_t start, uint64_t n, double *z) {
+  uint64_t i = start;
+  const uint64_t end = start + n;
+  if (i < end && (i & 1)) {
+    z[0] = unit_normal(key, i);
+    ++i;
+  }
+  for (; i + 1 < end; i += 2) normal_pair(key, i >> 1, &z[i - start], &z[i + 1 - start]);
+  if (i < end) z[i - start] = unit_normal(key, i);
 }
 
 static inline uint16_t f32_to_bf16_rne(float f) {
@@ -50,16 +105,25 @@ static inline uint16_t f32_to_bf16_rne(float f) {
   return (uint16_t)(u >> 16);
 }
 
+#define RUN 2048 /* elements per parallel work item (even, so that no pair straddles two items) */
+
 /* out[j] = float(mean + sigma * z) for element indices start .. start+n-1. */
 void synth_normal_f32(uint64_t seed, uint32_t tensor, uint32_t attempt, uint64_t start,
                       uint64_t n, double mean, double sigma, float *out) {
   const uint64_t key = synth_key(seed, tensor, attempt);
+  const uint64_t first = start & ~(uint64_t)(RUN - 1), items = (start + n - first + RUN - 1) / RUN;
 #pragma omp parallel for schedule(static)
-  for (int64_t j = 0; j < (int64_t)n; ++j) {
-    double z = unit_normal(draw(key, start + (uint64_t)j));
-    double v = z * sigma;
-    v = v + mean;
-    out[j] = (float)v;
+  for (int64_t it = 0; it < (int64_t)items; ++it) {
+    double z[RUN];
+    uint64_t i0 = first + (uint64_t)it * RUN, i1 = i0 + RUN;
+    if (i0 < start) i0 = start;
+    if (i1 > start + n) i1 = start + n;
+    normal_run(key, i0, i1 - i0, z);
+    for (uint64_t i = i0; i < i1; ++i) {
+      double v = z[i - i0] * sigma;
+      v = v + mean;
+      out[i - start] = (float)v;
+    }
   }
 }
 
@@ -67,13 +131,20 @@ void synth_normal_f32(uint64_t seed, uint32_t tensor, uint32_t attempt, uint64_t
 void synth_normal_bf16(uint64_t seed, uint32_t tensor, uint32_t attempt, uint64_t start,
                        uint64_t n, double mean, double sigma, double gain, uint16_t *out) {
   const uint64_t key = synth_key(seed, tensor, attempt);
+  const uint64_t first = start & ~(uint64_t)(RUN - 1), items = (start + n - first + RUN - 1) / RUN;
 #pragma omp parallel for schedule(static)
-  for (int64_t j = 0; j < (int64_t)n; ++j) {
-    double z = unit_normal(draw(key, start + (uint64_t)j));
-    double v = z * sigma;
-    v = v + mean;
-    v = v * gain;
-    out[j] = f32_to_bf16_rne((float)v);
+  for (int64_t it = 0; it < (int64_t)items; ++it) {
+    double z[RUN];
+    uint64_t i0 = first + (uint64_t)it * RUN, i1 = i0 + RUN;
+    if (i0 < start) i0 = start;
+    if (i1 > start + n) i1 = start + n;
+    normal_run(key, i0, i1 - i0, z);
+    for (uint64_t i = i0; i < i1; ++i) {
+      double v = z[i - i0] * sigma;
+      v = v + mean;
+      v = v * gain;
+      out[i - start] = f32_to_bf16_rne((float)v);
+    }
   }
 }
 
@@ -86,9 +157,11 @@ void synth_normal_rows_f32(uint64_t seed, uint32_t tensor, const int32_t *attemp
   for (int64_t r = 0; r < (int64_t)rows; ++r) {
     const uint64_t key = synth_key(seed, tensor, (uint32_t)attempts[r]);
     const uint64_t base = ((uint64_t)r + row0) * row_len;
-    for (uint64_t c = 0; c < row_len; ++c) {
-      double z = unit_normal(draw(key, base + c));
-      out[(uint64_t)r * row_len + c] = (float)(z * sigma);
+    double z[RUN];
+    for (uint64_t c0 = 0; c0 < row_len; c0 += RUN) {
+      const uint64_t m = row_len - c0 < RUN ? row_len - c0 : RUN;
+      normal_run(key, base + c0, m, z);
+      for (uint64_t c = 0; c < m; ++c) out[(uint64_t)r * row_len + c0 + c] = (float)(z[c] * sigma);
     }
   }
 }
@@ -197,9 +270,10 @@ void synth_normal_mxfp8(uint64_t seed, uint32_t tensor, uint64_t start, uint64_t
 #pragma omp parallel for schedule(static)
   for (int64_t b = 0; b < (int64_t)(n / 32); ++b) {
     float v[32];
+    double z[32];
+    normal_run(key, start + (uint64_t)(32 * b), 32, z);
     for (int k = 0; k < 32; ++k) {
-      double z = unit_normal(draw(key, start + (uint64_t)(32 * b + k)));
-      double x = z * sigma;
+      double x = z[k] * sigma;
       x = x + 0.0;
       v[k] = (float)x;
     }

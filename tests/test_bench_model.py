@@ -1,4 +1,4 @@
-"""The bench's algorithmic byte models (CPU): the figures the design doc and the JSON line report."""
+"""The bench's algorithmic byte models (CPU): the per-kernel byte figures its JSON line reports."""
 from dataclasses import replace
 
 import numpy as np

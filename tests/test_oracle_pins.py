@@ -134,6 +134,75 @@ def test_hc_post_orientation_and_post_term():
 
 # ---- routing -------------------------------------------------------------------------------------
 
+# ---- router projection (raw_matmul "MoE gate") ---------------------------------------------------
+
+def test_router_logits_brute_force_rows_are_experts():
+    # logits[r, e] = sum_d x[r, d] * gate[e, d]: gate rows are experts (a transposed operand or a
+    # sum over the wrong axis fails; the shapes are chosen so that both would still run)
+    x = RNG.standard_normal((3, 5))
+    g = RNG.standard_normal((5, 5))
+    got = O.router_logits(x, g)
+    for r in range(3):
+        for e in range(5):
+            assert abs(got[r, e] - sum(x[r, d] * g[e, d] for d in range(5))) < 1e-12
+    assert not np.allclose(got, x @ g)
+
+
+def test_router_logits_of_the_tiny_workload_by_loops():
+    # the block's logits are the dots of its own ffn_norm rows with the widened gate rows
+    case = synth.Case(synth.CONFIGS["c0_tiny"])
+    st = oracle.prelude_and_route(case)
+    gate = synth.bf16_bits_to_f32(case.gate).astype(np.float64)
+    xf = st["ffn_norm"]
+    c = case.cfg
+    for r in range(c.rows):
+        for e in range(c.experts):
+            ref = 0.0
+            for d in range(c.hidden):
+                ref += xf[r, d] * gate[e, d]
+            assert abs(st["logits"][r, e] - ref) < 1e-12 * (1 + abs(ref))
+
+
+class _HandCase:
+    """A one-row block with hc = 1 and zero HC weights (so pre = sigmoid(0) = 1/2), written out."""
+
+    def __init__(self, state_row, norm_w, gate_rows, eps=0.0):
+        hidden = len(state_row)
+        experts = len(gate_rows)
+        from types import SimpleNamespace
+        self.cfg = SimpleNamespace(rows=1, hc=1, hidden=hidden, experts=experts, top_k=1, rms_eps=eps,
+                                   sinkhorn_iters=20, is_hash=False, vocab=16)
+        self.state = np.asarray(state_row, np.float32).reshape(1, 1, hidden)
+        self.hc_fn = np.zeros((3, hidden), np.uint16)
+        self.hc_scale = np.ones(3, np.float32)
+        self.hc_base = np.zeros(3, np.float32)
+        self.ffn_norm = np.asarray(norm_w, np.float32)
+        self.gate = _bf16_bits(gate_rows)
+        self.exp_probs_b = np.zeros(experts, np.float32)
+        self.token_ids = np.zeros(1, np.int32)
+        self.tid2eid = None
+
+
+def test_router_reads_the_normalised_input():
+    # state [4, 3, 0, 0] -> ffn_input = pre * state = [2, 1.5, 0, 0]; mean square 1.5625, so with
+    # eps 0 the RMS is 1.25 and ffn_norm = [1.6, 1.2, 0, 0] * w = [0.8, 1.8, 0, 0] for
+    # w = [0.5, 1.5, 1, 1].  Gate rows e0 = d0, e1 = d1: logits [0.8, 1.8] choose expert 1, while
+    # the same projection of ffn_input ([2, 1.5]), of the state ([4, 3]) or of the unweighted
+    # normalised input ([1.6, 1.2]) would choose expert 0.
+    case = _HandCase([4.0, 3.0, 0.0, 0.0], [0.5, 1.5, 1.0, 1.0],
+                     [[1.0, 0.0, 0.0, 0.0], [0.0, 1.0, 0.0, 0.0]])
+    st = oracle.prelude_and_route(case)
+    assert np.allclose(st["pre"], 0.5, rtol=0, atol=0)
+    assert np.allclose(st["ffn_input"], [[2.0, 1.5, 0.0, 0.0]], rtol=1e-15)
+    assert np.allclose(st["ffn_norm"], [[0.8, 1.8, 0.0, 0.0]], rtol=1e-15)
+    assert np.allclose(st["logits"], [[0.8, 1.8]], rtol=1e-15)
+    assert st["indices"].tolist() == [[1]] and st["weights"].tolist() == [[1.0]]
+    # the eps term sits inside the square root of the norm: eps = 0.4375 makes the RMS sqrt(2)
+    st = oracle.prelude_and_route(_HandCase([4.0, 3.0, 0.0, 0.0], [1.0, 1.0, 1.0, 1.0],
+                                            [[1.0, 0.0, 0.0, 0.0], [0.0, 1.0, 0.0, 0.0]], eps=0.4375))
+    assert np.allclose(st["logits"], [[2 / math.sqrt(2), 1.5 / math.sqrt(2)]], rtol=1e-15)
+
+
 def test_score_route_brute_force_subsets_tiny():
     case = synth.Case(synth.CONFIGS["c0_tiny"])
     st = oracle.prelude_and_route(case)

@@ -15,13 +15,37 @@ def test_deterministic_and_offset_consistent():
     assert not np.array_equal(a, synth.normal_f32(7, synth.T_GATE, 1000))
 
 
-def test_normal_moments():
-    z = synth.normal_f32(3, synth.T_GATE, 1 << 20).astype(np.float64)
-    assert abs(z.mean()) < 5e-3
-    assert abs(z.std() - 1.0) < 5e-3
-    # Irwin-Hall(4) has excess kurtosis -6/(5*4) = -0.3
-    k = np.mean((z - z.mean()) ** 4) / z.var() ** 2 - 3
-    assert abs(k + 0.3) < 0.02
+def test_normal_moments_and_tails():
+    z = synth.normal_f32(3, synth.T_GATE, 1 << 22).astype(np.float64)
+    assert abs(z.mean()) < 3e-3
+    assert abs(z.std() - 1.0) < 3e-3
+    k = np.mean((z - z.mean()) ** 4) / z.var() ** 2 - 3  # a normal's excess kurtosis is 0
+    assert abs(k) < 0.03
+    # tails of a true normal: P(|z| > 3.5) = 4.65e-4, P(|z| > 4) = 6.33e-5 (unbounded, unlike a
+    # sum of a few uniforms); counts within 5 binomial standard deviations
+    for t, p in ((3.5, 4.6525e-4), (4.0, 6.3342e-5)):
+        n, c = z.size, int(np.sum(np.abs(z) > t))
+        assert abs(c - n * p) < 5 * np.sqrt(n * p), (t, c, n * p)
+    assert np.abs(z).max() > 4.5
+
+
+def test_normal_against_the_normal_cdf():
+    # Kolmogorov-Smirnov distance of 2^20 draws from Phi, written with math.erf
+    import math
+    z = np.sort(synth.normal_f32(11, synth.T_STATE, 1 << 20).astype(np.float64))
+    cdf = 0.5 * (1.0 + np.vectorize(math.erf)(z / math.sqrt(2.0)))
+    n = z.size
+    d = max(np.max(np.arange(1, n + 1) / n - cdf), np.max(cdf - np.arange(n) / n))
+    assert d < 1.63 / np.sqrt(n)  # the 1 % critical value
+
+
+def test_pairs_split_across_calls_and_rows():
+    # an odd start takes the second member of a pair; row draws equal flat draws of the same stream
+    a = synth.normal_f32(9, synth.T_STATE, 4099)
+    for s0, n in ((1, 7), (2047, 3), (2048, 2051), (4097, 2)):
+        assert np.array_equal(a[s0:s0 + n], synth.normal_f32(9, synth.T_STATE, n, start=s0))
+    rows = synth.normal_rows_f32(9, synth.T_STATE, np.zeros(2, np.int32), 2049)
+    assert np.array_equal(rows.ravel(), a[: 2 * 2049])
 
 
 def test_bf16_is_round_to_nearest_even_of_f32_draw():
