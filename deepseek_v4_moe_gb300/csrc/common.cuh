@@ -316,6 +316,35 @@ __device__ __forceinline__ uint32_t idesc_f16_f32(int M, int N) {
   return d;
 }
 
+// Instruction descriptor, kind::f16 with bf16 A and B (K-major), f32 accumulator, shape M x N.
+__device__ __forceinline__ uint32_t idesc_bf16_f32(int M, int N) {
+  uint32_t d = 0;
+  d |= 1u << 4;                                      // D format: f32
+  d |= 1u << 7;                                      // A format: bf16
+  d |= 1u << 10;                                     // B format: bf16
+  d |= (uint32_t)(N >> 3) << 17;
+  d |= (uint32_t)(M >> 4) << 24;
+  return d;
+}
+
+// x rounded to bf16 (nearest, ties to even), kept as an f32 whose low 16 bits are zero.  Integer
+// operations only.  For finite x the difference x - round_bf16(x) is exact in f32.
+__device__ __forceinline__ float round_bf16(float x) {
+  uint32_t u = __float_as_uint(x);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return __uint_as_float(u & 0xFFFF0000u);
+}
+
+// Two bf16-valued floats (low 16 bits zero) packed as a bf16 pair: a in the low half, b in the high.
+__device__ __forceinline__ uint32_t pack_bf16_pair(float a, float b) {
+  return __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x7632);
+}
+
+// Fire-and-forget f64 add in global memory (performed at the L2; no return value).
+__device__ __forceinline__ void red_add_f64(double *p, double v) {
+  asm volatile("red.global.add.f64 [%0], %1;" ::"l"(p), "d"(v) : "memory");
+}
+
 __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                            uint32_t accumulate) {
   asm volatile(

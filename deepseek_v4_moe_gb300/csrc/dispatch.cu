@@ -1,11 +1,12 @@
-// Token -> expert dispatch of the rows > 4 path, and the slot reduce + hc_post that closes it.
+// Token -> expert dispatch of the rows > 4 path, and the hc_post kernel that closes it.
 //
 // The pages' mm_id path (expert_matmul with IdMmScratch in forward_ffn_rows, docs.rs "hf2q 0.1.3
 // .../deepseek4/ffn_forward.rs") groups routed rows by expert; here that is a histogram (counted by
 // the router), an exclusive scan, a tile list for the persistent grouped GEMMs, and a scatter of
-// (row, slot) pairs with their fp16 activation rows into expert-sorted order.  The shared expert is
-// the last group and holds every row.  The order of rows inside a group comes from atomics and
-// does not affect any result: each token's output column is computed alone.
+// (row, slot) pairs with their activation rows (as bf16 hi and lo planes) into expert-sorted
+// order.  The shared expert is the last group and holds every row.  The order of rows inside a
+// group comes from atomics and does not affect the GEMMs' results: each token's output column is
+// computed alone.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -87,12 +88,14 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(int *__restrict__ cou
   }
 }
 
-// One warp per (row, slot), slot top_k being the shared expert.
+// One warp per (row, slot), slot top_k being the shared expert: claims the pair's position in its
+// group, then writes the row's normalised input as two bf16 planes, hi = rn(x) at row pos of x2
+// and lo = rn(x - hi) at row plane_rows + pos.
 __global__ void __launch_bounds__(256) scatter_kernel(const int *__restrict__ idx, const float *__restrict__ rw,
                                                       const float *__restrict__ x, int rows, int K, int E, int D,
                                                       const int *__restrict__ offsets, int *__restrict__ cursor,
                                                       int2 *__restrict__ list, float *__restrict__ list_w,
-                                                      __half *__restrict__ x16) {
+                                                      uint16_t *__restrict__ x2, int plane_rows) {
   const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (w >= rows * (K + 1)) return;
@@ -116,16 +119,21 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int *__restrict__ id
   }
   pos = __shfl_sync(0xffffffffu, pos, 0);
   const float *src = x + (size_t)r * D;
-  __half *dst = x16 + (size_t)pos * D;
+  uint16_t *dhi = x2 + (size_t)pos * D, *dlo = x2 + ((size_t)plane_rows + pos) * D;
   for (int c = lane * 8; c < D; c += 256) {
     const float4 a = *reinterpret_cast<const float4 *>(src + c);
     const float4 b = *reinterpret_cast<const float4 *>(src + c + 4);
-    __half2 h[4];
-    h[0] = __floats2half2_rn(a.x, a.y);
-    h[1] = __floats2half2_rn(a.z, a.w);
-    h[2] = __floats2half2_rn(b.x, b.y);
-    h[3] = __floats2half2_rn(b.z, b.w);
-    *reinterpret_cast<uint4 *>(dst + c) = *reinterpret_cast<uint4 *>(h);
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float h[8], l[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      h[j] = round_bf16(v[j]);
+      l[j] = round_bf16(v[j] - h[j]);
+    }
+    *reinterpret_cast<uint4 *>(dhi + c) = make_uint4(pack_bf16_pair(h[0], h[1]), pack_bf16_pair(h[2], h[3]),
+                                                     pack_bf16_pair(h[4], h[5]), pack_bf16_pair(h[6], h[7]));
+    *reinterpret_cast<uint4 *>(dlo + c) = make_uint4(pack_bf16_pair(l[0], l[1]), pack_bf16_pair(l[2], l[3]),
+                                                     pack_bf16_pair(l[4], l[5]), pack_bf16_pair(l[6], l[7]));
   }
 }
 
@@ -135,80 +143,25 @@ void launch_dispatch(const Dims &d, const Scratch &s, int rows, cudaStream_t st,
   stage(tm, "build_tiles", st);
   const int warps = rows * (d.top_k + 1);
   scatter_kernel<<<(warps + 7) / 8, 256, 0, st>>>(s.idx, s.rw, s.ffn_norm, rows, d.top_k, d.experts, d.hidden,
-                                                  s.offsets, s.cursor, s.list, s.list_w, s.x16);
+                                                  s.offsets, s.cursor, s.list, s.list_w, s.x2, s.max_positions);
   stage(tm, "scatter", st);
 }
 
-// ffn_out[r] = sum of the weighted slot outputs of row r (valid routed slots + shared);
-// out[r, i] = post[r, i] * ffn_out[r] + sum_j comb[r, i, j] * state[r, j].
-__global__ void __launch_bounds__(256) prefill_post_kernel(const float *__restrict__ y_slot,
-                                                           const int *__restrict__ idx, int K, int E,
-                                                           const float *__restrict__ state,
-                                                           const float *__restrict__ post,
-                                                           const float *__restrict__ comb, int D, int hc,
-                                                           float *__restrict__ ffn_out,
-                                                           float *__restrict__ out) {
-  const int r = blockIdx.x;
-  __shared__ int valid[kTopKMax];
-  __shared__ float pc[kHcMax + kHcMax * kHcMax];
-  if (threadIdx.x < K) {
-    const int e = idx[(size_t)r * K + threadIdx.x];
-    valid[threadIdx.x] = e >= 0 && e < E;
-  }
-  if (threadIdx.x < hc) pc[threadIdx.x] = post[(size_t)r * hc + threadIdx.x];
-  if (threadIdx.x < hc * hc) pc[kHcMax + threadIdx.x] = comb[(size_t)r * hc * hc + threadIdx.x];
-  __syncthreads();
-  const float *ys = y_slot + (size_t)r * (K + 1) * D;
-  for (int d = threadIdx.x * 4; d < D; d += blockDim.x * 4) {
-    float4 f = *reinterpret_cast<const float4 *>(ys + (size_t)K * D + d);
-#pragma unroll
-    for (int k = 0; k < kTopKMax; ++k) {
-      if (k >= K || !valid[k]) continue;
-      const float4 y = *reinterpret_cast<const float4 *>(ys + (size_t)k * D + d);
-      f.x += y.x;
-      f.y += y.y;
-      f.z += y.z;
-      f.w += y.w;
-    }
-    *reinterpret_cast<float4 *>(ffn_out + (size_t)r * D + d) = f;
-    float4 sv[kHcMax];
-#pragma unroll
-    for (int j = 0; j < kHcMax; ++j)
-      sv[j] = j < hc ? *reinterpret_cast<const float4 *>(state + ((size_t)r * hc + j) * D + d)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int o = 0; o < kHcMax; ++o) {
-      if (o >= hc) break;
-      const float p = pc[o];
-      float4 v = make_float4(p * f.x, p * f.y, p * f.z, p * f.w);
-#pragma unroll
-      for (int j = 0; j < kHcMax; ++j) {
-        if (j >= hc) break;
-        const float c = pc[kHcMax + o * hc + j];
-        v.x += c * sv[j].x;
-        v.y += c * sv[j].y;
-        v.z += c * sv[j].z;
-        v.w += c * sv[j].w;
-      }
-      *reinterpret_cast<float4 *>(out + ((size_t)r * hc + o) * D + d) = v;
-    }
-  }
-}
-
-void launch_prefill_post(const Dims &d, const Scratch &s, const float *state, int rows, float *out_state,
-                         cudaStream_t st, StageTimer *tm) {
-  prefill_post_kernel<<<rows, 256, 0, st>>>(s.y_slot, s.idx, d.top_k, d.experts, state, s.post, s.comb, d.hidden,
-                                            d.hc, s.ffn_out, out_state);
-  stage(tm, "post", st);
-}
-
-// hc_post of a sublayer whose output f is given (the attention sublayer's output projection, or
-// any body): out[r, i, d] = post[r, i] * f[r, d] + sum_j comb[r, i, j] * state[r, j, d].  One
-// thread per (row, 4 columns), a row's post and comb staged once per CTA.  Every byte is read or
-// written once, so loads and stores take the streaming (evict-first) path.
+// hc_post of a sublayer whose output f is given (the FFN's ffn_out on the rows > 4 path, the
+// attention sublayer's output projection, or any body): out[r, i, d] = post[r, i] * f[r, d] +
+// sum_j comb[r, i, j] * state[r, j, d].  One thread per (row, 4 columns), a row's post and comb
+// staged once per CTA.  Every byte is read or written once, so loads and stores take the streaming
+// (evict-first) path.
 constexpr int kHcPostThreads = 128;
 
-__global__ void __launch_bounds__(kHcPostThreads) hc_post_kernel(const float *__restrict__ f,
+__device__ __forceinline__ float4 ld_f4_stream(const float *p) { return __ldcs(reinterpret_cast<const float4 *>(p)); }
+__device__ __forceinline__ float4 ld_f4_stream(const double *p) {
+  const double2 a = __ldcs(reinterpret_cast<const double2 *>(p)), b = __ldcs(reinterpret_cast<const double2 *>(p) + 1);
+  return make_float4((float)a.x, (float)a.y, (float)b.x, (float)b.y);  // the f64 FFN output rounded to f32 once
+}
+
+template <typename F>
+__global__ void __launch_bounds__(kHcPostThreads) hc_post_kernel(const F *__restrict__ f,
                                                                   const float *__restrict__ state,
                                                                   const float *__restrict__ post,
                                                                   const float *__restrict__ comb, int D, int hc,
@@ -220,7 +173,7 @@ __global__ void __launch_bounds__(kHcPostThreads) hc_post_kernel(const float *__
   if (threadIdx.x < hc * hc) pc[kHcMax + threadIdx.x] = comb[(size_t)r * hc * hc + threadIdx.x];
   __syncthreads();
   if (d >= D) return;
-  const float4 fv = __ldcs(reinterpret_cast<const float4 *>(f + (size_t)r * D + d));
+  const float4 fv = ld_f4_stream(f + (size_t)r * D + d);
   float4 sv[kHcMax];
 #pragma unroll
   for (int j = 0; j < kHcMax; ++j)
@@ -244,11 +197,22 @@ __global__ void __launch_bounds__(kHcPostThreads) hc_post_kernel(const float *__
   }
 }
 
+template <typename F>
+static void hc_post_launch(const Dims &d, const F *f, const float *state, const float *post, const float *comb,
+                           int rows, float *out_state, cudaStream_t st) {
+  const int per_row = (d.hidden / 4 + kHcPostThreads - 1) / kHcPostThreads;
+  hc_post_kernel<F><<<(unsigned)rows * per_row, kHcPostThreads, 0, st>>>(f, state, post, comb, d.hidden, d.hc, per_row,
+                                                                        out_state);
+}
+
 void launch_hc_post(const Dims &d, const float *f, const float *state, const float *post, const float *comb,
                     int rows, float *out_state, cudaStream_t st) {
-  const int per_row = (d.hidden / 4 + kHcPostThreads - 1) / kHcPostThreads;
-  hc_post_kernel<<<(unsigned)rows * per_row, kHcPostThreads, 0, st>>>(f, state, post, comb, d.hidden, d.hc, per_row,
-                                                                     out_state);
+  hc_post_launch(d, f, state, post, comb, rows, out_state, st);
+}
+
+void launch_hc_post(const Dims &d, const double *f, const float *state, const float *post, const float *comb,
+                    int rows, float *out_state, cudaStream_t st) {
+  hc_post_launch(d, f, state, post, comb, rows, out_state, st);
 }
 
 }  // namespace moe

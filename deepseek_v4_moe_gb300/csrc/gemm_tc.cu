@@ -3,24 +3,37 @@
 //
 // docs.rs "hf2q 0.1.3 .../deepseek4/ffn_forward.rs", forward_ffn_rows: expert_matmul "routed
 // gate"/"routed up" + raw_matmul "shared gate"/"shared up" + dispatch_deepseek_moe_swiglu (fused
-// into the gate/up epilogue), and expert_matmul "routed down" + raw_matmul "shared down" with the
-// route weight of dispatch_deepseek_moe_weighted_reduce applied in the down epilogue.
+// into the gate/up epilogue), and expert_matmul "routed down" + raw_matmul "shared down" +
+// dispatch_deepseek_moe_weighted_reduce (fused into the down epilogue: each token's output column,
+// times its route weight, is added into the row's FFN output).
+//
+// The reduce: a row's top_k + 1 contributions come from different expert tiles, finished by
+// different CTAs in no fixed order.  Each contribution is rounded to f32 (y * w, as an f32 reduce
+// would take it) and added in f64 at the L2 (red.global.add.f64) into a zeroed f64 row.  The sum
+// of at most 9 f32 values is exact in f64 whenever their magnitudes lie within a factor 2^25 of
+// each other, so the result, rounded to f32 once by hc_post, does not depend on the order the
+// tiles finish in; only a contribution below 2^-25 of a larger one can leave a last-bit difference
+// between runs.
 //
 // Layout ("swap AB"): the expert's weight rows are the MMA's M = 128 side (operand A), the
 // expert's tokens the N side (operand B, N = 16..128 by tile), K = hidden (gate/up) or inter
 // (down), 64 per pipeline stage.  So a weight tile is read from HBM once per 128 tokens of its
 // expert however few tokens that is.  The shared expert is group `experts` (every row), so one
-// persistent launch covers routed and shared work.  Operands are fp16 (the weights' bf16 values
-// are exact in fp16 above 2^-14; activations get an 11-bit significand), accumulation is f32 in
-// TMEM.
+// persistent launch covers routed and shared work.
+//
+// Precision: the weights are the caller's bf16 matrices, read by TMA as they are.  The activations
+// (the normalised input for gate/up, the SwiGLU output for down) are f32 values held as two bf16
+// planes, hi = rn(x) and lo = rn(x - hi), so |x - hi - lo| <= 2^-16 |x|; two MMAs per k-step (hi
+// and lo against the same weight tile) accumulate in f32 in TMEM, and bf16 x bf16 products are
+// exact there.
 //
 // Roles per CTA (320 threads, one CTA per SM, persistent over a device-built tile list):
-//   warp 0     TMA producer: A (gate and up, or down) and B tiles into a multi-stage smem ring
+//   warp 0     TMA producer: A (gate and up, or down) and the two B planes into a multi-stage ring
 //   warp 1     TMEM allocator and MMA issuer (one thread), commits free smem stages / TMEM
 //   warps 2-9  epilogue: tcgen05.ld of the accumulator (double buffered in TMEM, so the next
-//              tile's MMAs run under this tile's epilogue), SwiGLU or route-weight scaling; two
-//              warps per TMEM lane quarter, each every other 16-column chunk, so that the
-//              epilogue keeps up with the MMAs
+//              tile's MMAs run under this tile's epilogue); SwiGLU and the hi/lo split of its
+//              output (gate/up), or route-weight scaling and the reduction into the FFN output (down);
+//              two warps per TMEM lane quarter, each every other 16-column chunk
 // Every mbarrier wait is bounded (2 s); on expiry the CTA raises the device timeout bit, all roles
 // leave their loops, and TMEM is freed before the kernel returns.
 #include <cuda.h>
@@ -31,17 +44,18 @@
 namespace moe {
 
 constexpr int BM = 128, BN = 128, BK = 64, UMMA_K = 16;
-constexpr int kTileBytes = BM * BK * 2;  // 16 KB: one 128 x 64 fp16 tile (A and B alike)
+constexpr int kTileBytes = BM * BK * 2;  // 16 KB: one 128 x 64 bf16 tile (A and B planes alike)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 template <bool GATEUP>
 struct GemmCfg {
-  static constexpr int kStages = GATEUP ? 4 : 6;
+  static constexpr int kStages = GATEUP ? 3 : 4;
   static constexpr int kATiles = GATEUP ? 2 : 1;
-  static constexpr int kStageBytes = (kATiles + 1) * kTileBytes;
+  static constexpr int kStageBytes = (kATiles + 2) * kTileBytes;  // A tiles, then B hi and B lo
   static constexpr int kAccCols = GATEUP ? 2 * BN : BN;  // gate and up accumulators side by side
   static constexpr int kTmemCols = 2 * kAccCols;         // two accumulator buffers
   static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 1024;
+  static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
 };
 
 struct GemmArgs {
@@ -50,10 +64,10 @@ struct GemmArgs {
   const int *offsets;  // first list position of each group
   const int2 *list;    // (row, slot) per position
   const float *list_w;
-  __half *act16;       // [positions, inter]
-  float *y_slot;       // [rows, top_k + 1, hidden]
+  uint16_t *act2;      // [2 * plane_rows, inter] bf16: SwiGLU output hi plane, then lo plane
+  double *ffn_acc;     // [rows, hidden], zero on entry to the down GEMM
   int *status;
-  int inter, hidden, top_k, k_blocks, a_rows_per_group, which;
+  int inter, hidden, k_blocks, a_rows_per_group, which, experts, plane_rows;
 };
 
 constexpr int kEpiWarps = 8, kGemmThreads = 32 * (2 + kEpiWarps);
@@ -61,6 +75,7 @@ constexpr int kEpiWarps = 8, kGemmThreads = 32 * (2 + kEpiWarps);
 template <bool GATEUP>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                        const __grid_constant__ CUtensorMap tmS0, const __grid_constant__ CUtensorMap tmS1,
                         const __grid_constant__ CUtensorMap tmB, GemmArgs a) {
   using C = GemmCfg<GATEUP>;
   extern __shared__ uint8_t smem_raw[];
@@ -82,7 +97,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     abort_flag = 0;
     fence_mbar_init();
     tmap_prefetch(&tmA0);
-    if (GATEUP) tmap_prefetch(&tmA1);
+    tmap_prefetch(&tmS0);
+    if (GATEUP) {
+      tmap_prefetch(&tmA1);
+      tmap_prefetch(&tmS1);
+    }
     tmap_prefetch(&tmB);
   }
   if (warp == 1) tmem_alloc(&tmem_base, C::kTmemCols);
@@ -99,15 +118,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t phase = 0;
     for (int t = blockIdx.x; t < ntiles && !*abort_p; t += gridDim.x) {
       const int4 tl = a.tiles[t];
-      const int a_row = tl.x * a.a_rows_per_group + tl.y * BM;
+      const bool shared = tl.x == a.experts;  // the shared expert's matrices are separate tensors
+      const CUtensorMap *m0 = shared ? &tmS0 : &tmA0;
+      const CUtensorMap *m1 = shared ? &tmS1 : &tmA1;
+      const int a_row = (shared ? 0 : tl.x * a.a_rows_per_group) + tl.y * BM;
       const int b_row = a.offsets[tl.x] + tl.z * BN;
       for (int kb = 0; kb < a.k_blocks; ++kb) {
         if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_p, a.status, kWaitLimitNs)) break;
         mbar_arrive_expect_tx(&full_bar[stage], C::kStageBytes);
         uint8_t *base = smem + (size_t)stage * C::kStageBytes;
-        tma_load_2d(base, &tmA0, &full_bar[stage], kb * BK, a_row);
-        if (GATEUP) tma_load_2d(base + kTileBytes, &tmA1, &full_bar[stage], kb * BK, a_row);
-        tma_load_2d(base + C::kATiles * kTileBytes, &tmB, &full_bar[stage], kb * BK, b_row);
+        tma_load_2d(base, m0, &full_bar[stage], kb * BK, a_row);
+        if (GATEUP) tma_load_2d(base + kTileBytes, m1, &full_bar[stage], kb * BK, a_row);
+        uint8_t *bp = base + C::kATiles * kTileBytes;
+        tma_load_2d(bp, &tmB, &full_bar[stage], kb * BK, b_row);
+        tma_load_2d(bp + kTileBytes, &tmB, &full_bar[stage], kb * BK, a.plane_rows + b_row);
         if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1u;
@@ -126,7 +150,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
       if (!mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1u, abort_p, a.status, kWaitLimitNs)) break;
       tc_fence_after();
-      const uint32_t idesc = idesc_f16_f32(BM, n_mma);
+      const uint32_t idesc = idesc_bf16_f32(BM, n_mma);
       const uint32_t d0 = tmem + (uint32_t)(acc * C::kAccCols);
       bool ok = true;
       for (int kb = 0; kb < a.k_blocks; ++kb) {
@@ -140,9 +164,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
         for (int k = 0; k < BK / UMMA_K; ++k) {
           const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
-          const uint64_t bdesc = smem_desc_sw128(sb + k * UMMA_K * 2);
-          tc_mma_f16(d0, smem_desc_sw128(sa + k * UMMA_K * 2), bdesc, idesc, accum);
-          if (GATEUP) tc_mma_f16(d0 + BN, smem_desc_sw128(sa + kTileBytes + k * UMMA_K * 2), bdesc, idesc, accum);
+          const uint64_t bhi = smem_desc_sw128(sb + k * UMMA_K * 2);
+          const uint64_t blo = smem_desc_sw128(sb + kTileBytes + k * UMMA_K * 2);
+          const uint64_t a0 = smem_desc_sw128(sa + k * UMMA_K * 2);
+          tc_mma_f16(d0, a0, bhi, idesc, accum);
+          tc_mma_f16(d0, a0, blo, idesc, 1u);
+          if (GATEUP) {
+            const uint64_t a1 = smem_desc_sw128(sa + kTileBytes + k * UMMA_K * 2);
+            tc_mma_f16(d0 + BN, a1, bhi, idesc, accum);
+            tc_mma_f16(d0 + BN, a1, blo, idesc, 1u);
+          }
         }
         tc_commit(&empty_bar[stage]);
         if (++stage == C::kStages) {
@@ -158,7 +189,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;  // which 16-column chunks of the quarter's rows
     const int row = q * 32 + lane;
-    const int K1 = a.top_k + 1;
+    bool nonfinite = false;
     int it = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
       const int4 tl = a.tiles[t];
@@ -173,18 +204,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const int pos0 = a.offsets[tl.x] + tl.z * BN;
       const int n_valid = tl.w;
+      const int m = tl.y * BM + row;  // this lane's weight row: a column of inter (gate/up) or hidden (down)
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
       for (int c0 = half * 16; c0 < n_valid; c0 += 32) {
         if (GATEUP) {
           float gv[16], uv[16];
           tmem_ld16(tbase + c0, gv);
           tmem_ld16(tbase + BN + c0, uv);
-          __half *dst = a.act16 + (size_t)(pos0 + c0) * a.inter + tl.y * BM + row;
+          uint16_t *dst = a.act2 + (size_t)(pos0 + c0) * a.inter + m;
+          const size_t lo_off = (size_t)a.plane_rows * a.inter;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             if (c0 + j < n_valid) {
               const float g = gv[j];
-              dst[(size_t)j * a.inter] = __float2half_rn(g * sigmoidf_(g) * uv[j]);
+              const float v = g * sigmoidf_(g) * uv[j];
+              nonfinite |= !isfinite(v);
+              const float hi = round_bf16(v);
+              const float lo = round_bf16(v - hi);
+              dst[(size_t)j * a.inter] = (uint16_t)(__float_as_uint(hi) >> 16);
+              dst[lo_off + (size_t)j * a.inter] = (uint16_t)(__float_as_uint(lo) >> 16);
             }
           }
         } else {
@@ -195,8 +233,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (c0 + j < n_valid) {
               const int p = pos0 + c0 + j;
               const int2 rk = a.list[p];
-              const float w = a.list_w[p];
-              a.y_slot[((size_t)rk.x * K1 + rk.y) * a.hidden + tl.y * BM + row] = yv[j] * w;
+              const float v = yv[j] * a.list_w[p];
+              nonfinite |= !isfinite(v);
+              red_add_f64(a.ffn_acc + (size_t)rk.x * a.hidden + m, (double)v);
             }
           }
         }
@@ -205,6 +244,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty_bar[acc]);
     }
+    if (__any_sync(0xffffffffu, nonfinite) && lane == 0) atomicOr(a.status, kDevNonFinite);
   }
   tc_fence_before();
   __syncthreads();
@@ -224,72 +264,57 @@ cudaError_t gemm_configure() {
                               (int)GemmCfg<false>::kSmem);
 }
 
-void launch_grouped_gemms(const Dims &d, const Scratch &s, const LayerDev &w, const CUtensorMap &tm_x16,
-                          const CUtensorMap &tm_act16, int num_sms, cudaStream_t st, StageTimer *tm) {
+void launch_grouped_gemms(const Dims &d, const Scratch &s, const LayerDev &w, const CUtensorMap &tm_x2,
+                          const CUtensorMap &tm_act2, int num_sms, cudaStream_t st, StageTimer *tm) {
   GemmArgs a;
   a.tiles = s.tiles_gu;
   a.n_tiles = s.n_tiles;
   a.offsets = s.offsets;
   a.list = s.list;
   a.list_w = s.list_w;
-  a.act16 = s.act16;
-  a.y_slot = s.y_slot;
+  a.act2 = s.act2;
+  a.ffn_acc = s.ffn_acc;
   a.status = s.status;
   a.inter = d.inter;
   a.hidden = d.hidden;
-  a.top_k = d.top_k;
   a.k_blocks = d.hidden / BK;
   a.a_rows_per_group = d.inter;
   a.which = 0;
+  a.experts = d.experts;
+  a.plane_rows = s.max_positions;
   const int grid_gu = num_sms < s.max_tiles_gu ? num_sms : s.max_tiles_gu;
-  grouped_gemm_kernel<true><<<grid_gu, kGemmThreads, GemmCfg<true>::kSmem, st>>>(w.tm_gate, w.tm_up, tm_x16, a);
+  grouped_gemm_kernel<true><<<grid_gu, kGemmThreads, GemmCfg<true>::kSmem, st>>>(w.tm_gate, w.tm_up, w.tm_gate_sh,
+                                                                                  w.tm_up_sh, tm_x2, a);
   stage(tm, "gemm_gateup", st);
   a.tiles = s.tiles_dn;
   a.k_blocks = d.inter / BK;
   a.a_rows_per_group = d.hidden;
   a.which = 1;
   const int grid_dn = num_sms < s.max_tiles_dn ? num_sms : s.max_tiles_dn;
-  grouped_gemm_kernel<false><<<grid_dn, kGemmThreads, GemmCfg<false>::kSmem, st>>>(w.tm_down, w.tm_down, tm_act16, a);
+  grouped_gemm_kernel<false><<<grid_dn, kGemmThreads, GemmCfg<false>::kSmem, st>>>(
+      w.tm_down, w.tm_down, w.tm_down_sh, w.tm_down_sh, tm_act2, a);
   stage(tm, "gemm_down", st);
 }
 
-// bf16 -> fp16 copy of the expert weights for the tensor-core path (init only).
-__global__ void bf16_to_f16_kernel(const uint16_t *__restrict__ src, __half *__restrict__ dst, size_t n) {
-  const size_t stride = (size_t)gridDim.x * blockDim.x * 8;
-  for (size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 8; i < n; i += stride) {
-    const uint4 v = *reinterpret_cast<const uint4 *>(src + i);
-    __half2 h[4];
-    h[0] = __floats2half2_rn(bf_lo(v.x), bf_hi(v.x));
-    h[1] = __floats2half2_rn(bf_lo(v.y), bf_hi(v.y));
-    h[2] = __floats2half2_rn(bf_lo(v.z), bf_hi(v.z));
-    h[3] = __floats2half2_rn(bf_lo(v.w), bf_hi(v.w));
-    *reinterpret_cast<uint4 *>(dst + i) = *reinterpret_cast<uint4 *>(h);
-  }
-}
-
-void launch_bf16_to_f16(const uint16_t *src, __half *dst, size_t n, cudaStream_t st) {
-  bf16_to_f16_kernel<<<1024, 256, 0, st>>>(src, dst, n);
-}
-
-// MXFP8 (E4M3 codes q[n], E8M0 scales s[n / 32]) to fp16 for the tensor-core operands: each 16-code
-// piece of a 32-element block decoded exactly in f32 (code value times 2^(s - 127)), then rounded to
-// f16, which is exact whenever the product is an f16 value (scales 2^-15 .. 2^7).
-__global__ void mxfp8_to_f16_kernel(const uint8_t *__restrict__ q, const uint8_t *__restrict__ sc,
-                                    __half *__restrict__ dst, size_t n) {
+// MXFP8 (E4M3 codes q[n], E8M0 scales s[n / 32]) to bf16, the operand format of the tensor-core
+// path: each code's value times 2^(s - 127), formed exactly in f32, has at most four significant
+// bits, so clearing the low 16 bits gives it exactly as bf16 (for products above 2^-133).
+__global__ void mxfp8_to_bf16_kernel(const uint8_t *__restrict__ q, const uint8_t *__restrict__ sc,
+                                     uint16_t *__restrict__ dst, size_t n) {
   const size_t stride = (size_t)gridDim.x * blockDim.x * 16;
   for (size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 16; i < n; i += stride) {
     float f[16];
     e4m3x16_to_float(*reinterpret_cast<const uint4 *>(q + i), f);
     const float x = e8m0_value(sc[i / 32]);
-    __half2 h[8];
+    uint32_t packed[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) h[k] = __floats2half2_rn(f[2 * k] * x, f[2 * k + 1] * x);
-    *reinterpret_cast<uint4 *>(dst + i) = *reinterpret_cast<uint4 *>(h);
-    *reinterpret_cast<uint4 *>(dst + i + 8) = *reinterpret_cast<uint4 *>(h + 4);
+    for (int k = 0; k < 8; ++k) packed[k] = pack_bf16_pair(f[2 * k] * x, f[2 * k + 1] * x);
+    *reinterpret_cast<uint4 *>(dst + i) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    *reinterpret_cast<uint4 *>(dst + i + 8) = make_uint4(packed[4], packed[5], packed[6], packed[7]);
   }
 }
-void launch_mxfp8_to_f16(const uint8_t *q, const uint8_t *s, __half *dst, size_t n, cudaStream_t st) {
-  mxfp8_to_f16_kernel<<<1024, 256, 0, st>>>(q, s, dst, n);
+void launch_mxfp8_to_bf16(const uint8_t *q, const uint8_t *s, uint16_t *dst, size_t n, cudaStream_t st) {
+  mxfp8_to_bf16_kernel<<<1024, 256, 0, st>>>(q, s, dst, n);
 }
 
 }  // namespace moe

@@ -61,7 +61,8 @@ struct Scratch {
   int *idx;               // [rows, top_k]
   float *rw;              // [rows, top_k]
   unsigned *safe;         // [rows, top_k]
-  float *ffn_out;         // [rows, hidden]
+  float *ffn_out;         // [rows, hidden] (decode path)
+  double *ffn_acc;        // [rows, hidden] the rows > 4 path's FFN output, accumulated by the down GEMM
   // decode path
   int *ngroups, *group_e, *group_mask;  // groups of (expert, rows using it); shared expert last
   float *group_w;         // [groups, 4]
@@ -78,9 +79,9 @@ struct Scratch {
   int *n_tiles;           // [2]: gate/up tiles, down tiles
   int2 *list;             // [positions] (row, slot) in expert-sorted order; slot top_k = shared expert
   float *list_w;          // [positions] route weight of that slot (1 for the shared expert)
-  __half *x16;            // [positions, hidden] ffn_norm rows in expert-sorted order (fp16)
-  __half *act16;          // [positions, inter] SwiGLU output in the same order (fp16)
-  float *y_slot;          // [rows, top_k + 1, hidden] weighted expert outputs
+  uint16_t *x2;           // [2 * max_positions, hidden] bf16: ffn_norm rows in expert-sorted order,
+                          // hi plane (rows 0..P-1) then lo plane (rows P..2P-1)
+  uint16_t *act2;         // [2 * max_positions, inter] bf16: SwiGLU output in the same order, hi then lo
   float *mix_tc_part;     // [splits, rows, 32] mix partials, then [splits, rows] sums of squares
   int max_rows, mix_chunks, router_chunks, max_positions, max_tiles_gu, max_tiles_dn;
 };
@@ -115,14 +116,15 @@ struct LayerDev {
   const uint16_t *gate;
   const int32_t *tid2eid;
   const uint16_t *gate_exps, *up_exps, *down_exps, *gate_sh, *up_sh, *down_sh;
-  __half *gate16, *up16, *down16;  // [(experts+1) * inter, hidden], [(experts+1) * hidden, inter]
-  __half *hcfn16;                  // [32, hc * hidden]: hc_fn in fp16, rows past the mix width zero
-  __half *router16;                // [experts rounded up to 256, hidden]: the router in fp16, padded
-  CUtensorMap tm_gate, tm_up, tm_down, tm_hcfn, tm_router;
+  // tensor maps of the rows > 4 path over the caller's bf16 matrices (routed experts, the shared
+  // expert, hc_fn in boxes of 32 rows, the router in boxes of 256 rows; rows past a matrix read as 0)
+  CUtensorMap tm_gate, tm_up, tm_down, tm_gate_sh, tm_up_sh, tm_down_sh, tm_hcfn, tm_router;
+  uint16_t *mx_bf16;  // bf16 expansion of MXFP8 experts for the rows > 4 path: gate, up, down (routed),
+                      // then the shared gate, up, down; null for bf16 layers
   // MXFP8 experts (moe_ffn_set_mxfp8_experts): E4M3 codes in the bf16 layouts, E8M0 scales [rows, K/32]
   const uint8_t *gate_q, *up_q, *down_q, *gate_sh_q, *up_sh_q, *down_sh_q;
   const uint8_t *gate_s, *up_s, *down_s, *gate_sh_s, *up_sh_s, *down_sh_s;
-  bool mx;            // the experts are the MXFP8 ones (decode streams them; prefill uses their fp16 copies)
+  bool mx;            // the experts are the MXFP8 ones (decode streams them; prefill their bf16 expansion)
   bool has_experts;   // some expert weights are registered (bf16 at init, or MXFP8 later)
   bool has_weights;
 };
@@ -152,12 +154,12 @@ void launch_decode(const Dims &d, const Scratch &s, const LayerDev &w, const flo
                    int rows, bool hash, float *out_state, cudaStream_t st, StageTimer *tm);
 cudaError_t decode_configure(int hidden);
 int decode_resident_ctas(int hidden, int rows, int num_sms, bool mx);
-void launch_mxfp8_to_f16(const uint8_t *q, const uint8_t *s, __half *dst, size_t n, cudaStream_t st);
+void launch_mxfp8_to_bf16(const uint8_t *q, const uint8_t *s, uint16_t *dst, size_t n, cudaStream_t st);
 // dispatch.cu
 void launch_dispatch(const Dims &d, const Scratch &s, int rows, cudaStream_t st, StageTimer *tm);
-void launch_prefill_post(const Dims &d, const Scratch &s, const float *state, int rows, float *out_state,
-                         cudaStream_t st, StageTimer *tm);
 void launch_hc_post(const Dims &d, const float *f, const float *state, const float *post, const float *comb,
+                    int rows, float *out_state, cudaStream_t st);
+void launch_hc_post(const Dims &d, const double *f, const float *state, const float *post, const float *comb,
                     int rows, float *out_state, cudaStream_t st);
 // splitgemm.cu
 void launch_prefill_mix(const Dims &d, const Scratch &s, const LayerDev &w, const float *state,
@@ -168,9 +170,8 @@ int mix_tc_part_floats(int max_rows, int hcd);
 int splitgemm_splits(int k);  // K splits of the tensor-core mix / router GEMMs
 cudaError_t splitgemm_configure();
 // gemm_tc.cu
-void launch_grouped_gemms(const Dims &d, const Scratch &s, const LayerDev &w, const CUtensorMap &tm_x16,
-                          const CUtensorMap &tm_act16, int num_sms, cudaStream_t st, StageTimer *tm);
-void launch_bf16_to_f16(const uint16_t *src, __half *dst, size_t n, cudaStream_t st);
+void launch_grouped_gemms(const Dims &d, const Scratch &s, const LayerDev &w, const CUtensorMap &tm_x2,
+                          const CUtensorMap &tm_act2, int num_sms, cudaStream_t st, StageTimer *tm);
 size_t gemm_smem_bytes(bool gateup);
 cudaError_t gemm_configure();
 

@@ -26,7 +26,7 @@ struct moe_ffn_handle {
   std::vector<LayerDev> layers;
   std::vector<LayerDev> attn;  // the attention sublayer's HC weights (hc fields and ffn_norm = attn_norm only)
   Scratch s;
-  CUtensorMap tm_x16, tm_act16, tm_ffn_norm;
+  CUtensorMap tm_x2, tm_act2, tm_ffn_norm;
   float *host_in = nullptr, *host_out = nullptr;  // device staging of moe_ffn_forward_host
   int32_t *host_tok = nullptr;
   std::vector<void *> allocs;
@@ -148,15 +148,16 @@ static bool make_tmap_f32(CUtensorMap *m, const void *base, uint64_t inner, uint
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D fp16 matrix [outer, inner], row-major; boxes of `box_rows` rows x 64 columns, 128-byte swizzle.
-static bool make_tmap(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_rows = 128) {
+// 2-D bf16 matrix [outer, inner], row-major; boxes of `box_rows` rows x 64 columns, 128-byte
+// swizzle (the K-major operand layout of the tensor-core GEMMs); rows past `outer` read as zeros.
+static bool make_tmap_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_rows = 128) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner * 2};
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -176,22 +177,14 @@ static void free_all(moe_ffn_handle *h) {
   h->allocs.clear();
 }
 
-// The fp16 copies of a layer's experts (routed, then the shared one as expert `experts`) that the
-// tensor-core GEMMs of the rows > 4 path read, and their tensor maps; allocated once per layer.
-static int alloc_f16_experts(moe_ffn_handle *h, LayerDev &L) {
-  if (L.gate16) return MOE_FFN_OK;
-  const size_t E = h->dims.experts, I = h->dims.inter, D = h->dims.hidden;
-  const size_t n = (E + 1) * I * D;
-  if (!dalloc(h, &L.gate16, n) || !dalloc(h, &L.up16, n) || !dalloc(h, &L.down16, n)) {
-    h->err = "device allocation of the fp16 expert copies failed";
-    return MOE_FFN_ERR_NO_MEMORY;
-  }
-  if (!make_tmap(&L.tm_gate, L.gate16, D, (E + 1) * I) || !make_tmap(&L.tm_up, L.up16, D, (E + 1) * I) ||
-      !make_tmap(&L.tm_down, L.down16, I, (E + 1) * D)) {
-    h->err = "cuTensorMapEncodeTiled failed for the fp16 expert copies";
-    return MOE_FFN_ERR_CUDA;
-  }
-  return MOE_FFN_OK;
+// Tensor maps of a layer's expert matrices for the rows > 4 path: routed gate/up [experts * inter,
+// hidden], routed down [experts * hidden, inter], and the shared expert's three matrices.
+static bool expert_tmaps(const moe_ffn_handle *h, LayerDev &L, const uint16_t *g, const uint16_t *u, const uint16_t *dn,
+                         const uint16_t *gs, const uint16_t *us, const uint16_t *ds) {
+  const uint64_t E = h->dims.experts, I = h->dims.inter, D = h->dims.hidden;
+  return make_tmap_bf16(&L.tm_gate, g, D, E * I) && make_tmap_bf16(&L.tm_up, u, D, E * I) &&
+         make_tmap_bf16(&L.tm_down, dn, I, E * D) && make_tmap_bf16(&L.tm_gate_sh, gs, D, I) &&
+         make_tmap_bf16(&L.tm_up_sh, us, D, I) && make_tmap_bf16(&L.tm_down_sh, ds, I, D);
 }
 
 extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weights *layers, moe_ffn_handle **out) {
@@ -258,7 +251,7 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
          dalloc(h, &s.router_part, (size_t)moe::splitgemm_splits((int)D) * R * E) &&
          dalloc(h, &s.tiles_gu, (size_t)s.max_tiles_gu) && dalloc(h, &s.tiles_dn, (size_t)s.max_tiles_dn) &&
          dalloc(h, &s.n_tiles, 2) && dalloc(h, &s.list, P) && dalloc(h, &s.list_w, P) &&
-         dalloc(h, &s.x16, P * D) && dalloc(h, &s.act16, P * I) && dalloc(h, &s.y_slot, R * (K + 1) * D) &&
+         dalloc(h, &s.x2, 2 * P * D) && dalloc(h, &s.act2, 2 * P * I) && dalloc(h, &s.ffn_acc, R * D) &&
          dalloc(h, &s.mix_tc_part, (size_t)moe::mix_tc_part_floats((int)R, (int)hcd));
   if (!ok) {
     free_all(h);
@@ -270,7 +263,7 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
   cudaMemset(s.tickets, 0, (R / 4 + 2) * sizeof(unsigned));
   if (prefill) {
     cudaMemset(s.counts, 0, E * sizeof(int));
-    if (!make_tmap(&h->tm_x16, s.x16, D, P) || !make_tmap(&h->tm_act16, s.act16, I, P) ||
+    if (!make_tmap_bf16(&h->tm_x2, s.x2, D, 2 * P) || !make_tmap_bf16(&h->tm_act2, s.act2, I, 2 * P) ||
         !make_tmap_f32(&h->tm_ffn_norm, s.ffn_norm, D, R)) {
       free_all(h);
       delete h;
@@ -324,35 +317,10 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
     L.up_sh = w.up_sh;
     L.down_sh = w.down_sh;
     if (!prefill) continue;
-    const size_t n_exp = E * I * D, n_sh = I * D;
-    if (L.has_experts) {
-      rc = alloc_f16_experts(h, L);
-      if (rc) {
-        const std::string msg = h->err;
-        free_all(h);
-        delete h;
-        return fail(nullptr, rc, "%s", msg.c_str());
-      }
-      moe::launch_bf16_to_f16(w.gate_exps, L.gate16, n_exp, 0);
-      moe::launch_bf16_to_f16(w.gate_sh, L.gate16 + n_exp, n_sh, 0);
-      moe::launch_bf16_to_f16(w.up_exps, L.up16, n_exp, 0);
-      moe::launch_bf16_to_f16(w.up_sh, L.up16 + n_exp, n_sh, 0);
-      moe::launch_bf16_to_f16(w.down_exps, L.down16, n_exp, 0);
-      moe::launch_bf16_to_f16(w.down_sh, L.down16 + n_exp, n_sh, 0);
-    }
-    // hc_fn and the router in fp16 for the tensor-core mix and router GEMMs, zero-padded to whole
-    // TMA boxes (32 mix rows; the experts to a multiple of 256)
-    const size_t e_pad = (E + 255) / 256 * 256;
-    if (!dalloc(h, &L.hcfn16, 32 * hcd) || !dalloc(h, &L.router16, e_pad * D)) {
-      free_all(h);
-      delete h;
-      return fail(nullptr, MOE_FFN_ERR_NO_MEMORY, "device allocation of the fp16 mix/router copies failed");
-    }
-    cudaMemset(L.hcfn16, 0, 32 * hcd * sizeof(__half));
-    cudaMemset(L.router16, 0, e_pad * D * sizeof(__half));
-    moe::launch_bf16_to_f16(w.hc_fn, L.hcfn16, M * hcd, 0);
-    moe::launch_bf16_to_f16(w.gate, L.router16, E * D, 0);
-    if (!make_tmap(&L.tm_hcfn, L.hcfn16, hcd, 32, 32) || !make_tmap(&L.tm_router, L.router16, D, e_pad, 256)) {
+    // the rows > 4 path reads the caller's bf16 matrices through tensor maps: hc_fn in boxes of 32
+    // rows (the mix's MMA width; rows past (2+hc)*hc read as zeros), the router in boxes of 256
+    if ((L.has_experts && !expert_tmaps(h, L, w.gate_exps, w.up_exps, w.down_exps, w.gate_sh, w.up_sh, w.down_sh)) ||
+        !make_tmap_bf16(&L.tm_hcfn, w.hc_fn, hcd, M, 32) || !make_tmap_bf16(&L.tm_router, w.gate, D, E, 256)) {
       free_all(h);
       delete h;
       return fail(nullptr, MOE_FFN_ERR_CUDA, "cuTensorMapEncodeTiled failed for layer %d", l);
@@ -408,8 +376,9 @@ static int enqueue_forward(moe_ffn_handle *h, const float *state, const int32_t 
     moe::launch_prefill_mix(h->dims, h->s, L, state, tm_state, rows, h->num_sms, st, tm);
     moe::launch_prefill_router(h->dims, h->s, L, state, token_ids, h->tm_ffn_norm, rows, hash, h->num_sms, st, tm);
     moe::launch_dispatch(h->dims, h->s, rows, st, tm);
-    moe::launch_grouped_gemms(h->dims, h->s, L, h->tm_x16, h->tm_act16, h->num_sms, st, tm);
-    moe::launch_prefill_post(h->dims, h->s, state, rows, out_state, st, tm);
+    moe::launch_grouped_gemms(h->dims, h->s, L, h->tm_x2, h->tm_act2, h->num_sms, st, tm);
+    moe::launch_hc_post(h->dims, h->s.ffn_acc, state, h->s.post, h->s.comb, rows, out_state, st);
+    moe::stage(tm, "post", st);
   }
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(h, MOE_FFN_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
@@ -542,20 +511,10 @@ extern "C" int moe_ffn_set_attn_hc(moe_ffn_handle *h, int32_t layer, const moe_f
   A.hc_base = w->hc_base;
   A.hc_scale = w->hc_scale;
   A.ffn_norm = w->norm;
-  if (c.max_rows > moe::kDecodeRows) {
-    const size_t hcd = (size_t)c.hc * c.hidden, M = h->dims.mix();
-    if (!A.hcfn16) {
-      if (!dalloc(h, &A.hcfn16, 32 * hcd)) {
-        A.has_weights = false;
-        return fail(h, MOE_FFN_ERR_NO_MEMORY, "device allocation of the fp16 attention hc_fn failed");
-      }
-      cudaMemset(A.hcfn16, 0, 32 * hcd * sizeof(__half));
-    }
-    moe::launch_bf16_to_f16(w->hc_fn, A.hcfn16, M * hcd, 0);
-    if (!make_tmap(&A.tm_hcfn, A.hcfn16, hcd, 32, 32)) {
-      A.has_weights = false;
-      return fail(h, MOE_FFN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the attention hc_fn of layer %d", layer);
-    }
+  if (c.max_rows > moe::kDecodeRows &&
+      !make_tmap_bf16(&A.tm_hcfn, w->hc_fn, (uint64_t)c.hc * c.hidden, (uint64_t)h->dims.mix(), 32)) {
+    A.has_weights = false;
+    return fail(h, MOE_FFN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the attention hc_fn of layer %d", layer);
   }
   const cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -647,16 +606,19 @@ extern "C" int moe_ffn_set_mxfp8_experts(moe_ffn_handle *h, int32_t layer, const
   L.up_sh_s = w->up_sh_scale;
   L.down_sh_q = w->down_sh;
   L.down_sh_s = w->down_sh_scale;
-  if (c.max_rows > moe::kDecodeRows) {  // the tensor-core path reads fp16 copies
-    const int rc = alloc_f16_experts(h, L);
-    if (rc) return fail(h, rc, "%s", h->err.c_str());
+  if (c.max_rows > moe::kDecodeRows) {  // the tensor-core path reads an exact bf16 expansion
     const size_t E = c.experts, I = c.inter, D = c.hidden, n_exp = E * I * D, n_sh = I * D;
-    moe::launch_mxfp8_to_f16(L.gate_q, L.gate_s, L.gate16, n_exp, 0);
-    moe::launch_mxfp8_to_f16(L.gate_sh_q, L.gate_sh_s, L.gate16 + n_exp, n_sh, 0);
-    moe::launch_mxfp8_to_f16(L.up_q, L.up_s, L.up16, n_exp, 0);
-    moe::launch_mxfp8_to_f16(L.up_sh_q, L.up_sh_s, L.up16 + n_exp, n_sh, 0);
-    moe::launch_mxfp8_to_f16(L.down_q, L.down_s, L.down16, n_exp, 0);
-    moe::launch_mxfp8_to_f16(L.down_sh_q, L.down_sh_s, L.down16 + n_exp, n_sh, 0);
+    if (!L.mx_bf16 && !dalloc(h, &L.mx_bf16, 3 * (n_exp + n_sh)))
+      return fail(h, MOE_FFN_ERR_NO_MEMORY, "device allocation of the bf16 expansion of layer %d failed", layer);
+    uint16_t *g = L.mx_bf16, *u = g + n_exp, *dn = u + n_exp, *gs = dn + n_exp, *us = gs + n_sh, *ds = us + n_sh;
+    moe::launch_mxfp8_to_bf16(L.gate_q, L.gate_s, g, n_exp, 0);
+    moe::launch_mxfp8_to_bf16(L.up_q, L.up_s, u, n_exp, 0);
+    moe::launch_mxfp8_to_bf16(L.down_q, L.down_s, dn, n_exp, 0);
+    moe::launch_mxfp8_to_bf16(L.gate_sh_q, L.gate_sh_s, gs, n_sh, 0);
+    moe::launch_mxfp8_to_bf16(L.up_sh_q, L.up_sh_s, us, n_sh, 0);
+    moe::launch_mxfp8_to_bf16(L.down_sh_q, L.down_sh_s, ds, n_sh, 0);
+    if (!expert_tmaps(h, L, g, u, dn, gs, us, ds))
+      return fail(h, MOE_FFN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the MXFP8 experts of layer %d", layer);
   }
   const cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return fail(h, MOE_FFN_ERR_CUDA, "set_mxfp8_experts: %s", cudaGetErrorString(e));
@@ -695,7 +657,15 @@ extern "C" int moe_ffn_debug_copy(moe_ffn_handle *h, int32_t which, void *host_d
   }
   if (bytes != n) return fail(h, MOE_FFN_ERR_BAD_CONFIG, "debug buffer %d holds %zu bytes, not %zu", which, n, bytes);
   cudaError_t e = cudaStreamSynchronize(h->last_stream);
-  if (e == cudaSuccess) e = cudaMemcpy(host_dst, src, n, cudaMemcpyDeviceToHost);
+  if (which == 8 && R > (size_t)moe::kDecodeRows) {
+    // the rows > 4 path accumulates the FFN output in f64; it is rounded to f32 as hc_post reads it
+    std::vector<double> tmp(R * D);
+    if (e == cudaSuccess) e = cudaMemcpy(tmp.data(), h->s.ffn_acc, R * D * sizeof(double), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess)
+      for (size_t i = 0; i < R * D; ++i) static_cast<float *>(host_dst)[i] = (float)tmp[i];
+  } else if (e == cudaSuccess) {
+    e = cudaMemcpy(host_dst, src, n, cudaMemcpyDeviceToHost);
+  }
   if (e != cudaSuccess) return fail(h, MOE_FFN_ERR_CUDA, "debug copy: %s", cudaGetErrorString(e));
   return MOE_FFN_OK;
 }

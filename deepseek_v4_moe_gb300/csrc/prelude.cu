@@ -359,10 +359,14 @@ RouteParams make_route(const Dims &d, const Scratch &s, const LayerDev &w, const
 // Rows > 4: per-row hc_pre + ffn_norm, a tiled f32 router GEMM, then one warp per row routes
 // and counts slots per expert for the dispatch.
 // ---------------------------------------------------------------------------------------------
+// One CTA per row: ffn_input = sum_h pre[h] * state[h] (in shared memory), then ffn_norm =
+// ffn_input * rsqrt(mean(ffn_input^2) + eps) * w.  With zero_acc set, also clears that row of the
+// f64 FFN output, which the down GEMM's epilogue accumulates into.
 __global__ void __launch_bounds__(256) prefill_prenorm_kernel(const float *__restrict__ state,
                                                               const float *__restrict__ pre,
                                                               const float *__restrict__ norm_w, int hidden, int hc,
-                                                              float eps, float *__restrict__ ffn_norm) {
+                                                              float eps, float *__restrict__ ffn_norm,
+                                                              double *__restrict__ zero_acc) {
   extern __shared__ __align__(16) float xin[];
   __shared__ float red[8];
   const int r = blockIdx.x, tid = threadIdx.x;
@@ -395,6 +399,11 @@ __global__ void __launch_bounds__(256) prefill_prenorm_kernel(const float *__res
     const float4 g = *reinterpret_cast<const float4 *>(norm_w + dd);
     *reinterpret_cast<float4 *>(ffn_norm + (size_t)r * hidden + dd) =
         make_float4(v.x * rs * g.x, v.y * rs * g.y, v.z * rs * g.z, v.w * rs * g.w);
+    if (zero_acc) {
+      double2 *z = reinterpret_cast<double2 *>(zero_acc + (size_t)r * hidden + dd);
+      z[0] = make_double2(0.0, 0.0);
+      z[1] = make_double2(0.0, 0.0);
+    }
   }
 }
 
@@ -418,7 +427,7 @@ void launch_prefill_router(const Dims &d, const Scratch &s, const LayerDev &w, c
                            const int32_t *token_ids, const CUtensorMap &tm_ffn_norm, int rows, bool hash, int num_sms,
                            cudaStream_t st, StageTimer *tm) {
   prefill_prenorm_kernel<<<rows, 256, d.hidden * sizeof(float), st>>>(state, s.pre, w.ffn_norm, d.hidden, d.hc,
-                                                                       d.eps, s.ffn_norm);
+                                                                       d.eps, s.ffn_norm, s.ffn_acc);
   stage(tm, "prenorm", st);
   // logits on the tensor cores (splitgemm.cu), split over K so that the grid fills the GPU
   const int nsplit = launch_router_tc(d, s, w, tm_ffn_norm, rows, num_sms, st);
@@ -444,7 +453,7 @@ void launch_hc_pre(const Dims &d, const Scratch &s, const LayerDev &w, const flo
   s2.comb = comb;
   launch_prefill_mix(d, s2, w, state, *tm_state, rows, num_sms, st, nullptr);
   prefill_prenorm_kernel<<<rows, 256, d.hidden * sizeof(float), st>>>(state, pre, w.ffn_norm, d.hidden, d.hc, d.eps,
-                                                                       x_norm);
+                                                                       x_norm, nullptr);
 }
 
 }  // namespace moe

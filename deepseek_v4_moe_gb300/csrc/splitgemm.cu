@@ -1,24 +1,24 @@
-// f32 activations times fp16 weights on the tensor cores (tcgen05, TMEM, TMA), sm_103a: the
+// f32 activations times bf16 weights on the tensor cores (tcgen05, TMEM, TMA), sm_103a: the
 // prefill HC mix and router projections.
 //
 // docs.rs "hf2q 0.1.3 .../deepseek4/ffn_forward.rs", forward_ffn_rows: raw_matmul "HC FFN function"
 // (with the sum of squares of rms_norm_no_scale_f32) and raw_matmul "MoE gate".
 //
 // Both are f32 GEMMs whose results decide integers later (the top-k) or feed a Sinkhorn, so they
-// must be about as exact as f32 arithmetic.  Each activation is split x = hi + lo into two fp16
-// values (hi = rn(x), lo = rn(x - hi), so |x - hi - lo| <= 2^-22 |x| where fp16 is normal; inputs
-// must stay below fp16's largest value, 65504), the weights are fp16
-// copies of the bf16 ones (exact above 2^-14), fp16 x fp16 products are exact in the f32
-// accumulator, and two MMAs per k-step (hi and lo) give f32-level dot products at tensor-core
-// rate.
+// must be about as exact as f32 arithmetic.  The weights are the caller's bf16 matrices, read by
+// TMA as they are (no copy).  Each f32 activation is split into three bf16 planes by truncation,
+// x = hi + mid + lo + r with hi = trunc(x), mid = trunc(x - hi), lo = trunc(x - hi - mid) (each
+// subtraction exact in f32), so |r| < 2^-21 |x| over the whole f32 range; bf16 x bf16 products are
+// exact in the f32 accumulator, and three MMAs per k-step (hi, mid, lo against the same weight
+// tile) give f32-level dot products at tensor-core rate.
 //
 //   C_part[s, r, n] = sum over k in split s of X[r, k] * W[n, k]
 //   ss_part[s, r]   = sum over k in split s of X[r, k]^2           (when asked for)
 //
-// Layout: A = the 128 activation rows of a tile (M = 128), converted in shared memory into two
-// 128 x 64 fp16 planes per k-stage in the 128-byte-swizzled K-major layout the MMA reads; B = BN
-// weight rows (N = BN), loaded by TMA.  Persistent: one CTA per SM walks (row tile, K split,
-// weight tile) items.  Roles:
+// Layout: A = the 128 activation rows of a tile (M = 128), converted in shared memory into three
+// 128 x 64 bf16 planes per k-stage in the 128-byte-swizzled K-major layout the MMA reads; B = BN
+// weight rows (N = BN), loaded by TMA (rows past the matrix arrive as zeros).  Persistent: one CTA
+// per SM walks (row tile, K split, weight tile) items.  Roles:
 //   next warp  TMEM allocator and activation producer: one 128 x 64 f32 TMA box per k-stage into
 //              a ring of f32 slots (the bytes in flight cost no registers)
 //   converters (kConvWarps): f32 from shared memory, split, swizzled stores, sums of squares; then
@@ -35,18 +35,19 @@ namespace moe {
 
 namespace sg {
 constexpr int BM = 128, BK = 64, UMMA_K = 16;
-constexpr int kPlaneBytes = BM * BK * 2;  // one 128 x 64 fp16 plane: 16 KB
+constexpr int kPlaneBytes = BM * BK * 2;  // one 128 x 64 bf16 plane: 16 KB
+constexpr int kPlanes = 3;                // hi, mid, lo
 constexpr int kXBytes = BM * BK * 4;      // one 128 x 64 f32 activation tile: 32 KB
 constexpr int kConvWarps = 8, kThreads = 32 * (kConvWarps + 3);
 constexpr int kConvSteps = BM / kConvWarps / 2;  // two tile rows per converter-warp step
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 // XS slots of staged f32 activations (bulk copies, so the bytes in flight cost no registers) and
-// CS slots of converted fp16 planes with their weight tile
+// CS slots of converted bf16 planes with their weight tile
 template <int BN, int XS, int CS>
 struct Cfg {
   static constexpr int kBBytes = BN * BK * 2;
-  static constexpr int kCBytes = 2 * kPlaneBytes + kBBytes;
+  static constexpr int kCBytes = kPlanes * kPlaneBytes + kBBytes;
   static constexpr size_t kSmem = (size_t)XS * kXBytes + (size_t)CS * kCBytes + 1024;
   static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;  // two accumulators
   // converter warps draining an accumulator: groups of four (one per TMEM lane quarter), each
@@ -64,30 +65,29 @@ struct SplitGemmArgs {
   int R, K, N, ldc, kb_per_split, splits, n_tiles;
 };
 
-// The 16-byte chunk `c` (0..7) of row `r` of a 128 x 64 fp16 K-major tile in the 128-byte
+// The 16-byte chunk `c` (0..7) of row `r` of a 128 x 64 bf16 K-major tile in the 128-byte
 // swizzled layout: rows of 128 B, 8-row groups 1024 B apart, chunk index XOR-ed with r % 8.
 __device__ __forceinline__ uint32_t sw128_chunk(int r, int c) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-// x rounded to fp16's 11-bit significand (round to nearest even on the 13 dropped bits), still in
-// f32: integer operations only, so that the conversion pipe (a quarter of the ALU rate) is spent
-// on the two packed conversions below alone.  Equal to fp16(x) wherever fp16 is normal; below
-// 2^-14 the fp16 conversion rounds once more, by at most 2^-25 in absolute terms.
-__device__ __forceinline__ float round_to_f16_precision(float x) {
-  uint32_t u = __float_as_uint(x);
-  u += 0x00000FFFu + ((u >> 13) & 1u);
-  return __uint_as_float(u & 0xFFFFE000u);
-}
+// x truncated to bf16 (the low 16 bits cleared), still an f32: x - trunc_bf16(x) is exact in f32.
+__device__ __forceinline__ float trunc_bf16(float x) { return __uint_as_float(__float_as_uint(x) & 0xFFFF0000u); }
 
-// Four activations as fp16 pairs: hi = rn(x) and lo = rn(x - hi), two packed conversions each.
-__device__ __forceinline__ void split4(const float4 v, uint2 &hi, uint2 &lo) {
-  const float hx = round_to_f16_precision(v.x), hy = round_to_f16_precision(v.y);
-  const float hz = round_to_f16_precision(v.z), hw = round_to_f16_precision(v.w);
-  const __half2 h01 = __floats2half2_rn(hx, hy), h23 = __floats2half2_rn(hz, hw);
-  const __half2 l01 = __floats2half2_rn(v.x - hx, v.y - hy), l23 = __floats2half2_rn(v.z - hz, v.w - hw);
-  hi = make_uint2(*reinterpret_cast<const uint32_t *>(&h01), *reinterpret_cast<const uint32_t *>(&h23));
-  lo = make_uint2(*reinterpret_cast<const uint32_t *>(&l01), *reinterpret_cast<const uint32_t *>(&l23));
+// Four activations as three bf16 planes: hi = trunc(x), mid = trunc(x - hi), lo = trunc(x - hi - mid).
+__device__ __forceinline__ void split3(const float4 v, uint2 &hi, uint2 &mid, uint2 &lo) {
+  const float x[4] = {v.x, v.y, v.z, v.w};
+  float h[4], m[4], l[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    h[k] = trunc_bf16(x[k]);
+    const float r1 = x[k] - h[k];
+    m[k] = trunc_bf16(r1);
+    l[k] = trunc_bf16(r1 - m[k]);
+  }
+  hi = make_uint2(pack_bf16_pair(h[0], h[1]), pack_bf16_pair(h[2], h[3]));
+  mid = make_uint2(pack_bf16_pair(m[0], m[1]), pack_bf16_pair(m[2], m[3]));
+  lo = make_uint2(pack_bf16_pair(l[0], l[1]), pack_bf16_pair(l[2], l[3]));
 }
 
 template <int BN, int XS, int CS>
@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(sg::kThreads, 1)
     // ---------------- converters, and the epilogue of the previous item ----------------
     // Warp w converts 2 kConvSteps rows of each tile, two rows per step: lane l takes float4
     // l % 16 of row 2 kConvSteps w + 2j + l / 16 (a conflict-free 512-byte read) and writes its
-    // 4 fp16 of each plane as 8 bytes of the row's swizzled 128-byte line.
+    // 4 bf16 of each plane as 8 bytes of the row's swizzled 128-byte line.
     auto drain = [&](int i) -> bool {
       if ((warp >> 2) >= C::kDrainGroups) return true;  // not a draining warp
       if (!warp_wait(&tfull[i & 1], (uint32_t)(i >> 1) & 1u)) return false;
@@ -191,17 +191,18 @@ __global__ void __launch_bounds__(sg::kThreads, 1)
       }
       const uint8_t *xp = xring + (size_t)xs * kXBytes;
       uint8_t *hi_p = cring + (size_t)cs * C::kCBytes;
-      uint8_t *lo_p = hi_p + kPlaneBytes;
+      uint8_t *mid_p = hi_p + kPlaneBytes, *lo_p = hi_p + 2 * kPlaneBytes;
 #pragma unroll
       for (int j = 0; j < kConvSteps; ++j) {
         const int row = warp * 2 * kConvSteps + 2 * j + sub;
         float4 v = *reinterpret_cast<const float4 *>(xp + row * 256 + f4 * 16);
         if (r0 + row >= a.R) v = make_float4(0.f, 0.f, 0.f, 0.f);  // past this call's rows
         ss[j] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-        uint2 hi, lo;
-        split4(v, hi, lo);
+        uint2 hi, mid, lo;
+        split3(v, hi, mid, lo);
         const uint32_t off = sw128_chunk(row, f4 >> 1) + (uint32_t)((f4 & 1) * 8);
         *reinterpret_cast<uint2 *>(hi_p + off) = hi;
+        *reinterpret_cast<uint2 *>(mid_p + off) = mid;
         *reinterpret_cast<uint2 *>(lo_p + off) = lo;
       }
       // the generic-proxy stores must be visible to the tensor core's async proxy
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(sg::kThreads, 1)
     }
   } else if (warp == kConvWarps + 1 && lane == 0) {
     // ---------------- MMA issuer: item i accumulates in TMEM buffer i % 2 ----------------
-    const uint32_t idesc = idesc_f16_f32(BM, BN);
+    const uint32_t idesc = idesc_bf16_f32(BM, BN);
     int g = 0;
     for (int i = 0; i < my_items && !*abort_p; ++i) {
       if (!mbar_wait_bounded(&tempty[i & 1], ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_p, a.status, kWaitNs)) break;
@@ -258,12 +259,14 @@ __global__ void __launch_bounds__(sg::kThreads, 1)
         }
         tc_fence_after();
         const uint32_t shi = smem_u32(cring + (size_t)cs * C::kCBytes);
-        const uint32_t slo = shi + kPlaneBytes, sb = shi + 2 * kPlaneBytes;
+        const uint32_t sb = shi + kPlanes * kPlaneBytes;
 #pragma unroll
         for (int k = 0; k < BK / UMMA_K; ++k) {
           const uint64_t bdesc = smem_desc_sw128(sb + k * UMMA_K * 2);
-          tc_mma_f16(acc, smem_desc_sw128(shi + k * UMMA_K * 2), bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
-          tc_mma_f16(acc, smem_desc_sw128(slo + k * UMMA_K * 2), bdesc, idesc, 1u);
+#pragma unroll
+          for (int pl = 0; pl < kPlanes; ++pl)
+            tc_mma_f16(acc, smem_desc_sw128(shi + pl * kPlaneBytes + k * UMMA_K * 2), bdesc, idesc,
+                       (kb > 0 || k > 0 || pl > 0) ? 1u : 0u);
         }
         tc_commit(&cempty[cs]);
       }
@@ -278,7 +281,7 @@ __global__ void __launch_bounds__(sg::kThreads, 1)
       item_of(g / nkb, r0, split, n0);
       if (!mbar_wait_bounded(&cempty[cs], ((uint32_t)(g / CS) & 1u) ^ 1u, abort_p, a.status, kWaitNs)) break;
       mbar_arrive_expect_tx(&cfull[cs], C::kBBytes);
-      tma_load_2d(cring + (size_t)cs * C::kCBytes + 2 * kPlaneBytes, &tmW, &cfull[cs], (split * nkb + g % nkb) * BK, n0);
+      tma_load_2d(cring + (size_t)cs * C::kCBytes + kPlanes * kPlaneBytes, &tmW, &cfull[cs], (split * nkb + g % nkb) * BK, n0);
     }
   }
   tc_fence_before();
@@ -293,8 +296,8 @@ __global__ void __launch_bounds__(sg::kThreads, 1)
 // Host side and the mix finish
 // ---------------------------------------------------------------------------------------------
 
-constexpr int kMixBN = 32, kMixXS = 3, kMixCS = 3;           // mix: up to 24 outputs, a light B tile
-constexpr int kRouterBN = 256, kRouterXS = 3, kRouterCS = 2;
+constexpr int kMixBN = 32, kMixXS = 3, kMixCS = 2;           // mix: up to 24 outputs, a light B tile
+constexpr int kRouterBN = 256, kRouterXS = 2, kRouterCS = 2;
 
 cudaError_t splitgemm_configure() {
   cudaError_t e = cudaFuncSetAttribute(splitgemm_kernel<kMixBN, kMixXS, kMixCS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -306,8 +309,8 @@ cudaError_t splitgemm_configure() {
 
 // Splits of K.  The tensor cores' f32 accumulation does not round every addition to nearest, so
 // its error grows with the number of MMAs accumulated in place; every split therefore sums at most
-// kMaxKbPerSplit k-blocks (8 x 2 MMAs of K = 16 each), and the splits are added on the CUDA cores
-// in a fixed order.
+// kMaxKbPerSplit k-blocks (8 x 4 k-steps x 3 planes of K = 16 each), and the splits are added on
+// the CUDA cores in a fixed order.
 constexpr int kMaxKbPerSplit = 8;
 int splitgemm_splits(int k) {
   const int kb = k / sg::BK;

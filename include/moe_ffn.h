@@ -60,7 +60,7 @@ extern "C" {
 /* Device-side status bits (moe_ffn_status returns their OR since the previous call). */
 #define MOE_FFN_DEV_TOKEN_RANGE 0x1   /* hash layer: token id outside [0, vocab); its slots masked */
 #define MOE_FFN_DEV_ROUTE_RANGE 0x2   /* a routed expert index outside [0, experts); slot masked */
-#define MOE_FFN_DEV_NONFINITE 0x4     /* a router logit was NaN or infinite */
+#define MOE_FFN_DEV_NONFINITE 0x4     /* a router logit, or (rows > 4) a SwiGLU or expert output, was NaN or infinite */
 #define MOE_FFN_DEV_TIMEOUT 0x8       /* a bounded wait inside a kernel gave up (kernel returned) */
 
 /* Shapes and constants of the block (the page's cfg fields).  Supported:

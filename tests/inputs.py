@@ -81,3 +81,14 @@ def compare_dot(got: np.ndarray, ref: np.ndarray, x: np.ndarray, w: np.ndarray, 
     assert ratio[worst] <= 1.0, (f"{what} |delta| {diff[worst]:.3e} at {worst} > {tau:g} x condition "
                                  f"{cond[worst]:.3e} (ratio {ratio[worst]:.2f})")
     return float(ratio[worst])
+
+
+def compare_scaled(got: np.ndarray, ref: np.ndarray, cond: np.ndarray, tau: float, what: str = ""):
+    """|got - ref| <= tau * cond elementwise, cond an entry's own error scale (the magnitude its
+    inputs carry before any cancellation); the message names the worst entry."""
+    diff = np.abs(got.astype(np.float64) - ref)
+    ratio = diff / (tau * cond + 1e-30)
+    worst = np.unravel_index(np.argmax(ratio), ratio.shape)
+    assert ratio[worst] <= 1.0, (f"{what} |delta| {diff[worst]:.3e} at {worst} (got {got[worst]:.8g}, ref "
+                                 f"{ref[worst]:.8g}) > {tau:g} x scale {cond[worst]:.3e}")
+    return float(ratio[worst])

@@ -157,3 +157,62 @@ def test_error_codes(cuda_lib):
                                torch.empty_like(s).data_ptr(), None) == -11
     assert m.status() == 0
     m.close()
+
+
+def _tie_free_fixed(case, plant):
+    """Redraws near-tied rows (new attempt numbers) while keeping the planted modification."""
+    for _ in range(20):
+        plant(case)
+        st = oracle.prelude_and_route(case)
+        bad = st["margin"] < 1e-5
+        if not bad.any():
+            return case, st
+        att = case.attempts.copy()
+        att[bad] += 1
+        case = case.with_attempts(att)
+    raise RuntimeError("ties")
+
+
+@pytest.mark.parametrize("rows", [3, 40])
+def test_outliers_and_activations_past_fp16_range(rows, cuda_lib):
+    # state elements at +-12..20 sigma, one row scaled by 1e5 (values far past fp16's 65504), and the
+    # ffn_norm weight scaled so that the SwiGLU output of most slots exceeds 65504 as well: both paths
+    # must keep f32 range end to end (compared row by row, so the big row hides nothing)
+    def plant(case):  # applied once to each freshly drawn case
+        case.ffn_norm = (case.ffn_norm * 2000.0).astype(np.float32)
+        case.state[0, 1, 5] = 20.0
+        case.state[0, 2, 7] = -12.0
+        case.state[1] *= 1e5
+        case.state[-1, 3, :9] = 16.0
+
+    cfg = replace(TINY, rows=rows, name=f"outl{rows}")
+    case, st = _tie_free_fixed(synth.Case(cfg), plant)
+    m, dev, res = _run(case)
+    ref = oracle.forward_ffn_rows(case, stages=st)
+    xf = st["ffn_norm"]
+    act = oracle.moe_ffn.swiglu(xf @ oracle.moe_ffn.expert_weights(case, "gate", None).T,
+                                xf @ oracle.moe_ffn.expert_weights(case, "up", None).T)
+    assert np.mean(np.abs(act) > 65504) > 0.1, "the case must carry activations past fp16 range"
+    assert res["status"] == 0
+    assert np.array_equal(res["indices"], ref["indices"])
+    for r in range(rows):
+        compare_state(res["out"][r], ref["out_state"][r])
+    m.close()
+
+
+@pytest.mark.parametrize("rows", [3, 40])
+def test_nonfinite_state_row_is_reported_and_contained(rows, cuda_lib):
+    # a NaN in one state row: the device status carries the non-finite bit, that row's output is
+    # not finite, and every other row still matches the oracle
+    cfg = replace(TINY, rows=rows, name=f"nan{rows}")
+    case, st = tie_free(cfg)
+    ref = oracle.forward_ffn_rows(case, stages=st)
+    case.state[1, 2, 3] = np.nan
+    m, dev, res = _run(case)
+    assert res["status"] & 0x4, f"status {res['status']:#x} lacks the non-finite bit"
+    assert not np.isfinite(res["out"][1]).all()
+    others = [r for r in range(rows) if r != 1]
+    assert np.array_equal(res["indices"][others], ref["indices"][others])
+    for r in others:
+        compare_state(res["out"][r], ref["out_state"][r])
+    m.close()

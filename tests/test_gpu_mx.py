@@ -1,6 +1,7 @@
 """GPU parity of the block on MXFP8 experts (moe_ffn_set_mxfp8_experts) against the oracle, which
 decodes the same codes and scales by the format's definition.  Rows <= 4 stream the codes in the
-decode kernel; larger batches run the tensor-core path on the fp16 copies made at registration."""
+decode kernel; larger batches run the tensor-core path on the exact bf16 expansion made at
+registration."""
 from dataclasses import replace
 
 import numpy as np
@@ -62,6 +63,19 @@ def test_forward_before_mx_registration_is_rejected():
         m.forward(dev["state"], dev["token_ids"], case.cfg.layer)
     assert e.value.code == L.ERR_NO_WEIGHTS
     m.close()
+
+
+def test_mx_full_shape_prefill():
+    # hidden 4096, inter 2048, 32 experts, 512 rows: every weight tile of the tensor-core path at its
+    # real shape, every row compared
+    cfg = replace(synth.PROFILE_CONFIGS["p_prefill_512_e32"], weights="mxfp8")
+    case, st, got, idx, status = _run(cfg, cfg.rows)
+    assert status == 0
+    assert np.array_equal(idx, st["indices"])
+    ref = oracle.forward_ffn_rows(case, stages=st)["out_state"]
+    compare_state(got, ref)
+    for r in range(cfg.rows):
+        compare_state(got[r], ref[r])
 
 
 @pytest.mark.parametrize("name", ["c1_decode_b1", "c2_decode_b4_hash"])
