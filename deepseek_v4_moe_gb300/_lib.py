@@ -101,6 +101,8 @@ def load(build: bool = True):
     lib.moe_ffn_hc_pre.restype = ctypes.c_int
     lib.moe_ffn_hc_post.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp]
     lib.moe_ffn_hc_post.restype = ctypes.c_int
+    lib.moe_ffn_set_fault_injection.argtypes = [vp, i32, ctypes.c_uint32]
+    lib.moe_ffn_set_fault_injection.restype = ctypes.c_int
     lib.moe_ffn_last_error.argtypes = [vp]
     lib.moe_ffn_last_error.restype = ctypes.c_char_p
     lib.moe_ffn_destroy.argtypes = [vp]

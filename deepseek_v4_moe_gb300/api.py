@@ -229,6 +229,15 @@ class MoeFFN:
         if rc != 0:
             self._err(rc)
 
+    def set_fault_injection(self, which: str | None, wait_limit_us: int = 0):
+        """Test hook: make one bounded in-kernel wait run out on later forwards ("decode": the decode
+        kernel's last phase; "gemm": CTA 0 of the gate/up GEMM; None: off), with every in-kernel
+        wait bounded by wait_limit_us (0: the kernels' defaults)."""
+        code = {None: 0, "decode": 1, "gemm": 2}[which]
+        rc = self._lib.moe_ffn_set_fault_injection(self._h, code, int(wait_limit_us))
+        if rc != 0:
+            self._err(rc)
+
     def stage_times(self) -> list[tuple[str, float]]:
         """(kernel name, ms) of each kernel of the last forward made with stage timing on."""
         ms = (ctypes.c_float * 16)()

@@ -1,37 +1,55 @@
-// Decode path (rows <= 4): the whole FFN block in one persistent launch.
+// Decode path (rows <= 4): the whole FFN block in one persistent launch, two CTAs per SM.
 //
 // docs.rs "hf2q 0.1.3 .../deepseek4/ffn_forward.rs", forward_ffn_rows, every stage in order:
-// rms_norm_no_scale_f32 + raw_matmul "HC FFN function" + dispatch_hc_split_sinkhorn (mix roles),
-// dispatch_hc_pre + rms_norm + raw_matmul "MoE gate" + dispatch_deepseek_moe_{score,hash}_route +
-// dispatch_deepseek_moe_sanitize_indices (router roles), expert_matmul "routed gate"/"routed up" +
-// raw_matmul "shared gate"/"shared up" + dispatch_deepseek_moe_swiglu (phase A), expert_matmul
-// "routed down" + raw_matmul "shared down" (phase B), dispatch_deepseek_moe_weighted_reduce +
-// dispatch_hc_post (phase C).
+// rms_norm_no_scale_f32 + raw_matmul "HC FFN function" + dispatch_hc_split_sinkhorn (mix CTAs),
+// dispatch_hc_pre + rms_norm (every CTA), raw_matmul "MoE gate" (router CTAs) +
+// dispatch_deepseek_moe_{score,hash}_route + dispatch_deepseek_moe_sanitize_indices (every CTA's
+// producer), expert_matmul "routed gate"/"routed up" + raw_matmul "shared gate"/"shared up" +
+// dispatch_deepseek_moe_swiglu (stream, kind A), expert_matmul "routed down" + raw_matmul "shared
+// down" (stream, kind B), dispatch_deepseek_moe_weighted_reduce + dispatch_hc_post (phase C).
 //
-// At 1-4 tokens every expert weight byte feeds 1-4 multiply-adds, so the block is bound by HBM
-// bandwidth once the weights stream, and by latency before that.  One launch holds all of it, so
-// no kernel boundary sits on the critical path and HBM never idles between the stages:
+// At 1-4 tokens every expert weight byte feeds 1-4 multiply-adds: the block is bound by HBM
+// bandwidth once the weights stream, and by latency before that.  Each CTA has 8 worker warps, one
+// producer warp and one publisher warp:
 //
-//   roles    the first CTAs to arrive take the prelude by a CTA ticket: `nm` mix CTAs (a column
-//            chunk of the flattened state each; the last one forms pre/post, publishes them and
-//            then forms the Sinkhorn comb), then `nr` router CTAs (a 64-wide chunk of hidden each:
-//            ffn_input, its RMS partial and the partial logits; the last one reduces, routes
-//            every row and groups the (row, slot) pairs by expert).  Router CTAs load their
-//            router-weight chunk before the mix is done.
-//   phase A  gate/up rows, group-major with the shared expert first (its tickets need no
-//            routing, so they start as soon as the normalised input is known):
-//            act[g, r, i] = silu(x_r . G[i]) * (x_r . U[i]); each row bumps its group's counter;
-//   phase B  down rows, group-major; a group's rows wait (bounded) until its gate/up rows are all
-//            published, then y[g, r, d] = act[g, r, :] . Dn[d, :]; each ticket bumps its d-block;
-//   phase C  per 32-wide d-block, once every group's rows of it are in: ffn_out = sum_g w * y and
-//            the hc_post output of that block.
+//   workers   (a) prelude: the first CTAs to arrive (a CTA ticket) are `nm` mix CTAs (a column chunk
+//             of the flattened state each: the partial mixes and sum of squares; the last one forms
+//             mixes, pre and post) and `nr` router CTAs.  Every CTA then forms x = ffn_norm(hc_pre)
+//             itself, on the 16 hidden columns each worker thread owns, from the mix partials and
+//             the state (in L2 by then), with the RMS over the CTA: x lands in the registers the
+//             stream needs and no CTA waits for another to publish it.  Router CTA j adds the
+//             logits of experts [j epc, (j + 1) epc) over the CTA and writes each (selection score
+//             sigmoid(logit) + bias, logit) pair with one 8-byte store.
+//             (b) the stream: every slot is consumed by all 8 warps at once (split K, x or the
+//             group's SwiGLU output in registers), each leaving its partial sums in shared memory:
+//               kind A: a gate row and an up row of one expert group;
+//               kind B: four down rows of one group, once its act is complete.
+//             (c) phase C: per 32-wide d-block, once every group's rows of it are in: ffn_out =
+//             sum_g w * y and the hc_post output of that block.
+//   producer  draws work tickets from a device-wide counter (in chunks of four consecutive numbers,
+//             two claims ahead) and moves each ticket's weight rows into a ring of shared-memory
+//             slots with bulk asynchronous copies (TMA, completion on the slot's mbarrier), so the
+//             bytes in flight cost no registers.  The shared expert needs no routing: its rows
+//             stream as soon as the mix CTAs have read the state.  At its first routed ticket it
+//             routes the batch itself, from the (score, logit) pairs (polled until written): the
+//             top_k by warp-shuffle argmax rounds, the same code on the same values in every CTA.
+//   publisher takes the slots in order: adds the 8 warps' partial sums, applies SwiGLU (kind A),
+//             stores act or y, frees the slot for the producer, and publishes completion counts
+//             in batches (one fence, then relaxed adds): a release fence waits microseconds under
+//             load, and no worker warp, which every slot needs, may stall on one.  It publishes
+//             whenever it has waited 2 us, so a batch never holds back work some CTA waits for.
+//             The last mix CTA's publisher also forms the comb (Sinkhorn) for phase C.
 //
-// Work is handed out by device-wide tickets, so only running CTAs ever hold work, and every wait
-// is for work that running CTAs hold: every wait ends whatever the number of co-resident CTAs.
-// Waits still give up after 1 s (device timeout bit).  The serial tails run once per call, out of
-// an instruction cache that streaming hundreds of MB through L2 leaves cold, so a few CTAs that
-// would otherwise idle first run them on scratch data ("dry" runs) to pull the code into L2.  The last CTA to leave resets the counters, so
-// the next launch (or a graph replay) starts from zero without a separate clearing step.
+// Code that runs once per launch runs out of an instruction cache that the weight stream (and a
+// benchmark's L2 flush) leaves cold; the producer therefore runs its routing code once on scratch
+// data at launch, so that the code is in L2 when the scores arrive.
+//
+// Tickets are drawn in order (all kind-A tickets before any kind-B ticket), a CTA consumes its
+// slots in ticket order, and a kind-B slot waits only for kind-A work, which running CTAs hold
+// ahead of it: every wait ends whatever the number of co-resident CTAs.  Waits still give up after
+// 1 s (device timeout bit), and a CTA that gives up first waits (bounded) for its own copies in
+// flight.  The last CTA to leave resets the counters and the score entries, so the next launch
+// (or a graph replay) starts clean without a separate clearing step.
 #include <math.h>
 #include <stddef.h>
 
@@ -56,96 +74,100 @@ struct DecodeArgs {
   // scratch
   float *mix_part;   // [nm, rows, M + 1] mix partial sums (the last entry: sum of squares)
   float *mixes, *pre, *post, *comb;
-  float *xw;         // [rows, hidden] ffn_input * ffn_norm weight (the RMS scale applied later)
-  float *ss_part;    // [nr, rows] partial sums of ffn_input^2
-  float *lg_part;    // [nr, rows, experts] partial logits (before the RMS scale)
-  float *row_rs;     // [rows] rsqrt(mean(ffn_input^2) + eps)
-  float *ffn_norm;   // [rows, hidden] stage tap, written by CTA 0
+  float *x;          // [rows, hidden] ffn_norm(ffn_input), written by router CTA 0 (also the stage tap)
+  float2 *sel;       // [4, experts] (selection score sigmoid(logit) + bias, logit); all-ones bits until written
+                     // in this launch (the last CTA out writes that pattern back)
   float *logits;     // [rows, experts]
-  int *ngroups, *group_e, *group_mask;
-  float *group_w;    // [groups, 4]
   float *act;        // [groups, 4, inter]
   float *y;          // [groups, 4, hidden]
   float *ffn_out, *out_state;
-  unsigned *counters;  // kDecCnt* layout below, zero at launch, zeroed again by the last CTA out
+  unsigned *counters;  // kCnt* layout below, zero at launch, zeroed again by the last CTA out
   int n_counters;
   int *status;
-  int rows, hidden, inter, experts, hc, M, iters, nm, nr, mix_chunk;
+  int rows, hidden, inter, experts, hc, M, iters, nm, nr, epc;
   float eps;
+  uint64_t wait_ns;  // bound of every wait
+  int inject;        // test hook: 1 = phase C first waits for a count that is never reached
 };
 
-// counter slots.  The prelude flags share one 128-byte line; each work-ticket counter, the group
-// counters and the d-block counters get lines of their own, so that the atomics of one phase do
-// not queue behind another's at the same L2 line.
-constexpr int kCntRole = 0, kCntMixDone = 1, kCntRtDone = 3, kCntRoute = 5,
-              kCntComb = 6, kCntExit = 7, kCntAbort = 8;
-constexpr int kCntTickA = 32, kCntTickB = 64, kCntTickC = 96, kCntGroups = 128;
+// counter slots.  The prelude flags share one 128-byte line; the ticket counters, the group
+// counters and the d-block counters get lines of their own.
+constexpr int kCntRole = 0, kCntMixDone = 1, kCntComb = 6, kCntExit = 7, kCntAbort = 8;
+constexpr unsigned kUnwritten = 0xFFFFFFFFu;  // an NaN pattern no arithmetic produces (CUDA's NaN is 0x7FFFFFFF)
+constexpr int kCntTick = 32, kCntTickC = 64, kCntGroups = 128;
 constexpr int kCntDBlocks = kCntGroups + 64;  // after the group counters, on a fresh line
 static_assert(kDecodeGroupsMax <= 64, "group counters fit before the d-block counters");
 
-constexpr uint64_t kSpinLimitNs = 1000000000ull;
-constexpr int kRouterChunk = 64;  // hidden columns per router CTA
+constexpr uint64_t kSpinLimitNs = 1000000000ull;  // default bound of every wait
+constexpr int kWorkerWarps = 8, kWorkers = 32 * kWorkerWarps, kDecThreads = kWorkers + 64;
+constexpr int kProducerWarp = kWorkerWarps, kPublisherWarp = kWorkerWarps + 1;
+constexpr int kPublishBatch = 16;  // slots a publisher may hold before it publishes their counts
 constexpr int kMixCols = 512;     // flattened-state columns per mix CTA (a multiple of 128)
-constexpr int kWarmCtas = 16;     // streaming-only CTAs that pre-run the prelude tails' code
-constexpr int kRowsPerTicketA = 1;  // gate/up rows per ticket
-constexpr int kRowsPerTicketB = 4;  // down rows per ticket (a 32-row d-block holds 8 tickets)
+constexpr int kRowsB = 4;         // down rows per kind-B slot
+constexpr int kChunk = 4;         // tickets claimed by one atomic of a producer (consecutive slots)
+// kind A: each worker thread owns 16 columns of a row (hidden <= 16 x 256 = 4096); kind B: 8
+// columns of a down row (inter <= 8 x 256 = 2048); moe_ffn_init enforces both limits
+constexpr int kMaxEpc = 4;        // experts per router CTA (64 CTAs up to 256 experts, 128 for 512)
 
-// Shared memory of the prelude roles (static; the streaming phases use the dynamic x buffer).
-// The arrays read or written as float4 come first, each 16-byte aligned (checked below).
-struct PreludeSmem {
-  alignas(16) float st[kDecodeRows][kMixCols];        // mix: state chunk; router: [rows][hc][64]
-  alignas(16) float xw[kDecodeRows][kRouterChunk];    // router: ffn_input * norm weight chunk
-  alignas(16) float lg[kDecodeRows][kExpertsMax];     // router tail: logits
-  alignas(16) float sc[kDecodeRows][kExpertsMax];     // router tail: selection scores
-  alignas(16) float bias[kExpertsMax];                // router: selection bias (score layers)
-  float sums[kDecodeRows][kMixMax + 1];               // mix tail: reduced sums
-  float nw[kRouterChunk];                             // router: norm weight chunk
-  float pre[kDecodeRows][kHcMax];
-  float hc_scale[3], hc_base[kMixMax];                // mix: split parameters
-  float red[8][kDecodeRows];
-  float rs[kDecodeRows];
-  int hash_e[kDecodeRows][kTopKMax];                  // router: tid2eid rows (hash layers)
-  int tok_ok[kDecodeRows];                            // router: token id in range (hash layers)
-  int sel[kDecodeRows][kTopKMax];
-  float w[kDecodeRows][kTopKMax];
-  int flag;
+template <bool MX>
+struct Ring {
+  static constexpr int kSlots = MX ? 10 : 6;  // two CTAs per SM: 2 x (96 or 85 KB) of slots
+  // bf16: a gate + up row pair (4 hidden bytes) or four down rows (8 inter bytes), 16 KB at most;
+  // MXFP8: the codes (2 hidden or 4 inter bytes) and their scales, each scale run copied as the
+  // 16-byte-aligned span that holds it
+  static constexpr int kSlotBytes = MX ? 8704 : 16384;
+  static constexpr int kRed = 16;  // partial sums per warp and slot (4 rows x 4 down rows at most)
+  static constexpr size_t kSmem = (size_t)kSlots * kSlotBytes + (size_t)kSlots * kWorkerWarps * kRed * 4;
 };
-static_assert(offsetof(PreludeSmem, st) % 16 == 0 && offsetof(PreludeSmem, xw) % 16 == 0 &&
-                  offsetof(PreludeSmem, lg) % 16 == 0 && offsetof(PreludeSmem, sc) % 16 == 0 &&
-                  (kMixCols * 4) % 16 == 0 && (kRouterChunk * 4) % 16 == 0 && (kExpertsMax * 4) % 16 == 0,
-              "float4 accesses of the prelude shared memory need 16-byte aligned rows");
 
-__device__ __forceinline__ uint4 ld_weight(const uint16_t *p) { return ld_stream(p); }
+enum : int { kKindA = 0, kKindB = 1, kKindEnd = 2 };
+struct SlotMeta {
+  int kind, g, row, e, mask, s0, s1;  // row: i (kind A) or the first of four down rows (kind B)
+};
 
-// act is written during this kernel, so it is read through L1 (ld.global.ca) only after the
-// reading warp has acquired its group's completion counter: no line of it can be cached earlier.
-__device__ __forceinline__ float4 ld_ca4(const float *p) {
-  float4 v;
-  asm volatile("ld.global.ca.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "l"(p)
-               : "memory");
-  return v;
-}
+// Shared memory outside the ring (static).
+struct DecSmem {
+  // mix role
+  alignas(16) float st[kDecodeRows][kMixCols];
+  float sums[kDecodeRows][kMixMax + 1];
+  float mixes[kDecodeRows][kMixMax];  // the last mix CTA's mixes, for its publisher's Sinkhorn
+  int comb_todo;                      // mix CTAs: 1 = the last one (its publisher forms the comb), 2 = not
+  float hc_scale[3], hc_base[kMixMax];
+  float red[kWorkerWarps][32];
+  float pre[kDecodeRows][kHcMax];
+  float rs[kDecodeRows];
+  // ring bookkeeping
+  SlotMeta meta[12];
+  // the producer's (row, slot) pairs while it groups them, then the group table
+  float rtw[32];
+  int ng;
+  int ge[kDecodeGroupsMax], gm[kDecodeGroupsMax];
+  float gw[kDecodeGroupsMax][kDecodeRows];
+  int flag, abort;
+};
+
+__device__ __forceinline__ void workers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory"); }
 
 // Adds n to a completion counter with release semantics: this thread's earlier writes (and those
 // ordered before them by a fence) are visible to whoever acquires the new value.
 __device__ __forceinline__ void publish(unsigned *counter, unsigned n) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(counter), "r"(n) : "memory");
 }
+// The same add without ordering of its own (after a fence, it publishes what the fence ordered).
+__device__ __forceinline__ void add_relaxed(unsigned *counter, unsigned n) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(counter), "r"(n) : "memory");
+}
 
 // Polls (one thread) until *counter >= target, with a bounded wait.  False on timeout; once any
-// wait of this launch has timed out (`abort`, a counter slot of the launch), every later wait of
-// the launch fails at once, so that a failed launch still ends quickly.
-// `nap`: sleep briefly between polls (waits that may last, with many waiters); without it the
-// poll spins, for the short waits at the end of the launch where latency is all that counts.
-__device__ bool poll_at_least(const unsigned *counter, unsigned target, int *status, unsigned *abort,
-                              bool nap = true) {
+// wait of this launch has timed out (the launch's abort counter), every later wait of the launch
+// fails at once, so that a failed launch still ends quickly.
+__device__ bool poll_at_least(const unsigned *counter, unsigned target, const DecodeArgs &a, bool nap = true) {
   if (ld_acquire_u32(counter) >= target) return true;
+  unsigned *abort = a.counters + kCntAbort;
   const uint64_t w0 = global_timer_ns();
   while (ld_acquire_u32(counter) < target) {
-    if (*reinterpret_cast<volatile unsigned *>(abort) != 0u || global_timer_ns() - w0 > kSpinLimitNs) {
-      atomicOr(status, kDevTimeout);
+    if (*reinterpret_cast<volatile unsigned *>(abort) != 0u || global_timer_ns() - w0 > a.wait_ns) {
+      atomicOr(a.status, kDevTimeout);
       atomicExch(abort, 1u);
       return false;
     }
@@ -156,43 +178,52 @@ __device__ bool poll_at_least(const unsigned *counter, unsigned target, int *sta
 
 // Warp-wide bounded wait: lane 0 polls, then every lane acquires the counter so that its later
 // reads see what the producers published.
-__device__ bool wait_at_least(const unsigned *counter, unsigned target, int *status, unsigned *abort,
-                              bool nap = true) {
+__device__ bool wait_at_least(const unsigned *counter, unsigned target, const DecodeArgs &a, bool nap = true) {
   int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = poll_at_least(counter, target, status, abort, nap) ? 1 : 0;
+  if ((threadIdx.x & 31) == 0) ok = poll_at_least(counter, target, a, nap) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
   if (ok) (void)ld_acquire_u32(counter);
   return ok != 0;
 }
 
-// CTA-wide bounded wait (every thread of the CTA calls it).
-__device__ bool cta_wait_at_least(const unsigned *counter, unsigned target, int *status, unsigned *abort,
-                                  int *s_flag) {
-  if (threadIdx.x == 0) *s_flag = poll_at_least(counter, target, status, abort) ? 1 : 0;
-  __syncthreads();
+// Worker-wide bounded wait (every worker thread calls it).
+__device__ bool workers_wait_at_least(const unsigned *counter, unsigned target, const DecodeArgs &a, int *s_flag) {
+  if (threadIdx.x == 0) *s_flag = poll_at_least(counter, target, a) ? 1 : 0;
+  workers_sync();
   const bool ok = *s_flag != 0;
   if (ok) (void)ld_acquire_u32(counter);
-  __syncthreads();
+  workers_sync();
   return ok;
 }
 
-// Next work ticket of a phase: lane 0 draws it, the warp shares it.
+// True in exactly one CTA: the last of `total` to finish its share of a role (all earlier global
+// writes of every worker thread of the CTA are fenced before the count).
+__device__ bool workers_arrive_last(unsigned *count, unsigned total, int *s_flag) {
+  __threadfence();
+  workers_sync();
+  if (threadIdx.x == 0) *s_flag = atomicAdd(count, 1u) == total - 1 ? 1 : 0;
+  workers_sync();
+  const bool last = *s_flag != 0;
+  if (last) __threadfence();
+  return last;
+}
+
+// Next phase-C ticket: lane 0 draws it, the warp shares it.
 __device__ __forceinline__ int draw_ticket(unsigned *tick) {
   int c = 0;
   if ((threadIdx.x & 31) == 0) c = (int)atomicAdd(tick, 1u);
   return __shfl_sync(0xffffffffu, c, 0);
 }
 
-// True in exactly one CTA: the last of `total` to finish its share of a role (all earlier global
-// writes of every thread of the CTA are fenced before the count).
-__device__ bool cta_arrive_last(unsigned *count, unsigned total, int *s_flag) {
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) *s_flag = atomicAdd(count, 1u) == total - 1 ? 1 : 0;
-  __syncthreads();
-  const bool last = *s_flag != 0;
-  if (last) __threadfence();
-  return last;
+// Warp-wide bounded mbarrier wait (lane 0 waits, the warp follows its verdict); a timeout also
+// raises the launch's abort flag.
+__device__ bool warp_mbar_wait(uint64_t *bar, uint32_t parity, DecSmem &sm, const DecodeArgs &a) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) {
+    ok = mbar_wait_bounded(bar, parity, &sm.abort, a.status, a.wait_ns) ? 1 : 0;
+    if (!ok) atomicExch(&a.counters[kCntAbort], 1u);
+  }
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 // One lane's share of the mix partial sums of item `it` (row r, output m; it = r * (M + 1) + m):
@@ -213,17 +244,42 @@ __device__ __forceinline__ float hc_gate(float sum, float rs, float scale, float
   return sigmoidf_(fmaf(sum * rs, scale, base));
 }
 
+// Sum over the warp of V values per lane (V a power of two, at most 32), scattered: afterwards lane
+// l holds the warp total of value l % V (V - 1 shuffles halve the live values, then the remaining
+// lanes are summed).
+template <int V>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[V]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int s = V / 2; s >= 1; s >>= 1) {
+    const bool hi = (lane & s) != 0;
+#pragma unroll
+    for (int i = 0; i < s; ++i) {
+      const float send = hi ? v[i] : v[i + s];
+      const float keep = hi ? v[i + s] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+  float x = v[0];
+#pragma unroll
+  for (int o = V; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+__host__ __device__ constexpr int pow2_at_least(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : n <= 8 ? 8 : n <= 16 ? 16 : 32; }
+
 // ---------------------------------------------------------------------------------------------
 // Mix role (rms_norm_no_scale_f32 + raw_matmul "HC FFN function" + dispatch_hc_split_sinkhorn).
 // Per row: ss = sum x^2 and dot_m = sum x * hc_fn[m] over the flattened hc*hidden state;
 // mixes = dot * rsqrt(ss / (hc*hidden) + eps) (the RMS scale factors out of the dot product).
 // ---------------------------------------------------------------------------------------------
 
-// Tail of the mix role, run by the last mix CTA, off the critical path (the router CTAs form pre
-// themselves from the same partials): the mixes, pre and post of every row, then the comb
-// (Sinkhorn), which only the final hc_post needs, published.
+// Tail of the mix role, run by the last mix CTA's workers: the mixes, pre and post of every row
+// (the router and stream CTAs form pre themselves from the same partials).  The comb (Sinkhorn),
+// which only the final hc_post needs, is left to the CTA's publisher warp, idle until the first
+// slot is full, so that the workers go on to form x at once.
 template <int ROWS>
-__device__ __noinline__ void mix_tail(const DecodeArgs &a, PreludeSmem &sm, unsigned *cnt) {
+__device__ __noinline__ void mix_tail(const DecodeArgs &a, DecSmem &sm) {
   constexpr int rows = ROWS;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, M = a.M, hc = a.hc;
   const int items = rows * (M + 1);
@@ -241,27 +297,37 @@ __device__ __noinline__ void mix_tail(const DecodeArgs &a, PreludeSmem &sm, unsi
     const float x = warp_sum(v[k]);
     if (lane == 0 && it < items) sm.sums[it / (M + 1)][it % (M + 1)] = x;
   }
-  __syncthreads();
+  workers_sync();
   if (tid < rows) {
     const float rs = mix_rs(sm.sums[tid][M], hc * a.hidden, a.eps);
     for (int h = 0; h < hc; ++h) {
       a.pre[tid * hc + h] = hc_gate(sm.sums[tid][h], rs, sm.hc_scale[0], sm.hc_base[h]);
       a.post[tid * hc + h] = 2.0f * hc_gate(sm.sums[tid][hc + h], rs, sm.hc_scale[1], sm.hc_base[hc + h]);
     }
-    for (int m = 0; m < M; ++m) a.mixes[tid * M + m] = sm.sums[tid][m] * rs;
+    for (int m = 0; m < M; ++m) {
+      const float mx = sm.sums[tid][m] * rs;
+      a.mixes[tid * M + m] = mx;
+      sm.mixes[tid][m] = mx;
+    }
   }
-  __syncthreads();
-  if (warp < rows) sinkhorn_comb_warp(a.mixes + warp * M, sm.hc_scale, sm.hc_base, hc, a.iters, a.comb + warp * hc * hc);
+  workers_sync();
+}
+
+// The comb of every row (split + Sinkhorn) by the last mix CTA's publisher warp, published for
+// phase C.
+template <int ROWS>
+__device__ __noinline__ void mix_comb(const DecodeArgs &a, DecSmem &sm, unsigned *cnt) {
+  for (int r = 0; r < ROWS; ++r) sinkhorn_comb_warp(&sm.mixes[r][0], sm.hc_scale, sm.hc_base, a.hc, a.iters, a.comb + r * a.hc * a.hc);
   __threadfence();
-  __syncthreads();
-  if (tid == 0) publish(&cnt[kCntComb], 1u);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) publish(&cnt[kCntComb], 1u);
 }
 
 // Mix CTA j: flattened-state columns [j * kMixCols, +kMixCols) (the last chunk may be shorter, a
 // multiple of 128).  Warp w forms outputs w, w + 8, w + 16; lane l covers columns 4l + 128p of the
 // chunk, so the shared-memory state reads are conflict-free and the hc_fn reads coalesced.
 template <int ROWS>
-__device__ void mix_role(const DecodeArgs &a, int j, PreludeSmem &sm, unsigned *cnt) {
+__device__ void mix_role(const DecodeArgs &a, int j, DecSmem &sm, unsigned *cnt) {
   constexpr int rows = ROWS;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hcd = a.hc * a.hidden, M = a.M;
@@ -280,7 +346,7 @@ __device__ void mix_role(const DecodeArgs &a, int j, PreludeSmem &sm, unsigned *
   if (tid < M) sm.hc_base[tid] = a.hc_base[tid];
   pdl_wait();
   // the state chunk (one float4 per thread and row)
-  static_assert(kMixCols / 4 <= 256, "one float4 of each row per thread");
+  static_assert(kMixCols / 4 <= kWorkers, "one float4 of each row per thread");
   float4 sv[kDecodeRows];
 #pragma unroll
   for (int r = 0; r < kDecodeRows; ++r)
@@ -293,7 +359,7 @@ __device__ void mix_role(const DecodeArgs &a, int j, PreludeSmem &sm, unsigned *
     if (tid < width / 4) *reinterpret_cast<float4 *>(&sm.st[r][tid * 4]) = v;
     ss[r] = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
   }
-  __syncthreads();
+  workers_sync();
   float acc[3][kDecodeRows];
 #pragma unroll
   for (int q = 0; q < 3; ++q)
@@ -328,615 +394,822 @@ __device__ void mix_role(const DecodeArgs &a, int j, PreludeSmem &sm, unsigned *
       if (lane == 0) sm.red[warp][r] = s;
     }
   }
-  __syncthreads();
+  workers_sync();
   if (tid < rows) {
     float s = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) s += sm.red[w][tid];
+    for (int w = 0; w < kWorkerWarps; ++w) s += sm.red[w][tid];
     a.mix_part[((size_t)j * rows + tid) * (M + 1) + M] = s;
   }
-  if (cta_arrive_last(&cnt[kCntMixDone], (unsigned)a.nm, &sm.flag)) mix_tail<ROWS>(a, sm, cnt);
+  const bool last = workers_arrive_last(&cnt[kCntMixDone], (unsigned)a.nm, &sm.flag);
+  if (last) mix_tail<ROWS>(a, sm);
+  if (tid == 0) {  // after mix_tail's shared-memory writes
+    __threadfence_block();
+    *reinterpret_cast<volatile int *>(&sm.comb_todo) = last ? 1 : 2;
+  }
 }
 
 // ---------------------------------------------------------------------------------------------
-// Router role (dispatch_hc_pre + rms_norm + raw_matmul "MoE gate" + the route and sanitize
-// dispatches).  ffn_input v = sum_h pre[h] * state[h]; logits = rs * sum_d (v_d * w_d) * gate[e, d]
-// with rs = rsqrt(mean(v^2) + eps): the RMS scale factors out of the dot product, so each router
-// CTA works on its own chunk of hidden and only the last one needs the whole row.
+// x in every CTA (dispatch_hc_pre + rms_norm), and the router role (raw_matmul "MoE gate" for a
+// share of the experts).  Each worker thread owns 16 columns of hidden: bf16 experts, 8t .. 8t + 7
+// and 2048 + 8t .. 2048 + 8t + 7 (conflict-free 16-byte reads of a shared-memory weight row);
+// MXFP8 experts, 16t .. 16t + 15 (one 16-byte load of codes).  Every CTA forms x on its own
+// columns from the mix partials and the state (in L2 by then), with the RMS over the CTA, so no CTA
+// waits for another to publish x; router CTA j then adds the logits of experts [j epc, (j + 1)
+// epc) over the CTA and publishes their selection scores sigmoid(logit) + bias (f32).
 // ---------------------------------------------------------------------------------------------
+template <bool MX>
+__device__ __forceinline__ int own_col(int tid, int h) { return MX ? 16 * tid + 8 * h : 8 * tid + 2048 * h; }
 
-// RMS scale of row r from the router CTAs' partial sums of squares, by one warp (lane l: router
-// CTAs l, l + 32, ...; then a warp sum).  The router tail and every streaming CTA form it this
-// way, so all of them get the same bits.
-__device__ __forceinline__ float row_rs_from_partials(const DecodeArgs &a, int rows, int r, int nsum) {
-  const int lane = threadIdx.x & 31;
-  float x = 0.f;
-  for (int c = lane; c < nsum; c += 32) x += __ldcg(a.ss_part + c * rows + r);
-  x = warp_sum(x);
-  return rsqrtf(x / (float)a.hidden + a.eps);
-}
-
-// Routing of row r by one warp.  Score layers: top_k on the selection scores sigmoid(logit) + bias
-// (formed beforehand in sm.sc, in f32; ties to the lower expert index), weights = the chosen
-// unbiased scores / their sum.  Hash layers: the tid2eid row in table order, weights =
-// sigmoid(logit) normalised over the valid slots.
-__device__ void route_row(const DecodeArgs &a, PreludeSmem &sm, int r, bool live) {
-  const RouteParams &p = a.rp;
-  const int lane = threadIdx.x & 31, E = p.experts, K = p.top_k;
-  int my_sel = -1;
-  if (!p.hash) {
-    uint32_t taken = 0;  // bit j: expert lane + 32 j already chosen
-#pragma unroll 1
-    for (int k = 0; k < K; ++k) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-#pragma unroll 1
-      for (int j = 0, e = lane; e < E; ++j, e += 32) {
-        const float x = sm.sc[r][e];
-        if (!((taken >> j) & 1u) && (x > bv || be == 0x7fffffff)) {
-          bv = x;
-          be = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (lane == k) my_sel = be;
-    }
-  } else {
-    const bool tok_ok = sm.tok_ok[r] != 0;
-    if (!tok_ok && lane == 0 && live) atomicOr(p.status, kDevTokenRange);
-    if (lane < K) my_sel = sm.hash_e[r][lane];
-    const bool bad_entry = tok_ok && lane < K && !(my_sel >= 0 && my_sel < E);
-    if (__any_sync(0xffffffffu, bad_entry) && lane == 0 && live) atomicOr(p.status, kDevRouteRange);
-  }
-  const bool valid = lane < K && my_sel >= 0 && my_sel < E;
-  const float sc = valid ? sigmoidf_(sm.lg[r][my_sel]) : 0.f;
-  const float tot = warp_sum(sc);
-  if (lane < K) {
-    const float w = tot > 0.f ? sc / tot : 0.f;
-    if (live) {
-      p.idx[r * K + lane] = my_sel;
-      p.rw[r * K + lane] = w;
-      p.safe[r * K + lane] = valid ? (unsigned)my_sel : 0u;
-    }
-    sm.sel[r][lane] = my_sel;
-    sm.w[r][lane] = w;
-  }
-}
-
-// Groups the (row, slot) pairs by expert, one pair per lane of one warp (rows * top_k <= 32).
-// Group 0 is the shared expert (weight 1 for every row); then the distinct routed experts in order
-// of first appearance, each with the mask of rows using it and their summed route weights.
-template <int ROWS>
-__device__ void group_rows(const DecodeArgs &a, PreludeSmem &sm, bool live) {
-  constexpr int rows = ROWS;
-  const int lane = threadIdx.x & 31, K = a.rp.top_k, E = a.experts;
-  int e = -1;
-  if (lane < rows * K) e = sm.sel[lane / K][lane % K];
-  const bool valid = lane < rows * K && e >= 0 && e < E;
-  const unsigned same = __match_any_sync(0xffffffffu, valid ? e : E + 1 + lane);
-  const unsigned below = (1u << lane) - 1u;
-  const bool leader = valid && (same & below) == 0u;
-  const unsigned leaders = __ballot_sync(0xffffffffu, leader);
-  if (leader && live) {
-    const int g = 1 + __popc(leaders & below);
-    int mask = 0;
-    float w0 = 0.f, w1 = 0.f, w2 = 0.f, w3 = 0.f;
-    for (unsigned m = same; m != 0u; m &= m - 1u) {
-      const int b = __ffs(m) - 1, rb = b / K;
-      const float wb = sm.w[rb][b - rb * K];
-      mask |= 1 << rb;
-      if (rb == 0) w0 += wb;
-      else if (rb == 1) w1 += wb;
-      else if (rb == 2) w2 += wb;
-      else w3 += wb;
-    }
-    a.group_e[g] = e;
-    a.group_mask[g] = mask;
-    *reinterpret_cast<float4 *>(a.group_w + g * 4) = make_float4(w0, w1, w2, w3);
-  }
-  if (lane == 0 && live) {
-    a.group_e[0] = E;
-    a.group_mask[0] = (1 << rows) - 1;
-    *reinterpret_cast<float4 *>(a.group_w) =
-        make_float4(1.f, rows > 1 ? 1.f : 0.f, rows > 2 ? 1.f : 0.f, rows > 3 ? 1.f : 0.f);
-    *a.ngroups = 1 + __popc(leaders);
-  }
-}
-
-// Tail of the router role, run by the last router CTA: the RMS scale of every row, the logits
-// reduced in a fixed order, the selection scores (every thread a share), routing (one
-// warp per row) and grouping (published).  `live` false: the same code
-// with one partial and no global write or publication, run by idle CTAs to bring it into L2.
-template <int ROWS>
-__device__ __noinline__ void router_tail(const DecodeArgs &a, PreludeSmem &sm, unsigned *cnt, bool live) {
+template <int ROWS, bool MX>
+__device__ __forceinline__ void form_x(const DecodeArgs &a, DecSmem &sm, unsigned *cnt, float4 (&xr)[ROWS][4]) {
   constexpr int rows = ROWS;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int E = a.experts;
-  const int nsum = live ? a.nr : 1;
-  // RMS scales (the streaming CTAs form the same values themselves)
-  if (warp < rows) {
-    const float rs = row_rs_from_partials(a, rows, warp, nsum);
-    if (lane == 0) {
-      sm.rs[warp] = rs;
-      if (live) a.row_rs[warp] = rs;
-    }
-  }
-  __syncthreads();
-  // logits: four quarters of the router CTAs per (row, 4 experts); each thread issues its quarter's
-  // loads back to back, then the quarters are added in a fixed order
-  const int E4 = E / 4, units = rows * E4, q4 = (nsum + 3) / 4;
-  for (int u0 = 0; u0 < units * 4; u0 += blockDim.x) {
-    const int u = u0 + tid;
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (u < units * 4) {
-      const int item = u >> 2, quarter = u & 3;
-      const int r = item / E4, e = (item - r * E4) * 4;
-      const float *p = a.lg_part + (size_t)r * E + e;
-      const int c0 = quarter * q4, c1 = min(nsum, c0 + q4);
-#pragma unroll 8
-      for (int c = c0; c < c1; ++c) {
-        const float4 v = __ldcg(reinterpret_cast<const float4 *>(p + (size_t)c * rows * E));
-        s.x += v.x;
-        s.y += v.y;
-        s.z += v.z;
-        s.w += v.w;
-      }
-    }
-    // the four quarters of an item sit in four neighbouring lanes
+  const int D = a.hidden, hc = a.hc, M = a.M;
+  float4 nw[4];
 #pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-      s.x += __shfl_xor_sync(0xffffffffu, s.x, o);
-      s.y += __shfl_xor_sync(0xffffffffu, s.y, o);
-      s.z += __shfl_xor_sync(0xffffffffu, s.z, o);
-      s.w += __shfl_xor_sync(0xffffffffu, s.w, o);
-    }
-    if (u < units * 4 && (u & 3) == 0) {
-      const int item = u >> 2, r = item / E4, e = (item - r * E4) * 4;
-      const float rs = sm.rs[r];
-      const float4 l = make_float4(s.x * rs, s.y * rs, s.z * rs, s.w * rs);
-      *reinterpret_cast<float4 *>(&sm.lg[r][e]) = l;
-      if (live) *reinterpret_cast<float4 *>(a.logits + (size_t)r * E + e) = l;
-    }
+  for (int h = 0; h < 2; ++h) {
+    const int c = own_col<MX>(tid, h);
+    const float4 *np = reinterpret_cast<const float4 *>(a.norm_w + c);
+    nw[2 * h] = c < D ? __ldg(np) : make_float4(0.f, 0.f, 0.f, 0.f);
+    nw[2 * h + 1] = c < D ? __ldg(np + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  if (tid == 0) sm.flag = 0;
-  __syncthreads();
-  // selection scores sigmoid(logit) + bias (score layers), a non-finite logit flagged
-  if (!a.rp.hash) {
-    bool bad = false;
-    for (int i = tid; i < rows * E; i += blockDim.x) {
-      const int r = i / E, e = i - r * E;
-      const float l = sm.lg[r][e];
-      bad |= !isfinite(l);
-      const float x = sigmoidf_(l) + sm.bias[e];
-      sm.sc[r][e] = isnan(x) ? -INFINITY : x;
-    }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) sm.flag = 1;
-  }
-  __syncthreads();
-  if (tid == 0 && sm.flag && live) atomicOr(a.rp.status, kDevNonFinite);
-  if (warp < rows) route_row(a, sm, warp, live);
-  __syncthreads();
-  if (warp == 0) group_rows<ROWS>(a, sm, live);
-  if (live) __threadfence();
-  __syncthreads();
-  if (tid == 0 && live) publish(&cnt[kCntRoute], 1u);
-}
-
-// Router CTA j: hidden columns [64 j, 64 j + 64).  Thread e holds expert e's 64 router weights of
-// the chunk in registers (experts beyond the block size are read when needed).  pre is formed
-// here from the mix CTAs' partial sums, as soon as all of them are in.
-template <int ROWS>
-__device__ void router_role(const DecodeArgs &a, int j, PreludeSmem &sm, unsigned *cnt) {
-  constexpr int rows = ROWS;
-  const RouteParams &p = a.rp;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int E = a.experts, D = a.hidden, hc = a.hc, K = p.top_k, M = a.M;
-  const int d0 = j * kRouterChunk;
-  // weights do not come from the previous kernel: load them before waiting for it
-  uint4 gw[8];
-#pragma unroll
-  for (int q = 0; q < 8; ++q)
-    gw[q] = tid < E ? __ldg(reinterpret_cast<const uint4 *>(a.gate + (size_t)tid * D + d0 + 8 * q))
-                    : make_uint4(0u, 0u, 0u, 0u);
-  if (tid < kRouterChunk) sm.nw[tid] = a.norm_w[d0 + tid];
-  for (int e = tid; e < E; e += blockDim.x) sm.bias[e] = p.hash ? 0.f : p.bias[e];
   if (tid == 0) sm.hc_scale[0] = a.hc_scale[0];
   if (tid < hc) sm.hc_base[tid] = a.hc_base[tid];
   pdl_wait();
-  float(&st)[kDecodeRows][kHcMax][kRouterChunk] =
-      *reinterpret_cast<float(*)[kDecodeRows][kHcMax][kRouterChunk]>(&sm.st[0][0]);
-  for (int i = tid; i < rows * hc * (kRouterChunk / 4); i += blockDim.x) {
-    const int rh = i / (kRouterChunk / 4), c = (i - rh * (kRouterChunk / 4)) * 4;
-    const int r = rh / hc, h = rh - r * hc;
-    *reinterpret_cast<float4 *>(&st[r][h][c]) =
-        __ldcg(reinterpret_cast<const float4 *>(a.state + ((size_t)r * hc + h) * D + d0 + c));
-  }
-  if (p.hash && tid < rows * K) {
-    const int r = tid / K, k = tid - r * K;
-    const int tok = p.token_ids[r];
-    const bool ok = tok >= 0 && tok < p.vocab;
-    sm.hash_e[r][k] = ok ? p.tid2eid[(size_t)tok * K + k] : -1;
-    if (k == 0) sm.tok_ok[r] = ok ? 1 : 0;
-  }
   // pre from the mix partials, once every mix CTA has written its own (bounded wait; on timeout
   // the status says so and the values below are not meaningful, but every CTA still finishes)
-  (void)cta_wait_at_least(&cnt[kCntMixDone], (unsigned)a.nm, a.status, &cnt[kCntAbort], &sm.flag);
+  (void)workers_wait_at_least(&cnt[kCntMixDone], (unsigned)a.nm, a, &sm.flag);
   {
     // items (r, h < hc) and (r, M): warp w reduces items w and w + 8, ...
     const int per = hc + 1, items = rows * per;
-    for (int k = warp; k < items; k += 8) {
+    for (int k = warp; k < items; k += kWorkerWarps) {
       const int r = k / per, h = k - r * per;
       const int m = h < hc ? h : M;
       const float x = warp_sum(mix_item_partial(a, rows * (M + 1), r * (M + 1) + m, lane));
       if (lane == 0) sm.sums[r][h] = x;
     }
   }
-  __syncthreads();
+  workers_sync();
   if (tid < rows * hc) {
     const int r = tid / hc, h = tid - r * hc;
     sm.pre[r][h] = hc_gate(sm.sums[r][h], mix_rs(sm.sums[r][hc], hc * D, a.eps), sm.hc_scale[0], sm.hc_base[h]);
   }
-  __syncthreads();
-  float ssq = 0.f;
-  if (tid < rows * kRouterChunk) {
-    const int r = tid / kRouterChunk, d = tid - r * kRouterChunk;
-    float v = 0.f;
-    for (int h = 0; h < hc; ++h) v += sm.pre[r][h] * st[r][h][d];
-    const float xw = v * sm.nw[d];
-    sm.xw[r][d] = xw;
-    a.xw[(size_t)r * D + d0 + d] = xw;
-    ssq = v * v;
-  }
-  ssq = warp_sum(ssq);
-  if (lane == 0) sm.red[warp][0] = ssq;
-  __syncthreads();
-  static_assert(kRouterChunk == 64, "two warps per row below");
-  if (tid < rows) a.ss_part[j * rows + tid] = sm.red[2 * tid][0] + sm.red[2 * tid + 1][0];
-  auto partial_logits = [&](int e, const uint4(&w)[8]) {
+  workers_sync();
+  // ffn_input = sum_h pre[h] * state[h] on the own columns, and its sum of squares per row
+  float ssq[kDecodeRows] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int r = 0; r < rows; ++r) {
+  for (int r = 0; r < rows; ++r) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) xr[r][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+    for (int h = 0; h < hc; ++h) {
+      const float ph = sm.pre[r][h];
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        const int c = own_col<MX>(tid, g);
+        if (c < D) {
+          const float4 *sp = reinterpret_cast<const float4 *>(a.state + ((size_t)r * hc + h) * D + c);
+          const float4 s0 = __ldcg(sp), s1 = __ldcg(sp + 1);
+          xr[r][2 * g] = make_float4(xr[r][2 * g].x + ph * s0.x, xr[r][2 * g].y + ph * s0.y, xr[r][2 * g].z + ph * s0.z,
+                                     xr[r][2 * g].w + ph * s0.w);
+          xr[r][2 * g + 1] = make_float4(xr[r][2 * g + 1].x + ph * s1.x, xr[r][2 * g + 1].y + ph * s1.y,
+                                         xr[r][2 * g + 1].z + ph * s1.z, xr[r][2 * g + 1].w + ph * s1.w);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      ssq[r] += xr[r][i].x * xr[r][i].x + xr[r][i].y * xr[r][i].y + xr[r][i].z * xr[r][i].z + xr[r][i].w * xr[r][i].w;
+  }
+  {
+    float t4[4] = {ssq[0], ssq[1], ssq[2], ssq[3]};
+    const float s = warp_reduce_scatter<4>(t4);  // lane l: the warp total of row l % 4
+    if (lane < 4) sm.red[warp][lane] = s;
+  }
+  workers_sync();
+  // x = ffn_input * rs * norm weight, rs = rsqrt(mean(ffn_input^2) + eps) over the CTA's columns
+  // (all of hidden); CTA 0 also writes x out (the ffn_norm stage tap)
+#pragma unroll
+  for (int r = 0; r < rows; ++r) {
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWorkerWarps; ++w) tot += sm.red[w][r];
+    const float rs = rsqrtf(tot / (float)D + a.eps);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      xr[r][i] = make_float4(xr[r][i].x * rs * nw[i].x, xr[r][i].y * rs * nw[i].y, xr[r][i].z * rs * nw[i].z,
+                             xr[r][i].w * rs * nw[i].w);
+    if (blockIdx.x == 0) {
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        const int c = own_col<MX>(tid, g);
+        if (c < D) {
+          float4 *xp = reinterpret_cast<float4 *>(a.x + (size_t)r * D + c);
+          xp[0] = xr[r][2 * g];
+          xp[1] = xr[r][2 * g + 1];
+        }
+      }
+    }
+  }
+  workers_sync();  // sm.red is free again
+}
+
+// Router CTA j: its experts' rows of the router matrix go to L2 at launch (they do not depend on
+// the previous kernel), and are read on the own columns once x is formed.
+__device__ __forceinline__ void router_prefetch(const DecodeArgs &a, int j) {
+  const int e0 = j * a.epc, ne = min(a.epc, a.experts - e0);
+  if ((int)threadIdx.x < ne) prefetch_l2(a.gate + (size_t)(e0 + threadIdx.x) * a.hidden, (uint32_t)(a.hidden * 2), make_policy_evict_last());
+}
+
+template <int ROWS, bool MX>
+__device__ __forceinline__ void router_logits(const DecodeArgs &a, DecSmem &sm, unsigned *cnt, int j,
+                                           const float4 (&xr)[ROWS][4]) {
+  constexpr int rows = ROWS;
+  const RouteParams &p = a.rp;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = a.experts, D = a.hidden;
+  const int e0 = j * a.epc, ne = min(a.epc, E - e0);
+  uint4 gw[kMaxEpc][2];
+#pragma unroll
+  for (int q = 0; q < kMaxEpc; ++q)
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      const int c = own_col<MX>(tid, g);
+      gw[q][g] = q < ne && c < D ? __ldg(reinterpret_cast<const uint4 *>(a.gate + (size_t)(e0 + q) * D + c))
+                                 : make_uint4(0u, 0u, 0u, 0u);
+    }
+  // item q * ROWS + r: expert e0 + q, row r; summed over the CTA (lane l of each warp holds the
+  // warp total of item l, then warp 0 adds the warps' totals)
+  constexpr int V = pow2_at_least(kMaxEpc * ROWS);
+  float lp[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) lp[i] = 0.f;
+#pragma unroll
+  for (int q = 0; q < kMaxEpc; ++q)
+#pragma unroll
+    for (int r = 0; r < rows; ++r)
+      lp[q * ROWS + r] = dot8(gw[q][0], xr[r][0], xr[r][1]) + dot8(gw[q][1], xr[r][2], xr[r][3]);
+  const float wt = warp_reduce_scatter<V>(lp);
+  if (lane < V) sm.red[warp][lane] = wt;
+  workers_sync();
+  if (warp == 0) {
+    bool bad = false;
+    if (lane < ne * ROWS) {
       float l = 0.f;
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        l += dot8(w[q], *reinterpret_cast<const float4 *>(&sm.xw[r][8 * q]),
-                  *reinterpret_cast<const float4 *>(&sm.xw[r][8 * q + 4]));
-      a.lg_part[((size_t)j * rows + r) * E + e] = l;
+      for (int w = 0; w < kWorkerWarps; ++w) l += sm.red[w][lane];
+      const int q = lane / ROWS, r = lane - q * ROWS, e = e0 + q;
+      bad = !isfinite(l);
+      a.logits[(size_t)r * E + e] = l;  // the stage tap
+      float sc = 0.f;
+      if (!p.hash) {
+        sc = sigmoidf_(l) + p.bias[e];
+        sc = isnan(sc) ? -INFINITY : sc;
+      }
+      // one 8-byte store: a reader that sees it sees both values (no fence or counter needed: the
+      // producers poll these entries until none holds the unwritten pattern)
+      a.sel[(size_t)r * E + e] = make_float2(sc, l);
     }
-  };
-  if (tid < E) partial_logits(tid, gw);
-  for (int e = tid + blockDim.x; e < E; e += blockDim.x) {
-    uint4 w[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) w[q] = __ldg(reinterpret_cast<const uint4 *>(a.gate + (size_t)e * D + d0 + 8 * q));
-    partial_logits(e, w);
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, kDevNonFinite);
   }
-  if (cta_arrive_last(&cnt[kCntRtDone], (unsigned)a.nr, &sm.flag)) router_tail<ROWS>(a, sm, cnt, true);
+  workers_sync();  // sm.red is free again
 }
 
 // ---------------------------------------------------------------------------------------------
-// Streaming phases
+// Routing, by each CTA's producer warp once the router CTAs have written every score: the top_k
+// of each row on sigmoid(logit) + bias (f32; ties to the lower expert index; slots in descending
+// order), or the tid2eid row of its token (hash layers); weights = the chosen sigmoid(logit)
+// normalised over the valid slots.  Then the (row, slot) pairs are grouped by expert: group 0 is
+// the shared expert (weight 1 for every row), then the distinct routed experts in order of first
+// appearance, each with the mask of rows using it and their summed route weights.  CTA 0 also
+// writes the idx / weight / safe-index outputs and the status bits.
+// ---------------------------------------------------------------------------------------------
+// `dry`: the same instructions on whatever the score and logit buffers hold, without waiting and
+// without any global write, run once at launch so that the code is in L2 when the scores arrive
+// (the weight stream and the L2 flush of a benchmark evict it between launches; a code path that
+// runs once per launch otherwise pays the instruction-fetch latency line by line).  Its group
+// table in shared memory is overwritten by the live run.
+template <int ROWS>
+__device__ __noinline__ void route_cta(const DecodeArgs &a, DecSmem &sm, unsigned *cnt, bool dry = false) {
+  constexpr int rows = ROWS;
+  const RouteParams &p = a.rp;
+  const int lane = threadIdx.x & 31, E = a.experts, K = p.top_k;
+  const bool live = blockIdx.x == 0 && !dry;
+  int sel[rows];
+  float wgt[rows];
+  if (!dry) pdl_wait();  // the token ids come from the previous kernel
+  {
+    const uint64_t t0 = dry ? 0 : global_timer_ns();
+#pragma unroll
+    for (int r = 0; r < rows; ++r) {
+      int my_sel = -1;
+      constexpr int J2 = kExpertsMax / 32;
+      float lg[J2];  // this lane's logits (score layers)
+      if (!p.hash) {
+        constexpr int J = J2;
+        float v[J];
+        // the row's (score, logit) pairs, read until every one has been written (bounded)
+        for (;;) {
+          bool pending = false;
+#pragma unroll
+          for (int jj = 0; jj < J; ++jj) {
+            const int e = lane + 32 * jj;
+            const float2 q = e < E ? __ldcg(a.sel + (size_t)r * E + e) : make_float2(-INFINITY, 0.f);
+            v[jj] = q.x;
+            lg[jj] = q.y;
+            pending |= __float_as_uint(q.x) == kUnwritten;
+          }
+          if (dry || !__any_sync(0xffffffffu, pending)) break;
+          if (global_timer_ns() - t0 > a.wait_ns || *reinterpret_cast<volatile unsigned *>(&cnt[kCntAbort]) != 0u) {
+            if (lane == 0) {
+              atomicOr(a.status, kDevTimeout);
+              atomicExch(&cnt[kCntAbort], 1u);
+            }
+            break;
+          }
+          __nanosleep(32);
+        }
+        uint32_t taken = 0;
+#pragma unroll 1
+        for (int k = 0; k < K; ++k) {
+          float bv = -INFINITY;
+          int be = 0x7fffffff;
+#pragma unroll
+          for (int jj = 0; jj < J; ++jj) {
+            const int e = lane + 32 * jj;
+            if (e < E && !((taken >> jj) & 1u) && (v[jj] > bv || be == 0x7fffffff)) {
+              bv = v[jj];
+              be = e;
+            }
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            if (ov > bv || (ov == bv && oe < be)) {
+              bv = ov;
+              be = oe;
+            }
+          }
+          if ((be & 31) == lane) taken |= 1u << (be >> 5);
+          if (lane == k) my_sel = be;
+        }
+      } else {
+        const int tok = p.token_ids[r];
+        const bool tok_ok = tok >= 0 && tok < p.vocab;
+        if (!tok_ok && lane == 0 && live) atomicOr(p.status, kDevTokenRange);
+        if (lane < K) my_sel = tok_ok ? p.tid2eid[(size_t)tok * K + lane] : -1;
+        const bool bad_entry = tok_ok && lane < K && !(my_sel >= 0 && my_sel < E);
+        if (__any_sync(0xffffffffu, bad_entry) && lane == 0 && live) atomicOr(p.status, kDevRouteRange);
+      }
+      const bool valid = lane < K && my_sel >= 0 && my_sel < E;
+      // the chosen logit sits in register my_sel / 32 of lane my_sel % 32 (score layers), else it is
+      // read now (hash layers)
+      float lsel = 0.f;
+      if (!p.hash) {
+        const int src = valid ? (my_sel & 31) : 0, jsel = valid ? (my_sel >> 5) : 0;
+        float got = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < J2; ++jj) {
+          const float cand = __shfl_sync(0xffffffffu, lg[jj], src);
+          if (jj == jsel) got = cand;
+        }
+        lsel = got;
+      } else {
+        // hash layers: the chosen experts' logits, read until written (bounded)
+        for (;;) {
+          const float2 q = valid ? __ldcg(a.sel + (size_t)r * E + my_sel) : make_float2(0.f, 0.f);
+          lsel = q.y;
+          const bool pending = valid && __float_as_uint(q.y) == kUnwritten;
+          if (dry || !__any_sync(0xffffffffu, pending)) break;
+          if (global_timer_ns() - t0 > a.wait_ns || *reinterpret_cast<volatile unsigned *>(&cnt[kCntAbort]) != 0u) {
+            if (lane == 0) {
+              atomicOr(a.status, kDevTimeout);
+              atomicExch(&cnt[kCntAbort], 1u);
+            }
+            break;
+          }
+          __nanosleep(32);
+        }
+      }
+      const float sc = valid ? sigmoidf_(lsel) : 0.f;
+      const float tot = warp_sum(sc);
+      const float w = lane < K && tot > 0.f ? sc / tot : 0.f;
+      if (lane < K && live) {
+        p.idx[r * K + lane] = my_sel;
+        p.rw[r * K + lane] = w;
+        p.safe[r * K + lane] = valid ? (unsigned)my_sel : 0u;
+      }
+      sel[r] = my_sel;
+      wgt[r] = w;
+    }
+  }
+  // lane rr * K + k takes slot k of row rr (rows * top_k <= 32)
+  const int rr = lane / K, kk = lane - rr * K;
+  int e = -1;
+  float wl = 0.f;
+#pragma unroll
+  for (int r = 0; r < rows; ++r) {
+    const int se = __shfl_sync(0xffffffffu, sel[r], kk & 31);
+    const float sw = __shfl_sync(0xffffffffu, wgt[r], kk & 31);
+    if (rr == r) {
+      e = se;
+      wl = sw;
+    }
+  }
+  const bool valid = lane < rows * K && e >= 0 && e < E;
+  sm.rtw[lane] = wl;
+  __syncwarp();
+  const unsigned same = __match_any_sync(0xffffffffu, valid ? e : E + 1 + lane);
+  const unsigned below = (1u << lane) - 1u;
+  const bool leader = valid && (same & below) == 0u;
+  const unsigned leaders = __ballot_sync(0xffffffffu, leader);
+  if (leader) {
+    const int g = 1 + __popc(leaders & below);
+    int mask = 0;
+    float w0 = 0.f, w1 = 0.f, w2 = 0.f, w3 = 0.f;
+    for (unsigned m = same; m != 0u; m &= m - 1u) {
+      const int b = __ffs(m) - 1, rb = b / K;
+      const float wb = sm.rtw[b];
+      mask |= 1 << rb;
+      if (rb == 0) w0 += wb;
+      else if (rb == 1) w1 += wb;
+      else if (rb == 2) w2 += wb;
+      else w3 += wb;
+    }
+    sm.ge[g] = e;
+    sm.gm[g] = mask;
+    sm.gw[g][0] = w0;
+    sm.gw[g][1] = w1;
+    sm.gw[g][2] = w2;
+    sm.gw[g][3] = w3;
+  }
+  if (lane == 0) {
+    sm.ge[0] = E;
+    sm.gm[0] = (1 << rows) - 1;
+    for (int r = 0; r < kDecodeRows; ++r) sm.gw[0][r] = r < rows ? 1.f : 0.f;
+    sm.ng = 1 + __popc(leaders);
+  }
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------------------------------------
+// The stream
 // ---------------------------------------------------------------------------------------------
 
+// The 16 E4M3 codes of a uint4 or the 8 of a uint2 as floats times 2^-120 (see
+// e4m3x16_to_float_scaled).
+__device__ __forceinline__ void e4m3x8_to_float_scaled(const uint2 w, float (&f)[8]) {
+  const unsigned words[2] = {w.x, w.y};
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      f[4 * q + k] = __int_as_float((static_cast<int>(words[q] << (24 - 8 * k)) >> 4) & static_cast<int>(0x87F00000u));
+}
+
+__device__ __forceinline__ float dot8f(const float (&f)[8], const float4 x0, const float4 x1) {
+  float s = f[0] * x0.x;
+  s = fmaf(f[1], x0.y, s);
+  s = fmaf(f[2], x0.z, s);
+  s = fmaf(f[3], x0.w, s);
+  s = fmaf(f[4], x1.x, s);
+  s = fmaf(f[5], x1.y, s);
+  s = fmaf(f[6], x1.z, s);
+  s = fmaf(f[7], x1.w, s);
+  return s;
+}
+
+__device__ __forceinline__ uint2 lds64(const void *p) {
+  uint2 r;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(smem_u32(p)));
+  return r;
+}
+
+// 1-D bulk copy global -> shared memory with an L2 cache policy.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 template <int ROWS, bool MX>
-__global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
-  extern __shared__ __align__(16) float xs[];  // [rows, hidden]: x = ffn_norm(ffn_input)
-  __shared__ __align__(16) PreludeSmem sm;
+__global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
+  using RG = Ring<MX>;
+  constexpr int S = RG::kSlots;
   constexpr int rows = ROWS;  // every row loop is unrolled exactly, without run-time guards
+  extern __shared__ __align__(128) uint8_t dsm[];
+  uint8_t *ring = dsm;
+  float *red = reinterpret_cast<float *>(dsm + (size_t)S * RG::kSlotBytes);  // [S][8 warps][kRed]
+  __shared__ __align__(16) DecSmem sm;
+  __shared__ __align__(8) uint64_t full_bar[S], empty_bar[S], red_bar[S];
   unsigned *cnt = a.counters;
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int D = a.hidden, I = a.inter, E = a.experts;
-  if (tid == 0) sm.flag = (int)atomicAdd(&cnt[kCntRole], 1u);
+  const int all_rows = (1 << rows) - 1;
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);             // the publisher has taken the slot's partial sums
+      mbar_init(&red_bar[s], kWorkerWarps);    // every worker warp has left its partial sums
+    }
+    sm.abort = 0;
+    sm.comb_todo = 0;
+    sm.flag = (int)atomicAdd(&cnt[kCntRole], 1u);
+    fence_mbar_init();
+  }
   __syncthreads();
   const int role = sm.flag;
   __syncthreads();
-  if (role < a.nm) {
-    mix_role<ROWS>(a, role, sm, cnt);
-  } else if (role < a.nm + a.nr) {
-    router_role<ROWS>(a, role - a.nm, sm, cnt);
-  } else {
-    // streaming only, idle until the prelude is done: the first few CTAs run the router tail on
-    // scratch data, which brings its code into L2 before the live tail needs it
-    if (role < a.nm + a.nr + kWarmCtas) router_tail<ROWS>(a, sm, cnt, false);
-  }
-  pdl_wait();  // the state (read by phase C) comes from the previous kernel
 
-  // ---- x = (ffn_input * norm weight) * rs, once every router CTA has written its share of xw and
-  // of the sums of squares: each CTA forms rs itself, so the shared expert, which needs no
-  // routing, streams while the router tail still routes ----
-  (void)cta_wait_at_least(&cnt[kCntRtDone], (unsigned)a.nr, a.status, &cnt[kCntAbort], &sm.flag);
-  if ((tid >> 5) < rows) {
-    const float rs = row_rs_from_partials(a, rows, tid >> 5, a.nr);
-    if (lane == 0) sm.rs[tid >> 5] = rs;
-  }
-  __syncthreads();
-  for (int i = tid * 4; i < rows * D; i += blockDim.x * 4) {
-    const int r = i / D;
-    const float rs = sm.rs[r];
-    const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.xw + i));
-    const float4 x = make_float4(v.x * rs, v.y * rs, v.z * rs, v.w * rs);
-    *reinterpret_cast<float4 *>(&xs[i]) = x;
-    if (blockIdx.x == 0) *reinterpret_cast<float4 *>(a.ffn_norm + i) = x;
-  }
-  __syncthreads();
   unsigned *group_done = cnt + kCntGroups;
   unsigned *dblock_done = cnt + kCntDBlocks;
-  const int nblk = D / kDecodeDBlock;
-  const int all_rows = (1 << rows) - 1;
+  // a kind-A slot: the gate and up rows i of group g; a kind-B slot: down rows d0 .. d0 + 3
+  const int perg = I, nb_per_g = D / kRowsB;
 
-  // ---- phase A: gate/up rows, tickets in group-major order (the shared expert first) ----
-  // A row's gate and up elements stream in batches of UA 16-byte loads per lane and matrix, all
-  // of a batch in flight at once (fewer for 3-4 rows, whose FMAs take longer).  Group 0 (the
-  // shared expert) needs no routing; the first ticket past it waits for the routing.
-  constexpr int UA = ROWS >= 3 ? 4 : 8;
-  constexpr int UQA = 4;  // MX: 16-byte loads per lane and matrix in flight (2048 codes a trip)
-  const int perg = I / kRowsPerTicketA;
-  int ng = -1;
-  // the group table, once routed, in registers: lane l holds groups l and l + 32 (group 0, the
-  // shared expert, is known without routing)
-  int gt_e0 = E, gt_e1 = E, gt_m0 = all_rows, gt_m1 = 0;
-  float gt_w0[rows], gt_w1[rows];  // route weights of groups lane and lane + 32, per row
-#pragma unroll
-  for (int r = 0; r < rows; ++r) gt_w0[r] = gt_w1[r] = 0.f;
-  auto group_of = [&](int g, int &e, int &mask) {
-    const int src = g & 31;
-    const int e0 = __shfl_sync(0xffffffffu, gt_e0, src), e1 = __shfl_sync(0xffffffffu, gt_e1, src);
-    const int m0 = __shfl_sync(0xffffffffu, gt_m0, src), m1 = __shfl_sync(0xffffffffu, gt_m1, src);
-    e = g < 32 ? e0 : e1;
-    mask = g < 32 ? m0 : m1;
-  };
-  for (int c = draw_ticket(&cnt[kCntTickA]);;) {
-    if (ng < 0 && c >= perg) {
-      if (wait_at_least(&cnt[kCntRoute], 1u, a.status, &cnt[kCntAbort])) {
-        ng = __ldcg(a.ngroups);
-        if (lane < ng) {
-          gt_e0 = __ldcg(a.group_e + lane);
-          gt_m0 = __ldcg(a.group_mask + lane);
-#pragma unroll
-          for (int r = 0; r < rows; ++r) gt_w0[r] = __ldcg(a.group_w + lane * kDecodeRows + r);
+  if (warp == kProducerWarp) {
+    // ================= producer =================
+    // routed rows are read once (evict first); the shared expert's rows keep the normal priority,
+    // so that no weight row crowds the kernel's own code or the prelude's data out of L2
+    const uint64_t pol_first = make_policy_evict_first(), pol_last = make_policy_evict_normal();
+    const int span = MX ? (((D / 32 + 32) + 15) & ~15) : 0;  // bytes per MX scale run slot of a kind-A slot
+    route_cta<ROWS>(a, sm, cnt, true);
+    // the prelude's loads are latency-bound chains: the stream starts once the mix CTAs have read
+    // the state (later prelude reads hit L2), so that they do not queue behind it.  Then the shared
+    // expert's gate/up rows that the first ring fills do not cover go to L2 (they are read again by
+    // whichever CTA draws their tickets).
+    (void)wait_at_least(&cnt[kCntMixDone], (unsigned)a.nm, a);
+    {
+      const int first = gridDim.x * S;
+      const int rest = perg - first;
+      if (rest > 0) {
+        const int per = (rest + gridDim.x - 1) / gridDim.x;
+        for (int i = first + blockIdx.x * per + lane; i < min(perg, first + (blockIdx.x + 1) * per); i += 32) {
+          if (MX) {
+            prefetch_l2(a.gate_sh_q + (size_t)i * D, (uint32_t)D, pol_last);
+            prefetch_l2(a.up_sh_q + (size_t)i * D, (uint32_t)D, pol_last);
+          } else {
+            prefetch_l2(a.gate_sh + (size_t)i * D, (uint32_t)(2 * D), pol_last);
+            prefetch_l2(a.up_sh + (size_t)i * D, (uint32_t)(2 * D), pol_last);
+          }
         }
-        if (lane + 32 < ng) {
-          gt_e1 = __ldcg(a.group_e + lane + 32);
-          gt_m1 = __ldcg(a.group_mask + lane + 32);
+      }
+    }
+    int ng = -1;
+    // tickets come in chunks of kChunk consecutive numbers; two chunk claims are in flight ahead of
+    // the slots, so the atomic's round trip (microseconds under load) never stalls the ring
+    int c0 = 0, c1 = 0, c2 = 0;  // the current chunk and the two claimed after it (lane 0)
+    if (lane == 0) {
+      c0 = (int)atomicAdd(&cnt[kCntTick], (unsigned)kChunk);
+      c1 = (int)atomicAdd(&cnt[kCntTick], (unsigned)kChunk);
+      c2 = (int)atomicAdd(&cnt[kCntTick], (unsigned)kChunk);
+    }
+    int phases[S];  // completions asked of each slot's full barrier (fills and end marks)
 #pragma unroll
-          for (int r = 0; r < rows; ++r) gt_w1[r] = __ldcg(a.group_w + (lane + 32) * kDecodeRows + r);
-        }
+    for (int s = 0; s < S; ++s) phases[s] = 0;
+    for (int k = 0;; ++k) {
+      const int s = k % S;
+      const int t = __shfl_sync(0xffffffffu, c0, 0) + k % kChunk;
+      SlotMeta m;
+      m.s0 = m.s1 = 0;
+      if (t < perg) {
+        m.kind = kKindA;
+        m.g = 0;
+        m.row = t;
+        m.e = E;
+        m.mask = all_rows;
       } else {
-        ng = 1;
+        if (ng < 0) {
+          route_cta<ROWS>(a, sm, cnt);
+          ng = sm.ng;
+        }
+        const int nA = ng * perg, nB = ng * nb_per_g;
+        if (t < nA) {
+          m.kind = kKindA;
+          m.g = t / perg;
+          m.row = t - m.g * perg;
+        } else if (t < nA + nB) {
+          m.kind = kKindB;
+          m.g = (t - nA) / nb_per_g;
+          m.row = (t - nA - m.g * nb_per_g) * kRowsB;
+        } else {
+          m.kind = kKindEnd;
+          m.g = 0;
+          m.row = 0;
+        }
+        m.e = sm.ge[m.g];
+        m.mask = sm.gm[m.g];
+      }
+      // the slot is free once every worker warp has read its previous contents
+      int got = 1;
+      if (lane == 0) {
+        got = mbar_wait_bounded(&empty_bar[s], ((uint32_t)(k / S) & 1u) ^ 1u, &sm.abort, a.status, a.wait_ns) ? 1 : 0;
+        if (!got) atomicExch(&cnt[kCntAbort], 1u);
+      }
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (!got) m.kind = kKindEnd;  // give up: the workers stop at this slot
+      if (lane == 0) {
+        uint8_t *dst = ring + (size_t)s * RG::kSlotBytes;
+        const bool routed = m.e < E;
+        const uint64_t pol = routed ? pol_first : pol_last;
+        // the slot's metadata is written before the barrier arrive that releases it to the workers
+        if (m.kind == kKindA) {
+          const size_t ro = routed ? (size_t)m.e * I + m.row : (size_t)m.row;
+          if (MX) {
+            const uint8_t *gs = (routed ? a.gate_s : a.gate_sh_s), *us = (routed ? a.up_s : a.up_sh_s);
+            const size_t so = ro * (D / 32), a0 = so & ~(size_t)15, a1 = (so + D / 32 + 15) & ~(size_t)15;
+            m.s0 = m.s1 = (int)(so - a0);
+            const uint32_t sb = (uint32_t)(a1 - a0);
+            sm.meta[s] = m;
+            mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(2 * D) + 2 * sb);
+            bulk_g2s(dst, (routed ? a.gate_q : a.gate_sh_q) + ro * D, (uint32_t)D, &full_bar[s], pol);
+            bulk_g2s(dst + D, (routed ? a.up_q : a.up_sh_q) + ro * D, (uint32_t)D, &full_bar[s], pol);
+            bulk_g2s(dst + 2 * D, gs + a0, sb, &full_bar[s], pol);
+            bulk_g2s(dst + 2 * D + span, us + a0, sb, &full_bar[s], pol);
+          } else {
+            sm.meta[s] = m;
+            mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(4 * D));
+            bulk_g2s(dst, (routed ? a.gate_exps : a.gate_sh) + ro * D, (uint32_t)(2 * D), &full_bar[s], pol);
+            bulk_g2s(dst + 2 * D, (routed ? a.up_exps : a.up_sh) + ro * D, (uint32_t)(2 * D), &full_bar[s], pol);
+          }
+        } else if (m.kind == kKindB) {
+          const size_t ro = routed ? (size_t)m.e * D + m.row : (size_t)m.row;
+          sm.meta[s] = m;
+          if (MX) {
+            mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(kRowsB * I + kRowsB * (I / 32)));
+            bulk_g2s(dst, (routed ? a.down_q : a.down_sh_q) + ro * I, (uint32_t)(kRowsB * I), &full_bar[s], pol);
+            bulk_g2s(dst + kRowsB * I, (routed ? a.down_s : a.down_sh_s) + ro * (I / 32), (uint32_t)(kRowsB * (I / 32)),
+                     &full_bar[s], pol);
+          } else {
+            mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(kRowsB * I * 2));
+            bulk_g2s(dst, (routed ? a.down_exps : a.down_sh) + ro * I, (uint32_t)(kRowsB * I * 2), &full_bar[s], pol);
+          }
+        } else {
+          sm.meta[s] = m;
+          mbar_arrive(&full_bar[s]);  // metadata only: the workers stop here
+        }
+        ++phases[s];
+      }
+      __syncwarp();
+      if (m.kind == kKindEnd) break;
+      if (k % kChunk == kChunk - 1 && lane == 0) {  // the chunk is used up: claim one more ahead
+        c0 = c1;
+        c1 = c2;
+        c2 = (int)atomicAdd(&cnt[kCntTick], (unsigned)kChunk);
       }
     }
-    if (ng >= 0 && c >= ng * perg) break;
-    int next = 0;
-    if (lane == 0) next = (int)atomicAdd(&cnt[kCntTickA], 1u);  // consumed after this ticket: latency hidden
-    const int g = c / perg, i0 = (c - g * perg) * kRowsPerTicketA;
-    int e, mask;
-    group_of(g, e, mask);
-    const bool routed = e < E;
-    for (int i = i0; i < i0 + kRowsPerTicketA; ++i) {
-      float ga[kDecodeRows] = {0.f, 0.f, 0.f, 0.f}, ua[kDecodeRows] = {0.f, 0.f, 0.f, 0.f};
-      if constexpr (MX) {
-        // 16 codes per lane and 16-byte load, all of a batch in flight; each 16-code piece lies in
-        // one 32-element scale block, so its partial dot takes the block's scale once
-        const size_t ro = routed ? (size_t)e * I + i : (size_t)i;
-        const uint8_t *gq = (routed ? a.gate_q : a.gate_sh_q) + ro * D;
-        const uint8_t *uq = (routed ? a.up_q : a.up_sh_q) + ro * D;
-        const uint8_t *gsc = (routed ? a.gate_s : a.gate_sh_s) + ro * (D / 32);
-        const uint8_t *usc = (routed ? a.up_s : a.up_sh_s) + ro * (D / 32);
-        // the loop runs the same trips on every lane (its shuffles need the whole warp); lanes past
-        // the row's end only skip the loads and the arithmetic.  Each trip covers 512 * UQA codes
-        // (up to 128 scale blocks); lane l loads scale word k0 / 128 + l of the row (four blocks)
-        // with the codes, and a code piece takes its block's byte from the lane that holds it.
-        const unsigned *gsw = reinterpret_cast<const unsigned *>(gsc), *usw = reinterpret_cast<const unsigned *>(usc);
-        for (int k0 = 0; k0 < D; k0 += 512 * UQA) {
-          uint4 gv[UQA], uv[UQA];
-          const bool wl = k0 / 128 + lane < D / 128;
-          const unsigned gword = wl ? __ldg(gsw + k0 / 128 + lane) : 0u, uword = wl ? __ldg(usw + k0 / 128 + lane) : 0u;
+    // copies still in flight (after a timeout) complete before the CTA may leave: wait (bounded)
+    // for the last completion asked of every slot (in a normal run every one has completed)
+    if (lane == 0) {
+      int no_abort = 0;
 #pragma unroll
-          for (int u = 0; u < UQA; ++u) {
-            const int cc = k0 + u * 512 + lane * 16;
-            if (cc < D) {
-              gv[u] = ld_stream(gq + cc);
-              uv[u] = ld_stream(uq + cc);
-            }
+      for (int s = 0; s < S; ++s)
+        if (phases[s] > 0)
+          (void)mbar_wait_bounded(&full_bar[s], (uint32_t)((phases[s] - 1) & 1), &no_abort, a.status, a.wait_ns);
+    }
+    __syncwarp();
+    if (ng < 0) {  // no routed ticket was drawn by this CTA: phase C still needs the group table
+      route_cta<ROWS>(a, sm, cnt);
+    }
+  } else if (warp == kPublisherWarp) {
+    // ================= publisher =================
+    if (role < a.nm) {  // a mix CTA: the last one's publisher forms the comb
+      int todo = 0;
+      const uint64_t t0 = global_timer_ns();
+      while ((todo = *reinterpret_cast<volatile int *>(&sm.comb_todo)) == 0) {
+        if (global_timer_ns() - t0 > a.wait_ns) {
+          if (lane == 0) {
+            atomicOr(a.status, kDevTimeout);
+            atomicExch(&cnt[kCntAbort], 1u);
           }
-#pragma unroll
-          for (int u = 0; u < UQA; ++u) {
-            const int cc = k0 + u * 512 + lane * 16;
-            // block cc / 32 is block 16u + lane / 2 of this trip: byte (lane / 2) % 4 of the trip's
-            // word 4u + lane / 8
-            const int src = 4 * u + lane / 8, sh = ((lane >> 1) & 3) * 8;
-            const unsigned gw = __shfl_sync(0xffffffffu, gword, src);
-            const unsigned uw = __shfl_sync(0xffffffffu, uword, src);
-            if (cc < D) {
-              // both matrices decoded, so each row's x is read from shared memory once for both
-              float fg[16], fu[16];
-              e4m3x16_to_float_scaled(gv[u], fg);
-              e4m3x16_to_float_scaled(uv[u], fu);
-              const float sg = e8m0_value((gw >> sh) & 0xFFu), su = e8m0_value((uw >> sh) & 0xFFu);
-#pragma unroll
-              for (int r = 0; r < kDecodeRows; ++r) {
-                if ((mask >> r) & 1) {
-                  const float4 *xp = reinterpret_cast<const float4 *>(&xs[r * D + cc]);
-                  const float4 x0 = xp[0], x1 = xp[1], x2 = xp[2], x3 = xp[3];
-                  ga[r] = fmaf(sg, dot16(fg, x0, x1, x2, x3) * kE4m3Unscale, ga[r]);
-                  ua[r] = fmaf(su, dot16(fu, x0, x1, x2, x3) * kE4m3Unscale, ua[r]);
-                }
-              }
-            }
-          }
+          break;
         }
+        __nanosleep(32);
+      }
+      __threadfence_block();
+      __syncwarp();
+      if (todo == 1) mix_comb<ROWS>(a, sm, cnt);
+    }
+    // unpublished counts: up to 8 counters (a group's rows, kind A; a d-block's rows, kind B)
+    int keys[8], cnts[8], nkeys = 0, held = 0;
+    auto flush = [&]() {
+      if (held > 0) {
+        __threadfence();  // every lane's act / y stores reach the device before the counts do
+        __syncwarp();
+        if (lane == 0)
+          for (int i = 0; i < nkeys; ++i)
+            add_relaxed(keys[i] < 1024 ? &group_done[keys[i]] : &dblock_done[keys[i] - 1024], (unsigned)cnts[i]);
+      }
+      nkeys = held = 0;
+    };
+    // a bounded wait that publishes what is held once it has waited 2 us: the counts are held back
+    // only while slots keep coming
+    auto idle_wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+      int ready = 0;
+      if (lane == 0) ready = mbar_try_wait(bar, parity) ? 1 : 0;
+      if (__shfl_sync(0xffffffffu, ready, 0)) return true;
+      const uint64_t t0 = global_timer_ns();
+      bool flushed = false;
+      while (true) {
+        if (lane == 0) ready = mbar_try_wait(bar, parity) ? 1 : 0;
+        if (__shfl_sync(0xffffffffu, ready, 0)) return true;
+        const uint64_t el = global_timer_ns() - t0;
+        if (!flushed && el > 2000u) {
+          flush();
+          flushed = true;
+        }
+        int give_up = 0;
+        if (lane == 0 && (*reinterpret_cast<volatile int *>(&sm.abort) != 0 || el > a.wait_ns)) {
+          give_up = 1;
+          sm.abort = 1;
+          atomicOr(a.status, kDevTimeout);
+          atomicExch(&cnt[kCntAbort], 1u);
+        }
+        if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+      }
+    };
+    for (int k = 0;; ++k) {
+      const int s = k % S;
+      const uint32_t par = (uint32_t)(k / S) & 1u;
+      if (!idle_wait(&full_bar[s], par)) break;
+      const SlotMeta m = sm.meta[s];
+      if (m.kind == kKindEnd) break;
+      if (!idle_wait(&red_bar[s], par)) break;
+      const float *rb = red + (size_t)s * kWorkerWarps * RG::kRed;
+      const int nv = m.kind == kKindA ? 2 * ROWS : kRowsB * ROWS;
+      float tot = 0.f;
+      if (lane < nv) {
+#pragma unroll
+        for (int w = 0; w < kWorkerWarps; ++w) tot += rb[w * RG::kRed + lane];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[s]);  // the slot is free for the producer
+      int key, n;
+      if (m.kind == kKindA) {
+        const float u = __shfl_sync(0xffffffffu, tot, (lane + ROWS) & 31);
+        if (lane < rows && ((m.mask >> lane) & 1))
+          a.act[((size_t)m.g * kDecodeRows + lane) * I + m.row] = tot * sigmoidf_(tot) * u;
+        key = m.g;
+        n = 1;
       } else {
-      const uint16_t *gw = routed ? a.gate_exps + ((size_t)e * I + i) * D : a.gate_sh + (size_t)i * D;
-      const uint16_t *uw = routed ? a.up_exps + ((size_t)e * I + i) * D : a.up_sh + (size_t)i * D;
-      for (int base = lane * 8; base < D; base += 256 * UA) {
-        uint4 gv[UA], uv[UA];
-#pragma unroll
-        for (int u = 0; u < UA; ++u) {
-          const int cc = base + u * 256;
-          if (cc < D) {
-            gv[u] = ld_weight(gw + cc);
-            uv[u] = ld_weight(uw + cc);
-          }
+        if (lane < kRowsB * ROWS) {  // zeros for rows this group does not serve
+          const int q = lane / ROWS, r = lane - q * ROWS;
+          a.y[((size_t)m.g * kDecodeRows + r) * D + m.row + q] = ((m.mask >> r) & 1) ? tot : 0.f;
         }
-#pragma unroll
-        for (int u = 0; u < UA; ++u) {
-          const int cc = base + u * 256;
-          if (cc < D) {
-#pragma unroll
-            for (int r = 0; r < kDecodeRows; ++r) {
-              if ((mask >> r) & 1) {  // rows this expert does not serve cost nothing
-                const float4 x0 = *reinterpret_cast<const float4 *>(&xs[r * D + cc]);
-                const float4 x1 = *reinterpret_cast<const float4 *>(&xs[r * D + cc + 4]);
-                ga[r] += dot8(gv[u], x0, x1);
-                ua[r] += dot8(uv[u], x0, x1);
-              }
-            }
-          }
+        key = 1024 + m.row / kDecodeDBlock;
+        n = kRowsB;
+      }
+      int i = 0;
+      while (i < nkeys && keys[i] != key) ++i;
+      if (i == nkeys) {
+        if (nkeys == 8) {
+          flush();
+          i = 0;
         }
+        keys[nkeys] = key;
+        cnts[nkeys] = 0;
+        ++nkeys;
       }
-      }
-#pragma unroll
-      for (int r = 0; r < kDecodeRows; ++r) {
-        if ((mask >> r) & 1) {
-          const float gs = warp_sum(ga[r]);
-          const float us = warp_sum(ua[r]);
-          if (lane == 0) a.act[((size_t)g * kDecodeRows + r) * I + i] = gs * sigmoidf_(gs) * us;
-        }
-      }
+      cnts[i] += n;
+      if (++held >= kPublishBatch) flush();
     }
-    if (lane == 0) publish(&group_done[g], (unsigned)kRowsPerTicketA);  // one release per ticket
-    c = __shfl_sync(0xffffffffu, next, 0);
-  }
-  if (ng < 0) ng = 1;
-
-  // ---- phase B: down rows, tickets in group-major order; a ticket's rows share one group and one
-  // d-block.  A group's rows wait (bounded) until all of its gate/up rows are published.
-  constexpr int UB = ROWS >= 3 ? 4 : 8;
-  constexpr int UQB = 4;  // MX: 16-byte loads per lane and down row in flight (4 x 512 codes: inter 2048)
-  const int nB = ng * D / kRowsPerTicketB;
-  int cur = -1;
-  bool ready = false;
-  for (int c = draw_ticket(&cnt[kCntTickB]); c < nB;) {
-    int next = 0;
-    if (lane == 0) next = (int)atomicAdd(&cnt[kCntTickB], 1u);
-    const int t0 = c * kRowsPerTicketB;
-    const int g = t0 / D, d0 = t0 - g * D;
-    if (g != cur) {
-      cur = g;
-      ready = wait_at_least(&group_done[g], (unsigned)I, a.status, &cnt[kCntAbort]);
-    }
-    int e, mask;
-    group_of(g, e, mask);
-    const bool routed = e < E;
-    if (ready) {
-      const float *act = a.act + (size_t)g * kDecodeRows * I;
-#pragma unroll 1
-      for (int q = 0; q < kRowsPerTicketB; q += 2) {
-        // two down rows in flight together
-        const int dd = d0 + q;
-        float acc0[kDecodeRows] = {0.f, 0.f, 0.f, 0.f}, acc1[kDecodeRows] = {0.f, 0.f, 0.f, 0.f};
+    flush();
+  } else {
+    // ================= workers =================
+    const bool router = role >= a.nm && role < a.nm + a.nr;
+    if (router) router_prefetch(a, role - a.nm);
+    if (role < a.nm) mix_role<ROWS>(a, role, sm, cnt);
+    // x in registers on the own columns (every CTA forms it), then the router CTAs' logits
+    float4 xr[rows][4];
+    form_x<ROWS, MX>(a, sm, cnt, xr);
+    if (router) router_logits<ROWS, MX>(a, sm, cnt, role - a.nm, xr);
+    pdl_wait();  // the state (read by phase C) comes from the previous kernel
+    constexpr int VA = pow2_at_least(2 * ROWS), VB = pow2_at_least(kRowsB * ROWS);
+    static_assert(VB <= RG::kRed && VA <= RG::kRed, "partial sums per warp and slot");
+    const int span = MX ? (((D / 32 + 32) + 15) & ~15) : 0;
+    // A CTA draws all of its kind-A tickets before its first kind-B one, so the slots come as a run
+    // of kind A, then a run of kind B: two loops, so that x and the SwiGLU slice are never held in
+    // registers at the same time
+    int k = 0;
+    bool stop = false;
+    for (;; ++k) {
+      const int s = k % S;
+      const uint32_t par = (uint32_t)(k / S) & 1u;
+      if (!warp_mbar_wait(&full_bar[s], par, sm, a)) {
+        stop = true;
+        break;
+      }
+      const SlotMeta m = sm.meta[s];
+      if (m.kind != kKindA) {
+        stop = m.kind != kKindB;
+        break;
+      }
+      const uint8_t *src = ring + (size_t)s * RG::kSlotBytes;
+      float *rp = red + ((size_t)s * kWorkerWarps + warp) * RG::kRed;
+        float pv[VA];
+#pragma unroll
+        for (int i = 0; i < VA; ++i) pv[i] = 0.f;
         if constexpr (MX) {
-          const size_t ro = routed ? (size_t)e * D + dd : (size_t)dd;
-          const uint8_t *dq0 = (routed ? a.down_q : a.down_sh_q) + ro * I, *dq1 = dq0 + I;
-          const uint8_t *ds0 = (routed ? a.down_s : a.down_sh_s) + ro * (I / 32), *ds1 = ds0 + I / 32;
-          // scale words as in phase A: lane l loads word k0 / 128 + l of each row with the codes
-          const unsigned *d0w = reinterpret_cast<const unsigned *>(ds0), *d1w = reinterpret_cast<const unsigned *>(ds1);
-          for (int k0 = 0; k0 < I; k0 += 512 * UQB) {  // warp-uniform trips, as in phase A
-            uint4 w0[UQB], w1[UQB];
-            const bool wl = k0 / 128 + lane < I / 128;
-            const unsigned word0 = wl ? __ldg(d0w + k0 / 128 + lane) : 0u, word1 = wl ? __ldg(d1w + k0 / 128 + lane) : 0u;
+          if (16 * tid < D) {
+            const uint4 gq = lds128(src + 16 * tid), uq = lds128(src + D + 16 * tid);
+            const float sg = e8m0_value(src[2 * D + m.s0 + tid / 2]);
+            const float su = e8m0_value(src[2 * D + span + m.s1 + tid / 2]);
+            float fg[16], fu[16];
+            e4m3x16_to_float_scaled(gq, fg);
+            e4m3x16_to_float_scaled(uq, fu);
 #pragma unroll
-            for (int u = 0; u < UQB; ++u) {
-              const int cc = k0 + u * 512 + lane * 16;
-              if (cc < I) {
-                w0[u] = ld_stream(dq0 + cc);
-                w1[u] = ld_stream(dq1 + cc);
-              }
-            }
-#pragma unroll
-            for (int u = 0; u < UQB; ++u) {
-              const int cc = k0 + u * 512 + lane * 16;
-              const int src = 4 * u + lane / 8, sh = ((lane >> 1) & 3) * 8;
-              const unsigned sw0 = __shfl_sync(0xffffffffu, word0, src);
-              const unsigned sw1 = __shfl_sync(0xffffffffu, word1, src);
-              if (cc < I) {
-                float f0[16], f1[16];
-                e4m3x16_to_float_scaled(w0[u], f0);
-                e4m3x16_to_float_scaled(w1[u], f1);
-                const float sc0 = e8m0_value((sw0 >> sh) & 0xFFu), sc1 = e8m0_value((sw1 >> sh) & 0xFFu);
-#pragma unroll
-                for (int r = 0; r < kDecodeRows; ++r) {
-                  if ((mask >> r) & 1) {
-                    const float *ar = act + (size_t)r * I + cc;
-                    const float4 x0 = ld_ca4(ar), x1 = ld_ca4(ar + 4), x2 = ld_ca4(ar + 8), x3 = ld_ca4(ar + 12);
-                    acc0[r] = fmaf(sc0, dot16(f0, x0, x1, x2, x3) * kE4m3Unscale, acc0[r]);
-                    acc1[r] = fmaf(sc1, dot16(f1, x0, x1, x2, x3) * kE4m3Unscale, acc1[r]);
-                  }
-                }
+            for (int r = 0; r < rows; ++r) {
+              if ((m.mask >> r) & 1) {
+                pv[r] = sg * (dot16(fg, xr[r][0], xr[r][1], xr[r][2], xr[r][3]) * kE4m3Unscale);
+                pv[ROWS + r] = su * (dot16(fu, xr[r][0], xr[r][1], xr[r][2], xr[r][3]) * kE4m3Unscale);
               }
             }
           }
         } else {
-        const uint16_t *dw0 = routed ? a.down_exps + ((size_t)e * D + dd) * I : a.down_sh + (size_t)dd * I;
-        const uint16_t *dw1 = dw0 + I;
-        for (int base = lane * 8; base < I; base += 256 * UB) {
-          uint4 w0[UB], w1[UB];
 #pragma unroll
-          for (int u = 0; u < UB; ++u) {
-            if (base + u * 256 < I) {
-              w0[u] = ld_weight(dw0 + base + u * 256);
-              w1[u] = ld_weight(dw1 + base + u * 256);
-            }
-          }
+          for (int h = 0; h < 2; ++h) {
+            const int c = 8 * tid + 2048 * h;
+            if (c < D) {
+              const uint4 gv = lds128(src + 2 * c), uv = lds128(src + 2 * D + 2 * c);
 #pragma unroll
-          for (int u = 0; u < UB; ++u) {
-            const int cc = base + u * 256;
-            if (cc < I) {
-#pragma unroll
-              for (int r = 0; r < kDecodeRows; ++r) {
-                if ((mask >> r) & 1) {
-                  const float4 x0 = ld_ca4(act + (size_t)r * I + cc);
-                  const float4 x1 = ld_ca4(act + (size_t)r * I + cc + 4);
-                  acc0[r] += dot8(w0[u], x0, x1);
-                  acc1[r] += dot8(w1[u], x0, x1);
+              for (int r = 0; r < rows; ++r) {
+                if ((m.mask >> r) & 1) {
+                  pv[r] += dot8(gv, xr[r][2 * h], xr[r][2 * h + 1]);
+                  pv[ROWS + r] += dot8(uv, xr[r][2 * h], xr[r][2 * h + 1]);
                 }
               }
             }
           }
         }
-        }
+        const float wt = warp_reduce_scatter<VA>(pv);
+        if (lane < VA) rp[lane] = wt;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&red_bar[s]);  // after this warp's reads of the slot and its partial sums
+    }
+    // the group's SwiGLU output (kind B): thread t owns columns 8t .. 8t + 7
+    float4 ar[rows][2];
+    int cur_g = -1;
+    bool act_ok = false;
+    for (; !stop; ++k) {  // from the first kind-B slot on (waiting again on its completed phase returns at once)
+      const int s = k % S;
+      const uint32_t par = (uint32_t)(k / S) & 1u;
+      if (!warp_mbar_wait(&full_bar[s], par, sm, a)) break;
+      const SlotMeta m = sm.meta[s];
+      if (m.kind != kKindB) break;
+      const uint8_t *src = ring + (size_t)s * RG::kSlotBytes;
+      float *rp = red + ((size_t)s * kWorkerWarps + warp) * RG::kRed;
+        if (m.g != cur_g) {  // the group's SwiGLU output, once its every gate/up row is published
+          cur_g = m.g;
+          act_ok = wait_at_least(&group_done[m.g], (unsigned)perg, a);
 #pragma unroll
-        for (int r = 0; r < kDecodeRows; ++r) {
-          if (r < rows) {
-            const float s0 = warp_sum(acc0[r]);
-            const float s1 = warp_sum(acc1[r]);
-            if (lane == 0) {  // zeros for rows this group does not serve
-              const bool use = (mask >> r) & 1;
-              a.y[((size_t)g * kDecodeRows + r) * D + dd] = use ? s0 : 0.f;
-              a.y[((size_t)g * kDecodeRows + r) * D + dd + 1] = use ? s1 : 0.f;
+          for (int r = 0; r < rows; ++r) {
+            const bool in = act_ok && 8 * tid < I && ((m.mask >> r) & 1);
+            const float4 *ap = reinterpret_cast<const float4 *>(a.act + ((size_t)m.g * kDecodeRows + r) * I + 8 * tid);
+            ar[r][0] = in ? __ldcg(ap) : make_float4(0.f, 0.f, 0.f, 0.f);
+            ar[r][1] = in ? __ldcg(ap + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+        float pv[VB];
+#pragma unroll
+        for (int i = 0; i < VB; ++i) pv[i] = 0.f;
+        if (8 * tid < I) {
+#pragma unroll
+          for (int q = 0; q < kRowsB; ++q) {
+            float f[8];
+            float sc = 1.f;
+            uint4 wv = make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (MX) {
+              e4m3x8_to_float_scaled(lds64(src + (size_t)q * I + 8 * tid), f);
+              sc = e8m0_value(src[kRowsB * I + q * (I / 32) + tid / 4]);
+            } else {
+              wv = lds128(src + (size_t)q * I * 2 + 16 * tid);
+            }
+#pragma unroll
+            for (int r = 0; r < rows; ++r) {
+              if ((m.mask >> r) & 1) {
+                if constexpr (MX) pv[q * ROWS + r] = sc * (dot8f(f, ar[r][0], ar[r][1]) * kE4m3Unscale);
+                else pv[q * ROWS + r] = dot8(wv, ar[r][0], ar[r][1]);
+              }
             }
           }
         }
-      }
+        const float wt = warp_reduce_scatter<VB>(pv);
+        if (lane < VB) rp[lane] = wt;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&red_bar[s]);
     }
-    if (lane == 0) publish(&dblock_done[d0 / kDecodeDBlock], (unsigned)kRowsPerTicketB);
-    c = __shfl_sync(0xffffffffu, next, 0);
   }
+  __syncthreads();  // the producer's group table is complete for phase C
 
   // ---- phase C: per 32-wide d-block, once every group's rows of it are in: ffn_out = sum_g w * y
   // and the hc_post output out_i = post_i * ffn_out + sum_j comb[i, j] * state_j.  The comb term
-  // needs no y, so it is formed before the block's wait; the wait then spins (it is short, at the
-  // end of the launch) and only the sum over groups follows it.
-  const int hc = a.hc;
-  const bool comb_ok = wait_at_least(&cnt[kCntComb], 1u, a.status, &cnt[kCntAbort]);
+  // needs no y, so it is formed before the block's wait.
+  const int hc = a.hc, ng = sm.ng, nblk = D / kDecodeDBlock;
+  // (test hook 1: a count that is never reached, so that this wait runs out)
+  const bool comb_ok = wait_at_least(&cnt[kCntComb], a.inject == 1 ? 2u : 1u, a);
   for (int c = draw_ticket(&cnt[kCntTickC]); c < nblk && comb_ok; c = draw_ticket(&cnt[kCntTickC])) {
     const int d = c * kDecodeDBlock + lane;
     float po[rows][kHcMax], t[rows][kHcMax];
@@ -955,26 +1228,16 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
         t[r][o] = v;
       }
     }
-    // Two passes over the same instructions: the first, before the wait and without stores, only
-    // brings this code into the instruction cache, so that the second runs warm right after it.
-#pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
-      const bool live = pass == 1;
-      if (live && !wait_at_least(&dblock_done[c], (unsigned)(ng * kDecodeDBlock), a.status, &cnt[kCntAbort], false))
-        break;
+    if (!wait_at_least(&dblock_done[c], (unsigned)(ng * kDecodeDBlock), a, false)) break;
 #pragma unroll
-      for (int r = 0; r < rows; ++r) {
-        float f = 0.f;
-#pragma unroll 8
-        for (int g = 0; g < ng; ++g) {
-          const float w = __shfl_sync(0xffffffffu, g < 32 ? gt_w0[r] : gt_w1[r], g & 31);
-          f += w * __ldcg(a.y + ((size_t)g * kDecodeRows + r) * D + d);
-        }
-        if (live) a.ffn_out[(size_t)r * D + d] = f;
+    for (int r = 0; r < rows; ++r) {
+      float f = 0.f;
+#pragma unroll 4
+      for (int g = 0; g < ng; ++g) f += sm.gw[g][r] * __ldcg(a.y + ((size_t)g * kDecodeRows + r) * D + d);
+      a.ffn_out[(size_t)r * D + d] = f;
 #pragma unroll
-        for (int o = 0; o < kHcMax; ++o)
-          if (live && o < hc) a.out_state[((size_t)r * hc + o) * D + d] = po[r][o] * f + t[r][o];
-      }
+      for (int o = 0; o < kHcMax; ++o)
+        if (o < hc) a.out_state[((size_t)r * hc + o) * D + d] = po[r][o] * f + t[r][o];
     }
   }
 
@@ -986,8 +1249,11 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
   if (sm.flag) {
     __threadfence();
     for (int i = tid; i < a.n_counters; i += blockDim.x) cnt[i] = 0u;
+    // every row's entries, whatever the next launch's row count
+    for (int i = tid; i < kDecodeRows * E; i += blockDim.x)
+      a.sel[i] = make_float2(__uint_as_float(kUnwritten), __uint_as_float(kUnwritten));
     // performed before this CTA retires: a decode launch that follows directly (programmatic
-    // dependent launch) draws its role ticket before its griddepcontrol.wait
+    // dependent launch) starts only after every CTA of this one has left
     __threadfence();
   }
 }
@@ -997,7 +1263,11 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
 // ---------------------------------------------------------------------------------------------
 
 int decode_mix_ctas(int hc, int hidden) { return (hc * hidden + kMixCols - 1) / kMixCols; }
-int decode_router_ctas(int hidden) { return hidden / kRouterChunk; }
+int decode_router_epc(int experts) { return (experts + 63) / 64 < kMaxEpc ? (experts + 63) / 64 : kMaxEpc; }
+int decode_router_ctas(int experts) {
+  const int epc = decode_router_epc(experts);
+  return (experts + epc - 1) / epc;
+}
 int decode_counter_count(const Dims &d) { return kCntDBlocks + d.hidden / kDecodeDBlock; }
 
 using DecodeKernel = void (*)(DecodeArgs);
@@ -1012,28 +1282,30 @@ static DecodeKernel decode_kernel_for(int rows, bool mx) {
          : rows == 3 ? decode_kernel<3, false>
                      : decode_kernel<4, false>;
 }
+static size_t decode_smem(bool mx) { return mx ? Ring<true>::kSmem : Ring<false>::kSmem; }
 
 cudaError_t decode_configure(int hidden) {
+  (void)hidden;
   for (int mx = 0; mx < 2; ++mx)
     for (int r = 1; r <= kDecodeRows; ++r) {
       const cudaError_t e = cudaFuncSetAttribute(decode_kernel_for(r, mx != 0),
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 r * hidden * (int)sizeof(float));
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)decode_smem(mx != 0));
       if (e != cudaSuccess) return e;
     }
   return cudaSuccess;
 }
 
 int decode_resident_ctas(int hidden, int rows, int num_sms, bool mx) {
+  (void)hidden;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel_for(rows, mx), 256,
-                                                    (size_t)rows * hidden * sizeof(float)) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel_for(rows, mx), kDecThreads,
+                                                    decode_smem(mx)) != cudaSuccess)
     return 0;
   return per_sm * num_sms;
 }
 
 void launch_decode(const Dims &d, const Scratch &s, const LayerDev &w, const float *state, const int32_t *token_ids,
-                   int rows, bool hash, float *out_state, cudaStream_t st, StageTimer *tm) {
+                   int rows, bool hash, float *out_state, cudaStream_t st, StageTimer *tm, const DebugOpts &dbg) {
   DecodeArgs a;
   a.state = state;
   a.hc_fn = w.hc_fn;
@@ -1061,22 +1333,16 @@ void launch_decode(const Dims &d, const Scratch &s, const LayerDev &w, const flo
   a.up_sh_s = w.up_sh_s;
   a.down_sh_s = w.down_sh_s;
   a.nm = decode_mix_ctas(d.hc, d.hidden);
-  a.nr = decode_router_ctas(d.hidden);
+  a.epc = decode_router_epc(d.experts);
+  a.nr = decode_router_ctas(d.experts);
   a.mix_part = s.mix_partial;
   a.mixes = s.mixes;
   a.pre = s.pre;
   a.post = s.post;
   a.comb = s.comb;
-  a.xw = s.ffn_input;
-  a.ss_part = s.dec_part;
-  a.lg_part = s.dec_part + (size_t)a.nr * kDecodeRows;
-  a.row_rs = s.row_rs;
-  a.ffn_norm = s.ffn_norm;
+  a.x = s.ffn_norm;
+  a.sel = reinterpret_cast<float2 *>(s.dec_part);
   a.logits = s.logits;
-  a.ngroups = s.ngroups;
-  a.group_e = s.group_e;
-  a.group_mask = s.group_mask;
-  a.group_w = s.group_w;
   a.act = s.act_dec;
   a.y = s.y_dec;
   a.ffn_out = s.ffn_out;
@@ -1091,11 +1357,11 @@ void launch_decode(const Dims &d, const Scratch &s, const LayerDev &w, const flo
   a.hc = d.hc;
   a.M = d.mix();
   a.iters = d.iters;
-  a.mix_chunk = kMixCols;
   a.eps = d.eps;
-  const size_t xs_bytes = (size_t)rows * d.hidden * sizeof(float);
-  launch_pdl(decode_kernel_for(rows, w.mx), dim3(w.mx ? s.decode_ctas_mx[rows] : s.decode_ctas_by_rows[rows]), dim3(256),
-             xs_bytes, st, a);
+  a.wait_ns = dbg.wait_ns ? dbg.wait_ns : kSpinLimitNs;
+  a.inject = dbg.inject;
+  launch_pdl(decode_kernel_for(rows, w.mx), dim3(w.mx ? s.decode_ctas_mx[rows] : s.decode_ctas_by_rows[rows]),
+             dim3(kDecThreads), decode_smem(w.mx), st, a);
   stage(tm, "decode", st);
 }
 

@@ -18,7 +18,8 @@
 // Layout ("swap AB"): the expert's weight rows are the MMA's M = 128 side (operand A), the
 // expert's tokens the N side (operand B, N = 16..128 by tile), K = hidden (gate/up) or inter
 // (down), 64 per pipeline stage.  So a weight tile is read from HBM once per 128 tokens of its
-// expert however few tokens that is.  The shared expert is group `experts` (every row), so one
+// expert however few tokens that is, and the B planes are loaded with a box of the tile's own
+// N rows (one tensor map per multiple of 16), not 128.  The shared expert is group `experts` (every row), so one
 // persistent launch covers routed and shared work.
 //
 // Precision: the weights are the caller's bf16 matrices, read by TMA as they are.  The activations
@@ -34,8 +35,10 @@
 //              tile's MMAs run under this tile's epilogue); SwiGLU and the hi/lo split of its
 //              output (gate/up), or route-weight scaling and the reduction into the FFN output (down);
 //              two warps per TMEM lane quarter, each every other 16-column chunk
-// Every mbarrier wait is bounded (2 s); on expiry the CTA raises the device timeout bit, all roles
-// leave their loops, and TMEM is freed before the kernel returns.
+// Every mbarrier wait is bounded (2 s unless a test sets a shorter limit); on expiry the CTA raises
+// the device timeout bit and all roles leave their loops; before the kernel returns, the producer
+// waits (bounded) for its own copies still in flight, the MMA issuer for its MMAs, and TMEM is
+// freed.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -45,7 +48,6 @@ namespace moe {
 
 constexpr int BM = 128, BN = 128, BK = 64, UMMA_K = 16;
 constexpr int kTileBytes = BM * BK * 2;  // 16 KB: one 128 x 64 bf16 tile (A and B planes alike)
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 template <bool GATEUP>
 struct GemmCfg {
@@ -68,6 +70,8 @@ struct GemmArgs {
   double *ffn_acc;     // [rows, hidden], zero on entry to the down GEMM
   int *status;
   int inter, hidden, k_blocks, a_rows_per_group, which, experts, plane_rows;
+  uint64_t wait_ns;  // bound of every wait
+  int inject;        // test hook: 2 = CTA 0's MMA issuer of the gate/up GEMM first waits on a barrier nothing arrives at
 };
 
 constexpr int kEpiWarps = 8, kGemmThreads = 32 * (2 + kEpiWarps);
@@ -76,13 +80,15 @@ template <bool GATEUP>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                         const __grid_constant__ CUtensorMap tmS0, const __grid_constant__ CUtensorMap tmS1,
-                        const __grid_constant__ CUtensorMap tmB, GemmArgs a) {
+                        const CUtensorMap *__restrict__ tmB, GemmArgs a) {
   using C = GemmCfg<GATEUP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full_bar[C::kStages], empty_bar[C::kStages], tfull_bar[2], tempty_bar[2];
+  __shared__ __align__(8) uint64_t mma_done_bar, never_bar;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
+  const uint64_t kWaitLimitNs = a.wait_ns;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -94,6 +100,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&tfull_bar[b], 1);
       mbar_init(&tempty_bar[b], kEpiWarps);
     }
+    mbar_init(&mma_done_bar, 1);
+    mbar_init(&never_bar, 1);
     abort_flag = 0;
     fence_mbar_init();
     tmap_prefetch(&tmA0);
@@ -102,7 +110,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tmap_prefetch(&tmA1);
       tmap_prefetch(&tmS1);
     }
-    tmap_prefetch(&tmB);
+    for (int i = 0; i < BN / 16; ++i) tmap_prefetch(&tmB[i]);
   }
   if (warp == 1) tmem_alloc(&tmem_base, C::kTmemCols);
   tc_fence_before();
@@ -116,6 +124,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ---------------- TMA producer ----------------
     int stage = 0;
     uint32_t phase = 0;
+    int issued = 0;  // stages handed to TMA
     for (int t = blockIdx.x; t < ntiles && !*abort_p; t += gridDim.x) {
       const int4 tl = a.tiles[t];
       const bool shared = tl.x == a.experts;  // the shared expert's matrices are separate tensors
@@ -123,26 +132,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const CUtensorMap *m1 = shared ? &tmS1 : &tmA1;
       const int a_row = (shared ? 0 : tl.x * a.a_rows_per_group) + tl.y * BM;
       const int b_row = a.offsets[tl.x] + tl.z * BN;
+      const int nb = (tl.w + 15) >> 4;  // B box: the tile's tokens in whole 16-row groups
+      const CUtensorMap *mb = &tmB[nb - 1];
+      const uint32_t bytes = C::kATiles * kTileBytes + 2u * (uint32_t)nb * 16u * BK * 2u;
       for (int kb = 0; kb < a.k_blocks; ++kb) {
         if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_p, a.status, kWaitLimitNs)) break;
-        mbar_arrive_expect_tx(&full_bar[stage], C::kStageBytes);
+        mbar_arrive_expect_tx(&full_bar[stage], bytes);
         uint8_t *base = smem + (size_t)stage * C::kStageBytes;
         tma_load_2d(base, m0, &full_bar[stage], kb * BK, a_row);
         if (GATEUP) tma_load_2d(base + kTileBytes, m1, &full_bar[stage], kb * BK, a_row);
         uint8_t *bp = base + C::kATiles * kTileBytes;
-        tma_load_2d(bp, &tmB, &full_bar[stage], kb * BK, b_row);
-        tma_load_2d(bp + kTileBytes, &tmB, &full_bar[stage], kb * BK, a.plane_rows + b_row);
+        tma_load_2d(bp, mb, &full_bar[stage], kb * BK, b_row);
+        tma_load_2d(bp + kTileBytes, mb, &full_bar[stage], kb * BK, a.plane_rows + b_row);
+        ++issued;
         if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
     }
+    // copies still in flight after an abort land before the CTA may leave: wait (bounded) for the
+    // last phase asked of every stage (in a normal run each has completed long ago)
+    int no_abort = 0;
+    for (int s = 0; s < C::kStages; ++s) {
+      const int n = issued / C::kStages + (s < issued % C::kStages ? 1 : 0);
+      if (n > 0) (void)mbar_wait_bounded(&full_bar[s], (uint32_t)((n - 1) & 1), &no_abort, a.status, kWaitLimitNs);
+    }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
     int stage = 0;
     uint32_t phase = 0;
     int it = 0;
+    if (GATEUP && a.inject == 2 && blockIdx.x == 0)  // test hook: a wait that runs out
+      (void)mbar_wait_bounded(&never_bar, 0u, abort_p, a.status, kWaitLimitNs);
     for (int t = blockIdx.x; t < ntiles && !*abort_p; t += gridDim.x, ++it) {
       const int4 tl = a.tiles[t];
       const int n_mma = (tl.w + 15) & ~15;
@@ -184,6 +206,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!ok) break;
       tc_commit(&tfull_bar[acc]);
     }
+    // every MMA this thread issued completes before TMEM is freed (immediate in a normal run)
+    tc_commit(&mma_done_bar);
+    int no_abort = 0;
+    (void)mbar_wait_bounded(&mma_done_bar, 0u, &no_abort, a.status, kWaitLimitNs);
   } else if (warp >= 2) {
     // ---------------- epilogue ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -264,8 +290,9 @@ cudaError_t gemm_configure() {
                               (int)GemmCfg<false>::kSmem);
 }
 
-void launch_grouped_gemms(const Dims &d, const Scratch &s, const LayerDev &w, const CUtensorMap &tm_x2,
-                          const CUtensorMap &tm_act2, int num_sms, cudaStream_t st, StageTimer *tm) {
+void launch_grouped_gemms(const Dims &d, const Scratch &s, const LayerDev &w, const CUtensorMap *tm_x2,
+                          const CUtensorMap *tm_act2, int num_sms, cudaStream_t st, StageTimer *tm,
+                          const DebugOpts &dbg) {
   GemmArgs a;
   a.tiles = s.tiles_gu;
   a.n_tiles = s.n_tiles;
@@ -282,6 +309,8 @@ void launch_grouped_gemms(const Dims &d, const Scratch &s, const LayerDev &w, co
   a.which = 0;
   a.experts = d.experts;
   a.plane_rows = s.max_positions;
+  a.wait_ns = dbg.wait_ns ? dbg.wait_ns : 2000000000ull;
+  a.inject = dbg.inject;
   const int grid_gu = num_sms < s.max_tiles_gu ? num_sms : s.max_tiles_gu;
   grouped_gemm_kernel<true><<<grid_gu, kGemmThreads, GemmCfg<true>::kSmem, st>>>(w.tm_gate, w.tm_up, w.tm_gate_sh,
                                                                                   w.tm_up_sh, tm_x2, a);

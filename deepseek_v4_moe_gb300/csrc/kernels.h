@@ -54,8 +54,7 @@ struct Scratch {
   float *mixes, *pre, *post, *comb;  // [rows, mix] [rows, hc] [rows, hc] [rows, hc, hc]
   float *ffn_input, *ffn_norm;       // [rows, hidden]
   float *row_rs;          // [rows] rsqrt(mean(ffn_input^2) + eps) (decode)
-  float *dec_part;        // decode router partials: [router CTAs, 4] sums of squares, then
-                          // [router CTAs, 4, experts] logits
+  float *dec_part;        // decode: [4, experts] (selection score, logit) pairs the router CTAs write
   float *logits;          // [rows, experts]
   float *router_part;     // [splits, rows, experts] split-K partial logits (rows > 4)
   int *idx;               // [rows, top_k]
@@ -106,6 +105,13 @@ struct StageTimer {
   }
 };
 
+// Test hooks (moe_ffn_set_fault_injection): the bound of every in-kernel wait, and which kernel, if
+// any, waits on a barrier or counter that nothing completes.
+struct DebugOpts {
+  uint64_t wait_ns = 0;  // 0: the kernels' defaults
+  int inject = 0;        // 1: the decode kernel; 2: the gate/up GEMM
+};
+
 inline void stage(StageTimer *t, const char *nm, cudaStream_t st) {
   if (t) t->mark(nm, st);
 }
@@ -149,9 +155,9 @@ constexpr int kDecodeGroupsMax = 4 * 8 + 1;  // rows x top_k distinct experts + 
 constexpr int kDecodeDBlock = 32;            // d-block of the decode reduce + hc_post (one d per lane)
 int decode_counter_count(const Dims &d);
 int decode_mix_ctas(int hc, int hidden);     // CTAs of the decode kernel's mix role
-int decode_router_ctas(int hidden);          // CTAs of its router role
+int decode_router_ctas(int experts);         // CTAs of its router role
 void launch_decode(const Dims &d, const Scratch &s, const LayerDev &w, const float *state, const int32_t *token_ids,
-                   int rows, bool hash, float *out_state, cudaStream_t st, StageTimer *tm);
+                   int rows, bool hash, float *out_state, cudaStream_t st, StageTimer *tm, const DebugOpts &dbg);
 cudaError_t decode_configure(int hidden);
 int decode_resident_ctas(int hidden, int rows, int num_sms, bool mx);
 void launch_mxfp8_to_bf16(const uint8_t *q, const uint8_t *s, uint16_t *dst, size_t n, cudaStream_t st);
@@ -170,8 +176,11 @@ int mix_tc_part_floats(int max_rows, int hcd);
 int splitgemm_splits(int k);  // K splits of the tensor-core mix / router GEMMs
 cudaError_t splitgemm_configure();
 // gemm_tc.cu
-void launch_grouped_gemms(const Dims &d, const Scratch &s, const LayerDev &w, const CUtensorMap &tm_x2,
-                          const CUtensorMap &tm_act2, int num_sms, cudaStream_t st, StageTimer *tm);
+// tm_x2, tm_act2: device arrays of 8 tensor maps each over the activation planes, with boxes of
+// 16, 32, ..., 128 rows
+void launch_grouped_gemms(const Dims &d, const Scratch &s, const LayerDev &w, const CUtensorMap *tm_x2,
+                          const CUtensorMap *tm_act2, int num_sms, cudaStream_t st, StageTimer *tm,
+                          const DebugOpts &dbg);
 size_t gemm_smem_bytes(bool gateup);
 cudaError_t gemm_configure();
 

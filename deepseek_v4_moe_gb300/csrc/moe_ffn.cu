@@ -26,13 +26,15 @@ struct moe_ffn_handle {
   std::vector<LayerDev> layers;
   std::vector<LayerDev> attn;  // the attention sublayer's HC weights (hc fields and ffn_norm = attn_norm only)
   Scratch s;
-  CUtensorMap tm_x2, tm_act2, tm_ffn_norm;
+  CUtensorMap tm_ffn_norm;
+  CUtensorMap *tm_b = nullptr;  // device: [2][8] maps over x2 and act2, boxes of 16 .. 128 rows
   float *host_in = nullptr, *host_out = nullptr;  // device staging of moe_ffn_forward_host
   int32_t *host_tok = nullptr;
   std::vector<void *> allocs;
   cudaStream_t last_stream = nullptr;
   int last_rows = 0;
   moe::StageTimer timer;
+  moe::DebugOpts dbg;  // test hooks (moe_ffn_set_fault_injection); defaults in normal use
   std::string err;
   // moe_ffn_forward_layers: captured chains (most recent use last) and the intermediate state
   struct Chain {
@@ -72,10 +74,10 @@ static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 static int check_config(const moe_ffn_config *c) {
   if (c->hc < 1 || c->hc > moe::kHcMax) return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "hc must be in 1..4");
-  if (c->hidden < 128 || c->hidden % 128 || c->hidden > 8192)
-    return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "hidden must be a multiple of 128 in 128..8192");
-  if (c->inter < 128 || c->inter % 128 || c->inter > 8192)
-    return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "inter must be a multiple of 128 in 128..8192");
+  if (c->hidden < 128 || c->hidden % 128 || c->hidden > 4096)
+    return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "hidden must be a multiple of 128 in 128..4096");
+  if (c->inter < 128 || c->inter % 128 || c->inter > 2048)
+    return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "inter must be a multiple of 128 in 128..2048");
   if (c->shared_inter != c->inter) return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "shared_inter must equal inter");
   if (c->experts < 16 || c->experts > moe::kExpertsMax || c->experts % 16)
     return fail(nullptr, MOE_FFN_ERR_BAD_CONFIG, "experts must be a multiple of 16 in 16..512");
@@ -233,7 +235,7 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
             dalloc(h, &s.mixes, R * M) && dalloc(h, &s.pre, R * HC) && dalloc(h, &s.post, R * HC) &&
             dalloc(h, &s.comb, R * HC * HC) && dalloc(h, &s.ffn_input, R * D) && dalloc(h, &s.ffn_norm, R * D) &&
             dalloc(h, &s.row_rs, R) &&
-            dalloc(h, &s.dec_part, (size_t)moe::decode_router_ctas((int)D) * 4 * (E + 1)) &&
+            dalloc(h, &s.dec_part, (size_t)moe::kDecodeRows * E * 2) &&
             dalloc(h, &s.logits, R * E) &&
             dalloc(h, &s.idx, R * K) && dalloc(h, &s.rw, R * K) && dalloc(h, &s.safe, R * K) &&
             dalloc(h, &s.ffn_out, R * D) && dalloc(h, &s.ngroups, 1) && dalloc(h, &s.group_e, G) &&
@@ -260,11 +262,17 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
   }
   cudaMemset(s.status, 0, sizeof(int));
   cudaMemset(s.dec_counters, 0, (size_t)moe::decode_counter_count(d) * sizeof(unsigned));
+  cudaMemset(s.dec_part, 0xFF, (size_t)moe::kDecodeRows * E * 2 * sizeof(float));  // "not written yet"
   cudaMemset(s.tickets, 0, (R / 4 + 2) * sizeof(unsigned));
   if (prefill) {
     cudaMemset(s.counts, 0, E * sizeof(int));
-    if (!make_tmap_bf16(&h->tm_x2, s.x2, D, 2 * P) || !make_tmap_bf16(&h->tm_act2, s.act2, I, 2 * P) ||
-        !make_tmap_f32(&h->tm_ffn_norm, s.ffn_norm, D, R)) {
+    CUtensorMap maps[16];
+    bool enc = make_tmap_f32(&h->tm_ffn_norm, s.ffn_norm, D, R);
+    for (int i = 0; i < 8 && enc; ++i)
+      enc = make_tmap_bf16(&maps[i], s.x2, D, 2 * P, 16u * (i + 1)) &&
+            make_tmap_bf16(&maps[8 + i], s.act2, I, 2 * P, 16u * (i + 1));
+    if (enc) enc = dalloc(h, &h->tm_b, 16) && cudaMemcpy(h->tm_b, maps, sizeof maps, cudaMemcpyHostToDevice) == cudaSuccess;
+    if (!enc) {
       free_all(h);
       delete h;
       return fail(nullptr, MOE_FFN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the activation buffers");
@@ -286,7 +294,7 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
         return fail(nullptr, MOE_FFN_ERR_CUDA, "the decode kernel does not fit on an SM");
       }
       // its prelude roles are claimed by the first CTAs to arrive; at least one CTA must be left
-      if (n <= moe::decode_mix_ctas(d.hc, d.hidden) + moe::decode_router_ctas(d.hidden)) {
+      if (n <= moe::decode_mix_ctas(d.hc, d.hidden) + moe::decode_router_ctas(d.experts)) {
         free_all(h);
         delete h;
         return fail(nullptr, MOE_FFN_ERR_CUDA, "too few co-resident CTAs (%d) for the decode kernel's roles", n);
@@ -367,7 +375,7 @@ static int enqueue_forward(moe_ffn_handle *h, const float *state, const int32_t 
   const LayerDev &L = h->layers[layer];
   const bool hash = layer < c.hash_layer_count;
   if (rows <= moe::kDecodeRows) {
-    moe::launch_decode(h->dims, h->s, L, state, token_ids, rows, hash, out_state, st, tm);
+    moe::launch_decode(h->dims, h->s, L, state, token_ids, rows, hash, out_state, st, tm, h->dbg);
   } else {
     // the state changes with every call: its tensor map is encoded here (host only, no GPU work)
     CUtensorMap tm_state;
@@ -376,7 +384,7 @@ static int enqueue_forward(moe_ffn_handle *h, const float *state, const int32_t 
     moe::launch_prefill_mix(h->dims, h->s, L, state, tm_state, rows, h->num_sms, st, tm);
     moe::launch_prefill_router(h->dims, h->s, L, state, token_ids, h->tm_ffn_norm, rows, hash, h->num_sms, st, tm);
     moe::launch_dispatch(h->dims, h->s, rows, st, tm);
-    moe::launch_grouped_gemms(h->dims, h->s, L, h->tm_x2, h->tm_act2, h->num_sms, st, tm);
+    moe::launch_grouped_gemms(h->dims, h->s, L, h->tm_b, h->tm_b + 8, h->num_sms, st, tm, h->dbg);
     moe::launch_hc_post(h->dims, h->s.ffn_acc, state, h->s.post, h->s.comb, rows, out_state, st);
     moe::stage(tm, "post", st);
   }
@@ -695,6 +703,15 @@ extern "C" int moe_ffn_stage_times(moe_ffn_handle *h, float *ms, const char **na
     if (names) names[i] = t.name[i];
   }
   return n;
+}
+
+extern "C" int moe_ffn_set_fault_injection(moe_ffn_handle *h, int32_t which, uint32_t wait_limit_us) {
+  if (!h) return fail(nullptr, MOE_FFN_ERR_NULL_PTR, "handle is NULL");
+  if (which < MOE_FFN_INJECT_NONE || which > MOE_FFN_INJECT_GEMM_WAIT)
+    return fail(h, MOE_FFN_ERR_BAD_CONFIG, "unknown fault injection %d", which);
+  h->dbg.inject = which;
+  h->dbg.wait_ns = (uint64_t)wait_limit_us * 1000ull;
+  return MOE_FFN_OK;
 }
 
 extern "C" const char *moe_ffn_last_error(const moe_ffn_handle *h) { return h ? h->err.c_str() : g_init_err.c_str(); }

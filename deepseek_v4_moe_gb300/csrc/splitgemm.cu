@@ -26,6 +26,8 @@
 //              item's MMAs (two TMEM accumulators)
 //   next warp  MMA issuer (one thread)
 //   last warp  weight producer (one thread, TMA)
+// Every wait is bounded (2 s); after a timeout every role leaves its loop, the producers wait
+// (bounded) for their own copies in flight and the MMA issuer for its MMAs, then TMEM is freed.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -99,7 +101,8 @@ __global__ void __launch_bounds__(sg::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *xring = smem, *cring = smem + (size_t)XS * kXBytes;
-  __shared__ __align__(8) uint64_t xfull[XS], xempty[XS], cfull[CS], cempty[CS], tfull[2], tempty[2];
+  __shared__ __align__(8) uint64_t xfull[XS], xempty[XS], cfull[CS], wfull[CS], cempty[CS], tfull[2], tempty[2];
+  __shared__ __align__(8) uint64_t mma_done;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -120,13 +123,15 @@ __global__ void __launch_bounds__(sg::kThreads, 1)
       mbar_init(&xempty[s], kConvWarps);  // every converter warp has read the slot
     }
     for (int s = 0; s < CS; ++s) {
-      mbar_init(&cfull[s], kConvWarps + 1);  // the converter warps + the weight producer's expect_tx
+      mbar_init(&cfull[s], kConvWarps);  // every converter warp has written its rows
+      mbar_init(&wfull[s], 1);           // the weight producer's expect_tx
       mbar_init(&cempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], 4 * C::kDrainGroups);
     }
+    mbar_init(&mma_done, 1);
     abort_flag = 0;
     fence_mbar_init();
     tmap_prefetch(&tmW);
@@ -234,13 +239,21 @@ __global__ void __launch_bounds__(sg::kThreads, 1)
   } else if (warp == kConvWarps && lane == 0) {
     // ---------------- activation producer: one 128 x 64 f32 TMA box per k-stage ----------------
     // (rows past the end of X arrive as zeros)
-    for (int g = 0; g < total && !*abort_p; ++g) {
+    int g = 0;
+    for (; g < total && !*abort_p; ++g) {
       const int xs = g % XS;
       int r0, split, n0;
       item_of(g / nkb, r0, split, n0);
       if (!mbar_wait_bounded(&xempty[xs], ((uint32_t)(g / XS) & 1u) ^ 1u, abort_p, a.status, kWaitNs)) break;
       mbar_arrive_expect_tx(&xfull[xs], kXBytes);
       tma_load_2d(xring + (size_t)xs * kXBytes, &tmX, &xfull[xs], (split * nkb + g % nkb) * BK, r0);
+    }
+    // copies still in flight after an abort land before the CTA may leave (bounded; immediate in
+    // a normal run)
+    int no_abort = 0;
+    for (int s = 0; s < XS; ++s) {
+      const int n = g / XS + (s < g % XS ? 1 : 0);
+      if (n > 0) (void)mbar_wait_bounded(&xfull[s], (uint32_t)((n - 1) & 1), &no_abort, a.status, kWaitNs);
     }
   } else if (warp == kConvWarps + 1 && lane == 0) {
     // ---------------- MMA issuer: item i accumulates in TMEM buffer i % 2 ----------------
@@ -253,7 +266,8 @@ __global__ void __launch_bounds__(sg::kThreads, 1)
       bool ok = true;
       for (int kb = 0; kb < nkb; ++kb, ++g) {
         const int cs = g % CS;
-        if (!mbar_wait_bounded(&cfull[cs], (uint32_t)(g / CS) & 1u, abort_p, a.status, kWaitNs)) {
+        if (!mbar_wait_bounded(&cfull[cs], (uint32_t)(g / CS) & 1u, abort_p, a.status, kWaitNs) ||
+            !mbar_wait_bounded(&wfull[cs], (uint32_t)(g / CS) & 1u, abort_p, a.status, kWaitNs)) {
           ok = false;
           break;
         }
@@ -273,15 +287,25 @@ __global__ void __launch_bounds__(sg::kThreads, 1)
       if (!ok) break;
       tc_commit(&tfull[i & 1]);
     }
+    // every MMA issued here completes before TMEM is freed (immediate in a normal run)
+    tc_commit(&mma_done);
+    int no_abort = 0;
+    (void)mbar_wait_bounded(&mma_done, 0u, &no_abort, a.status, kWaitNs);
   } else if (warp == kConvWarps + 2 && lane == 0) {
     // ---------------- weight producer ----------------
-    for (int g = 0; g < total && !*abort_p; ++g) {
+    int g = 0;
+    for (; g < total && !*abort_p; ++g) {
       const int cs = g % CS;
       int r0, split, n0;
       item_of(g / nkb, r0, split, n0);
       if (!mbar_wait_bounded(&cempty[cs], ((uint32_t)(g / CS) & 1u) ^ 1u, abort_p, a.status, kWaitNs)) break;
-      mbar_arrive_expect_tx(&cfull[cs], C::kBBytes);
-      tma_load_2d(cring + (size_t)cs * C::kCBytes + kPlanes * kPlaneBytes, &tmW, &cfull[cs], (split * nkb + g % nkb) * BK, n0);
+      mbar_arrive_expect_tx(&wfull[cs], C::kBBytes);
+      tma_load_2d(cring + (size_t)cs * C::kCBytes + kPlanes * kPlaneBytes, &tmW, &wfull[cs], (split * nkb + g % nkb) * BK, n0);
+    }
+    int no_abort = 0;  // copies in flight land before the CTA may leave, as above
+    for (int s = 0; s < CS; ++s) {
+      const int n = g / CS + (s < g % CS ? 1 : 0);
+      if (n > 0) (void)mbar_wait_bounded(&wfull[s], (uint32_t)((n - 1) & 1), &no_abort, a.status, kWaitNs);
     }
   }
   tc_fence_before();

@@ -64,7 +64,7 @@ extern "C" {
 #define MOE_FFN_DEV_TIMEOUT 0x8       /* a bounded wait inside a kernel gave up (kernel returned) */
 
 /* Shapes and constants of the block (the page's cfg fields).  Supported:
- *   1 <= hc <= 4;  128 <= hidden <= 8192, hidden % 128 == 0;  128 <= inter <= 8192, inter % 128 == 0;  shared_inter == inter;
+ *   1 <= hc <= 4;  128 <= hidden <= 4096, hidden % 128 == 0;  128 <= inter <= 2048, inter % 128 == 0;  shared_inter == inter;
  *   16 <= experts <= 512, experts % 16 == 0;  1 <= top_k <= 8, top_k <= experts;
  *   hash_layer_count <= n_layers;  1 <= max_rows <= 65536;  vocab >= 1;  sinkhorn_iters >= 0. */
 typedef struct moe_ffn_config {
@@ -278,6 +278,23 @@ typedef struct moe_ffn_mxfp8_experts {
  * this fills the fp16 copies the tensor-core path reads (allocating them if init did not).
  * Synchronous.  Returns MOE_FFN_OK, LAYER_RANGE, NO_WEIGHTS, NULL_PTR, ALIGNMENT, NO_MEMORY or CUDA. */
 int moe_ffn_set_mxfp8_experts(moe_ffn_handle *h, int32_t layer, const moe_ffn_mxfp8_experts *w);
+
+/* Test hook: failure detection without a GPU fault.  Every wait inside the kernels is bounded; on
+ * expiry a kernel sets MOE_FFN_DEV_TIMEOUT, stops its work, waits (bounded) for its own copies and
+ * tensor-core operations in flight, frees its tensor memory and returns, leaving the handle usable.
+ * This call makes one such wait run out on purpose, on the handle's later forwards:
+ *   which = MOE_FFN_INJECT_DECODE_WAIT: rows <= 4, the decode kernel's final phase first waits for
+ *           a count that nothing reaches;
+ *   which = MOE_FFN_INJECT_GEMM_WAIT:   rows > 4, CTA 0 of the gate/up GEMM first waits on an
+ *           mbarrier that nothing arrives at;
+ *   which = MOE_FFN_INJECT_NONE:        no injected wait (the default).
+ * wait_limit_us bounds every in-kernel wait of those forwards (0: the kernels' defaults, 1-2 s).
+ * Outputs of a forward with an injected wait are not meaningful; its status carries the timeout bit.
+ * Returns MOE_FFN_OK, NULL_PTR or BAD_CONFIG.  Nothing in the pages corresponds to it. */
+#define MOE_FFN_INJECT_NONE 0
+#define MOE_FFN_INJECT_DECODE_WAIT 1
+#define MOE_FFN_INJECT_GEMM_WAIT 2
+int moe_ffn_set_fault_injection(moe_ffn_handle *h, int32_t which, uint32_t wait_limit_us);
 
 /* Text of the last error on this handle, or, when h is NULL, of the last failed call made without
  * a handle (init, the allocation-free split, a NULL handle) on the calling thread: that message

@@ -100,3 +100,4 @@ def test_new_entry_points_reject_a_null_handle(lib):
     assert lib.moe_ffn_hc_pre(None, 0, 0, None, 1, None, None, None, None, None) == _lib.ERR_NULL_PTR
     assert lib.moe_ffn_hc_post(None, None, None, None, None, 1, None, None) == _lib.ERR_NULL_PTR
     assert lib.moe_ffn_forward_layers(None, None, None, 1, 0, 2, None, None) == _lib.ERR_NULL_PTR
+    assert lib.moe_ffn_set_fault_injection(None, 1, 1000) == _lib.ERR_NULL_PTR
