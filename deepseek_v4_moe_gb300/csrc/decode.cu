@@ -18,8 +18,8 @@
 //             itself, on the 16 hidden columns each worker thread owns, from the mix partials and
 //             the state (in L2 by then), with the RMS over the CTA: x lands in the registers the
 //             stream needs and no CTA waits for another to publish it.  Router CTA j adds the
-//             logits of experts [j epc, (j + 1) epc) over the CTA and writes each (selection score
-//             sigmoid(logit) + bias, logit) pair with one 8-byte store.
+//             logits of experts [j epc, (j + 1) epc) over the CTA and writes each sigmoid(logit)
+//             with one 4-byte store into a table that starts all-ones.
 //             (b) the stream: every slot is consumed by all 8 warps at once (split K, x or the
 //             group's SwiGLU output in registers), each leaving its partial sums in shared memory:
 //               kind A: a gate row and an up row of one expert group;
@@ -30,9 +30,10 @@
 //             two claims ahead) and moves each ticket's weight rows into a ring of shared-memory
 //             slots with bulk asynchronous copies (TMA, completion on the slot's mbarrier), so the
 //             bytes in flight cost no registers.  The shared expert needs no routing: its rows
-//             stream as soon as the mix CTAs have read the state.  At its first routed ticket it
-//             routes the batch itself, from the (score, logit) pairs (polled until written): the
-//             top_k by warp-shuffle argmax rounds, the same code on the same values in every CTA.
+//             stream as soon as the mix CTAs have read the state.  Between fills it keeps one bulk
+//             copy of the sigmoid table in flight into shared memory; once a copy holds no
+//             all-ones entry it routes the batch itself: the top_k by warp-shuffle argmax rounds,
+//             the same code on the same values in every CTA.
 //   publisher takes the slots in order: adds the 8 warps' partial sums, applies SwiGLU (kind A),
 //             stores act or y, frees the slot for the producer, and publishes completion counts
 //             in batches (one fence, then relaxed adds): a release fence waits microseconds under
@@ -75,7 +76,7 @@ struct DecodeArgs {
   float *mix_part;   // [nm, rows, M + 1] mix partial sums (the last entry: sum of squares)
   float *mixes, *pre, *post, *comb;
   float *x;          // [rows, hidden] ffn_norm(ffn_input), written by router CTA 0 (also the stage tap)
-  float2 *sel;       // [4, experts] (selection score sigmoid(logit) + bias, logit); all-ones bits until written
+  float *sel;        // [4, experts] sigmoid(logit) of each row and expert; all-ones bits until written
                      // in this launch (the last CTA out writes that pattern back)
   float *logits;     // [rows, experts]
   float *act;        // [groups, 4, inter]
@@ -103,7 +104,6 @@ constexpr int kWorkerWarps = 8, kWorkers = 32 * kWorkerWarps, kDecThreads = kWor
 constexpr int kProducerWarp = kWorkerWarps, kPublisherWarp = kWorkerWarps + 1;
 constexpr int kPublishBatch = 16;  // slots a publisher may hold before it publishes their counts
 constexpr int kMixCols = 512;     // flattened-state columns per mix CTA (a multiple of 128)
-constexpr int kRowsB = 4;         // down rows per kind-B slot
 constexpr int kChunk = 4;         // tickets claimed by one atomic of a producer (consecutive slots)
 // kind A: each worker thread owns 16 columns of a row (hidden <= 16 x 256 = 4096); kind B: 8
 // columns of a down row (inter <= 8 x 256 = 2048); moe_ffn_init enforces both limits
@@ -111,12 +111,15 @@ constexpr int kMaxEpc = 4;        // experts per router CTA (64 CTAs up to 256 e
 
 template <bool MX>
 struct Ring {
-  static constexpr int kSlots = MX ? 10 : 6;  // two CTAs per SM: 2 x (96 or 85 KB) of slots
-  // bf16: a gate + up row pair (4 hidden bytes) or four down rows (8 inter bytes), 16 KB at most;
-  // MXFP8: the codes (2 hidden or 4 inter bytes) and their scales, each scale run copied as the
-  // 16-byte-aligned span that holds it
-  static constexpr int kSlotBytes = MX ? 8704 : 16384;
-  static constexpr int kRed = 16;  // partial sums per warp and slot (4 rows x 4 down rows at most)
+  // bf16: one gate + up row pair (4 hidden bytes) or four down rows (8 inter bytes), 16 KB at most,
+  // six slots.  MXFP8 (whose codes take more decoding per byte): two row pairs (4 hidden bytes of
+  // codes) or eight down rows (8 inter bytes) and their scales, each scale run copied as the
+  // 16-byte-aligned span that holds it, five slots.  Two CTAs per SM: 2 x (96 or 85 KB) of slots.
+  static constexpr int kRowsA = MX ? 2 : 1;  // gate/up row pairs per kind-A slot
+  static constexpr int kRowsB = MX ? 8 : 4;  // down rows per kind-B slot
+  static constexpr int kSlots = MX ? 5 : 6;
+  static constexpr int kSlotBytes = MX ? 17408 : 16384;
+  static constexpr int kRed = 4 * kRowsB;  // partial sums per warp and slot (4 rows x the down rows at most)
   static constexpr size_t kSmem = (size_t)kSlots * kSlotBytes + (size_t)kSlots * kWorkerWarps * kRed * 4;
 };
 
@@ -127,8 +130,12 @@ struct SlotMeta {
 
 // Shared memory outside the ring (static).
 struct DecSmem {
-  // mix role
-  alignas(16) float st[kDecodeRows][kMixCols];
+  union {
+    alignas(16) float st[kDecodeRows][kMixCols];  // mix role: the state columns
+    alignas(16) float sel[kDecodeRows * kExpertsMax];  // routing: the score table as the bulk copy left it
+  };
+  float bias[kExpertsMax];                        // routing (score layers): exp_probs_b
+  int hsel[kDecodeRows][kTopKMax], hbad[kDecodeRows];  // routing (hash layers): tid2eid rows, token out of range
   float sums[kDecodeRows][kMixMax + 1];
   float mixes[kDecodeRows][kMixMax];  // the last mix CTA's mixes, for its publisher's Sinkhorn
   int comb_todo;                      // mix CTAs: 1 = the last one (its publisher forms the comb), 2 = not
@@ -137,7 +144,7 @@ struct DecSmem {
   float pre[kDecodeRows][kHcMax];
   float rs[kDecodeRows];
   // ring bookkeeping
-  SlotMeta meta[12];
+  SlotMeta meta[8];
   // the producer's (row, slot) pairs while it groups them, then the group table
   float rtw[32];
   int ng;
@@ -215,9 +222,31 @@ __device__ __forceinline__ int draw_ticket(unsigned *tick) {
   return __shfl_sync(0xffffffffu, c, 0);
 }
 
-// Warp-wide bounded mbarrier wait (lane 0 waits, the warp follows its verdict); a timeout also
-// raises the launch's abort flag.
+// The producer and publisher wait with a short sleep between tests, so that their spinning takes
+// few issue slots from the worker warps of the SM.
+constexpr unsigned kBackoffNs = 64;
+
+// mbar_wait_bounded with a sleep between tests.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                                  int *dev_status, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    __nanosleep(kBackoffNs);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      atomicOr(dev_status, kDevTimeout);
+      return false;
+    }
+  }
+}
+
+// Warp-wide bounded mbarrier wait: every lane tests the phase; unless all saw it complete, lane 0
+// waits (bounded) and the warp follows its verdict.  A timeout also raises the launch's abort flag.
 __device__ bool warp_mbar_wait(uint64_t *bar, uint32_t parity, DecSmem &sm, const DecodeArgs &a) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   int ok = 0;
   if ((threadIdx.x & 31) == 0) {
     ok = mbar_wait_bounded(bar, parity, &sm.abort, a.status, a.wait_ns) ? 1 : 0;
@@ -421,6 +450,19 @@ __device__ void mix_role(const DecodeArgs &a, int j, DecSmem &sm, unsigned *cnt)
 template <bool MX>
 __device__ __forceinline__ int own_col(int tid, int h) { return MX ? 16 * tid + 8 * h : 8 * tid + 2048 * h; }
 
+// The state of row r, streams h < hc, on the own column group g (8 columns), into v[h][0..1].
+template <bool MX>
+__device__ __forceinline__ void load_state_group(const DecodeArgs &a, int r, int g, float4 (&v)[kHcMax][2]) {
+  const int c = own_col<MX>(threadIdx.x, g);
+#pragma unroll
+  for (int h = 0; h < kHcMax; ++h) {
+    const bool in = h < a.hc && c < a.hidden;
+    const float4 *sp = reinterpret_cast<const float4 *>(a.state + ((size_t)r * a.hc + h) * a.hidden + c);
+    v[h][0] = in ? __ldcg(sp) : make_float4(0.f, 0.f, 0.f, 0.f);
+    v[h][1] = in ? __ldcg(sp + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
 template <int ROWS, bool MX>
 __device__ __forceinline__ void form_x(const DecodeArgs &a, DecSmem &sm, unsigned *cnt, float4 (&xr)[ROWS][4]) {
   constexpr int rows = ROWS;
@@ -437,6 +479,11 @@ __device__ __forceinline__ void form_x(const DecodeArgs &a, DecSmem &sm, unsigne
   if (tid == 0) sm.hc_scale[0] = a.hc_scale[0];
   if (tid < hc) sm.hc_base[tid] = a.hc_base[tid];
   pdl_wait();
+  // the state loads of a row and column group go out together (one L2 round trip each); at one or
+  // two rows (registers to spare) row 0's first group goes out before the mix partials are read
+  constexpr bool kEarly = ROWS <= 2;
+  float4 sv0[kHcMax][2];
+  if (kEarly) load_state_group<MX>(a, 0, 0, sv0);
   // pre from the mix partials, once every mix CTA has written its own (bounded wait; on timeout
   // the status says so and the values below are not meaningful, but every CTA still finishes)
   (void)workers_wait_at_least(&cnt[kCntMixDone], (unsigned)a.nm, a, &sm.flag);
@@ -462,20 +509,27 @@ __device__ __forceinline__ void form_x(const DecodeArgs &a, DecSmem &sm, unsigne
   for (int r = 0; r < rows; ++r) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) xr[r][i] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
-    for (int h = 0; h < hc; ++h) {
-      const float ph = sm.pre[r][h];
 #pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        const int c = own_col<MX>(tid, g);
-        if (c < D) {
-          const float4 *sp = reinterpret_cast<const float4 *>(a.state + ((size_t)r * hc + h) * D + c);
-          const float4 s0 = __ldcg(sp), s1 = __ldcg(sp + 1);
-          xr[r][2 * g] = make_float4(xr[r][2 * g].x + ph * s0.x, xr[r][2 * g].y + ph * s0.y, xr[r][2 * g].z + ph * s0.z,
-                                     xr[r][2 * g].w + ph * s0.w);
-          xr[r][2 * g + 1] = make_float4(xr[r][2 * g + 1].x + ph * s1.x, xr[r][2 * g + 1].y + ph * s1.y,
-                                         xr[r][2 * g + 1].z + ph * s1.z, xr[r][2 * g + 1].w + ph * s1.w);
+    for (int g = 0; g < 2; ++g) {
+      float4 sv[kHcMax][2];
+      if (kEarly && r == 0 && g == 0) {
+#pragma unroll
+        for (int h = 0; h < kHcMax; ++h) {
+          sv[h][0] = sv0[h][0];
+          sv[h][1] = sv0[h][1];
         }
+      } else {
+        load_state_group<MX>(a, r, g, sv);
+      }
+      // streams in order h = 0, 1, ... (absent streams add zeros)
+#pragma unroll
+      for (int h = 0; h < kHcMax; ++h) {
+        const float ph = h < hc ? sm.pre[r][h] : 0.f;
+        const float4 s0 = sv[h][0], s1 = sv[h][1];
+        xr[r][2 * g] = make_float4(xr[r][2 * g].x + ph * s0.x, xr[r][2 * g].y + ph * s0.y, xr[r][2 * g].z + ph * s0.z,
+                                   xr[r][2 * g].w + ph * s0.w);
+        xr[r][2 * g + 1] = make_float4(xr[r][2 * g + 1].x + ph * s1.x, xr[r][2 * g + 1].y + ph * s1.y,
+                                       xr[r][2 * g + 1].z + ph * s1.z, xr[r][2 * g + 1].w + ph * s1.w);
       }
     }
 #pragma unroll
@@ -562,14 +616,10 @@ __device__ __forceinline__ void router_logits(const DecodeArgs &a, DecSmem &sm, 
       const int q = lane / ROWS, r = lane - q * ROWS, e = e0 + q;
       bad = !isfinite(l);
       a.logits[(size_t)r * E + e] = l;  // the stage tap
-      float sc = 0.f;
-      if (!p.hash) {
-        sc = sigmoidf_(l) + p.bias[e];
-        sc = isnan(sc) ? -INFINITY : sc;
-      }
-      // one 8-byte store: a reader that sees it sees both values (no fence or counter needed: the
-      // producers poll these entries until none holds the unwritten pattern)
-      a.sel[(size_t)r * E + e] = make_float2(sc, l);
+      // one 4-byte store, the NaN made canonical so that it never reads as the unwritten pattern
+      // (no fence or counter: the producers copy the table until no entry holds that pattern)
+      const float sg = sigmoidf_(l);
+      a.sel[(size_t)r * E + e] = isnan(sg) ? __uint_as_float(0x7FFFFFFFu) : sg;
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, kDevNonFinite);
   }
@@ -584,126 +634,114 @@ __device__ __forceinline__ void router_logits(const DecodeArgs &a, DecSmem &sm, 
 // the shared expert (weight 1 for every row), then the distinct routed experts in order of first
 // appearance, each with the mask of rows using it and their summed route weights.  CTA 0 also
 // writes the idx / weight / safe-index outputs and the status bits.
+//
+// The producer never blocks on the scores while it still has weight rows to fill: it keeps one
+// bulk copy of the rows' sigmoid(logit) table (rows x experts f32) in flight into shared memory and
+// looks at it between fills; a copy that still holds the unwritten pattern anywhere is issued
+// again.  The bias and the hash rows (which do not depend on the scores) are read at launch.
 // ---------------------------------------------------------------------------------------------
-// `dry`: the same instructions on whatever the score and logit buffers hold, without waiting and
-// without any global write, run once at launch so that the code is in L2 when the scores arrive
-// (the weight stream and the L2 flush of a benchmark evict it between launches; a code path that
-// runs once per launch otherwise pays the instruction-fetch latency line by line).  Its group
-// table in shared memory is overwritten by the live run.
+
+// Non-blocking look at an mbarrier phase.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// At launch (producer warp): the bias into shared memory (score layers), or each row's tid2eid
+// entries (hash layers; -1 for a token out of range, whose status bit CTA 0 raises).
 template <int ROWS>
-__device__ __noinline__ void route_cta(const DecodeArgs &a, DecSmem &sm, unsigned *cnt, bool dry = false) {
+__device__ __forceinline__ void route_setup(const DecodeArgs &a, DecSmem &sm) {
+  const RouteParams &p = a.rp;
+  const int lane = threadIdx.x & 31, E = a.experts, K = p.top_k;
+  if (!p.hash) {
+    for (int e = lane; e < E; e += 32) sm.bias[e] = p.bias[e];
+  } else {
+    pdl_wait();  // the token ids come from the previous kernel
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+      const int tok = p.token_ids[r];
+      const bool tok_ok = tok >= 0 && tok < p.vocab;
+      if (!tok_ok && lane == 0 && blockIdx.x == 0) atomicOr(p.status, kDevTokenRange);
+      if (lane < K) sm.hsel[r][lane] = tok_ok ? p.tid2eid[(size_t)tok * K + lane] : -1;
+      if (lane == 0) sm.hbad[r] = tok_ok ? 0 : 1;
+    }
+  }
+  __syncwarp();
+}
+
+// The group table from the score table in shared memory (sm.sel, row stride experts).  `dry`:
+// the same instructions on whatever shared memory holds, without any global write, run once at
+// launch so that the code is in L2 when the scores arrive (the weight stream and the L2 flush of
+// a benchmark evict it between launches; code that runs once per launch otherwise pays the
+// instruction-fetch latency line by line).  Its table is overwritten by the live run.
+template <int ROWS, int J2>  // J2: candidates per lane, experts / 32 rounded up to 8 or 16
+__device__ __noinline__ void route_compute(const DecodeArgs &a, DecSmem &sm, bool dry) {
   constexpr int rows = ROWS;
   const RouteParams &p = a.rp;
   const int lane = threadIdx.x & 31, E = a.experts, K = p.top_k;
   const bool live = blockIdx.x == 0 && !dry;
   int sel[rows];
   float wgt[rows];
-  if (!dry) pdl_wait();  // the token ids come from the previous kernel
-  {
-    const uint64_t t0 = dry ? 0 : global_timer_ns();
 #pragma unroll
-    for (int r = 0; r < rows; ++r) {
-      int my_sel = -1;
-      constexpr int J2 = kExpertsMax / 32;
-      float lg[J2];  // this lane's logits (score layers)
-      if (!p.hash) {
-        constexpr int J = J2;
-        float v[J];
-        // the row's (score, logit) pairs, read until every one has been written (bounded)
-        for (;;) {
-          bool pending = false;
+  for (int r = 0; r < rows; ++r) {
+    const float *s_row = sm.sel + r * E;
+    int my_sel = -1;
+    if (!p.hash) {
+      float v[J2];
 #pragma unroll
-          for (int jj = 0; jj < J; ++jj) {
-            const int e = lane + 32 * jj;
-            const float2 q = e < E ? __ldcg(a.sel + (size_t)r * E + e) : make_float2(-INFINITY, 0.f);
-            v[jj] = q.x;
-            lg[jj] = q.y;
-            pending |= __float_as_uint(q.x) == kUnwritten;
-          }
-          if (dry || !__any_sync(0xffffffffu, pending)) break;
-          if (global_timer_ns() - t0 > a.wait_ns || *reinterpret_cast<volatile unsigned *>(&cnt[kCntAbort]) != 0u) {
-            if (lane == 0) {
-              atomicOr(a.status, kDevTimeout);
-              atomicExch(&cnt[kCntAbort], 1u);
-            }
-            break;
-          }
-          __nanosleep(32);
-        }
-        uint32_t taken = 0;
-#pragma unroll 1
-        for (int k = 0; k < K; ++k) {
-          float bv = -INFINITY;
-          int be = 0x7fffffff;
-#pragma unroll
-          for (int jj = 0; jj < J; ++jj) {
-            const int e = lane + 32 * jj;
-            if (e < E && !((taken >> jj) & 1u) && (v[jj] > bv || be == 0x7fffffff)) {
-              bv = v[jj];
-              be = e;
-            }
-          }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            if (ov > bv || (ov == bv && oe < be)) {
-              bv = ov;
-              be = oe;
-            }
-          }
-          if ((be & 31) == lane) taken |= 1u << (be >> 5);
-          if (lane == k) my_sel = be;
-        }
-      } else {
-        const int tok = p.token_ids[r];
-        const bool tok_ok = tok >= 0 && tok < p.vocab;
-        if (!tok_ok && lane == 0 && live) atomicOr(p.status, kDevTokenRange);
-        if (lane < K) my_sel = tok_ok ? p.tid2eid[(size_t)tok * K + lane] : -1;
-        const bool bad_entry = tok_ok && lane < K && !(my_sel >= 0 && my_sel < E);
-        if (__any_sync(0xffffffffu, bad_entry) && lane == 0 && live) atomicOr(p.status, kDevRouteRange);
+      for (int jj = 0; jj < J2; ++jj) {
+        const int e = lane + 32 * jj;
+        const float key = e < E ? s_row[e] + sm.bias[e] : -INFINITY;
+        v[jj] = isnan(key) ? -INFINITY : key;
       }
-      const bool valid = lane < K && my_sel >= 0 && my_sel < E;
-      // the chosen logit sits in register my_sel / 32 of lane my_sel % 32 (score layers), else it is
-      // read now (hash layers)
-      float lsel = 0.f;
-      if (!p.hash) {
-        const int src = valid ? (my_sel & 31) : 0, jsel = valid ? (my_sel >> 5) : 0;
-        float got = 0.f;
+      uint32_t taken = 0;
+#pragma unroll 1
+      for (int k = 0; k < K; ++k) {
+        float bv = -INFINITY;
+        int be = 0x7fffffff;
 #pragma unroll
         for (int jj = 0; jj < J2; ++jj) {
-          const float cand = __shfl_sync(0xffffffffu, lg[jj], src);
-          if (jj == jsel) got = cand;
-        }
-        lsel = got;
-      } else {
-        // hash layers: the chosen experts' logits, read until written (bounded)
-        for (;;) {
-          const float2 q = valid ? __ldcg(a.sel + (size_t)r * E + my_sel) : make_float2(0.f, 0.f);
-          lsel = q.y;
-          const bool pending = valid && __float_as_uint(q.y) == kUnwritten;
-          if (dry || !__any_sync(0xffffffffu, pending)) break;
-          if (global_timer_ns() - t0 > a.wait_ns || *reinterpret_cast<volatile unsigned *>(&cnt[kCntAbort]) != 0u) {
-            if (lane == 0) {
-              atomicOr(a.status, kDevTimeout);
-              atomicExch(&cnt[kCntAbort], 1u);
-            }
-            break;
+          const int e = lane + 32 * jj;
+          if (e < E && !((taken >> jj) & 1u) && (v[jj] > bv || be == 0x7fffffff)) {
+            bv = v[jj];
+            be = e;
           }
-          __nanosleep(32);
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+          if (ov > bv || (ov == bv && oe < be)) {
+            bv = ov;
+            be = oe;
+          }
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        if (lane == k) my_sel = be;
       }
-      const float sc = valid ? sigmoidf_(lsel) : 0.f;
-      const float tot = warp_sum(sc);
-      const float w = lane < K && tot > 0.f ? sc / tot : 0.f;
-      if (lane < K && live) {
-        p.idx[r * K + lane] = my_sel;
-        p.rw[r * K + lane] = w;
-        p.safe[r * K + lane] = valid ? (unsigned)my_sel : 0u;
-      }
-      sel[r] = my_sel;
-      wgt[r] = w;
+    } else {
+      if (lane < K) my_sel = sm.hsel[r][lane];
+      const bool bad_entry = !sm.hbad[r] && lane < K && !(my_sel >= 0 && my_sel < E);
+      if (__any_sync(0xffffffffu, bad_entry) && lane == 0 && live) atomicOr(p.status, kDevRouteRange);
     }
+    const bool valid = lane < K && my_sel >= 0 && my_sel < E;
+    const float sc = valid ? s_row[my_sel] : 0.f;  // sigmoid(logit) as the router CTA formed it
+    const float tot = warp_sum(sc);
+    const float w = lane < K && tot > 0.f ? sc / tot : 0.f;
+    if (lane < K && live) {
+      p.idx[r * K + lane] = my_sel;
+      p.rw[r * K + lane] = w;
+      p.safe[r * K + lane] = valid ? (unsigned)my_sel : 0u;
+    }
+    sel[r] = my_sel;
+    wgt[r] = w;
   }
   // lane rr * K + k takes slot k of row rr (rows * top_k <= 32)
   const int rr = lane / K, kk = lane - rr * K;
@@ -752,6 +790,76 @@ __device__ __noinline__ void route_cta(const DecodeArgs &a, DecSmem &sm, unsigne
     sm.ng = 1 + __popc(leaders);
   }
   __syncwarp();
+}
+
+template <int ROWS>
+__device__ __forceinline__ void route_compute(const DecodeArgs &a, DecSmem &sm, bool dry) {
+  if (a.experts <= 256) route_compute<ROWS, 8>(a, sm, dry);
+  else route_compute<ROWS, 16>(a, sm, dry);
+}
+
+// The producer's view of the score table: one bulk copy of it in flight at a time.
+struct ScorePoll {
+  uint64_t *bar;
+  uint32_t phase;    // parity of the copy in flight
+  bool in_flight;
+  bool routed;       // the group table is the live one
+  uint64_t t0;       // first issue (bound of the wait)
+};
+
+__device__ __forceinline__ void score_copy_issue(const DecodeArgs &a, DecSmem &sm, ScorePoll &q, int rows) {
+  if ((threadIdx.x & 31) == 0) {
+    const uint32_t bytes = (uint32_t)(rows * a.experts * 4);  // experts % 16 == 0: a multiple of 16
+    mbar_arrive_expect_tx(q.bar, bytes);
+    tma_bulk_g2s(sm.sel, a.sel, bytes, q.bar);
+  }
+  q.in_flight = true;
+}
+
+// Looks at the copy in flight (blocking: until the table is complete, bounded); when it has landed
+// and every entry is written, forms the group table.  Returns q.routed.  Warp-uniform.
+template <int ROWS>
+__device__ bool score_poll(const DecodeArgs &a, DecSmem &sm, unsigned *cnt, ScorePoll &q, bool block) {
+  const int lane = threadIdx.x & 31;
+  if (q.routed) return true;
+  for (;;) {
+    int landed = 0;
+    if (lane == 0) landed = mbar_test_wait(q.bar, q.phase) ? 1 : 0;
+    if (__shfl_sync(0xffffffffu, landed, 0)) {
+      q.phase ^= 1u;
+      q.in_flight = false;
+      bool pending = false;
+      for (int i = lane; i < ROWS * a.experts; i += 32) pending |= __float_as_uint(sm.sel[i]) == kUnwritten;
+      if (!__any_sync(0xffffffffu, pending)) {
+        route_compute<ROWS>(a, sm, false);
+        q.routed = true;
+        return true;
+      }
+      // the reads above come before the next copy's writes to the same bytes
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      score_copy_issue(a, sm, q, ROWS);
+    }
+    if (!block) return false;
+    if (global_timer_ns() - q.t0 > a.wait_ns || *reinterpret_cast<volatile unsigned *>(&cnt[kCntAbort]) != 0u ||
+        *reinterpret_cast<volatile int *>(&sm.abort) != 0) {
+      if (lane == 0) {
+        atomicOr(a.status, kDevTimeout);
+        atomicExch(&cnt[kCntAbort], 1u);
+      }
+      // give up: a table of the shared expert only, so that the stream and phase C end at once
+      if (lane == 0) {
+        sm.ge[0] = a.experts;
+        sm.gm[0] = (1 << ROWS) - 1;
+        for (int r = 0; r < kDecodeRows; ++r) sm.gw[0][r] = r < ROWS ? 1.f : 0.f;
+        sm.ng = 1;
+      }
+      __syncwarp();
+      q.routed = true;
+      return true;
+    }
+    __nanosleep(64);
+  }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -805,7 +913,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
   uint8_t *ring = dsm;
   float *red = reinterpret_cast<float *>(dsm + (size_t)S * RG::kSlotBytes);  // [S][8 warps][kRed]
   __shared__ __align__(16) DecSmem sm;
-  __shared__ __align__(8) uint64_t full_bar[S], empty_bar[S], red_bar[S];
+  __shared__ __align__(8) uint64_t full_bar[S], empty_bar[S], red_bar[S], score_bar;
   unsigned *cnt = a.counters;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int D = a.hidden, I = a.inter, E = a.experts;
@@ -816,6 +924,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
       mbar_init(&empty_bar[s], 1);             // the publisher has taken the slot's partial sums
       mbar_init(&red_bar[s], kWorkerWarps);    // every worker warp has left its partial sums
     }
+    mbar_init(&score_bar, 1);                  // a copy of the score table has landed
     sm.abort = 0;
     sm.comb_todo = 0;
     sm.flag = (int)atomicAdd(&cnt[kCntRole], 1u);
@@ -827,27 +936,34 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
 
   unsigned *group_done = cnt + kCntGroups;
   unsigned *dblock_done = cnt + kCntDBlocks;
-  // a kind-A slot: the gate and up rows i of group g; a kind-B slot: down rows d0 .. d0 + 3
-  const int perg = I, nb_per_g = D / kRowsB;
+  // a kind-A slot: the gate and up rows i, i + 1 of group g; a kind-B slot: down rows d0 .. d0 + 7
+  const int perg = I / RG::kRowsA, nb_per_g = D / RG::kRowsB;
 
   if (warp == kProducerWarp) {
     // ================= producer =================
-    // routed rows are read once (evict first); the shared expert's rows keep the normal priority,
-    // so that no weight row crowds the kernel's own code or the prelude's data out of L2
-    const uint64_t pol_first = make_policy_evict_first(), pol_last = make_policy_evict_normal();
-    const int span = MX ? (((D / 32 + 32) + 15) & ~15) : 0;  // bytes per MX scale run slot of a kind-A slot
-    route_cta<ROWS>(a, sm, cnt, true);
+    // every weight row is read once (evict first), so that none crowds the kernel's own code or the
+    // prelude's data out of L2 (the shared expert's rows prefetched to L2 are the newest lines, read
+    // again within microseconds)
+    const uint64_t pol_first = make_policy_evict_first(), pol_last = pol_first;
+    const int span = MX ? (((RG::kRowsA * D / 32 + 32) + 15) & ~15) : 0;  // bytes per MX scale run of a kind-A slot
+    route_setup<ROWS>(a, sm);
+    route_compute<ROWS>(a, sm, true);
+    ScorePoll sp{&score_bar, 0u, false, false, 0};
     // the prelude's loads are latency-bound chains: the stream starts once the mix CTAs have read
     // the state (later prelude reads hit L2), so that they do not queue behind it.  Then the shared
     // expert's gate/up rows that the first ring fills do not cover go to L2 (they are read again by
     // whichever CTA draws their tickets).
     (void)wait_at_least(&cnt[kCntMixDone], (unsigned)a.nm, a);
+    // the mix role's reads of the shared-memory rows the score table overlays are done (mix CTAs
+    // arrive on that count after them)
+    sp.t0 = global_timer_ns();
+    score_copy_issue(a, sm, sp, ROWS);
     {
-      const int first = gridDim.x * S;
-      const int rest = perg - first;
+      const int first = gridDim.x * S * RG::kRowsA;  // rows of the first fills
+      const int rest = I - first;
       if (rest > 0) {
         const int per = (rest + gridDim.x - 1) / gridDim.x;
-        for (int i = first + blockIdx.x * per + lane; i < min(perg, first + (blockIdx.x + 1) * per); i += 32) {
+        for (int i = first + blockIdx.x * per + lane; i < min(I, first + (blockIdx.x + 1) * per); i += 32) {
           if (MX) {
             prefetch_l2(a.gate_sh_q + (size_t)i * D, (uint32_t)D, pol_last);
             prefetch_l2(a.up_sh_q + (size_t)i * D, (uint32_t)D, pol_last);
@@ -873,28 +989,29 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
     for (int k = 0;; ++k) {
       const int s = k % S;
       const int t = __shfl_sync(0xffffffffu, c0, 0) + k % kChunk;
+      if (!sp.routed) (void)score_poll<ROWS>(a, sm, cnt, sp, false);
       SlotMeta m;
       m.s0 = m.s1 = 0;
       if (t < perg) {
         m.kind = kKindA;
         m.g = 0;
-        m.row = t;
+        m.row = t * RG::kRowsA;
         m.e = E;
         m.mask = all_rows;
       } else {
         if (ng < 0) {
-          route_cta<ROWS>(a, sm, cnt);
+          (void)score_poll<ROWS>(a, sm, cnt, sp, true);
           ng = sm.ng;
         }
         const int nA = ng * perg, nB = ng * nb_per_g;
         if (t < nA) {
           m.kind = kKindA;
           m.g = t / perg;
-          m.row = t - m.g * perg;
+          m.row = (t - m.g * perg) * RG::kRowsA;
         } else if (t < nA + nB) {
           m.kind = kKindB;
           m.g = (t - nA) / nb_per_g;
-          m.row = (t - nA - m.g * nb_per_g) * kRowsB;
+          m.row = (t - nA - m.g * nb_per_g) * RG::kRowsB;
         } else {
           m.kind = kKindEnd;
           m.g = 0;
@@ -906,7 +1023,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
       // the slot is free once every worker warp has read its previous contents
       int got = 1;
       if (lane == 0) {
-        got = mbar_wait_bounded(&empty_bar[s], ((uint32_t)(k / S) & 1u) ^ 1u, &sm.abort, a.status, a.wait_ns) ? 1 : 0;
+        got = mbar_wait_backoff(&empty_bar[s], ((uint32_t)(k / S) & 1u) ^ 1u, &sm.abort, a.status, a.wait_ns) ? 1 : 0;
         if (!got) atomicExch(&cnt[kCntAbort], 1u);
       }
       got = __shfl_sync(0xffffffffu, got, 0);
@@ -920,32 +1037,34 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
           const size_t ro = routed ? (size_t)m.e * I + m.row : (size_t)m.row;
           if (MX) {
             const uint8_t *gs = (routed ? a.gate_s : a.gate_sh_s), *us = (routed ? a.up_s : a.up_sh_s);
-            const size_t so = ro * (D / 32), a0 = so & ~(size_t)15, a1 = (so + D / 32 + 15) & ~(size_t)15;
+            const size_t so = ro * (D / 32), a0 = so & ~(size_t)15;
+            const size_t a1 = (so + RG::kRowsA * D / 32 + 15) & ~(size_t)15;
             m.s0 = m.s1 = (int)(so - a0);
             const uint32_t sb = (uint32_t)(a1 - a0);
             sm.meta[s] = m;
-            mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(2 * D) + 2 * sb);
-            bulk_g2s(dst, (routed ? a.gate_q : a.gate_sh_q) + ro * D, (uint32_t)D, &full_bar[s], pol);
-            bulk_g2s(dst + D, (routed ? a.up_q : a.up_sh_q) + ro * D, (uint32_t)D, &full_bar[s], pol);
-            bulk_g2s(dst + 2 * D, gs + a0, sb, &full_bar[s], pol);
-            bulk_g2s(dst + 2 * D + span, us + a0, sb, &full_bar[s], pol);
+            mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(2 * RG::kRowsA * D) + 2 * sb);
+            bulk_g2s(dst, (routed ? a.gate_q : a.gate_sh_q) + ro * D, (uint32_t)(RG::kRowsA * D), &full_bar[s], pol);
+            bulk_g2s(dst + RG::kRowsA * D, (routed ? a.up_q : a.up_sh_q) + ro * D, (uint32_t)(RG::kRowsA * D), &full_bar[s], pol);
+            bulk_g2s(dst + 2 * RG::kRowsA * D, gs + a0, sb, &full_bar[s], pol);
+            bulk_g2s(dst + 2 * RG::kRowsA * D + span, us + a0, sb, &full_bar[s], pol);
           } else {
             sm.meta[s] = m;
-            mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(4 * D));
-            bulk_g2s(dst, (routed ? a.gate_exps : a.gate_sh) + ro * D, (uint32_t)(2 * D), &full_bar[s], pol);
-            bulk_g2s(dst + 2 * D, (routed ? a.up_exps : a.up_sh) + ro * D, (uint32_t)(2 * D), &full_bar[s], pol);
+            mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(4 * RG::kRowsA * D));
+            bulk_g2s(dst, (routed ? a.gate_exps : a.gate_sh) + ro * D, (uint32_t)(2 * RG::kRowsA * D), &full_bar[s], pol);
+            bulk_g2s(dst + 2 * RG::kRowsA * D, (routed ? a.up_exps : a.up_sh) + ro * D, (uint32_t)(2 * RG::kRowsA * D), &full_bar[s],
+                     pol);
           }
         } else if (m.kind == kKindB) {
           const size_t ro = routed ? (size_t)m.e * D + m.row : (size_t)m.row;
           sm.meta[s] = m;
           if (MX) {
-            mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(kRowsB * I + kRowsB * (I / 32)));
-            bulk_g2s(dst, (routed ? a.down_q : a.down_sh_q) + ro * I, (uint32_t)(kRowsB * I), &full_bar[s], pol);
-            bulk_g2s(dst + kRowsB * I, (routed ? a.down_s : a.down_sh_s) + ro * (I / 32), (uint32_t)(kRowsB * (I / 32)),
+            mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(RG::kRowsB * I + RG::kRowsB * (I / 32)));
+            bulk_g2s(dst, (routed ? a.down_q : a.down_sh_q) + ro * I, (uint32_t)(RG::kRowsB * I), &full_bar[s], pol);
+            bulk_g2s(dst + RG::kRowsB * I, (routed ? a.down_s : a.down_sh_s) + ro * (I / 32), (uint32_t)(RG::kRowsB * (I / 32)),
                      &full_bar[s], pol);
           } else {
-            mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(kRowsB * I * 2));
-            bulk_g2s(dst, (routed ? a.down_exps : a.down_sh) + ro * I, (uint32_t)(kRowsB * I * 2), &full_bar[s], pol);
+            mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(RG::kRowsB * I * 2));
+            bulk_g2s(dst, (routed ? a.down_exps : a.down_sh) + ro * I, (uint32_t)(RG::kRowsB * I * 2), &full_bar[s], pol);
           }
         } else {
           sm.meta[s] = m;
@@ -971,9 +1090,13 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
           (void)mbar_wait_bounded(&full_bar[s], (uint32_t)((phases[s] - 1) & 1), &no_abort, a.status, a.wait_ns);
     }
     __syncwarp();
-    if (ng < 0) {  // no routed ticket was drawn by this CTA: phase C still needs the group table
-      route_cta<ROWS>(a, sm, cnt);
+    // phase C needs the group table even where no routed ticket was drawn
+    (void)score_poll<ROWS>(a, sm, cnt, sp, true);
+    if (sp.in_flight && lane == 0) {  // after a timeout: the copy lands before the CTA may leave
+      int no_abort = 0;
+      (void)mbar_wait_bounded(&score_bar, sp.phase, &no_abort, a.status, a.wait_ns);
     }
+    __syncwarp();
   } else if (warp == kPublisherWarp) {
     // ================= publisher =================
     if (role < a.nm) {  // a mix CTA: the last one's publisher forms the comb
@@ -1014,6 +1137,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
       const uint64_t t0 = global_timer_ns();
       bool flushed = false;
       while (true) {
+        __nanosleep(kBackoffNs);
         if (lane == 0) ready = mbar_try_wait(bar, parity) ? 1 : 0;
         if (__shfl_sync(0xffffffffu, ready, 0)) return true;
         const uint64_t el = global_timer_ns() - t0;
@@ -1039,7 +1163,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
       if (m.kind == kKindEnd) break;
       if (!idle_wait(&red_bar[s], par)) break;
       const float *rb = red + (size_t)s * kWorkerWarps * RG::kRed;
-      const int nv = m.kind == kKindA ? 2 * ROWS : kRowsB * ROWS;
+      const int nv = m.kind == kKindA ? 2 * RG::kRowsA * ROWS : RG::kRowsB * ROWS;
       float tot = 0.f;
       if (lane < nv) {
 #pragma unroll
@@ -1049,18 +1173,20 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
       if (lane == 0) mbar_arrive(&empty_bar[s]);  // the slot is free for the producer
       int key, n;
       if (m.kind == kKindA) {
-        const float u = __shfl_sync(0xffffffffu, tot, (lane + ROWS) & 31);
-        if (lane < rows && ((m.mask >> lane) & 1))
-          a.act[((size_t)m.g * kDecodeRows + lane) * I + m.row] = tot * sigmoidf_(tot) * u;
+        // item (ii * ROWS + r) is gate row m.row + ii of batch row r; RG::kRowsA * ROWS later, its up row
+        const float u = __shfl_sync(0xffffffffu, tot, (lane + RG::kRowsA * ROWS) & 31);
+        const int ii = lane / ROWS, r = lane - ii * ROWS;
+        if (lane < RG::kRowsA * ROWS && ((m.mask >> r) & 1))
+          a.act[((size_t)m.g * kDecodeRows + r) * I + m.row + ii] = tot * sigmoidf_(tot) * u;
         key = m.g;
-        n = 1;
+        n = RG::kRowsA;
       } else {
-        if (lane < kRowsB * ROWS) {  // zeros for rows this group does not serve
+        if (lane < RG::kRowsB * ROWS) {  // zeros for rows this group does not serve
           const int q = lane / ROWS, r = lane - q * ROWS;
           a.y[((size_t)m.g * kDecodeRows + r) * D + m.row + q] = ((m.mask >> r) & 1) ? tot : 0.f;
         }
         key = 1024 + m.row / kDecodeDBlock;
-        n = kRowsB;
+        n = RG::kRowsB;
       }
       int i = 0;
       while (i < nkeys && keys[i] != key) ++i;
@@ -1087,9 +1213,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
     form_x<ROWS, MX>(a, sm, cnt, xr);
     if (router) router_logits<ROWS, MX>(a, sm, cnt, role - a.nm, xr);
     pdl_wait();  // the state (read by phase C) comes from the previous kernel
-    constexpr int VA = pow2_at_least(2 * ROWS), VB = pow2_at_least(kRowsB * ROWS);
+    constexpr int VA = pow2_at_least(2 * RG::kRowsA * ROWS), VB = pow2_at_least(RG::kRowsB * ROWS);
     static_assert(VB <= RG::kRed && VA <= RG::kRed, "partial sums per warp and slot");
-    const int span = MX ? (((D / 32 + 32) + 15) & ~15) : 0;
+    const int span = MX ? (((RG::kRowsA * D / 32 + 32) + 15) & ~15) : 0;
     // A CTA draws all of its kind-A tickets before its first kind-B one, so the slots come as a run
     // of kind A, then a run of kind B: two loops, so that x and the SwiGLU slice are never held in
     // registers at the same time
@@ -1109,22 +1235,25 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
       }
       const uint8_t *src = ring + (size_t)s * RG::kSlotBytes;
       float *rp = red + ((size_t)s * kWorkerWarps + warp) * RG::kRed;
-        float pv[VA];
+      float pv[VA];
 #pragma unroll
-        for (int i = 0; i < VA; ++i) pv[i] = 0.f;
+      for (int i = 0; i < VA; ++i) pv[i] = 0.f;
+      // item (ii * ROWS + r): gate row m.row + ii, batch row r; RG::kRowsA * ROWS later, its up row
+#pragma unroll
+      for (int ii = 0; ii < RG::kRowsA; ++ii) {
         if constexpr (MX) {
           if (16 * tid < D) {
-            const uint4 gq = lds128(src + 16 * tid), uq = lds128(src + D + 16 * tid);
-            const float sg = e8m0_value(src[2 * D + m.s0 + tid / 2]);
-            const float su = e8m0_value(src[2 * D + span + m.s1 + tid / 2]);
+            const uint4 gq = lds128(src + ii * D + 16 * tid), uq = lds128(src + (RG::kRowsA + ii) * D + 16 * tid);
+            const float sg = e8m0_value(src[2 * RG::kRowsA * D + m.s0 + ii * (D / 32) + tid / 2]);
+            const float su = e8m0_value(src[2 * RG::kRowsA * D + span + m.s1 + ii * (D / 32) + tid / 2]);
             float fg[16], fu[16];
             e4m3x16_to_float_scaled(gq, fg);
             e4m3x16_to_float_scaled(uq, fu);
 #pragma unroll
             for (int r = 0; r < rows; ++r) {
               if ((m.mask >> r) & 1) {
-                pv[r] = sg * (dot16(fg, xr[r][0], xr[r][1], xr[r][2], xr[r][3]) * kE4m3Unscale);
-                pv[ROWS + r] = su * (dot16(fu, xr[r][0], xr[r][1], xr[r][2], xr[r][3]) * kE4m3Unscale);
+                pv[ii * ROWS + r] = sg * (dot16(fg, xr[r][0], xr[r][1], xr[r][2], xr[r][3]) * kE4m3Unscale);
+                pv[(RG::kRowsA + ii) * ROWS + r] = su * (dot16(fu, xr[r][0], xr[r][1], xr[r][2], xr[r][3]) * kE4m3Unscale);
               }
             }
           }
@@ -1133,19 +1262,20 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
           for (int h = 0; h < 2; ++h) {
             const int c = 8 * tid + 2048 * h;
             if (c < D) {
-              const uint4 gv = lds128(src + 2 * c), uv = lds128(src + 2 * D + 2 * c);
+              const uint4 gv = lds128(src + 2 * (ii * D + c)), uv = lds128(src + 2 * ((RG::kRowsA + ii) * D + c));
 #pragma unroll
               for (int r = 0; r < rows; ++r) {
                 if ((m.mask >> r) & 1) {
-                  pv[r] += dot8(gv, xr[r][2 * h], xr[r][2 * h + 1]);
-                  pv[ROWS + r] += dot8(uv, xr[r][2 * h], xr[r][2 * h + 1]);
+                  pv[ii * ROWS + r] += dot8(gv, xr[r][2 * h], xr[r][2 * h + 1]);
+                  pv[(RG::kRowsA + ii) * ROWS + r] += dot8(uv, xr[r][2 * h], xr[r][2 * h + 1]);
                 }
               }
             }
           }
         }
-        const float wt = warp_reduce_scatter<VA>(pv);
-        if (lane < VA) rp[lane] = wt;
+      }
+      const float wt = warp_reduce_scatter<VA>(pv);
+      if (lane < VA) rp[lane] = wt;
       __syncwarp();
       if (lane == 0) mbar_arrive(&red_bar[s]);  // after this warp's reads of the slot and its partial sums
     }
@@ -1161,43 +1291,43 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
       if (m.kind != kKindB) break;
       const uint8_t *src = ring + (size_t)s * RG::kSlotBytes;
       float *rp = red + ((size_t)s * kWorkerWarps + warp) * RG::kRed;
-        if (m.g != cur_g) {  // the group's SwiGLU output, once its every gate/up row is published
-          cur_g = m.g;
-          act_ok = wait_at_least(&group_done[m.g], (unsigned)perg, a);
+      if (m.g != cur_g) {  // the group's SwiGLU output, once its every gate/up row is published
+        cur_g = m.g;
+        act_ok = wait_at_least(&group_done[m.g], (unsigned)I, a);
+#pragma unroll
+        for (int r = 0; r < rows; ++r) {
+          const bool in = act_ok && 8 * tid < I && ((m.mask >> r) & 1);
+          const float4 *ap = reinterpret_cast<const float4 *>(a.act + ((size_t)m.g * kDecodeRows + r) * I + 8 * tid);
+          ar[r][0] = in ? __ldcg(ap) : make_float4(0.f, 0.f, 0.f, 0.f);
+          ar[r][1] = in ? __ldcg(ap + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      float pv[VB];
+#pragma unroll
+      for (int i = 0; i < VB; ++i) pv[i] = 0.f;
+      if (8 * tid < I) {
+#pragma unroll
+        for (int q = 0; q < RG::kRowsB; ++q) {
+          float f[8];
+          float sc = 1.f;
+          uint4 wv = make_uint4(0u, 0u, 0u, 0u);
+          if constexpr (MX) {
+            e4m3x8_to_float_scaled(lds64(src + (size_t)q * I + 8 * tid), f);
+            sc = e8m0_value(src[RG::kRowsB * I + q * (I / 32) + tid / 4]);
+          } else {
+            wv = lds128(src + (size_t)q * I * 2 + 16 * tid);
+          }
 #pragma unroll
           for (int r = 0; r < rows; ++r) {
-            const bool in = act_ok && 8 * tid < I && ((m.mask >> r) & 1);
-            const float4 *ap = reinterpret_cast<const float4 *>(a.act + ((size_t)m.g * kDecodeRows + r) * I + 8 * tid);
-            ar[r][0] = in ? __ldcg(ap) : make_float4(0.f, 0.f, 0.f, 0.f);
-            ar[r][1] = in ? __ldcg(ap + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
-        float pv[VB];
-#pragma unroll
-        for (int i = 0; i < VB; ++i) pv[i] = 0.f;
-        if (8 * tid < I) {
-#pragma unroll
-          for (int q = 0; q < kRowsB; ++q) {
-            float f[8];
-            float sc = 1.f;
-            uint4 wv = make_uint4(0u, 0u, 0u, 0u);
-            if constexpr (MX) {
-              e4m3x8_to_float_scaled(lds64(src + (size_t)q * I + 8 * tid), f);
-              sc = e8m0_value(src[kRowsB * I + q * (I / 32) + tid / 4]);
-            } else {
-              wv = lds128(src + (size_t)q * I * 2 + 16 * tid);
-            }
-#pragma unroll
-            for (int r = 0; r < rows; ++r) {
-              if ((m.mask >> r) & 1) {
-                if constexpr (MX) pv[q * ROWS + r] = sc * (dot8f(f, ar[r][0], ar[r][1]) * kE4m3Unscale);
-                else pv[q * ROWS + r] = dot8(wv, ar[r][0], ar[r][1]);
-              }
+            if ((m.mask >> r) & 1) {
+              if constexpr (MX) pv[q * ROWS + r] = sc * (dot8f(f, ar[r][0], ar[r][1]) * kE4m3Unscale);
+              else pv[q * ROWS + r] = dot8(wv, ar[r][0], ar[r][1]);
             }
           }
         }
-        const float wt = warp_reduce_scatter<VB>(pv);
-        if (lane < VB) rp[lane] = wt;
+      }
+      const float wt = warp_reduce_scatter<VB>(pv);
+      if (lane < VB) rp[lane] = wt;
       __syncwarp();
       if (lane == 0) mbar_arrive(&red_bar[s]);
     }
@@ -1250,8 +1380,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
     __threadfence();
     for (int i = tid; i < a.n_counters; i += blockDim.x) cnt[i] = 0u;
     // every row's entries, whatever the next launch's row count
-    for (int i = tid; i < kDecodeRows * E; i += blockDim.x)
-      a.sel[i] = make_float2(__uint_as_float(kUnwritten), __uint_as_float(kUnwritten));
+    for (int i = tid; i < kDecodeRows * E; i += blockDim.x) a.sel[i] = __uint_as_float(kUnwritten);
     // performed before this CTA retires: a decode launch that follows directly (programmatic
     // dependent launch) starts only after every CTA of this one has left
     __threadfence();
@@ -1341,7 +1470,7 @@ void launch_decode(const Dims &d, const Scratch &s, const LayerDev &w, const flo
   a.post = s.post;
   a.comb = s.comb;
   a.x = s.ffn_norm;
-  a.sel = reinterpret_cast<float2 *>(s.dec_part);
+  a.sel = s.dec_part;
   a.logits = s.logits;
   a.act = s.act_dec;
   a.y = s.y_dec;

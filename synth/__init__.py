@@ -196,6 +196,7 @@ CONFIGS = {
 # Smaller variants for profiler captures (a few GB on the device): full hidden/inter, 32 experts.
 PROFILE_CONFIGS = {
     "p_decode_b1_e32": MoeConfig("p_decode_b1_e32", rows=1, experts=32, seed=21),
+    "p_decode_b4_e32": MoeConfig("p_decode_b4_e32", rows=4, experts=32, layer=0, seed=22),
     "p_prefill_512_e32": MoeConfig("p_prefill_512_e32", rows=512, experts=32, seed=23),
     # full router and HC shapes (256 experts, hidden 4096) with inter 128: 0.8 GB of expert weights
     "p_decode_b1_i128": MoeConfig("p_decode_b1_i128", rows=1, inter=128, shared_inter=128, seed=25),
