@@ -138,7 +138,8 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int *__restrict__ id
 }
 
 void launch_dispatch(const Dims &d, const Scratch &s, int rows, cudaStream_t st, StageTimer *tm) {
-  build_tiles_kernel<<<1, 1024, 0, st>>>(s.counts, d.experts, rows, d.inter / 128, d.hidden / 128, s.offsets,
+  // down tiles cover two 128-row blocks of hidden each
+  build_tiles_kernel<<<1, 1024, 0, st>>>(s.counts, d.experts, rows, d.inter / 128, (d.hidden + 255) / 256, s.offsets,
                                          s.cursor, s.tiles_gu, s.tiles_dn, s.n_tiles);
   stage(tm, "build_tiles", st);
   const int warps = rows * (d.top_k + 1);

@@ -17,7 +17,9 @@
 //
 // Layout ("swap AB"): the expert's weight rows are the MMA's M = 128 side (operand A), the
 // expert's tokens the N side (operand B, N = 16..128 by tile), K = hidden (gate/up) or inter
-// (down), 64 per pipeline stage.  So a weight tile is read from HBM once per 128 tokens of its
+// (down), 64 per pipeline stage.  Every tile holds two A operands against the same B: the gate and
+// the up rows of one 128-row block (gate/up), or two adjacent 128-row blocks of the down matrix
+// (down), so each stage carries 32 KB of weights and three stages keep 96 KB of them in flight.  So a weight tile is read from HBM once per 128 tokens of its
 // expert however few tokens that is, and the B planes are loaded with a box of the tile's own
 // N rows (one tensor map per multiple of 16), not 128.  The shared expert is group `experts` (every row), so one
 // persistent launch covers routed and shared work.
@@ -51,17 +53,17 @@ constexpr int kTileBytes = BM * BK * 2;  // 16 KB: one 128 x 64 bf16 tile (A and
 
 template <bool GATEUP>
 struct GemmCfg {
-  static constexpr int kStages = GATEUP ? 3 : 4;
-  static constexpr int kATiles = GATEUP ? 2 : 1;
+  static constexpr int kStages = 3;
+  static constexpr int kATiles = 2;
   static constexpr int kStageBytes = (kATiles + 2) * kTileBytes;  // A tiles, then B hi and B lo
-  static constexpr int kAccCols = GATEUP ? 2 * BN : BN;  // gate and up accumulators side by side
+  static constexpr int kAccCols = 2 * BN;                // the two A operands' accumulators side by side
   static constexpr int kTmemCols = 2 * kAccCols;         // two accumulator buffers
   static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 1024;
   static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
 };
 
 struct GemmArgs {
-  const int4 *tiles;   // (group, m-block, n-block, valid tokens)
+  const int4 *tiles;   // (group, m-block, n-block, valid tokens); a down m-block is 256 rows
   const int *n_tiles;  // [0] gate/up, [1] down
   const int *offsets;  // first list position of each group
   const int2 *list;    // (row, slot) per position
@@ -106,10 +108,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fence_mbar_init();
     tmap_prefetch(&tmA0);
     tmap_prefetch(&tmS0);
-    if (GATEUP) {
-      tmap_prefetch(&tmA1);
-      tmap_prefetch(&tmS1);
-    }
+    tmap_prefetch(&tmA1);
+    tmap_prefetch(&tmS1);
     for (int i = 0; i < BN / 16; ++i) tmap_prefetch(&tmB[i]);
   }
   if (warp == 1) tmem_alloc(&tmem_base, C::kTmemCols);
@@ -130,7 +130,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const bool shared = tl.x == a.experts;  // the shared expert's matrices are separate tensors
       const CUtensorMap *m0 = shared ? &tmS0 : &tmA0;
       const CUtensorMap *m1 = shared ? &tmS1 : &tmA1;
-      const int a_row = (shared ? 0 : tl.x * a.a_rows_per_group) + tl.y * BM;
+      // gate/up: the gate and up rows of block tl.y; down: blocks 2 tl.y and 2 tl.y + 1 (rows past
+      // the matrix read as zeros, or as the next expert's rows, whose products are not stored)
+      const int a_row = (shared ? 0 : tl.x * a.a_rows_per_group) + tl.y * (GATEUP ? BM : 2 * BM);
       const int b_row = a.offsets[tl.x] + tl.z * BN;
       const int nb = (tl.w + 15) >> 4;  // B box: the tile's tokens in whole 16-row groups
       const CUtensorMap *mb = &tmB[nb - 1];
@@ -140,7 +142,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         mbar_arrive_expect_tx(&full_bar[stage], bytes);
         uint8_t *base = smem + (size_t)stage * C::kStageBytes;
         tma_load_2d(base, m0, &full_bar[stage], kb * BK, a_row);
-        if (GATEUP) tma_load_2d(base + kTileBytes, m1, &full_bar[stage], kb * BK, a_row);
+        tma_load_2d(base + kTileBytes, m1, &full_bar[stage], kb * BK, GATEUP ? a_row : a_row + BM);
         uint8_t *bp = base + C::kATiles * kTileBytes;
         tma_load_2d(bp, mb, &full_bar[stage], kb * BK, b_row);
         tma_load_2d(bp + kTileBytes, mb, &full_bar[stage], kb * BK, a.plane_rows + b_row);
@@ -189,13 +191,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint64_t bhi = smem_desc_sw128(sb + k * UMMA_K * 2);
           const uint64_t blo = smem_desc_sw128(sb + kTileBytes + k * UMMA_K * 2);
           const uint64_t a0 = smem_desc_sw128(sa + k * UMMA_K * 2);
+          const uint64_t a1 = smem_desc_sw128(sa + kTileBytes + k * UMMA_K * 2);
           tc_mma_f16(d0, a0, bhi, idesc, accum);
           tc_mma_f16(d0, a0, blo, idesc, 1u);
-          if (GATEUP) {
-            const uint64_t a1 = smem_desc_sw128(sa + kTileBytes + k * UMMA_K * 2);
-            tc_mma_f16(d0 + BN, a1, bhi, idesc, accum);
-            tc_mma_f16(d0 + BN, a1, blo, idesc, 1u);
-          }
+          tc_mma_f16(d0 + BN, a1, bhi, idesc, accum);
+          tc_mma_f16(d0 + BN, a1, blo, idesc, 1u);
         }
         tc_commit(&empty_bar[stage]);
         if (++stage == C::kStages) {
@@ -230,7 +230,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const int pos0 = a.offsets[tl.x] + tl.z * BN;
       const int n_valid = tl.w;
-      const int m = tl.y * BM + row;  // this lane's weight row: a column of inter (gate/up) or hidden (down)
+      // this lane's weight row: a column of inter (gate/up), or of hidden (down: m and m + 128)
+      const int m = tl.y * (GATEUP ? BM : 2 * BM) + row;
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
       for (int c0 = half * 16; c0 < n_valid; c0 += 32) {
         if (GATEUP) {
@@ -252,16 +253,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
           }
         } else {
-          float yv[16];
+          float yv[16], yv1[16];
           tmem_ld16(tbase + c0, yv);
+          tmem_ld16(tbase + BN + c0, yv1);
+          const bool second = m + BM < a.hidden;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             if (c0 + j < n_valid) {
               const int p = pos0 + c0 + j;
               const int2 rk = a.list[p];
-              const float v = yv[j] * a.list_w[p];
-              nonfinite |= !isfinite(v);
-              red_add_f64(a.ffn_acc + (size_t)rk.x * a.hidden + m, (double)v);
+              const float w = a.list_w[p];
+              const float v = yv[j] * w, v1 = yv1[j] * w;
+              nonfinite |= !isfinite(v) || (second && !isfinite(v1));
+              double *dst = a.ffn_acc + (size_t)rk.x * a.hidden + m;
+              red_add_f64(dst, (double)v);
+              if (second) red_add_f64(dst + BM, (double)v1);
             }
           }
         }

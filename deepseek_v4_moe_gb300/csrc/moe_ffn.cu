@@ -247,7 +247,7 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
   s.max_positions = (int)(R * K + R);
   const size_t P = prefill ? s.max_positions : 0;
   s.max_tiles_gu = (int)((P / 128 + E + 1) * (I / 128));
-  s.max_tiles_dn = (int)((P / 128 + E + 1) * (D / 128));
+  s.max_tiles_dn = (int)((P / 128 + E + 1) * ((D + 255) / 256));
   if (ok && prefill)
     ok = dalloc(h, &s.counts, E) && dalloc(h, &s.offsets, E + 2) && dalloc(h, &s.cursor, E + 1) &&
          dalloc(h, &s.router_part, (size_t)moe::splitgemm_splits((int)D) * R * E) &&

@@ -201,6 +201,10 @@ PROFILE_CONFIGS = {
     # full router and HC shapes (256 experts, hidden 4096) with inter 128: 0.8 GB of expert weights
     "p_decode_b1_i128": MoeConfig("p_decode_b1_i128", rows=1, inter=128, shared_inter=128, seed=25),
     "p_prefill_4096_e32": MoeConfig("p_prefill_4096_e32", rows=4096, experts=32, seed=27),
+    # 512 rows over all 256 experts with the Zipf bias, inter 512: the small expert tiles of the
+    # 512-row prefill in 3.2 GB of expert weights
+    "p_prefill_512_i512": MoeConfig("p_prefill_512_i512", rows=512, inter=512, shared_inter=512, seed=3,
+                                    bias="zipf"),
 }
 ALL_CONFIGS = {**CONFIGS, **PROFILE_CONFIGS}
 
