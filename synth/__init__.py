@@ -205,6 +205,9 @@ PROFILE_CONFIGS = {
     # 512-row prefill in 3.2 GB of expert weights
     "p_prefill_512_i512": MoeConfig("p_prefill_512_i512", rows=512, inter=512, shared_inter=512, seed=3,
                                     bias="zipf"),
+    # 4096 rows with the 8 hot experts, inter 512: the 4096-row prefill's tiles in 3.2 GB of weights
+    "p_prefill_4096_i512": MoeConfig("p_prefill_4096_i512", rows=4096, inter=512, shared_inter=512, seed=4,
+                                     hot_experts=8),
 }
 ALL_CONFIGS = {**CONFIGS, **PROFILE_CONFIGS}
 
