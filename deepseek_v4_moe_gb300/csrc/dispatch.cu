@@ -39,18 +39,23 @@ __device__ int block_scan_incl(int v, int *tmp) {
 }
 
 // Groups 0..E-1 are the routed experts (counts from the router), group E the shared expert (every
-// row).  Exclusive scans give each group's first list position and first tile; the gate/up and down
-// tile lists are (group, weight block, token block, valid tokens), group-major then weight-block-major
-// so the token blocks of one weight tile run side by side.  Resets the counts for the next forward.
+// row).  Exclusive scans give each group's first list position.  The gate/up and down tile lists are
+// (group, weight block, token block, valid tokens) in two parts: first the tiles of the heavy groups
+// (more than one token block, so each weight tile is multiplied several times: MMA-bound), then those
+// of the light groups (one token block: bound by the weight bytes).  Within a part, group-major then
+// weight-block-major, so the token blocks of one weight tile run side by side.  The GEMMs take tiles
+// from both parts at once, which keeps the tensor pipes and DRAM busy together.  Resets the counts
+// for the next forward and the GEMMs' claim counters.
 __global__ void __launch_bounds__(1024) build_tiles_kernel(int *__restrict__ counts, int E, int rows, int mb_gu,
                                                            int mb_dn, int *__restrict__ offsets,
                                                            int *__restrict__ cursor, int4 *__restrict__ tiles_gu,
                                                            int4 *__restrict__ tiles_dn, int *__restrict__ n_tiles) {
-  __shared__ int cnt[kExpertsMax + 1], nb[kExpertsMax + 1], toff[kExpertsMax + 2];
-  __shared__ int tmp[32];
+  __shared__ int cnt[kExpertsMax + 1], nb[kExpertsMax + 1], toff[kExpertsMax + 2], poff[kExpertsMax + 1];
+  __shared__ int tmp[32], parts[2];
   const int G = E + 1, g = threadIdx.x;
   const int c = g < G ? (g < E ? counts[g] : rows) : 0;
   const int n = (c + 127) / 128;
+  const bool heavy = n >= 2;
   if (g < G) {
     cnt[g] = c;
     nb[g] = n;
@@ -59,18 +64,25 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(int *__restrict__ cou
   }
   const int off_incl = block_scan_incl(c, tmp);
   const int tb_incl = block_scan_incl(n, tmp);
+  const int hb_incl = block_scan_incl(heavy ? n : 0, tmp);  // token blocks of heavy groups
+  const int lb_incl = block_scan_incl(heavy ? 0 : n, tmp);  // and of light ones
   if (g < G) {
     offsets[g] = off_incl - c;
     toff[g] = tb_incl - n;
+    poff[g] = heavy ? hb_incl - n : lb_incl - n;  // first token block of the group within its part
   }
   if (g == G - 1) {
     offsets[G] = off_incl;
     toff[G] = tb_incl;
+    parts[0] = hb_incl;  // heavy token blocks
     n_tiles[0] = tb_incl * mb_gu;
     n_tiles[1] = tb_incl * mb_dn;
+    n_tiles[2] = hb_incl * mb_gu;
+    n_tiles[3] = hb_incl * mb_dn;
+    for (int i = 4; i < 8; ++i) n_tiles[i] = 0;
   }
   __syncthreads();
-  const int total_b = toff[G];
+  const int total_b = toff[G], heavy_b = parts[0];
   // every (group, token block) pair, found by binary search over the group tile offsets
   for (int t = threadIdx.x; t < total_b * (mb_gu > mb_dn ? mb_gu : mb_dn); t += blockDim.x) {
     const int mb_max = mb_gu > mb_dn ? mb_gu : mb_dn;
@@ -82,9 +94,10 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(int *__restrict__ cou
       else hi = mid - 1;
     }
     const int gg = lo, b = bt - toff[gg], nbg = nb[gg];
+    const int base = nbg >= 2 ? poff[gg] : heavy_b + poff[gg];  // the group's first block in the list
     const int4 tile = make_int4(gg, m, b, min(128, cnt[gg] - b * 128));
-    if (m < mb_gu) tiles_gu[toff[gg] * mb_gu + m * nbg + b] = tile;
-    if (m < mb_dn) tiles_dn[toff[gg] * mb_dn + m * nbg + b] = tile;
+    if (m < mb_gu) tiles_gu[base * mb_gu + m * nbg + b] = tile;
+    if (m < mb_dn) tiles_dn[base * mb_dn + m * nbg + b] = tile;
   }
 }
 

@@ -19,7 +19,13 @@
 // expert's tokens the N side (operand B, N = 16..128 by tile), K = hidden (gate/up) or inter
 // (down), 64 per pipeline stage.  Every tile holds two A operands against the same B: the gate and
 // the up rows of one 128-row block (gate/up), or two adjacent 128-row blocks of the down matrix
-// (down), so each stage carries 32 KB of weights and three stages keep 96 KB of them in flight.  So a weight tile is read from HBM once per 128 tokens of its
+// (down).
+//
+// Pipeline: the weights (A, from DRAM) and the activation planes (B, mostly from L2) sit in two
+// rings of 32 KB slots, four for A and three for B.  Step j (one 64-wide k-block of some tile) uses
+// A slot j % 4 and B slot j % 3 and completes on full barrier j % 4, which takes two arrivals: the
+// A copies of step j are issued one step before its B copies, so three weight slots (96 KB) are in
+// flight while the MMAs read the fourth, with the B planes of a 128-token tile still fitting.  So a weight tile is read from HBM once per 128 tokens of its
 // expert however few tokens that is, and the B planes are loaded with a box of the tile's own
 // N rows (one tensor map per multiple of 16), not 128.  The shared expert is group `experts` (every row), so one
 // persistent launch covers routed and shared work.
@@ -31,7 +37,14 @@
 // exact there.
 //
 // Roles per CTA (320 threads, one CTA per SM, persistent over a device-built tile list):
-//   warp 0     TMA producer: A (gate and up, or down) and the two B planes into a multi-stage ring
+//   warp 0     TMA producer: claims tiles (one claim ahead), hands each tile number to the other
+//              roles through a small shared-memory queue, and loads A (gate and up, or down) and
+//              the two B planes into the rings.  The list has a heavy part (groups of several token
+//              blocks: MMA-bound, their weight tiles mostly from L2) and a light part (one token
+//              block: bound by the weight bytes).  Even CTAs claim from the heavy part first, odd
+//              ones from the light part, each turning to the other part when its own runs out,
+//              so the tensor pipes and DRAM are busy together; a device-wide counter per part
+//              keeps every SM loaded whatever each tile costs
 //   warp 1     TMEM allocator and MMA issuer (one thread), commits free smem stages / TMEM
 //   warps 2-9  epilogue: tcgen05.ld of the accumulator (double buffered in TMEM, so the next
 //              tile's MMAs run under this tile's epilogue); SwiGLU and the hi/lo split of its
@@ -53,18 +66,19 @@ constexpr int kTileBytes = BM * BK * 2;  // 16 KB: one 128 x 64 bf16 tile (A and
 
 template <bool GATEUP>
 struct GemmCfg {
-  static constexpr int kStages = 3;
-  static constexpr int kATiles = 2;
-  static constexpr int kStageBytes = (kATiles + 2) * kTileBytes;  // A tiles, then B hi and B lo
+  static constexpr int kSA = 4, kSB = 3;           // A (weight) and B (activation) ring slots
+  static constexpr int kLag = kSA - kSB;           // steps by which a step's B copies follow its A copies
+  static constexpr int kSlotBytes = 2 * kTileBytes;  // A: the two weight tiles; B: the hi and lo planes
   static constexpr int kAccCols = 2 * BN;                // the two A operands' accumulators side by side
   static constexpr int kTmemCols = 2 * kAccCols;         // two accumulator buffers
-  static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 1024;
+  static constexpr size_t kSmem = (size_t)(kSA + kSB) * kSlotBytes + 1024;
   static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
 };
 
 struct GemmArgs {
   const int4 *tiles;   // (group, m-block, n-block, valid tokens); a down m-block is 256 rows
   const int *n_tiles;  // [0] gate/up, [1] down
+  int *tile_ctr;       // [2 which], [2 which + 1]: heavy and light tile claim counters, zero on entry
   const int *offsets;  // first list position of each group
   const int2 *list;    // (row, slot) per position
   const float *list_w;
@@ -77,6 +91,7 @@ struct GemmArgs {
 };
 
 constexpr int kEpiWarps = 8, kGemmThreads = 32 * (2 + kEpiWarps);
+constexpr int kTQ = 4;  // tile queue entries (the producer runs at most about two tiles ahead)
 
 template <bool GATEUP>
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -86,24 +101,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   using C = GemmCfg<GATEUP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full_bar[C::kStages], empty_bar[C::kStages], tfull_bar[2], tempty_bar[2];
-  __shared__ __align__(8) uint64_t mma_done_bar, never_bar;
+  __shared__ __align__(8) uint64_t full_bar[C::kSA], emptyA_bar[C::kSA], emptyB_bar[C::kSB], tfull_bar[2], tempty_bar[2];
+  __shared__ __align__(8) uint64_t mma_done_bar, never_bar, tq_full[kTQ], tq_empty[kTQ];
+  __shared__ int tq[kTQ];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   const uint64_t kWaitLimitNs = a.wait_ns;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+    for (int s = 0; s < C::kSA; ++s) {
+      mbar_init(&full_bar[s], 2);  // the A copies' arrival and the B copies' arrival
+      mbar_init(&emptyA_bar[s], 1);
     }
+    for (int s = 0; s < C::kSB; ++s) mbar_init(&emptyB_bar[s], 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull_bar[b], 1);
       mbar_init(&tempty_bar[b], kEpiWarps);
     }
     mbar_init(&mma_done_bar, 1);
     mbar_init(&never_bar, 1);
+    for (int i = 0; i < kTQ; ++i) {
+      mbar_init(&tq_full[i], 1);              // the producer has written the entry
+      mbar_init(&tq_empty[i], 1 + kEpiWarps);  // the MMA issuer and every epilogue warp have read it
+    }
     abort_flag = 0;
     fence_mbar_init();
     tmap_prefetch(&tmA0);
@@ -122,10 +143,58 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
-    int stage = 0;
-    uint32_t phase = 0;
-    int issued = 0;  // stages handed to TMA
-    for (int t = blockIdx.x; t < ntiles && !*abort_p; t += gridDim.x) {
+    uint8_t *ringA = smem, *ringB = smem + (size_t)C::kSA * C::kSlotBytes;
+    int j = 0;   // steps whose A copies are issued
+    int jb = 0;  // steps whose B copies are issued (jb <= j)
+    // the B side of the last kLag steps: (activation row, tensor map) of each
+    int hist_row[C::kLag > 0 ? C::kLag : 1];
+    const CUtensorMap *hist_map[C::kLag > 0 ? C::kLag : 1];
+    // B copies of step jb: wait until its slot is free, then both planes onto step jb's full barrier
+    auto issue_b = [&](int b_row, const CUtensorMap *mb, int kb) -> bool {
+      const int sb = jb % C::kSB;
+      if (!mbar_wait_bounded(&emptyB_bar[sb], (uint32_t)((jb / C::kSB) & 1) ^ 1u, abort_p, a.status, kWaitLimitNs))
+        return false;
+      const int nrows = (int)(mb - tmB) + 1;  // B box height in 16-row groups
+      uint64_t *fb = &full_bar[jb % C::kSA];
+      mbar_arrive_expect_tx(fb, 2u * (uint32_t)nrows * 16u * BK * 2u);
+      uint8_t *bp = ringB + (size_t)sb * C::kSlotBytes;
+      tma_load_2d(bp, mb, fb, kb * BK, b_row);
+      tma_load_2d(bp + kTileBytes, mb, fb, kb * BK, a.plane_rows + b_row);
+      ++jb;
+      return true;
+    };
+    int hist_kb[C::kLag > 0 ? C::kLag : 1];
+    bool ok = true;
+    const int n_heavy = a.n_tiles[2 + a.which];
+    int *ctr_h = a.tile_ctr + 2 * a.which, *ctr_l = ctr_h + 1;
+    bool heavy_done = false, light_done = false;
+    const bool heavy_first = (blockIdx.x & 1) == 0;
+    auto claim = [&]() -> int {  // the next tile, or ntiles once both parts are used up
+      for (int pass = 0; pass < 2; ++pass) {
+        const bool h = (pass == 0) == heavy_first;
+        if (h && !heavy_done) {
+          const int t = atomicAdd(ctr_h, 1);
+          if (t < n_heavy) return t;
+          heavy_done = true;
+        }
+        if (!h && !light_done) {
+          const int t = n_heavy + atomicAdd(ctr_l, 1);
+          if (t < ntiles) return t;
+          light_done = true;
+        }
+      }
+      return ntiles;
+    };
+    int next = claim();
+    for (int i = 0; ok && !*abort_p; ++i) {
+      // hand tile `next` (or the end mark, a number past the list) to the other roles
+      const int t = next;
+      const int q = i % kTQ;
+      if (!mbar_wait_bounded(&tq_empty[q], (uint32_t)((i / kTQ) & 1) ^ 1u, abort_p, a.status, kWaitLimitNs)) break;
+      tq[q] = t;
+      mbar_arrive(&tq_full[q]);
+      if (t >= ntiles) break;
+      next = claim();  // used at the next tile: its latency hides under this one
       const int4 tl = a.tiles[t];
       const bool shared = tl.x == a.experts;  // the shared expert's matrices are separate tensors
       const CUtensorMap *m0 = shared ? &tmS0 : &tmA0;
@@ -136,38 +205,66 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int b_row = a.offsets[tl.x] + tl.z * BN;
       const int nb = (tl.w + 15) >> 4;  // B box: the tile's tokens in whole 16-row groups
       const CUtensorMap *mb = &tmB[nb - 1];
-      const uint32_t bytes = C::kATiles * kTileBytes + 2u * (uint32_t)nb * 16u * BK * 2u;
       for (int kb = 0; kb < a.k_blocks; ++kb) {
-        if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_p, a.status, kWaitLimitNs)) break;
-        mbar_arrive_expect_tx(&full_bar[stage], bytes);
-        uint8_t *base = smem + (size_t)stage * C::kStageBytes;
-        tma_load_2d(base, m0, &full_bar[stage], kb * BK, a_row);
-        tma_load_2d(base + kTileBytes, m1, &full_bar[stage], kb * BK, GATEUP ? a_row : a_row + BM);
-        uint8_t *bp = base + C::kATiles * kTileBytes;
-        tma_load_2d(bp, mb, &full_bar[stage], kb * BK, b_row);
-        tma_load_2d(bp + kTileBytes, mb, &full_bar[stage], kb * BK, a.plane_rows + b_row);
-        ++issued;
-        if (++stage == C::kStages) {
-          stage = 0;
-          phase ^= 1u;
+        const int sa = j % C::kSA;
+        if (!mbar_wait_bounded(&emptyA_bar[sa], (uint32_t)((j / C::kSA) & 1) ^ 1u, abort_p, a.status, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        uint64_t *fb = &full_bar[sa];
+        mbar_arrive_expect_tx(fb, 2u * kTileBytes);
+        uint8_t *ap = ringA + (size_t)sa * C::kSlotBytes;
+        tma_load_2d(ap, m0, fb, kb * BK, a_row);
+        tma_load_2d(ap + kTileBytes, m1, fb, kb * BK, GATEUP ? a_row : a_row + BM);
+        if (C::kLag > 0) {
+          if (j >= C::kLag) {  // the B copies of step j - kLag
+            const int h = jb % C::kLag;
+            if (!issue_b(hist_row[h], hist_map[h], hist_kb[h])) {
+              ok = false;
+              ++j;
+              break;
+            }
+          }
+          hist_row[j % C::kLag] = b_row;
+          hist_map[j % C::kLag] = mb;
+          hist_kb[j % C::kLag] = kb;
+          ++j;
+        } else {
+          ++j;
+          if (!issue_b(b_row, mb, kb)) {
+            ok = false;
+            break;
+          }
         }
       }
     }
+    // the B copies of the last steps
+    while (ok && jb < j && !*abort_p) {
+      const int h = jb % C::kLag;
+      if (!issue_b(hist_row[h], hist_map[h], hist_kb[h])) break;
+    }
+    // after an abort: the B arrival of every step still missing one, so that each full barrier
+    // completes once its A copies have landed
+    for (; jb < j; ++jb) mbar_arrive(&full_bar[jb % C::kSA]);
     // copies still in flight after an abort land before the CTA may leave: wait (bounded) for the
-    // last phase asked of every stage (in a normal run each has completed long ago)
+    // last phase asked of every full barrier (in a normal run each has completed long ago)
     int no_abort = 0;
-    for (int s = 0; s < C::kStages; ++s) {
-      const int n = issued / C::kStages + (s < issued % C::kStages ? 1 : 0);
+    for (int s = 0; s < C::kSA; ++s) {
+      const int n = j / C::kSA + (s < j % C::kSA ? 1 : 0);
       if (n > 0) (void)mbar_wait_bounded(&full_bar[s], (uint32_t)((n - 1) & 1), &no_abort, a.status, kWaitLimitNs);
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
-    int stage = 0;
-    uint32_t phase = 0;
+    int j = 0;  // step
     int it = 0;
     if (GATEUP && a.inject == 2 && blockIdx.x == 0)  // test hook: a wait that runs out
       (void)mbar_wait_bounded(&never_bar, 0u, abort_p, a.status, kWaitLimitNs);
-    for (int t = blockIdx.x; t < ntiles && !*abort_p; t += gridDim.x, ++it) {
+    for (;; ++it) {
+      const int q = it % kTQ;
+      if (!mbar_wait_bounded(&tq_full[q], (uint32_t)((it / kTQ) & 1), abort_p, a.status, kWaitLimitNs)) break;
+      const int t = tq[q];
+      mbar_arrive(&tq_empty[q]);
+      if (t >= ntiles || *abort_p) break;
       const int4 tl = a.tiles[t];
       const int n_mma = (tl.w + 15) & ~15;
       const int acc = it & 1;
@@ -177,14 +274,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t idesc = idesc_bf16_f32(BM, n_mma);
       const uint32_t d0 = tmem + (uint32_t)(acc * C::kAccCols);
       bool ok = true;
-      for (int kb = 0; kb < a.k_blocks; ++kb) {
-        if (!mbar_wait_bounded(&full_bar[stage], phase, abort_p, a.status, kWaitLimitNs)) {
+      for (int kb = 0; kb < a.k_blocks; ++kb, ++j) {
+        const int slot_a = j % C::kSA, slot_b = j % C::kSB;
+        if (!mbar_wait_bounded(&full_bar[slot_a], (uint32_t)((j / C::kSA) & 1), abort_p, a.status, kWaitLimitNs)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t sa = smem_u32(smem + (size_t)stage * C::kStageBytes);
-        const uint32_t sb = sa + C::kATiles * kTileBytes;
+        const uint32_t sa = smem_u32(smem + (size_t)slot_a * C::kSlotBytes);
+        const uint32_t sb = smem_u32(smem + (size_t)(C::kSA + slot_b) * C::kSlotBytes);
 #pragma unroll
         for (int k = 0; k < BK / UMMA_K; ++k) {
           const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
@@ -197,11 +295,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_mma_f16(d0 + BN, a1, bhi, idesc, accum);
           tc_mma_f16(d0 + BN, a1, blo, idesc, 1u);
         }
-        tc_commit(&empty_bar[stage]);
-        if (++stage == C::kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        tc_commit(&emptyA_bar[slot_a]);  // both slots are free once these MMAs have read them
+        tc_commit(&emptyB_bar[slot_b]);
       }
       if (!ok) break;
       tc_commit(&tfull_bar[acc]);
@@ -217,7 +312,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int row = q * 32 + lane;
     bool nonfinite = false;
     int it = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+    for (;; ++it) {
+      // the next tile number from the queue (lane 0 reads it, the warp follows)
+      const int qe = it % kTQ;
+      int t = 0, got = 0;
+      if (lane == 0) {
+        got = mbar_wait_bounded(&tq_full[qe], (uint32_t)((it / kTQ) & 1), abort_p, a.status, kWaitLimitNs) ? 1 : 0;
+        if (got) {
+          t = tq[qe];
+          mbar_arrive(&tq_empty[qe]);
+        }
+      }
+      got = __shfl_sync(0xffffffffu, got, 0);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      if (!got || t >= ntiles) break;
       const int4 tl = a.tiles[t];
       const int acc = it & 1;
       const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
@@ -302,6 +410,7 @@ void launch_grouped_gemms(const Dims &d, const Scratch &s, const LayerDev &w, co
   GemmArgs a;
   a.tiles = s.tiles_gu;
   a.n_tiles = s.n_tiles;
+  a.tile_ctr = s.n_tiles + 4;
   a.offsets = s.offsets;
   a.list = s.list;
   a.list_w = s.list_w;

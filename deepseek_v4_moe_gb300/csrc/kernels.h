@@ -75,7 +75,8 @@ struct Scratch {
   int *offsets;           // [experts + 2]
   int *cursor;            // [experts + 1]
   int4 *tiles_gu, *tiles_dn;  // (group, m-block, n-block, valid columns)
-  int *n_tiles;           // [2]: gate/up tiles, down tiles
+  int *n_tiles;           // [8]: gate/up tiles, down tiles, the heavy ones of each (listed first),
+                          // then claim counters: gate/up heavy and light, down heavy and light
   int2 *list;             // [positions] (row, slot) in expert-sorted order; slot top_k = shared expert
   float *list_w;          // [positions] route weight of that slot (1 for the shared expert)
   uint16_t *x2;           // [2 * max_positions, hidden] bf16: ffn_norm rows in expert-sorted order,

@@ -252,7 +252,7 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
     ok = dalloc(h, &s.counts, E) && dalloc(h, &s.offsets, E + 2) && dalloc(h, &s.cursor, E + 1) &&
          dalloc(h, &s.router_part, (size_t)moe::splitgemm_splits((int)D) * R * E) &&
          dalloc(h, &s.tiles_gu, (size_t)s.max_tiles_gu) && dalloc(h, &s.tiles_dn, (size_t)s.max_tiles_dn) &&
-         dalloc(h, &s.n_tiles, 2) && dalloc(h, &s.list, P) && dalloc(h, &s.list_w, P) &&
+         dalloc(h, &s.n_tiles, 8) && dalloc(h, &s.list, P) && dalloc(h, &s.list_w, P) &&
          dalloc(h, &s.x2, 2 * P * D) && dalloc(h, &s.act2, 2 * P * I) && dalloc(h, &s.ffn_acc, R * D) &&
          dalloc(h, &s.mix_tc_part, (size_t)moe::mix_tc_part_floats((int)R, (int)hcd));
   if (!ok) {
