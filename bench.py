@@ -112,7 +112,7 @@ def kernel_work(name: str, wm: dict, cfg) -> tuple[float, float]:
 # every touched expert once, so a capture on the 32-expert profiling workload with the same
 # routing width (6 routed + shared) carries the same bytes as the full workload.  A kernel change
 # removes its entry until it is captured again.
-NCU_TRAFFIC = {("decode", 1, 7): 353_645_312 + 3_415_040}
+NCU_TRAFFIC = {}
 
 
 def roofline_entry(name: str, avg_ms: float, wm: dict, cfg, peaks: dict, peak_kind: str) -> dict:

@@ -20,7 +20,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_ffn.so")
-SOURCES = ["moe_ffn.cu", "prelude.cu", "decode.cu", "dispatch.cu", "gemm_tc.cu", "splitgemm.cu", "noalloc.cu"]
+SOURCES = ["moe_ffn.cu", "prelude.cu", "decode.cu", "decode_tc.cu", "dispatch.cu", "gemm_tc.cu", "splitgemm.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

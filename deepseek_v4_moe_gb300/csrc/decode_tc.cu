@@ -1,0 +1,647 @@
+// Decode path (rows <= 4) on the tensor cores, for bf16 experts: the whole FFN block in one
+// persistent launch, one CTA per SM.
+//
+// docs.rs "hf2q 0.1.3 .../deepseek4/ffn_forward.rs", forward_ffn_rows, every stage in order, as in
+// decode.cu: the prelude (mix CTAs, x in every CTA, router CTAs, routing by every producer) is the
+// same code.  What differs is the expert stream: instead of CUDA-core dot products, the weight
+// tiles go by TMA into a shared-memory ring and tcgen05.mma multiplies them, in TMEM, against the
+// batch rows held in shared memory as bf16 hi and lo planes (x = hi + lo with |x - hi - lo| <=
+// 2^-16 |x|, the same split as the rows > 4 path).
+//
+// Layout of one MMA ("swap AB"): A = 128 weight rows x 64 k (a 16 KB tile, 128-byte swizzled, as
+// TMA leaves it); B = 16 rows x 64 k: rows 0-3 the hi planes of batch rows 0-3, rows 4-7 their lo
+// planes (rows 8-15 are never read back); D = 128 x 16 f32 in TMEM, column r + column 4 + r being
+// the dot of weight row i with batch row r.
+//
+// Work units, claimed from per-split queues so that every CTA keeps its own K range:
+//   kind A  (group g, 128-row block of inter, K split s of hidden): the gate and the up tiles of
+//           each 64-wide k-step (32 KB a step) against the CTA's slice of x, which its worker
+//           threads wrote into shared memory once x was formed.  The partial dots are added in
+//           f64 at the L2 (red.add.f64: the sum of the few f32 partials is exact, so it does not
+//           depend on their order); the last of the splits of a (g, block, lane quarter) forms
+//           SwiGLU, stores act as bf16 hi/lo planes, and publishes the group's progress.
+//   kind B  (group g, two 128-row blocks of hidden, K split s of inter): two down tiles a step
+//           against the group's act planes, loaded by TMA once the group's act is complete.  The
+//           epilogue scales each batch row by its route weight and adds it in f64 into the FFN
+//           output; each 32-row block of hidden counts the units that have landed.
+// Every CTA draws all of its kind A units before its first kind B unit, and a kind B unit waits only
+// for kind A work, which running CTAs hold: every wait ends.
+//
+// Roles: warps 0-7 run the prelude; then warps 0-3 are the epilogue (one TMEM lane quarter each);
+// warp 8 is the producer (routing, unit claims, TMA), warp 9 the MMA issuer and TMEM owner.  Phase C
+// (per 32-wide block of hidden: ffn_out and hc_post) is shared by all warps at the end.  Waits are
+// bounded (1 s); after a timeout every later wait fails at once, the producer waits (bounded) for
+// its copies in flight and the MMA issuer for its MMAs, and TMEM is freed.  The last CTA out resets
+// the counters and the score table; the f64 accumulators are left zero by the roles that read them.
+#include "common.cuh"
+#include "decode_prelude.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace dtc {
+constexpr int kStages = 5;                 // A ring slots of 32 KB
+constexpr int kTile = 128 * 64 * 2;        // one A tile, 16 KB
+constexpr int kSlotBytes = 2 * kTile;      // gate + up tile, or two down tiles
+constexpr int kBTile = 16 * 64 * 2;        // one B tile (16 rows x 64 k), 2 KB
+constexpr int kMaxChunks = 8;              // 64-wide k-chunks of one unit
+constexpr int kBSlice = kMaxChunks * kBTile;  // 16 KB: x slice, or one act slice
+constexpr int kEpiWarps = 4;
+constexpr int kMmaWarp = 9;
+constexpr int kTQ = 4;                     // unit queue entries
+constexpr int kTmemCols = 64;              // two accumulator buffers of 32 columns
+constexpr size_t kSmem = (size_t)kStages * kSlotBytes + 3 * kBSlice + 1024;
+static_assert(kSmem <= 227 * 1024 - sizeof(DecSmem) - 512, "shared memory of one CTA");
+enum : int { kUnitA = 0, kUnitB = 1, kUnitEnd = 2 };
+}  // namespace dtc
+
+// Tensor maps of one launch (grid constants): the layer's expert matrices (boxes of 64 k x 128
+// rows) and the act planes (boxes of 64 k x 16 rows).
+struct DecodeTcMaps {
+  CUtensorMap gate, up, down, gate_sh, up_sh, down_sh, act2;
+};
+
+// Where the tensor-core kernel keeps its f64 partial sums and act planes, and how its K range is
+// split (host-computed).
+struct DecodeTcArgs {
+  double *acc_gu;   // [groups, 2, 4, inter]: gate and up partial sums (zero between launches)
+  double *acc_y;    // [4, hidden]: route-weighted FFN output (zero between launches)
+  uint16_t *act2;   // [groups, 16, inter] bf16: rows 0-3 the hi planes of act, rows 4-7 the lo planes
+  int sa, ca;       // kind A: K splits of hidden and 64-wide chunks per split
+  int sb, cb;       // kind B: K splits of inter and chunks per split
+  int cnt_tick_a, cnt_tick_b, cnt_units;  // counter slots: per-split tickets, SwiGLU unit counts
+  int n_acc_gu, n_acc_y;                  // element counts of the two accumulators
+};
+
+// Counter slots of the tensor-core kernel past the d-block counters: the kind A and kind B tickets
+// of each K split (a 128-byte line each, up to 64 splits), then the SwiGLU unit counts per (group,
+// 128-row block of inter, lane quarter).
+constexpr int kMaxSplits = 64;
+static int tc_counter_base(const Dims &d) { return kCntDBlocks + d.hidden / kDecodeDBlock; }
+int decode_tc_counter_count(const Dims &d) {
+  return tc_counter_base(d) + 2 * kMaxSplits * 32 + kDecodeGroupsMax * (d.inter / 128) * 4;
+}
+
+__device__ __forceinline__ void tma_load_2d_hint(void *smem_dst, const void *tmap, uint64_t *bar, int c_inner,
+                                                 int c_outer, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
+      "%4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(tmap), "r"(smem_u32(bar)), "r"(c_inner), "r"(c_outer), "l"(policy)
+      : "memory");
+}
+
+// Byte offset of element (row n, k) in a 16-row x 64-k bf16 tile with the 128-byte swizzle that TMA
+// writes and the MMA descriptors expect: 16-byte chunk k / 8 of row n lands at chunk (k / 8) ^ (n % 8).
+__device__ __forceinline__ uint32_t btile_offset(int n, int k) {
+  return (uint32_t)(n * 128 + ((((k >> 3) ^ (n & 7)) & 7) << 4) + (k & 7) * 2);
+}
+
+// hi = rn(x), lo = rn(x - hi) of 8 values, packed as bf16.
+__device__ __forceinline__ void split8(const float4 a, const float4 b, uint4 &hi, uint4 &lo) {
+  const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  float h[8], l[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    h[j] = round_bf16(v[j]);
+    l[j] = round_bf16(v[j] - h[j]);
+  }
+  hi = make_uint4(pack_bf16_pair(h[0], h[1]), pack_bf16_pair(h[2], h[3]), pack_bf16_pair(h[4], h[5]),
+                  pack_bf16_pair(h[6], h[7]));
+  lo = make_uint4(pack_bf16_pair(l[0], l[1]), pack_bf16_pair(l[2], l[3]), pack_bf16_pair(l[4], l[5]),
+                  pack_bf16_pair(l[6], l[7]));
+}
+
+__device__ __forceinline__ double ld_cg_f64(const double *p) {
+  double v;
+  asm volatile("ld.global.cg.f64 %0, [%1];" : "=d"(v) : "l"(p) : "memory");
+  return v;
+}
+
+template <int ROWS>
+__global__ void __launch_bounds__(kDecThreads, 1)
+    decode_tc_kernel(const __grid_constant__ DecodeTcMaps tm, DecodeArgs a, DecodeTcArgs t) {
+  using namespace dtc;
+  constexpr int rows = ROWS;
+  extern __shared__ uint8_t dsm_raw[];
+  uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *xs = ring + (size_t)kStages * kSlotBytes;  // this CTA's slice of x as B tiles
+  uint8_t *as = xs + kBSlice;                          // two act slices
+  __shared__ __align__(16) DecSmem sm;
+  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], tfull[2], tempty[2], afull[2], aempty[2];
+  __shared__ __align__(8) uint64_t xready, score_bar, tq_full[kTQ], tq_empty[kTQ], mma_done;
+  __shared__ int4 tq[kTQ];
+  __shared__ uint32_t tmem_base;
+  unsigned *cnt = a.counters;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int D = a.hidden, I = a.inter, E = a.experts;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], kEpiWarps);
+      mbar_init(&afull[b], 1);
+      mbar_init(&aempty[b], 1);
+    }
+    mbar_init(&xready, 1);
+    mbar_init(&score_bar, 1);
+    for (int q = 0; q < kTQ; ++q) {
+      mbar_init(&tq_full[q], 1);
+      mbar_init(&tq_empty[q], 1 + kEpiWarps);
+    }
+    mbar_init(&mma_done, 1);
+    sm.abort = 0;
+    sm.comb_todo = 0;
+    sm.flag = (int)atomicAdd(&cnt[kCntRole], 1u);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(&tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const int role = sm.flag;
+  const uint32_t tmem = tmem_base;
+  __syncthreads();
+
+  unsigned *group_done = cnt + kCntGroups;
+  unsigned *dblock_done = cnt + kCntDBlocks;
+  const int ka = (int)blockIdx.x % t.sa, kbs = (int)blockIdx.x % t.sb;  // this CTA's K splits
+  const int rba = I / 128, rbb = (D + 255) / 256;  // kind A row blocks, kind B row-block pairs
+
+  if (warp < kWorkerWarps) {
+    // ================= prelude (every worker warp), then the epilogue (warps 0-3) =================
+    const bool router = role >= a.nm && role < a.nm + a.nr;
+    if (router) router_prefetch(a, role - a.nm);
+    if (role < a.nm) mix_role<ROWS>(a, role, sm, cnt);
+    float4 xr[rows][4];
+    form_x<ROWS, false>(a, sm, cnt, xr);
+    if (router) router_logits<ROWS, false>(a, sm, cnt, role - a.nm, xr);
+    // this CTA's K slice of x as B tiles: batch row r's hi plane in tile row r, its lo plane in row 4 + r
+    const int k0 = ka * t.ca * 64, k1 = k0 + t.ca * 64;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int c = own_col<false>(tid, h);
+      if (c >= k0 && c < k1 && c < D) {
+        const int kk = c - k0;
+        uint8_t *tile = xs + (size_t)(kk >> 6) * kBTile;
+#pragma unroll
+        for (int r = 0; r < rows; ++r) {
+          uint4 hi, lo;
+          split8(xr[r][2 * h], xr[r][2 * h + 1], hi, lo);
+          *reinterpret_cast<uint4 *>(tile + btile_offset(r, kk & 63)) = hi;
+          *reinterpret_cast<uint4 *>(tile + btile_offset(4 + r, kk & 63)) = lo;
+        }
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the MMAs read them through the async proxy
+    workers_sync();
+    if (tid == 0) mbar_arrive(&xready);
+    if (warp < kEpiWarps) {
+      // ---------------- epilogue: TMEM lane quarter `warp` ----------------
+      bool nonfinite = false;
+      for (int u = 0;; ++u) {
+        const int q = u % kTQ;
+        int4 e = make_int4(kUnitEnd, 0, 0, 0);
+        int ok = 0;
+        if (lane == 0) {
+          ok = mbar_wait_bounded(&tq_full[q], (uint32_t)((u / kTQ) & 1), &sm.abort, a.status, a.wait_ns) ? 1 : 0;
+          if (ok) {
+            e = tq[q];
+            mbar_arrive(&tq_empty[q]);
+            ok = (e.x & 15) == kUnitEnd ||
+                 mbar_wait_bounded(&tfull[u & 1], (uint32_t)((u >> 1) & 1), &sm.abort, a.status, a.wait_ns);
+          }
+          if (!ok) atomicExch(&cnt[kCntAbort], 1u);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        const int kind = __shfl_sync(0xffffffffu, e.x, 0) & 15;
+        if (!ok || kind == kUnitEnd) break;
+        const int g = __shfl_sync(0xffffffffu, e.y, 0), blk = __shfl_sync(0xffffffffu, e.z, 0);
+        tc_fence_after();
+        float v0[16], v1[16];
+        const uint32_t tb = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)((u & 1) * 32);
+        tmem_ld16(tb, v0);
+        tmem_ld16(tb + 16, v1);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[u & 1]);  // the accumulator buffer is free for the next unit
+        if (kind == kUnitA) {
+          const int i = blk * 128 + warp * 32 + lane;  // this lane's row of inter
+          double *acc = t.acc_gu + (size_t)g * 2 * 4 * I + i;
+#pragma unroll
+          for (int r = 0; r < rows; ++r) {
+            red_add_f64(acc + (size_t)r * I, (double)(v0[r] + v0[4 + r]));            // gate
+            red_add_f64(acc + (size_t)(4 + r) * I, (double)(v1[r] + v1[4 + r]));      // up
+          }
+          __threadfence();
+          __syncwarp();
+          int last = 0;
+          if (lane == 0) last = atomicAdd(&cnt[t.cnt_units + (g * rba + blk) * 4 + warp], 1u) == (unsigned)(t.sa - 1);
+          if (__shfl_sync(0xffffffffu, last, 0)) {
+            // every split of this (group, block, quarter) is in: SwiGLU, as bf16 hi / lo planes
+            __threadfence();
+#pragma unroll
+            for (int r = 0; r < rows; ++r) {
+              const float gv = (float)ld_cg_f64(acc + (size_t)r * I), uv = (float)ld_cg_f64(acc + (size_t)(4 + r) * I);
+              acc[(size_t)r * I] = 0.0;  // zero again for the next launch
+              acc[(size_t)(4 + r) * I] = 0.0;
+              const float v = gv * sigmoidf_(gv) * uv;
+              nonfinite |= !isfinite(v);
+              const float hi = round_bf16(v), lo = round_bf16(v - hi);
+              t.act2[((size_t)g * 16 + r) * I + i] = (uint16_t)(__float_as_uint(hi) >> 16);
+              t.act2[((size_t)g * 16 + 4 + r) * I + i] = (uint16_t)(__float_as_uint(lo) >> 16);
+            }
+            asm volatile("fence.proxy.async.global;" ::: "memory");  // read back by TMA
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) publish(&group_done[g], 32u);
+          }
+        } else {
+          // kind B: rows d0 (first block of the pair) and d0 + 128 of hidden, scaled by the route weights
+          const int d0 = blk * 256 + warp * 32 + lane, d1 = d0 + 128;
+          const int mask = sm.gm[g];
+#pragma unroll
+          for (int r = 0; r < rows; ++r) {
+            if ((mask >> r) & 1) {
+              const float w = sm.gw[g][r];
+              const float y0 = w * (v0[r] + v0[4 + r]), y1 = w * (v1[r] + v1[4 + r]);
+              nonfinite |= !isfinite(y0);
+              red_add_f64(t.acc_y + (size_t)r * D + d0, (double)y0);
+              if (d1 < D) {
+                nonfinite |= !isfinite(y1);
+                red_add_f64(t.acc_y + (size_t)r * D + d1, (double)y1);
+              }
+            }
+          }
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) {
+            add_relaxed(&dblock_done[(blk * 256 + warp * 32) / kDecodeDBlock], 1u);
+            if (blk * 256 + 128 < D) add_relaxed(&dblock_done[(blk * 256 + 128 + warp * 32) / kDecodeDBlock], 1u);
+          }
+        }
+      }
+      if (__any_sync(0xffffffffu, nonfinite) && lane == 0) atomicOr(a.status, kDevNonFinite);
+    } else if (warp == kEpiWarps && role < a.nm) {
+      // the last mix CTA's warp 4 forms the comb
+      int todo = 0;
+      const uint64_t t0 = global_timer_ns();
+      while ((todo = *reinterpret_cast<volatile int *>(&sm.comb_todo)) == 0) {
+        if (global_timer_ns() - t0 > a.wait_ns) {
+          if (lane == 0) {
+            atomicOr(a.status, kDevTimeout);
+            atomicExch(&cnt[kCntAbort], 1u);
+          }
+          break;
+        }
+        __nanosleep(32);
+      }
+      __threadfence_block();
+      __syncwarp();
+      if (todo == 1) mix_comb<ROWS>(a, sm, cnt);
+    }
+  }
+  else if (warp == kProducerWarp) {
+    // ================= producer: routing, unit claims, TMA =================
+    route_setup<ROWS>(a, sm);
+    route_compute<ROWS>(a, sm, true);
+    ScorePoll sp{&score_bar, 0u, false, false, 0};
+    // the stream starts once the mix CTAs have read the state (the prelude's loads are latency-bound
+    // chains that must not queue behind it)
+    (void)wait_at_least(&cnt[kCntMixDone], (unsigned)a.nm, a);
+    sp.t0 = global_timer_ns();
+    score_copy_issue(a, sm, sp, ROWS);
+    const uint64_t pol = make_policy_evict_first();  // every weight byte is read once
+    int j = 0;    // A ring steps issued
+    int nab = 0;  // act slices issued
+    int u = 0;    // units handed to the MMA issuer and the epilogue
+    int ng = -1;
+    bool ok = true;
+    // a unit into the queue (lane 0 writes, the warp follows its verdict)
+    auto hand = [&](int kind, int g, int blk, int e) -> bool {
+      const int q = u % kTQ;
+      int r = 0;
+      if (lane == 0) {
+        r = mbar_wait_backoff(&tq_empty[q], (uint32_t)((u / kTQ) & 1) ^ 1u, &sm.abort, a.status, a.wait_ns) ? 1 : 0;
+        if (r) {
+          tq[q] = make_int4(kind, g, blk, e);
+          mbar_arrive(&tq_full[q]);
+        } else {
+          atomicExch(&cnt[kCntAbort], 1u);
+        }
+      }
+      ++u;
+      return __shfl_sync(0xffffffffu, r, 0) != 0;
+    };
+    // the next free ring slot (lane 0 waits, the warp follows)
+    auto slot = [&]() -> int {
+      const int s = j % kStages;
+      int r = 1;
+      if (lane == 0) {
+        r = mbar_wait_backoff(&empty_bar[s], (uint32_t)((j / kStages) & 1) ^ 1u, &sm.abort, a.status, a.wait_ns) ? 1 : 0;
+        if (!r) atomicExch(&cnt[kCntAbort], 1u);
+      }
+      return __shfl_sync(0xffffffffu, r, 0) ? s : -1;
+    };
+    // The units of this CTA's two K splits, from two queues in group order: kind A (group, 128-row
+    // block of inter), then, once that queue is used up, kind B (group, pair of 128-row blocks of
+    // hidden).  (Taking kind B units of groups whose act was complete between kind A units, and
+    // holding the fills until the CTA's own prelude was done, both measured slower.)
+    unsigned *tick_a = cnt + t.cnt_tick_a + 32 * ka, *tick_b = cnt + t.cnt_tick_b + 32 * kbs;
+    bool a_done = false;
+    while (ok) {
+      if (!sp.routed) (void)score_poll<ROWS>(a, sm, cnt, sp, false);
+      if (a_done) {
+        // ---- a kind B unit: this CTA's split of inter, two 128-row blocks of hidden ----
+        int tk = 0;
+        if (lane == 0) tk = (int)atomicAdd(tick_b, 1u);
+        tk = __shfl_sync(0xffffffffu, tk, 0);
+        const int g = tk / rbb, blk = tk - g * rbb;
+        if (g >= ng) break;
+        const int e = sm.ge[g];
+        // the group's act planes, once every 128-row block of inter has published them
+        if (!wait_at_least(&group_done[g], (unsigned)I, a)) {
+          ok = false;
+          break;
+        }
+        const int ab = nab & 1;
+        int r = 1;
+        if (lane == 0) {
+          r = mbar_wait_backoff(&aempty[ab], (uint32_t)((nab >> 1) & 1) ^ 1u, &sm.abort, a.status, a.wait_ns) ? 1 : 0;
+          if (r) {
+            // written by other CTAs' generic stores, read here by TMA
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            mbar_arrive_expect_tx(&afull[ab], (uint32_t)(t.cb * kBTile));
+            for (int c = 0; c < t.cb; ++c)
+              tma_load_2d(as + (size_t)ab * kBSlice + (size_t)c * kBTile, &tm.act2, &afull[ab],
+                          (kbs * t.cb + c) * 64, g * 16);
+          } else {
+            atomicExch(&cnt[kCntAbort], 1u);
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, r, 0)) {
+          ok = false;
+          break;
+        }
+        ++nab;
+        if (!hand(kUnitB | (ab << 4), g, blk, e)) {
+          ok = false;
+          break;
+        }
+        const CUtensorMap *md = g == 0 ? &tm.down_sh : &tm.down;
+        const int row = (g == 0 ? 0 : e * D) + blk * 256;
+        for (int c = 0; c < t.cb; ++c, ++j) {
+          const int s = slot();
+          if (s < 0) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            uint8_t *dst = ring + (size_t)s * kSlotBytes;
+            const int kc = (kbs * t.cb + c) * 64;
+            mbar_arrive_expect_tx(&full_bar[s], 2u * kTile);
+            tma_load_2d_hint(dst, md, &full_bar[s], kc, row, pol);
+            tma_load_2d_hint(dst + kTile, md, &full_bar[s], kc, row + 128, pol);
+          }
+          __syncwarp();
+        }
+        continue;
+      }
+      // ---- a kind A unit: this CTA's split of hidden, a 128-row block of inter ----
+      int tk = 0;
+      if (lane == 0) tk = (int)atomicAdd(tick_a, 1u);
+      tk = __shfl_sync(0xffffffffu, tk, 0);
+      const int g = tk / rba, blk = tk - g * rba;
+      if (g > 0 && ng < 0) {  // the first routed unit: the group table
+        (void)score_poll<ROWS>(a, sm, cnt, sp, true);
+        ng = sm.ng;
+      }
+      if (g > 0 && g >= ng) {  // every kind A unit of this split is claimed
+        a_done = true;
+        continue;
+      }
+      const int e = g == 0 ? E : sm.ge[g];
+      if (!hand(kUnitA, g, blk, e)) {
+        ok = false;
+        break;
+      }
+      const CUtensorMap *mg = g == 0 ? &tm.gate_sh : &tm.gate, *mu = g == 0 ? &tm.up_sh : &tm.up;
+      const int row = (g == 0 ? 0 : e * I) + blk * 128;
+      for (int c = 0; c < t.ca; ++c, ++j) {
+        const int s = slot();
+        if (s < 0) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          uint8_t *dst = ring + (size_t)s * kSlotBytes;
+          const int kc = (ka * t.ca + c) * 64;
+          mbar_arrive_expect_tx(&full_bar[s], 2u * kTile);
+          tma_load_2d_hint(dst, mg, &full_bar[s], kc, row, pol);
+          tma_load_2d_hint(dst + kTile, mu, &full_bar[s], kc, row, pol);
+        }
+        __syncwarp();
+      }
+    }
+    (void)hand(kUnitEnd, 0, 0, 0);
+    // phase C needs the group table even where no routed unit was drawn
+    (void)score_poll<ROWS>(a, sm, cnt, sp, true);
+    // copies still in flight (after a timeout) land before the CTA may leave
+    if (lane == 0) {
+      int no_abort = 0;
+      for (int s = 0; s < kStages; ++s) {
+        const int n = j / kStages + (s < j % kStages ? 1 : 0);
+        if (n > 0) (void)mbar_wait_bounded(&full_bar[s], (uint32_t)((n - 1) & 1), &no_abort, a.status, a.wait_ns);
+      }
+      for (int b = 0; b < 2; ++b) {
+        const int n = nab / 2 + (b < nab % 2 ? 1 : 0);
+        if (n > 0) (void)mbar_wait_bounded(&afull[b], (uint32_t)((n - 1) & 1), &no_abort, a.status, a.wait_ns);
+      }
+      if (sp.in_flight) (void)mbar_wait_bounded(&score_bar, sp.phase, &no_abort, a.status, a.wait_ns);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp && lane == 0) {
+    // ================= MMA issuer =================
+    int ok = mbar_wait_bounded(&xready, 0u, &sm.abort, a.status, a.wait_ns) ? 1 : 0;
+    const uint32_t idesc = idesc_bf16_f32(128, 16);
+    int j = 0, na = 0;
+    for (int u = 0; ok; ++u) {
+      const int q = u % kTQ;
+      if (!mbar_wait_bounded(&tq_full[q], (uint32_t)((u / kTQ) & 1), &sm.abort, a.status, a.wait_ns)) break;
+      const int4 e = tq[q];
+      mbar_arrive(&tq_empty[q]);
+      const int kind = e.x & 15;
+      if (kind == kUnitEnd) break;
+      const int b = u & 1;
+      if (!mbar_wait_bounded(&tempty[b], (uint32_t)((u >> 1) & 1) ^ 1u, &sm.abort, a.status, a.wait_ns)) break;
+      tc_fence_after();
+      const uint32_t d0 = tmem + (uint32_t)(b * 32), d1 = d0 + 16;
+      const int ab = (e.x >> 4) & 1;
+      if (kind == kUnitB &&
+          !mbar_wait_bounded(&afull[ab], (uint32_t)((na >> 1) & 1), &sm.abort, a.status, a.wait_ns))
+        break;
+      const int nc = kind == kUnitA ? t.ca : t.cb;
+      const uint32_t bbase = smem_u32(kind == kUnitA ? xs : as + (size_t)ab * kBSlice);
+      for (int c = 0; c < nc; ++c, ++j) {
+        const int s = j % kStages;
+        if (!mbar_wait_bounded(&full_bar[s], (uint32_t)((j / kStages) & 1), &sm.abort, a.status, a.wait_ns)) {
+          ok = 0;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = smem_u32(ring + (size_t)s * kSlotBytes), sb = bbase + (uint32_t)(c * kBTile);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t accum = (c > 0 || k > 0) ? 1u : 0u;
+          const uint64_t bd = smem_desc_sw128(sb + k * 32);
+          tc_mma_f16(d0, smem_desc_sw128(sa + k * 32), bd, idesc, accum);
+          tc_mma_f16(d1, smem_desc_sw128(sa + kTile + k * 32), bd, idesc, accum);
+        }
+        tc_commit(&empty_bar[s]);  // the slot is free once these MMAs have read it
+      }
+      if (!ok) break;
+      if (kind == kUnitB) {
+        tc_commit(&aempty[ab]);
+        ++na;
+      }
+      tc_commit(&tfull[b]);
+    }
+    // every MMA issued completes before TMEM is freed (immediate in a normal run)
+    tc_commit(&mma_done);
+    int no_abort = 0;
+    (void)mbar_wait_bounded(&mma_done, 0u, &no_abort, a.status, a.wait_ns);
+  }
+  __syncthreads();  // the group table is complete for phase C; no unit is in flight
+  pdl_wait();       // phase C reads the state, which comes from the previous kernel
+
+  // ---- phase C: per 32-wide block of hidden, once every group's kind B units of it are in: ffn_out
+  // (the f64 sum, rounded once) and the hc_post output out_i = post_i * ffn_out + sum_j comb[i, j] *
+  // state_j.  The comb term needs no FFN output, so it is formed before the block's wait.
+  const int hc = a.hc, ng = sm.ng, nblk = D / kDecodeDBlock;
+  const bool comb_ok = wait_at_least(&cnt[kCntComb], a.inject == 1 ? 2u : 1u, a);
+  for (int c = draw_ticket(&cnt[kCntTickC]); c < nblk && comb_ok; c = draw_ticket(&cnt[kCntTickC])) {
+    const int d = c * kDecodeDBlock + lane;
+    float po[rows][kHcMax], tt[rows][kHcMax];
+#pragma unroll
+    for (int r = 0; r < rows; ++r) {
+      float sj[kHcMax];
+#pragma unroll
+      for (int q = 0; q < kHcMax; ++q) sj[q] = q < hc ? a.state[((size_t)r * hc + q) * D + d] : 0.f;
+#pragma unroll
+      for (int o = 0; o < kHcMax; ++o) {
+        po[r][o] = o < hc ? __ldcg(a.post + r * hc + o) : 0.f;
+        float v = 0.f;
+#pragma unroll
+        for (int q = 0; q < kHcMax; ++q)
+          if (o < hc && q < hc) v += __ldcg(a.comb + (r * hc + o) * hc + q) * sj[q];
+        tt[r][o] = v;
+      }
+    }
+    if (!wait_at_least(&dblock_done[c], (unsigned)(ng * t.sb), a, false)) break;
+#pragma unroll
+    for (int r = 0; r < rows; ++r) {
+      double *src = t.acc_y + (size_t)r * D + d;
+      const float f = (float)ld_cg_f64(src);
+      *src = 0.0;  // zero again for the next launch
+      a.ffn_out[(size_t)r * D + d] = f;
+#pragma unroll
+      for (int o = 0; o < kHcMax; ++o)
+        if (o < hc) a.out_state[((size_t)r * hc + o) * D + d] = po[r][o] * f + tt[r][o];
+    }
+  }
+
+  // ---- the last CTA out resets the counters and the score table for the next launch ----
+  __threadfence();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if (tid == 0) sm.flag = atomicAdd(&cnt[kCntExit], 1u) == gridDim.x - 1 ? 1 : 0;
+  __syncthreads();
+  if (sm.flag) {
+    __threadfence();
+    // a launch that gave up somewhere may have left partial sums that their readers never took:
+    // zero both accumulators (every CTA has left its loops and fenced its adds)
+    if (*reinterpret_cast<volatile unsigned *>(&cnt[kCntAbort]) != 0u) {
+      for (int i = tid; i < t.n_acc_gu; i += blockDim.x) t.acc_gu[i] = 0.0;
+      for (int i = tid; i < t.n_acc_y; i += blockDim.x) t.acc_y[i] = 0.0;
+    }
+    __syncthreads();
+    for (int i = tid; i < a.n_counters; i += blockDim.x) cnt[i] = 0u;
+    for (int i = tid; i < kDecodeRows * E; i += blockDim.x) a.sel[i] = __uint_as_float(kUnwritten);
+    __threadfence();
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------------------------
+
+using DecodeTcKernel = void (*)(DecodeTcMaps, DecodeArgs, DecodeTcArgs);
+static DecodeTcKernel decode_tc_kernel_for(int rows) {
+  return rows == 1 ? decode_tc_kernel<1> : rows == 2 ? decode_tc_kernel<2> : rows == 3 ? decode_tc_kernel<3>
+                                                                                        : decode_tc_kernel<4>;
+}
+
+cudaError_t decode_tc_configure() {
+  for (int r = 1; r <= kDecodeRows; ++r) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(decode_tc_kernel_for(r), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dtc::kSmem);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+int decode_tc_resident_ctas(int rows, int num_sms) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_tc_kernel_for(rows), kDecThreads, dtc::kSmem) !=
+      cudaSuccess)
+    return 0;
+  return per_sm * num_sms;
+}
+
+// The fewest K splits of `chunks` 64-wide chunks that leave at most kMaxChunks chunks to a split.
+static void tc_split(int chunks, int &splits, int &per) {
+  for (splits = 1; splits < chunks; ++splits)
+    if (chunks % splits == 0 && chunks / splits <= dtc::kMaxChunks) break;
+  per = chunks / splits;
+}
+
+bool decode_tc_fits(const Dims &d, int grid) {
+  int sa, ca, sb, cb;
+  tc_split(d.hidden / 64, sa, ca);
+  tc_split(d.inter / 64, sb, cb);
+  return ca <= dtc::kMaxChunks && cb <= dtc::kMaxChunks && sa <= kMaxSplits && sb <= kMaxSplits && grid >= sa &&
+         grid >= sb;
+}
+
+void launch_decode_tc(const DecodeArgs &a, const Dims &d, const Scratch &s, const LayerDev &w, int rows, int grid,
+                      cudaStream_t st) {
+  DecodeTcMaps m;
+  m.gate = w.tm_gate;
+  m.up = w.tm_up;
+  m.down = w.tm_down;
+  m.gate_sh = w.tm_gate_sh;
+  m.up_sh = w.tm_up_sh;
+  m.down_sh = w.tm_down_sh;
+  m.act2 = s.tm_dtc_act2;
+  DecodeTcArgs t;
+  t.acc_gu = s.dtc_acc_gu;
+  t.acc_y = s.dtc_acc_y;
+  t.act2 = s.dtc_act2;
+  tc_split(d.hidden / 64, t.sa, t.ca);
+  tc_split(d.inter / 64, t.sb, t.cb);
+  t.cnt_tick_a = tc_counter_base(d);
+  t.cnt_tick_b = t.cnt_tick_a + kMaxSplits * 32;
+  t.cnt_units = t.cnt_tick_b + kMaxSplits * 32;
+  t.n_acc_gu = (d.top_k * kDecodeRows + 1) * 2 * 4 * d.inter;
+  t.n_acc_y = 4 * d.hidden;
+  launch_pdl(decode_tc_kernel_for(rows), dim3(grid), dim3(kDecThreads), dtc::kSmem, st, m, a, t);
+}
+
+}  // namespace moe

@@ -69,7 +69,13 @@ struct Scratch {
   float *y_dec;           // [groups, 4, hidden]
   unsigned *dec_counters; // the decode kernel's tickets and completion counters (zero between launches)
   int decode_ctas_by_rows[5];  // co-resident CTAs of the persistent decode kernel, per row count
-  int decode_ctas_mx[5];       // the same for its MXFP8-expert instances
+  int decode_ctas_mx[5];       // the same for its MXFP8-expert instances (CUDA-core kernel)
+  // decode on the tensor cores (bf16 experts)
+  double *dtc_acc_gu;          // [groups, 2, 4, inter] gate and up partial sums (zero between launches)
+  double *dtc_acc_y;           // [4, hidden] the FFN output (zero between launches)
+  uint16_t *dtc_act2;          // [groups, 16, inter] bf16: act hi planes (rows 0-3), lo planes (rows 4-7)
+  CUtensorMap tm_dtc_act2;     // over dtc_act2, boxes of 64 x 16 rows
+  bool dtc;                    // the tensor-core decode kernel fits this configuration
   // rows > 4 path
   int *counts;            // [experts] routed slots per expert (zero between launches)
   int *offsets;           // [experts + 2]
@@ -161,6 +167,11 @@ void launch_decode(const Dims &d, const Scratch &s, const LayerDev &w, const flo
                    int rows, bool hash, float *out_state, cudaStream_t st, StageTimer *tm, const DebugOpts &dbg);
 cudaError_t decode_configure(int hidden);
 int decode_resident_ctas(int hidden, int rows, int num_sms, bool mx);
+// decode_tc.cu
+int decode_tc_counter_count(const Dims &d);
+cudaError_t decode_tc_configure();
+int decode_tc_resident_ctas(int rows, int num_sms);
+bool decode_tc_fits(const Dims &d, int grid);
 void launch_mxfp8_to_bf16(const uint8_t *q, const uint8_t *s, uint16_t *dst, size_t n, cudaStream_t st);
 // dispatch.cu
 void launch_dispatch(const Dims &d, const Scratch &s, int rows, cudaStream_t st, StageTimer *tm);

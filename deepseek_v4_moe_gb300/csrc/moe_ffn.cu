@@ -241,6 +241,8 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
             dalloc(h, &s.ffn_out, R * D) && dalloc(h, &s.ngroups, 1) && dalloc(h, &s.group_e, G) &&
             dalloc(h, &s.group_mask, G) && dalloc(h, &s.group_w, G * 4) && dalloc(h, &s.act_dec, G * 4 * I) &&
             dalloc(h, &s.y_dec, G * 4 * D) && dalloc(h, &s.dec_counters, (size_t)moe::decode_counter_count(d)) &&
+            dalloc(h, &s.dtc_acc_gu, G * 2 * 4 * I) && dalloc(h, &s.dtc_acc_y, 4 * D) &&
+            dalloc(h, &s.dtc_act2, G * 16 * I) &&
             dalloc(h, &h->host_in, R * hcd) &&
             dalloc(h, &h->host_out, R * hcd) && dalloc(h, &h->host_tok, R);
   const bool prefill = R > (size_t)moe::kDecodeRows;
@@ -263,6 +265,14 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
   cudaMemset(s.status, 0, sizeof(int));
   cudaMemset(s.dec_counters, 0, (size_t)moe::decode_counter_count(d) * sizeof(unsigned));
   cudaMemset(s.dec_part, 0xFF, (size_t)moe::kDecodeRows * E * 2 * sizeof(float));  // "not written yet"
+  cudaMemset(s.dtc_acc_gu, 0, G * 2 * 4 * I * sizeof(double));
+  cudaMemset(s.dtc_acc_y, 0, 4 * D * sizeof(double));
+  cudaMemset(s.dtc_act2, 0, G * 16 * I * sizeof(uint16_t));
+  if (!make_tmap_bf16(&s.tm_dtc_act2, s.dtc_act2, I, G * 16, 16)) {
+    free_all(h);
+    delete h;
+    return fail(nullptr, MOE_FFN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the decode act planes");
+  }
   cudaMemset(s.tickets, 0, (R / 4 + 2) * sizeof(unsigned));
   if (prefill) {
     cudaMemset(s.counts, 0, E * sizeof(int));
@@ -279,7 +289,7 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
     }
   }
   if (moe::gemm_configure() != cudaSuccess || moe::decode_configure(d.hidden) != cudaSuccess ||
-      moe::splitgemm_configure() != cudaSuccess) {
+      moe::decode_tc_configure() != cudaSuccess || moe::splitgemm_configure() != cudaSuccess) {
     free_all(h);
     delete h;
     return fail(nullptr, MOE_FFN_ERR_CUDA, "kernel attribute setup failed");
@@ -287,7 +297,10 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
   for (int mx = 0; mx < 2; ++mx)
     for (int r = 1; r <= moe::kDecodeRows; ++r) {
       int &n = mx ? s.decode_ctas_mx[r] : s.decode_ctas_by_rows[r];
-      n = moe::decode_resident_ctas(d.hidden, r, h->num_sms, mx != 0);
+      // bf16 experts stream on the tensor cores (one CTA per SM) where the K splits fit the grid
+      const int tc = mx ? 0 : moe::decode_tc_resident_ctas(r, h->num_sms);
+      s.dtc = !mx ? tc > 0 && moe::decode_tc_fits(d, tc) : s.dtc;
+      n = !mx && s.dtc ? tc : moe::decode_resident_ctas(d.hidden, r, h->num_sms, mx != 0);
       if (n <= 0) {
         free_all(h);
         delete h;
@@ -324,11 +337,12 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
     L.gate_sh = w.gate_sh;
     L.up_sh = w.up_sh;
     L.down_sh = w.down_sh;
-    if (!prefill) continue;
-    // the rows > 4 path reads the caller's bf16 matrices through tensor maps: hc_fn in boxes of 32
-    // rows (the mix's MMA width; rows past (2+hc)*hc read as zeros), the router in boxes of 256
+    // the tensor-core paths read the caller's bf16 expert matrices through tensor maps (both
+    // paths); the rows > 4 path also hc_fn in boxes of 32 rows (the mix's MMA width; rows past
+    // (2+hc)*hc read as zeros) and the router in boxes of 256
     if ((L.has_experts && !expert_tmaps(h, L, w.gate_exps, w.up_exps, w.down_exps, w.gate_sh, w.up_sh, w.down_sh)) ||
-        !make_tmap_bf16(&L.tm_hcfn, w.hc_fn, hcd, M, 32) || !make_tmap_bf16(&L.tm_router, w.gate, D, E, 256)) {
+        (prefill && (!make_tmap_bf16(&L.tm_hcfn, w.hc_fn, hcd, M, 32) ||
+                     !make_tmap_bf16(&L.tm_router, w.gate, D, E, 256)))) {
       free_all(h);
       delete h;
       return fail(nullptr, MOE_FFN_ERR_CUDA, "cuTensorMapEncodeTiled failed for layer %d", l);
