@@ -27,7 +27,8 @@
 // Every CTA draws all of its kind A units before its first kind B unit, and a kind B unit waits only
 // for kind A work, which running CTAs hold: every wait ends.
 //
-// Roles: warps 0-7 run the prelude; then warps 0-3 are the epilogue (one TMEM lane quarter each);
+// Roles: warps 0-7 run the prelude, then the epilogue (two groups of four alternating units, one TMEM
+// lane quarter per warp);
 // warp 8 is the producer (routing, unit claims, TMA), warp 9 the MMA issuer and TMEM owner.  Phase C
 // (per 32-wide block of hidden: ffn_out and hc_post) is shared by all warps at the end.  Waits are
 // bounded (1 s); after a timeout every later wait fails at once, the producer waits (bounded) for
@@ -112,6 +113,12 @@ __device__ __forceinline__ void split8(const float4 a, const float4 b, uint4 &hi
                   pack_bf16_pair(l[6], l[7]));
 }
 
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned *p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ double ld_cg_f64(const double *p) {
   double v;
   asm volatile("ld.global.cg.f64 %0, [%1];" : "=d"(v) : "l"(p) : "memory");
@@ -150,7 +157,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     mbar_init(&score_bar, 1);
     for (int q = 0; q < kTQ; ++q) {
       mbar_init(&tq_full[q], 1);
-      mbar_init(&tq_empty[q], 1 + kEpiWarps);
+      mbar_init(&tq_empty[q], 1 + kWorkerWarps);  // the MMA issuer and all eight epilogue warps
     }
     mbar_init(&mma_done, 1);
     sm.abort = 0;
@@ -199,94 +206,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the MMAs read them through the async proxy
     workers_sync();
     if (tid == 0) mbar_arrive(&xready);
-    if (warp < kEpiWarps) {
-      // ---------------- epilogue: TMEM lane quarter `warp` ----------------
-      bool nonfinite = false;
-      for (int u = 0;; ++u) {
-        const int q = u % kTQ;
-        int4 e = make_int4(kUnitEnd, 0, 0, 0);
-        int ok = 0;
-        if (lane == 0) {
-          ok = mbar_wait_bounded(&tq_full[q], (uint32_t)((u / kTQ) & 1), &sm.abort, a.status, a.wait_ns) ? 1 : 0;
-          if (ok) {
-            e = tq[q];
-            mbar_arrive(&tq_empty[q]);
-            ok = (e.x & 15) == kUnitEnd ||
-                 mbar_wait_bounded(&tfull[u & 1], (uint32_t)((u >> 1) & 1), &sm.abort, a.status, a.wait_ns);
-          }
-          if (!ok) atomicExch(&cnt[kCntAbort], 1u);
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        const int kind = __shfl_sync(0xffffffffu, e.x, 0) & 15;
-        if (!ok || kind == kUnitEnd) break;
-        const int g = __shfl_sync(0xffffffffu, e.y, 0), blk = __shfl_sync(0xffffffffu, e.z, 0);
-        tc_fence_after();
-        float v0[16], v1[16];
-        const uint32_t tb = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)((u & 1) * 32);
-        tmem_ld16(tb, v0);
-        tmem_ld16(tb + 16, v1);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[u & 1]);  // the accumulator buffer is free for the next unit
-        if (kind == kUnitA) {
-          const int i = blk * 128 + warp * 32 + lane;  // this lane's row of inter
-          double *acc = t.acc_gu + (size_t)g * 2 * 4 * I + i;
-#pragma unroll
-          for (int r = 0; r < rows; ++r) {
-            red_add_f64(acc + (size_t)r * I, (double)(v0[r] + v0[4 + r]));            // gate
-            red_add_f64(acc + (size_t)(4 + r) * I, (double)(v1[r] + v1[4 + r]));      // up
-          }
-          __threadfence();
-          __syncwarp();
-          int last = 0;
-          if (lane == 0) last = atomicAdd(&cnt[t.cnt_units + (g * rba + blk) * 4 + warp], 1u) == (unsigned)(t.sa - 1);
-          if (__shfl_sync(0xffffffffu, last, 0)) {
-            // every split of this (group, block, quarter) is in: SwiGLU, as bf16 hi / lo planes
-            __threadfence();
-#pragma unroll
-            for (int r = 0; r < rows; ++r) {
-              const float gv = (float)ld_cg_f64(acc + (size_t)r * I), uv = (float)ld_cg_f64(acc + (size_t)(4 + r) * I);
-              acc[(size_t)r * I] = 0.0;  // zero again for the next launch
-              acc[(size_t)(4 + r) * I] = 0.0;
-              const float v = gv * sigmoidf_(gv) * uv;
-              nonfinite |= !isfinite(v);
-              const float hi = round_bf16(v), lo = round_bf16(v - hi);
-              t.act2[((size_t)g * 16 + r) * I + i] = (uint16_t)(__float_as_uint(hi) >> 16);
-              t.act2[((size_t)g * 16 + 4 + r) * I + i] = (uint16_t)(__float_as_uint(lo) >> 16);
-            }
-            asm volatile("fence.proxy.async.global;" ::: "memory");  // read back by TMA
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) publish(&group_done[g], 32u);
-          }
-        } else {
-          // kind B: rows d0 (first block of the pair) and d0 + 128 of hidden, scaled by the route weights
-          const int d0 = blk * 256 + warp * 32 + lane, d1 = d0 + 128;
-          const int mask = sm.gm[g];
-#pragma unroll
-          for (int r = 0; r < rows; ++r) {
-            if ((mask >> r) & 1) {
-              const float w = sm.gw[g][r];
-              const float y0 = w * (v0[r] + v0[4 + r]), y1 = w * (v1[r] + v1[4 + r]);
-              nonfinite |= !isfinite(y0);
-              red_add_f64(t.acc_y + (size_t)r * D + d0, (double)y0);
-              if (d1 < D) {
-                nonfinite |= !isfinite(y1);
-                red_add_f64(t.acc_y + (size_t)r * D + d1, (double)y1);
-              }
-            }
-          }
-          __threadfence();
-          __syncwarp();
-          if (lane == 0) {
-            add_relaxed(&dblock_done[(blk * 256 + warp * 32) / kDecodeDBlock], 1u);
-            if (blk * 256 + 128 < D) add_relaxed(&dblock_done[(blk * 256 + 128 + warp * 32) / kDecodeDBlock], 1u);
-          }
-        }
-      }
-      if (__any_sync(0xffffffffu, nonfinite) && lane == 0) atomicOr(a.status, kDevNonFinite);
-    } else if (warp == kEpiWarps && role < a.nm) {
-      // the last mix CTA's warp 4 forms the comb
+    if (warp == kEpiWarps && role < a.nm) {
+      // the last mix CTA's warp 4 forms the comb before it joins the epilogue
       int todo = 0;
       const uint64_t t0 = global_timer_ns();
       while ((todo = *reinterpret_cast<volatile int *>(&sm.comb_todo)) == 0) {
@@ -303,6 +224,97 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       __syncwarp();
       if (todo == 1) mix_comb<ROWS>(a, sm, cnt);
     }
+    // ---------------- epilogue: warps 0-3 take the even units, warps 4-7 the odd ones (accumulator
+    // buffer u & 1), each warp its TMEM lane quarter, so each has two units' time for its
+    // reductions ----------------
+    const int quarter = warp & 3, group = warp >> 2;
+    bool nonfinite = false;
+    for (int u = 0;; ++u) {
+      const int q = u % kTQ;
+      int4 e = make_int4(kUnitEnd, 0, 0, 0);
+      int ok = 0;
+      const bool mine = (u & 1) == group;
+      if (lane == 0) {
+        ok = mbar_wait_bounded(&tq_full[q], (uint32_t)((u / kTQ) & 1), &sm.abort, a.status, a.wait_ns) ? 1 : 0;
+        if (ok) {
+          e = tq[q];
+          mbar_arrive(&tq_empty[q]);
+          ok = (e.x & 15) == kUnitEnd || !mine ||
+               mbar_wait_bounded(&tfull[u & 1], (uint32_t)((u >> 1) & 1), &sm.abort, a.status, a.wait_ns);
+        }
+        if (!ok) atomicExch(&cnt[kCntAbort], 1u);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      const int kind = __shfl_sync(0xffffffffu, e.x, 0) & 15;
+      if (!ok || kind == kUnitEnd) break;
+      if (!mine) continue;
+      const int g = __shfl_sync(0xffffffffu, e.y, 0), blk = __shfl_sync(0xffffffffu, e.z, 0);
+      tc_fence_after();
+      float v0[16], v1[16];
+      const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)((u & 1) * 32);
+      tmem_ld16(tb, v0);
+      tmem_ld16(tb + 16, v1);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[u & 1]);  // the accumulator buffer is free for the next unit
+      if (kind == kUnitA) {
+        const int i = blk * 128 + quarter * 32 + lane;  // this lane's row of inter
+        double *acc = t.acc_gu + (size_t)g * 2 * 4 * I + i;
+#pragma unroll
+        for (int r = 0; r < rows; ++r) {
+          red_add_f64(acc + (size_t)r * I, (double)(v0[r] + v0[4 + r]));            // gate
+          red_add_f64(acc + (size_t)(4 + r) * I, (double)(v1[r] + v1[4 + r]));      // up
+        }
+        // the count is an acquire-release add: it publishes the warp's adds (ordered before it by the
+        // warp barrier) and, in the last split, makes every other split's adds visible
+        __syncwarp();
+        int last = 0;
+        if (lane == 0)
+          last = atom_add_acq_rel(&cnt[t.cnt_units + (g * rba + blk) * 4 + quarter], 1u) == (unsigned)(t.sa - 1);
+        __syncwarp();  // lane 0's acquire is ordered before every lane's reads below
+        if (__shfl_sync(0xffffffffu, last, 0)) {
+          // every split of this (group, block, quarter) is in: SwiGLU, as bf16 hi / lo planes
+          asm volatile("fence.acq_rel.gpu;" ::: "memory");
+#pragma unroll
+          for (int r = 0; r < rows; ++r) {
+            const float gv = (float)ld_cg_f64(acc + (size_t)r * I), uv = (float)ld_cg_f64(acc + (size_t)(4 + r) * I);
+            acc[(size_t)r * I] = 0.0;  // zero again for the next launch
+            acc[(size_t)(4 + r) * I] = 0.0;
+            const float v = gv * sigmoidf_(gv) * uv;
+            nonfinite |= !isfinite(v);
+            const float hi = round_bf16(v), lo = round_bf16(v - hi);
+            t.act2[((size_t)g * 16 + r) * I + i] = (uint16_t)(__float_as_uint(hi) >> 16);
+            t.act2[((size_t)g * 16 + 4 + r) * I + i] = (uint16_t)(__float_as_uint(lo) >> 16);
+          }
+          asm volatile("fence.proxy.async.global;" ::: "memory");  // read back by TMA
+          __syncwarp();
+          if (lane == 0) publish(&group_done[g], 32u);
+        }
+      } else {
+        // kind B: rows d0 (first block of the pair) and d0 + 128 of hidden, scaled by the route weights
+        const int d0 = blk * 256 + quarter * 32 + lane, d1 = d0 + 128;
+        const int mask = sm.gm[g];
+#pragma unroll
+        for (int r = 0; r < rows; ++r) {
+          if ((mask >> r) & 1) {
+            const float w = sm.gw[g][r];
+            const float y0 = w * (v0[r] + v0[4 + r]), y1 = w * (v1[r] + v1[4 + r]);
+            nonfinite |= !isfinite(y0);
+            red_add_f64(t.acc_y + (size_t)r * D + d0, (double)y0);
+            if (d1 < D) {
+              nonfinite |= !isfinite(y1);
+              red_add_f64(t.acc_y + (size_t)r * D + d1, (double)y1);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {  // release adds: the warp's reductions before the counts
+          publish(&dblock_done[(blk * 256 + quarter * 32) / kDecodeDBlock], 1u);
+          if (blk * 256 + 128 < D) publish(&dblock_done[(blk * 256 + 128 + quarter * 32) / kDecodeDBlock], 1u);
+        }
+      }
+    }
+    if (__any_sync(0xffffffffu, nonfinite) && lane == 0) atomicOr(a.status, kDevNonFinite);
   }
   else if (warp == kProducerWarp) {
     // ================= producer: routing, unit claims, TMA =================
