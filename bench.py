@@ -112,7 +112,7 @@ def kernel_work(name: str, wm: dict, cfg) -> tuple[float, float]:
 # every touched expert once, so a capture on the 32-expert profiling workload with the same
 # routing width (6 routed + shared) carries the same bytes as the full workload.  A kernel change
 # removes its entry until it is captured again.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {("decode", 1, 7): 354_256_128 + 3_561_728}
 
 
 def roofline_entry(name: str, avg_ms: float, wm: dict, cfg, peaks: dict, peak_kind: str) -> dict:
@@ -286,7 +286,8 @@ def run_ours(cfg, steps: int, warmup: int, device, rank: int, world: int, dist, 
     res["roofline"] = {"bound": rl["bound"], "kernel": top["name"], "achieved": rl["achieved"], "peak": rl["peak"],
                        "unit": rl["unit"], "frac": rl["frac"], "traffic": traffic, "peak_source": rl["peak_source"],
                        "alg_per_launch": rl["alg"],
-                       "traffic_source": "ncu capture on p_decode_b1_e32 (same 7 expert groups)" if traffic else None}
+                       "traffic_source": "ncu capture of decode_tc_kernel on p_decode_b1_e32 (same 7 expert groups)"
+                       if traffic else None}
     # whole forward against its binding roofline
     t_hbm = wm["bytes_total"] / (peaks["hbm_gbs"] * 1e9)
     t_tc = wm["flops_total"] / (peaks["bf16_tflops"] * 1e12)
@@ -600,8 +601,7 @@ def main():
         line = {"metric": METRIC, "value": round(main_res["value"], 1), "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": warmup, "ms_per_step": round(main_res["ms_per_step"], 5),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": ("f32 (bf16 weights)" if cfg.rows <= 4 else
-                          "bf16 weights, split-bf16 activations (hi + lo), f32 accumulate"),
+                "dtype": "bf16 weights, split-bf16 activations (hi + lo), f32 accumulate, f64 reductions",
                 "data": "synthetic", "config": config, "roofline": main_res["roofline"],
                 "forward_roofline": main_res["forward_roofline"], "kernels": main_res["kernels"],
                 "cpu_baseline": cpu, "e2e": main_res.get("e2e"), "gpu_launches": main_res["gpu_launches"],
