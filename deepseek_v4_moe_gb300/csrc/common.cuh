@@ -71,43 +71,6 @@ __device__ __forceinline__ void e4m3x16_to_float(const uint4 w, float (&f)[16]) 
   }
 }
 
-// The same 16 codes as floats times 2^-120, by integer operations alone (no format conversion):
-// the code moved to the top byte and shifted right arithmetically by 4 puts its sign in bit 31,
-// copies of it in bits 27-30 (masked off) and its exponent and mantissa fields in f32 bits 23-26
-// and 20-22.  A normal code (exponent field e >= 1) then reads as 2^(e - 127) (1 + m/8), its value
-// times 2^-120; a subnormal one lands on the f32 subnormal (m/8) 2^-126, again its value times
-// 2^-120.  The caller multiplies 2^120 back once per partial sum.  (NaN codes read as finite.)
-__device__ __forceinline__ void e4m3x16_to_float_scaled(const uint4 w, float (&f)[16]) {
-  const unsigned words[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      f[4 * q + k] = __int_as_float((static_cast<int>(words[q] << (24 - 8 * k)) >> 4) & static_cast<int>(0x87F00000u));
-}
-constexpr float kE4m3Unscale = 0x1p120f;  // undoes e4m3x16_to_float_scaled's 2^-120
-
-// sum_k f[k] * x[k] over 16 elements, x as four float4
-__device__ __forceinline__ float dot16(const float (&f)[16], const float4 x0, const float4 x1, const float4 x2,
-                                       const float4 x3) {
-  float s = f[0] * x0.x;
-  s = fmaf(f[1], x0.y, s);
-  s = fmaf(f[2], x0.z, s);
-  s = fmaf(f[3], x0.w, s);
-  s = fmaf(f[4], x1.x, s);
-  s = fmaf(f[5], x1.y, s);
-  s = fmaf(f[6], x1.z, s);
-  s = fmaf(f[7], x1.w, s);
-  s = fmaf(f[8], x2.x, s);
-  s = fmaf(f[9], x2.y, s);
-  s = fmaf(f[10], x2.z, s);
-  s = fmaf(f[11], x2.w, s);
-  s = fmaf(f[12], x3.x, s);
-  s = fmaf(f[13], x3.y, s);
-  s = fmaf(f[14], x3.z, s);
-  s = fmaf(f[15], x3.w, s);
-  return s;
-}
 
 __device__ __forceinline__ uint4 ld_stream_hint(const void *p, uint64_t policy) {
   uint4 r;
