@@ -52,6 +52,13 @@ __device__ __forceinline__ float e8m0_value(unsigned s) {
   return __uint_as_float(s == 0u ? 0x00400000u : s == 255u ? 0x7FC00000u : s << 23);
 }
 
+// two floats as one 64-bit operand of the packed f32x2 instructions (lo in the low half)
+__device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
 // The 16 E4M3 codes of w (element k in byte k) as floats: the hardware converts pairs to f16
 // (exact: every E4M3 value is an f16 value), then to f32.
 __device__ __forceinline__ void e4m3x16_to_float(const uint4 w, float (&f)[16]) {
@@ -297,11 +304,13 @@ __device__ __forceinline__ uint32_t idesc_bf16_f32(int M, int N) {
 }
 
 // x rounded to bf16 (nearest, ties to even), kept as an f32 whose low 16 bits are zero.  Integer
-// operations only.  For finite x the difference x - round_bf16(x) is exact in f32.
+// operations only; a NaN is returned as it is (the rounding add would carry a NaN with a full
+// mantissa into the sign bit), and its high half is a bf16 NaN.  For finite x the difference
+// x - round_bf16(x) is exact in f32.
 __device__ __forceinline__ float round_bf16(float x) {
   uint32_t u = __float_as_uint(x);
   u += 0x7FFFu + ((u >> 16) & 1u);
-  return __uint_as_float(u & 0xFFFF0000u);
+  return x != x ? x : __uint_as_float(u & 0xFFFF0000u);
 }
 
 // Two bf16-valued floats (low 16 bits zero) packed as a bf16 pair: a in the low half, b in the high.

@@ -87,11 +87,6 @@ __device__ __forceinline__ void e4m3x8_to_float_cvt(const uint2 w, float (&f)[8]
 }
 
 // Packed f32 pairs (sm_100 and later: one fma.rn.f32x2 does two FMAs).
-__device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi) {
-  unsigned long long r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
 __device__ __forceinline__ void fma_f32x2(unsigned long long &acc, unsigned long long a, unsigned long long b) {
   asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
 }
@@ -574,6 +569,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
   const int hc = a.hc, ng = sm.ng, nblk = D / kDecodeDBlock;
   // (test hook 1: a count that is never reached, so that this wait runs out)
   const bool comb_ok = wait_at_least(&cnt[kCntComb], a.inject == 1 ? 2u : 1u, a);
+  bool nonfinite = false;  // an FFN output element (a sum of expert outputs) that is NaN or infinite
   for (int c = draw_ticket(&cnt[kCntTickC]); c < nblk && comb_ok; c = draw_ticket(&cnt[kCntTickC])) {
     const int d = c * kDecodeDBlock + lane;
     float po[rows][kHcMax], t[rows][kHcMax];
@@ -598,12 +594,15 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
       float f = 0.f;
 #pragma unroll 4
       for (int g = 0; g < ng; ++g) f += sm.gw[g][r] * __ldcg(a.y + ((size_t)g * kDecodeRows + r) * D + d);
+      nonfinite |= !isfinite(f);
       a.ffn_out[(size_t)r * D + d] = f;
 #pragma unroll
       for (int o = 0; o < kHcMax; ++o)
         if (o < hc) a.out_state[((size_t)r * hc + o) * D + d] = po[r][o] * f + t[r][o];
     }
   }
+
+  if (__any_sync(0xffffffffu, nonfinite) && lane == 0) atomicOr(a.status, kDevNonFinite);
 
   // ---- the last CTA out resets the counters for the next launch ----
   __threadfence();
@@ -728,10 +727,10 @@ void launch_decode(const Dims &d, const Scratch &s, const LayerDev &w, const flo
   a.eps = d.eps;
   a.wait_ns = dbg.wait_ns ? dbg.wait_ns : kSpinLimitNs;
   a.inject = dbg.inject;
-  if (!w.mx && s.dtc)  // bf16 experts: the tensor-core kernel
-    launch_decode_tc(a, d, s, w, rows, s.decode_ctas_by_rows[rows], st);
+  if (w.mx ? s.dtc_mx && w.mx_tc : s.dtc)  // the tensor-core kernel
+    launch_decode_tc(a, d, s, w, rows, w.mx ? s.decode_ctas_mx[rows] : s.decode_ctas_by_rows[rows], st);
   else
-    launch_pdl(decode_kernel_for(rows, w.mx), dim3(w.mx ? s.decode_ctas_mx[rows] : s.decode_ctas_by_rows[rows]),
+    launch_pdl(decode_kernel_for(rows, w.mx), dim3(w.mx ? s.decode_ctas_mx_cc[rows] : s.decode_ctas_by_rows[rows]),
                dim3(kDecThreads), decode_smem(w.mx), st, a);
   stage(tm, "decode", st);
 }

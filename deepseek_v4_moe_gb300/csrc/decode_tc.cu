@@ -1,5 +1,5 @@
-// Decode path (rows <= 4) on the tensor cores, for bf16 experts: the whole FFN block in one
-// persistent launch, one CTA per SM.
+// Decode path (rows <= 4) on the tensor cores: the whole FFN block in one persistent launch, one
+// CTA per SM, for bf16 experts and for MXFP8 experts.
 //
 // docs.rs "hf2q 0.1.3 .../deepseek4/ffn_forward.rs", forward_ffn_rows, every stage in order, as in
 // decode.cu: the prelude (mix CTAs, x in every CTA, router CTAs, routing by every producer) is the
@@ -41,25 +41,37 @@
 namespace moe {
 
 namespace dtc {
-constexpr int kStages = 5;                 // A ring slots of 32 KB
+constexpr int kStages = 5;                 // bf16 experts: A ring slots of 32 KB, filled by TMA
+constexpr int kStagesMx = 2;               // MXFP8 experts: A ring slots the converter warps fill
+constexpr int kCodeStages = 5;             // MXFP8 experts: code slots (two 128 x 64 code tiles) filled by TMA
+constexpr int kCodeTile = 128 * 64;        // one code tile, 8 KB
+constexpr int kCodeSlot = 2 * kCodeTile;   // 16 KB
+constexpr int kScaleSlot = 2 * 128 * 16;   // one unit's scales: [tile][row][16 bytes], one byte per 32 k
 constexpr int kTile = 128 * 64 * 2;        // one A tile, 16 KB
 constexpr int kSlotBytes = 2 * kTile;      // gate + up tile, or two down tiles
 constexpr int kBTile = 16 * 64 * 2;        // one B tile (16 rows x 64 k), 2 KB
 constexpr int kMaxChunks = 8;              // 64-wide k-chunks of one unit
 constexpr int kBSlice = kMaxChunks * kBTile;  // 16 KB: x slice, or one act slice
 constexpr int kEpiWarps = 4;
+constexpr int kConvWarps = 4;              // MXFP8 experts: warps 4-7 convert, warps 0-3 run the epilogue
 constexpr int kMmaWarp = 9;
 constexpr int kTQ = 4;                     // unit queue entries
 constexpr int kTmemCols = 64;              // two accumulator buffers of 32 columns
 constexpr size_t kSmem = (size_t)kStages * kSlotBytes + 3 * kBSlice + 1024;
+constexpr size_t kSmemMx =
+    (size_t)kStagesMx * kSlotBytes + (size_t)kCodeStages * kCodeSlot + 2 * kScaleSlot + 3 * kBSlice + 1024;
 static_assert(kSmem <= 227 * 1024 - sizeof(DecSmem) - 512, "shared memory of one CTA");
+static_assert(kSmemMx <= 227 * 1024 - sizeof(DecSmem) - 512, "shared memory of one CTA (MXFP8 experts)");
+static_assert(kEpiWarps + kConvWarps == kWorkerWarps, "the worker warps split into epilogue and converters");
 enum : int { kUnitA = 0, kUnitB = 1, kUnitEnd = 2 };
 }  // namespace dtc
 
-// Tensor maps of one launch (grid constants): the layer's expert matrices (boxes of 64 k x 128
-// rows) and the act planes (boxes of 64 k x 16 rows).
+// Tensor maps of one launch (grid constants): the layer's bf16 expert matrices (boxes of 64 k x 128
+// rows), the act planes (boxes of 64 k x 16 rows), and for MXFP8 layers the E4M3 code matrices
+// (boxes of 64 codes x 128 rows).
 struct DecodeTcMaps {
   CUtensorMap gate, up, down, gate_sh, up_sh, down_sh, act2;
+  CUtensorMap gate_q, up_q, down_q, gate_sh_q, up_sh_q, down_sh_q;
 };
 
 // Where the tensor-core kernel keeps its f64 partial sums and act planes, and how its K range is
@@ -67,11 +79,14 @@ struct DecodeTcMaps {
 struct DecodeTcArgs {
   double *acc_gu;   // [groups, 2, 4, inter]: gate and up partial sums (zero between launches)
   double *acc_y;    // [4, hidden]: route-weighted FFN output (zero between launches)
-  uint16_t *act2;   // [groups, 16, inter] bf16: rows 0-3 the hi planes of act, rows 4-7 the lo planes
+  uint16_t *act2;   // [groups, 16, inter]: bf16 experts, rows 0-3 the bf16 hi planes of act, rows 4-7
+                    // the lo planes; MXFP8 experts, rows 0-3 / 4-7 / 8-11 its three f16 planes
   int sa, ca;       // kind A: K splits of hidden and 64-wide chunks per split
   int sb, cb;       // kind B: K splits of inter and chunks per split
   int cnt_tick_a, cnt_tick_b, cnt_units;  // counter slots: per-split tickets, SwiGLU unit counts
   int n_acc_gu, n_acc_y;                  // element counts of the two accumulators
+  int mx_c;                               // MXFP8 experts: the f16 weights are code x 2^(S - 127 + mx_c)
+  float mx_unscale;                       // 2^-mx_c
 };
 
 // Counter slots of the tensor-core kernel past the d-block counters: the kind A and kind B tickets
@@ -125,27 +140,146 @@ __device__ __forceinline__ double ld_cg_f64(const double *p) {
   return v;
 }
 
-template <int ROWS>
+// ---- MXFP8 experts on the f16 tensor path ----
+// A layer whose E8M0 scales all lie within 22 binades of its largest, Smax, streams its weights as
+// A' = code x 2^(S - 127 + c) in f16, c = 134 - Smax: the largest |A'| is 448 x 2^7 < 65504, and the
+// smallest nonzero one, 2^-9 x 2^(S - Smax + 7) >= 2^-24, is still a multiple of f16's finest step;
+// with at most 4 significant bits a code, every A' is exact.  The batch rows are f16 planes too
+// (split3_f16), and the epilogue multiplies by 2^-c.  Layers outside that range, or with a NaN code
+// or scale, decode on the CUDA-core kernel.
+
+// f16 bits of 2^k (k in [-24, 15]) in both halves
+__device__ __forceinline__ uint32_t f16x2_pow2(int k) {
+  const uint32_t h = k >= -14 ? (uint32_t)(k + 15) << 10 : 1u << (k + 24);
+  return h * 0x00010001u;
+}
+// 16 E4M3 codes (element k in byte k) times 2^k (fac = f16x2_pow2(k)), as 16 f16 (elements 0-7 in o0,
+// 8-15 in o1): the hardware turns each code pair into an f16 pair, exactly, and one f16 multiply by
+// the power of two scales it, exactly (by the range argument above).
+__device__ __forceinline__ void e4m3x16_scaled_f16(const uint4 q, uint32_t fac, uint4 &o0, uint4 &o1) {
+  const unsigned words[4] = {q.x, q.y, q.z, q.w};
+  uint32_t p[8];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    unsigned h0, h1;
+    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n cvt.rn.f16x2.e4m3x2 %1, hi;\n}"
+        : "=r"(h0), "=r"(h1)
+        : "r"(words[w]));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(p[2 * w]) : "r"(h0), "r"(fac));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(p[2 * w + 1]) : "r"(h1), "r"(fac));
+  }
+  o0 = make_uint4(p[0], p[1], p[2], p[3]);
+  o1 = make_uint4(p[4], p[5], p[6], p[7]);
+}
+
+// x as three f16 planes, x ~ 2^16 p0 + 2^5 p1 + 2^-6 p2, each plane the f16 rounding of what the
+// planes before it left (the residuals are exact in f32).  For |x| < 2^32 every plane is in range and
+// |x - sum| <= 2^-33 |x| + 2^-31; beyond, p0 is infinite.  The epilogue weighs the three column
+// groups of the MMA output the same way (mx_planes).
+__device__ __forceinline__ void split3_f16(float x, uint16_t &p0, uint16_t &p1, uint16_t &p2) {
+  const __half h0 = __float2half_rn(x * 0x1p-16f);
+  const float r0 = x - __half2float(h0) * 0x1p16f;
+  const __half h1 = __float2half_rn(r0 * 0x1p-5f);
+  const float r1 = r0 - __half2float(h1) * 0x1p5f;
+  const __half h2 = __float2half_rn(r1 * 0x1p6f);
+  p0 = __half_as_ushort(h0);
+  p1 = __half_as_ushort(h1);
+  p2 = __half_as_ushort(h2);
+}
+__device__ __forceinline__ uint32_t pack_u16(uint16_t lo, uint16_t hi) { return (uint32_t)lo | ((uint32_t)hi << 16); }
+__device__ __forceinline__ void split3_f16x8(const float4 a, const float4 b, uint4 &q0, uint4 &q1, uint4 &q2) {
+  const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint16_t h[3][8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) split3_f16(v[j], h[0][j], h[1][j], h[2][j]);
+  q0 = make_uint4(pack_u16(h[0][0], h[0][1]), pack_u16(h[0][2], h[0][3]), pack_u16(h[0][4], h[0][5]),
+                  pack_u16(h[0][6], h[0][7]));
+  q1 = make_uint4(pack_u16(h[1][0], h[1][1]), pack_u16(h[1][2], h[1][3]), pack_u16(h[1][4], h[1][5]),
+                  pack_u16(h[1][6], h[1][7]));
+  q2 = make_uint4(pack_u16(h[2][0], h[2][1]), pack_u16(h[2][2], h[2][3]), pack_u16(h[2][4], h[2][5]),
+                  pack_u16(h[2][6], h[2][7]));
+}
+// batch row r's dot from a row of MMA output: bf16 experts, columns r (hi) + 4 + r (lo); MXFP8 experts,
+// the three planes' columns r, 4 + r, 8 + r, weighed as split3_f16 split them, times 2^-c
+template <bool MX>
+__device__ __forceinline__ float plane_sum(const float (&v)[16], int r, float unscale) {
+  if (MX) return unscale * (v[r] * 0x1p16f + v[4 + r] * 0x1p5f + v[8 + r] * 0x1p-6f);
+  return v[r] + v[4 + r];
+}
+
+// One unit's E8M0 scales into a scale slot ([tile][row][16 bytes]; byte b of a row is the scale of
+// the unit's 32-wide k-block b): for each of the two tiles, `rows` rows from src[t] on, `stride`
+// bytes apart, `nbytes` (<= 16) bytes a row.  The producer warp's lanes copy them with cp.async
+// where every row start is 4-byte aligned, with plain loads otherwise; each lane then arrives once
+// on `bar` (32 arrivals), the cp.async ones when the copies have landed.
+__device__ __forceinline__ void scale_copy(uint8_t *dst, const uint8_t *src0, const uint8_t *src1, int rows0,
+                                           int rows1, int stride, int nbytes, uint64_t *bar, int lane) {
+  const uint8_t *src[2] = {src0, src1};
+  const int rows[2] = {rows0, rows1};
+  const uintptr_t al = reinterpret_cast<uintptr_t>(src0) | reinterpret_cast<uintptr_t>(src1) |
+                       (uintptr_t)stride | (uintptr_t)nbytes;
+  const int w = (al & 15) == 0 ? 16 : (al & 7) == 0 ? 8 : (al & 3) == 0 ? 4 : 0;
+  if (w) {
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+      for (int n = lane; n < rows[t]; n += 32)
+        for (int b = 0; b < nbytes; b += w) {
+          const uint32_t d = smem_u32(dst + t * 2048 + n * 16 + b);
+          const uint8_t *sp = src[t] + (size_t)n * stride + b;
+          if (w == 16)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(sp) : "memory");
+          else if (w == 8)
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d), "l"(sp) : "memory");
+          else
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(sp) : "memory");
+        }
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+  } else {
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+      for (int n = lane; n < rows[t]; n += 32)
+        for (int b = 0; b < nbytes; ++b) dst[t * 2048 + n * 16 + b] = __ldg(src[t] + (size_t)n * stride + b);
+    mbar_arrive(bar);
+  }
+}
+
+template <int ROWS, bool MX>
 __global__ void __launch_bounds__(kDecThreads, 1)
     decode_tc_kernel(const __grid_constant__ DecodeTcMaps tm, DecodeArgs a, DecodeTcArgs t) {
   using namespace dtc;
   constexpr int rows = ROWS;
+  constexpr int NA = MX ? kStagesMx : kStages;  // A ring slots
   extern __shared__ uint8_t dsm_raw[];
   uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *xs = ring + (size_t)kStages * kSlotBytes;  // this CTA's slice of x as B tiles
+  uint8_t *codes = ring + (size_t)NA * kSlotBytes;                 // MXFP8: the code ring
+  uint8_t *scales = codes + (MX ? (size_t)kCodeStages * kCodeSlot : 0);  // MXFP8: two scale slots
+  uint8_t *xs = scales + (MX ? 2 * kScaleSlot : 0);  // this CTA's slice of x as B tiles
   uint8_t *as = xs + kBSlice;                          // two act slices
   __shared__ __align__(16) DecSmem sm;
-  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], tfull[2], tempty[2], afull[2], aempty[2];
+  __shared__ __align__(8) uint64_t full_bar[NA], empty_bar[NA], tfull[2], tempty[2], afull[2], aempty[2];
   __shared__ __align__(8) uint64_t xready, score_bar, tq_full[kTQ], tq_empty[kTQ], mma_done;
+  // MXFP8: code slots (TMA in, converters out) and scale slots (producer in, converters out)
+  __shared__ __align__(8) uint64_t code_full[MX ? kCodeStages : 1], code_empty[MX ? kCodeStages : 1];
+  __shared__ __align__(8) uint64_t scale_full[2], scale_empty[2];
   __shared__ int4 tq[kTQ];
   __shared__ uint32_t tmem_base;
   unsigned *cnt = a.counters;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int D = a.hidden, I = a.inter, E = a.experts;
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full_bar[s], 1);
+    for (int s = 0; s < NA; ++s) {
+      mbar_init(&full_bar[s], MX ? kConvWarps : 1);  // MXFP8: each converter warp's share of the slot
       mbar_init(&empty_bar[s], 1);
+    }
+    if (MX) {
+      for (int s = 0; s < kCodeStages; ++s) {
+        mbar_init(&code_full[s], 1);
+        mbar_init(&code_empty[s], kConvWarps);
+      }
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&scale_full[b], 32);  // one arrival per producer lane
+        mbar_init(&scale_empty[b], kConvWarps);
+      }
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -157,7 +291,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     mbar_init(&score_bar, 1);
     for (int q = 0; q < kTQ; ++q) {
       mbar_init(&tq_full[q], 1);
-      mbar_init(&tq_empty[q], 1 + kWorkerWarps);  // the MMA issuer and all eight epilogue warps
+      mbar_init(&tq_empty[q], 1 + kWorkerWarps);  // the MMA issuer and the eight worker warps
     }
     mbar_init(&mma_done, 1);
     sm.abort = 0;
@@ -184,7 +318,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     if (router) router_prefetch(a, role - a.nm);
     if (role < a.nm) mix_role<ROWS>(a, role, sm, cnt);
     float4 xr[rows][4];
-    form_x<ROWS, false>(a, sm, cnt, xr);
+    form_x<ROWS, false>(a, sm, cnt, xr);  // (x and the logits do not depend on the expert format)
     if (router) router_logits<ROWS, false>(a, sm, cnt, role - a.nm, xr);
     // this CTA's K slice of x as B tiles: batch row r's hi plane in tile row r, its lo plane in row 4 + r
     const int k0 = ka * t.ca * 64, k1 = k0 + t.ca * 64;
@@ -196,10 +330,18 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         uint8_t *tile = xs + (size_t)(kk >> 6) * kBTile;
 #pragma unroll
         for (int r = 0; r < rows; ++r) {
-          uint4 hi, lo;
-          split8(xr[r][2 * h], xr[r][2 * h + 1], hi, lo);
-          *reinterpret_cast<uint4 *>(tile + btile_offset(r, kk & 63)) = hi;
-          *reinterpret_cast<uint4 *>(tile + btile_offset(4 + r, kk & 63)) = lo;
+          if (MX) {  // three f16 planes in rows r, 4 + r, 8 + r
+            uint4 q0, q1, q2;
+            split3_f16x8(xr[r][2 * h], xr[r][2 * h + 1], q0, q1, q2);
+            *reinterpret_cast<uint4 *>(tile + btile_offset(r, kk & 63)) = q0;
+            *reinterpret_cast<uint4 *>(tile + btile_offset(4 + r, kk & 63)) = q1;
+            *reinterpret_cast<uint4 *>(tile + btile_offset(8 + r, kk & 63)) = q2;
+          } else {
+            uint4 hi, lo;
+            split8(xr[r][2 * h], xr[r][2 * h + 1], hi, lo);
+            *reinterpret_cast<uint4 *>(tile + btile_offset(r, kk & 63)) = hi;
+            *reinterpret_cast<uint4 *>(tile + btile_offset(4 + r, kk & 63)) = lo;
+          }
         }
       }
     }
@@ -224,16 +366,87 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       __syncwarp();
       if (todo == 1) mix_comb<ROWS>(a, sm, cnt);
     }
+    if (MX && warp >= kEpiWarps) {
+      // ---------------- converters (MXFP8 experts): each k-step's two 128 x 64 code tiles times
+      // their scales, as bf16 into an A ring slot in the MMA's swizzled layout.  Thread (warp w,
+      // lane l) takes rows 32 (w - 4) + 8 i + l / 4 (i = 0..3) of both tiles, 16-code chunk l % 4:
+      // its reads of a code tile are conflict-free, and so are its swizzled 16-byte stores. ----------------
+      const int cw = warp - kEpiWarps, ch = lane & 3;
+      int j = 0;  // k-steps converted
+      for (int u = 0;; ++u) {
+        const int q = u % kTQ;
+        int4 e = make_int4(kUnitEnd, 0, 0, 0);
+        int ok = 0;
+        if (lane == 0) {
+          ok = mbar_wait_bounded(&tq_full[q], (uint32_t)((u / kTQ) & 1), &sm.abort, a.status, a.wait_ns) ? 1 : 0;
+          if (ok) {
+            e = tq[q];
+            mbar_arrive(&tq_empty[q]);
+          } else {
+            atomicExch(&cnt[kCntAbort], 1u);
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        const int kind = __shfl_sync(0xffffffffu, e.x, 0) & 15;
+        if (kind == kUnitEnd) break;
+        // every lane tests each phase itself once the warp's verdict is in (its own acquire of the
+        // copies; a phase that has completed cannot complete again while this warp holds the slot)
+        if (!warp_mbar_wait(&scale_full[u & 1], (uint32_t)((u >> 1) & 1), sm, a)) break;
+        (void)mbar_try_wait(&scale_full[u & 1], (uint32_t)((u >> 1) & 1));
+        const uint8_t *sc = scales + (size_t)(u & 1) * kScaleSlot;
+        const int nc = kind == kUnitA ? t.ca : t.cb;
+        bool good = true;
+        for (int c = 0; c < nc; ++c, ++j) {
+          const int cs = j % kCodeStages, s = j % NA;
+          const uint32_t pc = (uint32_t)((j / kCodeStages) & 1), pa = (uint32_t)((j / NA) & 1) ^ 1u;
+          if (!warp_mbar_wait(&code_full[cs], pc, sm, a) || !warp_mbar_wait(&empty_bar[s], pa, sm, a)) {
+            good = false;
+            break;
+          }
+          (void)mbar_try_wait(&code_full[cs], pc);
+          const uint8_t *src = codes + (size_t)cs * kCodeSlot;
+          uint8_t *dst = ring + (size_t)s * kSlotBytes;
+          // all eight items' codes and scales first: the conversions then overlap (the stores into
+          // the A slot would otherwise order every later load behind them)
+          uint4 qv[8];
+          unsigned sv[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int tt = i >> 2, n = cw * 32 + (i & 3) * 8 + (lane >> 2);
+            qv[i] = *reinterpret_cast<const uint4 *>(src + tt * kCodeTile + n * 64 + ch * 16);
+            sv[i] = sc[tt * 2048 + n * 16 + 2 * c + (ch >> 1)];
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int tt = i >> 2, n = cw * 32 + (i & 3) * 8 + (lane >> 2);
+            uint4 o0, o1;
+            e4m3x16_scaled_f16(qv[i], f16x2_pow2((int)sv[i] - 127 + t.mx_c), o0, o1);
+            uint8_t *row = dst + tt * kTile + n * 128;
+            *reinterpret_cast<uint4 *>(row + (((2 * ch) ^ (n & 7)) << 4)) = o0;
+            *reinterpret_cast<uint4 *>(row + (((2 * ch + 1) ^ (n & 7)) << 4)) = o1;
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the MMAs read the tiles
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&full_bar[s]);
+            mbar_arrive(&code_empty[cs]);
+          }
+        }
+        if (!good) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&scale_empty[u & 1]);
+      }
+    } else {
     // ---------------- epilogue: warps 0-3 take the even units, warps 4-7 the odd ones (accumulator
     // buffer u & 1), each warp its TMEM lane quarter, so each has two units' time for its
-    // reductions ----------------
+    // reductions; with MXFP8 experts warps 0-3 take every unit ----------------
     const int quarter = warp & 3, group = warp >> 2;
     bool nonfinite = false;
     for (int u = 0;; ++u) {
       const int q = u % kTQ;
       int4 e = make_int4(kUnitEnd, 0, 0, 0);
       int ok = 0;
-      const bool mine = (u & 1) == group;
+      const bool mine = MX || (u & 1) == group;
       if (lane == 0) {
         ok = mbar_wait_bounded(&tq_full[q], (uint32_t)((u / kTQ) & 1), &sm.abort, a.status, a.wait_ns) ? 1 : 0;
         if (ok) {
@@ -262,8 +475,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         double *acc = t.acc_gu + (size_t)g * 2 * 4 * I + i;
 #pragma unroll
         for (int r = 0; r < rows; ++r) {
-          red_add_f64(acc + (size_t)r * I, (double)(v0[r] + v0[4 + r]));            // gate
-          red_add_f64(acc + (size_t)(4 + r) * I, (double)(v1[r] + v1[4 + r]));      // up
+          red_add_f64(acc + (size_t)r * I, (double)plane_sum<MX>(v0, r, t.mx_unscale));        // gate
+          red_add_f64(acc + (size_t)(4 + r) * I, (double)plane_sum<MX>(v1, r, t.mx_unscale));  // up
         }
         // the count is an acquire-release add: it publishes the warp's adds (ordered before it by the
         // warp barrier) and, in the last split, makes every other split's adds visible
@@ -282,9 +495,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             acc[(size_t)(4 + r) * I] = 0.0;
             const float v = gv * sigmoidf_(gv) * uv;
             nonfinite |= !isfinite(v);
-            const float hi = round_bf16(v), lo = round_bf16(v - hi);
-            t.act2[((size_t)g * 16 + r) * I + i] = (uint16_t)(__float_as_uint(hi) >> 16);
-            t.act2[((size_t)g * 16 + 4 + r) * I + i] = (uint16_t)(__float_as_uint(lo) >> 16);
+            if (MX) {  // three f16 planes in rows r, 4 + r, 8 + r
+              uint16_t p0, p1, p2;
+              split3_f16(v, p0, p1, p2);
+              t.act2[((size_t)g * 16 + r) * I + i] = p0;
+              t.act2[((size_t)g * 16 + 4 + r) * I + i] = p1;
+              t.act2[((size_t)g * 16 + 8 + r) * I + i] = p2;
+            } else {
+              const float hi = round_bf16(v), lo = round_bf16(v - hi);
+              t.act2[((size_t)g * 16 + r) * I + i] = (uint16_t)(__float_as_uint(hi) >> 16);
+              t.act2[((size_t)g * 16 + 4 + r) * I + i] = (uint16_t)(__float_as_uint(lo) >> 16);
+            }
           }
           asm volatile("fence.proxy.async.global;" ::: "memory");  // read back by TMA
           __syncwarp();
@@ -298,7 +519,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         for (int r = 0; r < rows; ++r) {
           if ((mask >> r) & 1) {
             const float w = sm.gw[g][r];
-            const float y0 = w * (v0[r] + v0[4 + r]), y1 = w * (v1[r] + v1[4 + r]);
+            const float y0 = w * plane_sum<MX>(v0, r, t.mx_unscale), y1 = w * plane_sum<MX>(v1, r, t.mx_unscale);
             nonfinite |= !isfinite(y0);
             red_add_f64(t.acc_y + (size_t)r * D + d0, (double)y0);
             if (d1 < D) {
@@ -315,8 +536,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
     }
     if (__any_sync(0xffffffffu, nonfinite) && lane == 0) atomicOr(a.status, kDevNonFinite);
-  }
-  else if (warp == kProducerWarp) {
+    }
+  } else if (warp == kProducerWarp) {
     // ================= producer: routing, unit claims, TMA =================
     route_setup<ROWS>(a, sm);
     route_compute<ROWS>(a, sm, true);
@@ -349,14 +570,45 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       return __shfl_sync(0xffffffffu, r, 0) != 0;
     };
     // the next free ring slot (lane 0 waits, the warp follows)
+    // (bf16 experts: the A ring; MXFP8 experts: the code ring)
+    constexpr int NF = MX ? kCodeStages : NA;
+    uint64_t *fill_full = MX ? code_full : full_bar, *fill_empty = MX ? code_empty : empty_bar;
     auto slot = [&]() -> int {
-      const int s = j % kStages;
+      const int s = j % NF;
       int r = 1;
       if (lane == 0) {
-        r = mbar_wait_backoff(&empty_bar[s], (uint32_t)((j / kStages) & 1) ^ 1u, &sm.abort, a.status, a.wait_ns) ? 1 : 0;
+        r = mbar_wait_backoff(&fill_empty[s], (uint32_t)((j / NF) & 1) ^ 1u, &sm.abort, a.status, a.wait_ns) ? 1 : 0;
         if (!r) atomicExch(&cnt[kCntAbort], 1u);
       }
       return __shfl_sync(0xffffffffu, r, 0) ? s : -1;
+    };
+    // one k-step's two tiles into slot s: tile 0 from m0 at (kc, r0), tile 1 from m1 at (kc, r1)
+    auto fill = [&](int s, const CUtensorMap *m0, const CUtensorMap *m1, int kc, int r0, int r1) {
+      if (lane == 0) {
+        const int tb = MX ? kCodeTile : kTile;
+        uint8_t *dst = MX ? codes + (size_t)s * kCodeSlot : ring + (size_t)s * kSlotBytes;
+        mbar_arrive_expect_tx(&fill_full[s], 2u * tb);
+        tma_load_2d_hint(dst, m0, &fill_full[s], kc, r0, pol);
+        tma_load_2d_hint(dst + tb, m1, &fill_full[s], kc, r1, pol);
+      }
+      __syncwarp();
+    };
+    // MXFP8: the scales of the unit just handed into its scale slot, once the converters are done
+    // with the unit two before it
+    auto unit_scales = [&](const uint8_t *s0, const uint8_t *s1, int rows0, int rows1, int stride,
+                           int nbytes) -> bool {
+      const int us = u - 1;
+      int r = 1;
+      if (lane == 0) {
+        r = mbar_wait_backoff(&scale_empty[us & 1], (uint32_t)((us >> 1) & 1) ^ 1u, &sm.abort, a.status, a.wait_ns)
+                ? 1
+                : 0;
+        if (!r) atomicExch(&cnt[kCntAbort], 1u);
+      }
+      if (!__shfl_sync(0xffffffffu, r, 0)) return false;
+      scale_copy(scales + (size_t)(us & 1) * kScaleSlot, s0, s1, rows0, rows1, stride, nbytes, &scale_full[us & 1],
+                 lane);
+      return true;
     };
     // The units of this CTA's two K splits, from two queues in group order: kind A (group, 128-row
     // block of inter), then, once that queue is used up, kind B (group, pair of 128-row blocks of
@@ -403,22 +655,24 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           ok = false;
           break;
         }
-        const CUtensorMap *md = g == 0 ? &tm.down_sh : &tm.down;
+        const CUtensorMap *md = MX ? (g == 0 ? &tm.down_sh_q : &tm.down_q) : (g == 0 ? &tm.down_sh : &tm.down);
         const int row = (g == 0 ? 0 : e * D) + blk * 256;
+        if (MX) {
+          const int st = I / 32;
+          const uint8_t *s0 = (g == 0 ? a.down_sh_s : a.down_s) + (size_t)row * st + kbs * t.cb * 2;
+          if (!unit_scales(s0, s0 + (size_t)128 * st, min(128, D - blk * 256), max(0, min(128, D - blk * 256 - 128)),
+                           st, 2 * t.cb)) {
+            ok = false;
+            break;
+          }
+        }
         for (int c = 0; c < t.cb; ++c, ++j) {
           const int s = slot();
           if (s < 0) {
             ok = false;
             break;
           }
-          if (lane == 0) {
-            uint8_t *dst = ring + (size_t)s * kSlotBytes;
-            const int kc = (kbs * t.cb + c) * 64;
-            mbar_arrive_expect_tx(&full_bar[s], 2u * kTile);
-            tma_load_2d_hint(dst, md, &full_bar[s], kc, row, pol);
-            tma_load_2d_hint(dst + kTile, md, &full_bar[s], kc, row + 128, pol);
-          }
-          __syncwarp();
+          fill(s, md, md, (kbs * t.cb + c) * 64, row, row + 128);
         }
         continue;
       }
@@ -440,22 +694,25 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         ok = false;
         break;
       }
-      const CUtensorMap *mg = g == 0 ? &tm.gate_sh : &tm.gate, *mu = g == 0 ? &tm.up_sh : &tm.up;
+      const CUtensorMap *mg = MX ? (g == 0 ? &tm.gate_sh_q : &tm.gate_q) : (g == 0 ? &tm.gate_sh : &tm.gate);
+      const CUtensorMap *mu = MX ? (g == 0 ? &tm.up_sh_q : &tm.up_q) : (g == 0 ? &tm.up_sh : &tm.up);
       const int row = (g == 0 ? 0 : e * I) + blk * 128;
+      if (MX) {
+        const int st = D / 32;
+        const size_t off = (size_t)row * st + ka * t.ca * 2;
+        if (!unit_scales((g == 0 ? a.gate_sh_s : a.gate_s) + off, (g == 0 ? a.up_sh_s : a.up_s) + off, 128, 128, st,
+                         2 * t.ca)) {
+          ok = false;
+          break;
+        }
+      }
       for (int c = 0; c < t.ca; ++c, ++j) {
         const int s = slot();
         if (s < 0) {
           ok = false;
           break;
         }
-        if (lane == 0) {
-          uint8_t *dst = ring + (size_t)s * kSlotBytes;
-          const int kc = (ka * t.ca + c) * 64;
-          mbar_arrive_expect_tx(&full_bar[s], 2u * kTile);
-          tma_load_2d_hint(dst, mg, &full_bar[s], kc, row, pol);
-          tma_load_2d_hint(dst + kTile, mu, &full_bar[s], kc, row, pol);
-        }
-        __syncwarp();
+        fill(s, mg, mu, (ka * t.ca + c) * 64, row, row);
       }
     }
     (void)hand(kUnitEnd, 0, 0, 0);
@@ -464,9 +721,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     // copies still in flight (after a timeout) land before the CTA may leave
     if (lane == 0) {
       int no_abort = 0;
-      for (int s = 0; s < kStages; ++s) {
-        const int n = j / kStages + (s < j % kStages ? 1 : 0);
-        if (n > 0) (void)mbar_wait_bounded(&full_bar[s], (uint32_t)((n - 1) & 1), &no_abort, a.status, a.wait_ns);
+      for (int s = 0; s < NF; ++s) {
+        const int n = j / NF + (s < j % NF ? 1 : 0);
+        if (n > 0) (void)mbar_wait_bounded(&fill_full[s], (uint32_t)((n - 1) & 1), &no_abort, a.status, a.wait_ns);
       }
       for (int b = 0; b < 2; ++b) {
         const int n = nab / 2 + (b < nab % 2 ? 1 : 0);
@@ -474,11 +731,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
       if (sp.in_flight) (void)mbar_wait_bounded(&score_bar, sp.phase, &no_abort, a.status, a.wait_ns);
     }
+    if (MX) asm volatile("cp.async.wait_all;" ::: "memory");  // this lane's scale copies
     __syncwarp();
   } else if (warp == kMmaWarp && lane == 0) {
     // ================= MMA issuer =================
     int ok = mbar_wait_bounded(&xready, 0u, &sm.abort, a.status, a.wait_ns) ? 1 : 0;
-    const uint32_t idesc = idesc_bf16_f32(128, 16);
+    const uint32_t idesc = MX ? idesc_f16_f32(128, 16) : idesc_bf16_f32(128, 16);
     int j = 0, na = 0;
     for (int u = 0; ok; ++u) {
       const int q = u % kTQ;
@@ -498,8 +756,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       const int nc = kind == kUnitA ? t.ca : t.cb;
       const uint32_t bbase = smem_u32(kind == kUnitA ? xs : as + (size_t)ab * kBSlice);
       for (int c = 0; c < nc; ++c, ++j) {
-        const int s = j % kStages;
-        if (!mbar_wait_bounded(&full_bar[s], (uint32_t)((j / kStages) & 1), &sm.abort, a.status, a.wait_ns)) {
+        const int s = j % NA;
+        if (!mbar_wait_bounded(&full_bar[s], (uint32_t)((j / NA) & 1), &sm.abort, a.status, a.wait_ns)) {
           ok = 0;
           break;
         }
@@ -595,24 +853,34 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 // ---------------------------------------------------------------------------------------------
 
 using DecodeTcKernel = void (*)(DecodeTcMaps, DecodeArgs, DecodeTcArgs);
-static DecodeTcKernel decode_tc_kernel_for(int rows) {
-  return rows == 1 ? decode_tc_kernel<1> : rows == 2 ? decode_tc_kernel<2> : rows == 3 ? decode_tc_kernel<3>
-                                                                                        : decode_tc_kernel<4>;
+static DecodeTcKernel decode_tc_kernel_for(int rows, bool mx) {
+  if (mx)
+    return rows == 1 ? decode_tc_kernel<1, true>
+           : rows == 2 ? decode_tc_kernel<2, true>
+           : rows == 3 ? decode_tc_kernel<3, true>
+                       : decode_tc_kernel<4, true>;
+  return rows == 1 ? decode_tc_kernel<1, false>
+         : rows == 2 ? decode_tc_kernel<2, false>
+         : rows == 3 ? decode_tc_kernel<3, false>
+                     : decode_tc_kernel<4, false>;
 }
+static size_t decode_tc_smem(bool mx) { return mx ? dtc::kSmemMx : dtc::kSmem; }
 
 cudaError_t decode_tc_configure() {
-  for (int r = 1; r <= kDecodeRows; ++r) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(decode_tc_kernel_for(r), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dtc::kSmem);
-    if (e != cudaSuccess) return e;
-  }
+  for (int mx = 0; mx < 2; ++mx)
+    for (int r = 1; r <= kDecodeRows; ++r) {
+      const cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel_for(r, mx != 0),
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)decode_tc_smem(mx != 0));
+      if (e != cudaSuccess) return e;
+    }
   return cudaSuccess;
 }
 
-int decode_tc_resident_ctas(int rows, int num_sms) {
+int decode_tc_resident_ctas(int rows, int num_sms, bool mx) {
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_tc_kernel_for(rows), kDecThreads, dtc::kSmem) !=
-      cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_tc_kernel_for(rows, mx), kDecThreads,
+                                                    decode_tc_smem(mx)) != cudaSuccess)
     return 0;
   return per_sm * num_sms;
 }
@@ -642,6 +910,12 @@ void launch_decode_tc(const DecodeArgs &a, const Dims &d, const Scratch &s, cons
   m.up_sh = w.tm_up_sh;
   m.down_sh = w.tm_down_sh;
   m.act2 = s.tm_dtc_act2;
+  m.gate_q = w.tm_gate_q;
+  m.up_q = w.tm_up_q;
+  m.down_q = w.tm_down_q;
+  m.gate_sh_q = w.tm_gate_sh_q;
+  m.up_sh_q = w.tm_up_sh_q;
+  m.down_sh_q = w.tm_down_sh_q;
   DecodeTcArgs t;
   t.acc_gu = s.dtc_acc_gu;
   t.acc_y = s.dtc_acc_y;
@@ -653,7 +927,9 @@ void launch_decode_tc(const DecodeArgs &a, const Dims &d, const Scratch &s, cons
   t.cnt_units = t.cnt_tick_b + kMaxSplits * 32;
   t.n_acc_gu = (d.top_k * kDecodeRows + 1) * 2 * 4 * d.inter;
   t.n_acc_y = 4 * d.hidden;
-  launch_pdl(decode_tc_kernel_for(rows), dim3(grid), dim3(kDecThreads), dtc::kSmem, st, m, a, t);
+  t.mx_c = w.mx_c;
+  t.mx_unscale = ldexpf(1.f, -w.mx_c);
+  launch_pdl(decode_tc_kernel_for(rows, w.mx), dim3(grid), dim3(kDecThreads), decode_tc_smem(w.mx), st, m, a, t);
 }
 
 }  // namespace moe

@@ -461,4 +461,46 @@ void launch_mxfp8_to_bf16(const uint8_t *q, const uint8_t *s, uint16_t *dst, siz
   mxfp8_to_bf16_kernel<<<1024, 256, 0, st>>>(q, s, dst, n);
 }
 
+// Sets *flag when one of the n E4M3 codes (n a multiple of 16) is a NaN (S.1111.111): a byte whose
+// low seven bits are all ones carries into its top bit when 1 is added to them.
+__global__ void e4m3_nan_scan_kernel(const uint8_t *__restrict__ q, size_t n, int *flag) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x * 16;
+  unsigned any = 0u;
+  for (size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 16; i < n; i += stride) {
+    const uint4 w = *reinterpret_cast<const uint4 *>(q + i);
+    any |= ((w.x & 0x7F7F7F7Fu) + 0x01010101u) | ((w.y & 0x7F7F7F7Fu) + 0x01010101u) |
+           ((w.z & 0x7F7F7F7Fu) + 0x01010101u) | ((w.w & 0x7F7F7F7Fu) + 0x01010101u);
+  }
+  if (__any_sync(0xffffffffu, (any & 0x80808080u) != 0u) && (threadIdx.x & 31) == 0) atomicOr(flag, 1);
+}
+void launch_e4m3_nan_scan(const uint8_t *q, size_t n, int *flag, cudaStream_t st) {
+  e4m3_nan_scan_kernel<<<1024, 256, 0, st>>>(q, n, flag);
+}
+
+// The smallest and the largest of n E8M0 scale codes (n a multiple of 16) into mm[0] and mm[1]
+// (atomic min / max; mm[0] starts at 255 and mm[1] at 0).
+__global__ void e8m0_range_kernel(const uint8_t *__restrict__ sc, size_t n, unsigned *mm) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x * 16;
+  unsigned lo = 0xFFFFFFFFu, hi = 0u;  // four byte lanes each
+  for (size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 16; i < n; i += stride) {
+    const uint4 w = *reinterpret_cast<const uint4 *>(sc + i);
+    lo = __vminu4(__vminu4(lo, w.x), __vminu4(w.y, __vminu4(w.z, w.w)));
+    hi = __vmaxu4(__vmaxu4(hi, w.x), __vmaxu4(w.y, __vmaxu4(w.z, w.w)));
+  }
+  unsigned l = min(min(lo & 0xFFu, (lo >> 8) & 0xFFu), min((lo >> 16) & 0xFFu, lo >> 24));
+  unsigned h = max(max(hi & 0xFFu, (hi >> 8) & 0xFFu), max((hi >> 16) & 0xFFu, hi >> 24));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    l = min(l, __shfl_xor_sync(0xffffffffu, l, o));
+    h = max(h, __shfl_xor_sync(0xffffffffu, h, o));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicMin(&mm[0], l);
+    atomicMax(&mm[1], h);
+  }
+}
+void launch_e8m0_range(const uint8_t *sc, size_t n, unsigned *mm, cudaStream_t st) {
+  e8m0_range_kernel<<<512, 256, 0, st>>>(sc, n, mm);
+}
+
 }  // namespace moe

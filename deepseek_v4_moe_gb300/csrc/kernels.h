@@ -69,13 +69,15 @@ struct Scratch {
   float *y_dec;           // [groups, 4, hidden]
   unsigned *dec_counters; // the decode kernel's tickets and completion counters (zero between launches)
   int decode_ctas_by_rows[5];  // co-resident CTAs of the persistent decode kernel, per row count
-  int decode_ctas_mx[5];       // the same for its MXFP8-expert instances (CUDA-core kernel)
+  int decode_ctas_mx[5];       // the same for its MXFP8-expert instances
+  int decode_ctas_mx_cc[5];    // the CUDA-core kernel's MXFP8 instances (layers with NaN codes)
   // decode on the tensor cores (bf16 experts)
   double *dtc_acc_gu;          // [groups, 2, 4, inter] gate and up partial sums (zero between launches)
   double *dtc_acc_y;           // [4, hidden] the FFN output (zero between launches)
   uint16_t *dtc_act2;          // [groups, 16, inter] bf16: act hi planes (rows 0-3), lo planes (rows 4-7)
   CUtensorMap tm_dtc_act2;     // over dtc_act2, boxes of 64 x 16 rows
-  bool dtc;                    // the tensor-core decode kernel fits this configuration
+  bool dtc;                    // the tensor-core decode kernel fits this configuration (bf16 experts)
+  bool dtc_mx;                 // ... and its MXFP8 instance
   // rows > 4 path
   int *counts;            // [experts] routed slots per expert (zero between launches)
   int *offsets;           // [experts + 2]
@@ -137,6 +139,11 @@ struct LayerDev {
   // MXFP8 experts (moe_ffn_set_mxfp8_experts): E4M3 codes in the bf16 layouts, E8M0 scales [rows, K/32]
   const uint8_t *gate_q, *up_q, *down_q, *gate_sh_q, *up_sh_q, *down_sh_q;
   const uint8_t *gate_s, *up_s, *down_s, *gate_sh_s, *up_sh_s, *down_sh_s;
+  // tensor maps over the code matrices for the tensor-core decode (boxes of 128 rows x 64 codes)
+  CUtensorMap tm_gate_q, tm_up_q, tm_down_q, tm_gate_sh_q, tm_up_sh_q, tm_down_sh_q;
+  bool mx_tc;         // MXFP8: no NaN code or scale and every scale within 22 binades of the largest,
+                      // so the tensor-core decode's f16 weights are exact (else the CUDA-core kernel)
+  int mx_c;           // MXFP8: 134 - the largest scale code (the f16 weights are code x 2^(S - 127 + mx_c))
   bool mx;            // the experts are the MXFP8 ones (decode streams them; prefill their bf16 expansion)
   bool has_experts;   // some expert weights are registered (bf16 at init, or MXFP8 later)
   bool has_weights;
@@ -170,9 +177,11 @@ int decode_resident_ctas(int hidden, int rows, int num_sms, bool mx);
 // decode_tc.cu
 int decode_tc_counter_count(const Dims &d);
 cudaError_t decode_tc_configure();
-int decode_tc_resident_ctas(int rows, int num_sms);
+int decode_tc_resident_ctas(int rows, int num_sms, bool mx);
 bool decode_tc_fits(const Dims &d, int grid);
 void launch_mxfp8_to_bf16(const uint8_t *q, const uint8_t *s, uint16_t *dst, size_t n, cudaStream_t st);
+void launch_e4m3_nan_scan(const uint8_t *q, size_t n, int *flag, cudaStream_t st);
+void launch_e8m0_range(const uint8_t *sc, size_t n, unsigned *mm, cudaStream_t st);
 // dispatch.cu
 void launch_dispatch(const Dims &d, const Scratch &s, int rows, cudaStream_t st, StageTimer *tm);
 void launch_hc_post(const Dims &d, const float *f, const float *state, const float *post, const float *comb,

@@ -164,6 +164,21 @@ static bool make_tmap_bf16(CUtensorMap *m, const void *base, uint64_t inner, uin
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D byte matrix [outer, inner] (E4M3 codes), row-major; boxes of 128 rows x 64 bytes, unswizzled
+// (the converter warps of the tensor-core decode read them row by row); rows past `outer` read as
+// zeros.
+static bool make_tmap_u8(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename T>
 static bool dalloc(moe_ffn_handle *h, T **p, size_t count) {
   void *q = nullptr;
@@ -298,22 +313,25 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
     for (int r = 1; r <= moe::kDecodeRows; ++r) {
       int &n = mx ? s.decode_ctas_mx[r] : s.decode_ctas_by_rows[r];
       // bf16 experts stream on the tensor cores (one CTA per SM) where the K splits fit the grid
-      const int tc = mx ? 0 : moe::decode_tc_resident_ctas(r, h->num_sms);
-      s.dtc = !mx ? tc > 0 && moe::decode_tc_fits(d, tc) : s.dtc;
-      n = !mx && s.dtc ? tc : moe::decode_resident_ctas(d.hidden, r, h->num_sms, mx != 0);
-      if (n <= 0) {
+      const int tc = moe::decode_tc_resident_ctas(r, h->num_sms, mx != 0);
+      bool &fits = mx ? s.dtc_mx : s.dtc;
+      fits = tc > 0 && moe::decode_tc_fits(d, tc);
+      const int cc = moe::decode_resident_ctas(d.hidden, r, h->num_sms, mx != 0);
+      n = fits ? tc : cc;
+      if (mx) s.decode_ctas_mx_cc[r] = cc;
+      if (n <= 0 || cc <= 0) {
         free_all(h);
         delete h;
         return fail(nullptr, MOE_FFN_ERR_CUDA, "the decode kernel does not fit on an SM");
       }
       // its prelude roles are claimed by the first CTAs to arrive; at least one CTA must be left
-      if (n <= moe::decode_mix_ctas(d.hc, d.hidden) + moe::decode_router_ctas(d.experts)) {
+      if ((n < cc ? n : cc) <= moe::decode_mix_ctas(d.hc, d.hidden) + moe::decode_router_ctas(d.experts)) {
         free_all(h);
         delete h;
         return fail(nullptr, MOE_FFN_ERR_CUDA, "too few co-resident CTAs (%d) for the decode kernel's roles", n);
       }
     }
-  s.decode_ctas_by_rows[0] = s.decode_ctas_mx[0] = 0;
+  s.decode_ctas_by_rows[0] = s.decode_ctas_mx[0] = s.decode_ctas_mx_cc[0] = 0;
   h->layers.resize(cfg->n_layers);
   h->attn.resize(cfg->n_layers);
   for (LayerDev &A : h->attn) std::memset(&A, 0, sizeof A);
@@ -628,6 +646,36 @@ extern "C" int moe_ffn_set_mxfp8_experts(moe_ffn_handle *h, int32_t layer, const
   L.up_sh_s = w->up_sh_scale;
   L.down_sh_q = w->down_sh;
   L.down_sh_s = w->down_sh_scale;
+  {
+    // the tensor-core decode streams the weights as f16 (code x 2^(S - 127 + c)); that is exact when
+    // no code or scale is NaN and every scale lies within 22 binades of the largest
+    unsigned *scan = nullptr;  // [0] NaN code found, [1] smallest scale, [2] largest scale
+    unsigned host[3] = {0u, 255u, 0u};
+    const size_t n_exp = (size_t)c.experts * c.inter * c.hidden, n_sh = (size_t)c.inter * c.hidden;
+    cudaError_t e = cudaMalloc(&scan, sizeof host);
+    if (e == cudaSuccess) e = cudaMemcpy(scan, host, sizeof host, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) {
+      const uint8_t *q[6] = {L.gate_q, L.up_q, L.down_q, L.gate_sh_q, L.up_sh_q, L.down_sh_q};
+      const uint8_t *sc[6] = {L.gate_s, L.up_s, L.down_s, L.gate_sh_s, L.up_sh_s, L.down_sh_s};
+      for (int i = 0; i < 6; ++i) {
+        const size_t n = i < 3 ? n_exp : n_sh;
+        moe::launch_e4m3_nan_scan(q[i], n, reinterpret_cast<int *>(scan), 0);
+        moe::launch_e8m0_range(sc[i], n / 32, scan + 1, 0);
+      }
+      e = cudaMemcpy(host, scan, sizeof host, cudaMemcpyDeviceToHost);
+    }
+    if (scan) cudaFree(scan);
+    if (e != cudaSuccess) return fail(h, MOE_FFN_ERR_CUDA, "set_mxfp8_experts: %s", cudaGetErrorString(e));
+    L.mx_tc = host[0] == 0u && host[2] != 255u && host[2] - host[1] <= 22u;
+    L.mx_c = 134 - (int)host[2];
+  }
+  {
+    const uint64_t E = h->dims.experts, I = h->dims.inter, D = h->dims.hidden;
+    if (!make_tmap_u8(&L.tm_gate_q, L.gate_q, D, E * I) || !make_tmap_u8(&L.tm_up_q, L.up_q, D, E * I) ||
+        !make_tmap_u8(&L.tm_down_q, L.down_q, I, E * D) || !make_tmap_u8(&L.tm_gate_sh_q, L.gate_sh_q, D, I) ||
+        !make_tmap_u8(&L.tm_up_sh_q, L.up_sh_q, D, I) || !make_tmap_u8(&L.tm_down_sh_q, L.down_sh_q, I, D))
+      return fail(h, MOE_FFN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the MXFP8 codes of layer %d", layer);
+  }
   if (c.max_rows > moe::kDecodeRows) {  // the tensor-core path reads an exact bf16 expansion
     const size_t E = c.experts, I = c.inter, D = c.hidden, n_exp = E * I * D, n_sh = I * D;
     if (!L.mx_bf16 && !dalloc(h, &L.mx_bf16, 3 * (n_exp + n_sh)))

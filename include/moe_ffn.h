@@ -60,7 +60,7 @@ extern "C" {
 /* Device-side status bits (moe_ffn_status returns their OR since the previous call). */
 #define MOE_FFN_DEV_TOKEN_RANGE 0x1   /* hash layer: token id outside [0, vocab); its slots masked */
 #define MOE_FFN_DEV_ROUTE_RANGE 0x2   /* a routed expert index outside [0, experts); slot masked */
-#define MOE_FFN_DEV_NONFINITE 0x4     /* a router logit, or (rows > 4) a SwiGLU or expert output, was NaN or infinite */
+#define MOE_FFN_DEV_NONFINITE 0x4     /* a router logit, a SwiGLU output or an expert's output was NaN or infinite */
 #define MOE_FFN_DEV_TIMEOUT 0x8       /* a bounded wait inside a kernel gave up (kernel returned) */
 
 /* Shapes and constants of the block (the page's cfg fields).  Supported:
@@ -106,10 +106,9 @@ typedef struct moe_ffn_handle moe_ffn_handle;
 
 /* Creates a handle on the current CUDA device.  Validates the config (BAD_CONFIG) and, for every
  * layer with weights, the routing source its layer type needs (NO_ROUTING_SOURCE) and pointer
- * alignment (ALIGNMENT).  Allocates the scratch for max_rows and, per layer with weights, an fp16
- * copy of the routed and shared expert matrices (the tensor-core operands of the rows > 4 path;
- * fp16 holds every bf16 value of magnitude >= 2^-14 exactly): 2 * (experts+1) * 3 * inter *
- * hidden bytes per layer.  Synchronous.  On failure *out is NULL and nothing stays allocated. */
+ * alignment (ALIGNMENT).  Allocates the scratch for max_rows; the weights are read in place (no
+ * copies: the tensor-core kernels take the bf16 matrices as they are).  Synchronous.  On failure
+ * *out is NULL and nothing stays allocated. */
 int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weights *layers, moe_ffn_handle **out);
 
 /* Enqueues the block for `rows` tokens of `layer` on `stream` (a cudaStream_t; NULL = legacy
@@ -225,9 +224,8 @@ typedef struct moe_ffn_hc_weights {
 } moe_ffn_hc_weights;
 
 /* Registers the attention sublayer's HC weights for `layer`; they must stay valid for the life of
- * the handle, and a later call for the same layer replaces them.  On a handle with max_rows > 4
- * this also makes an fp16 copy of hc_fn (the tensor-core operand of the many-row path,
- * 32 * hc * hidden * 2 bytes, owned by the handle).  Synchronous.  Returns MOE_FFN_OK,
+ * the handle, and a later call for the same layer replaces them (hc_fn is read in place, also by
+ * the tensor-core mix of the many-row path).  Synchronous.  Returns MOE_FFN_OK,
  * LAYER_RANGE, NULL_PTR, ALIGNMENT, NO_MEMORY or CUDA. */
 int moe_ffn_set_attn_hc(moe_ffn_handle *h, int32_t layer, const moe_ffn_hc_weights *w);
 
@@ -260,9 +258,13 @@ int moe_ffn_hc_post(moe_ffn_handle *h, const float *f, const float *state, const
  * mode here reads them as MXFP8 (OCP Microscaling): E4M3 codes (1 sign, 4 exponent bits with bias
  * 7, 3 mantissa bits; no infinities) in the bf16 matrices' layouts, and one E8M0 scale (2^(s-127))
  * per 32 consecutive elements of a row, so element k of a row is value(code) * 2^(scale[k/32] - 127).
- * The rest of the block is unchanged.  Rows <= 4 stream the codes and scales (half the bytes of
- * bf16); larger batches run the tensor-core path on fp16 copies made at registration, exact when
- * every element is an f16 value (scales 2^-15 .. 2^7). */
+ * The rest of the block is unchanged.  Rows <= 4 stream the codes and scales (about half the bytes
+ * of bf16).  The decode kernel turns each tile into exact f16 weights in shared memory for the
+ * tensor cores (the batch rows go in as three f16 planes: values of magnitude 2^32 and above come
+ * out infinite); that needs every scale of the layer within 22 binades of its largest and no NaN
+ * code or scale, and a layer outside that decodes on the CUDA-core kernel instead.  Larger batches
+ * run the tensor-core path on a bf16 expansion made at registration, exact wherever code x scale
+ * is a normal bf16. */
 typedef struct moe_ffn_mxfp8_experts {
   const uint8_t *gate_exps, *gate_exps_scale;  /* E4M3 [experts, inter, hidden], E8M0 [experts, inter, hidden/32] */
   const uint8_t *up_exps, *up_exps_scale;      /* the same layouts */
@@ -274,9 +276,9 @@ typedef struct moe_ffn_mxfp8_experts {
 
 /* Makes `layer` run on these MXFP8 experts (DEVICE pointers, caller-owned, 16-byte aligned, valid
  * for the life of the handle), in place of any bf16 experts given at init; a later call replaces
- * them.  The layer must have its other weights from moe_ffn_init.  On a handle with max_rows > 4
- * this fills the fp16 copies the tensor-core path reads (allocating them if init did not).
- * Synchronous.  Returns MOE_FFN_OK, LAYER_RANGE, NO_WEIGHTS, NULL_PTR, ALIGNMENT, NO_MEMORY or CUDA. */
+ * them.  The layer must have its other weights from moe_ffn_init.  Reads every code and scale once
+ * on the device (NaN codes, the range of the scales).  On a handle with max_rows > 4 this also fills the bf16 expansion the
+ * tensor-core path reads (allocating it on first use).  Synchronous.  Returns MOE_FFN_OK, LAYER_RANGE, NO_WEIGHTS, NULL_PTR, ALIGNMENT, NO_MEMORY or CUDA. */
 int moe_ffn_set_mxfp8_experts(moe_ffn_handle *h, int32_t layer, const moe_ffn_mxfp8_experts *w);
 
 /* Test hook: failure detection without a GPU fault.  Every wait inside the kernels is bounded; on

@@ -44,6 +44,74 @@ def test_mx_tiny_against_oracle(rows):
     compare_state(got, oracle.forward_ffn_rows(case, stages=st)["out_state"])
 
 
+# hidden 640: K splits of 5 chunks, so a row's scales for one split are 10 bytes at a 2-byte offset
+# (copied with plain loads), and the last pair of 128-row down tiles is half past the matrix; inter 384:
+# 12 scale bytes a row (4-byte copies)
+RAGGED = replace(TINY, hidden=640, inter=384, shared_inter=384, seed=31)
+
+
+@pytest.mark.parametrize("rows", [1, 3])
+def test_mx_decode_ragged_splits(rows):
+    case, st, got, idx, status = _run(RAGGED, rows)
+    assert status == 0
+    assert np.array_equal(idx, st["indices"])
+    compare_state(got, oracle.forward_ffn_rows(case, stages=st)["out_state"])
+
+
+@pytest.mark.parametrize("what", ["code", "scale"])
+@pytest.mark.parametrize("rows", [1, 4, 40])
+def test_mx_nan_weight(what, rows):
+    # one NaN element in the shared expert's gate: its act entry is NaN, so is every element of the
+    # FFN output and of the new state, and the status reports it.  At rows <= 4 a NaN code or a NaN
+    # scale (E8M0 255) sends the layer to the CUDA-core decode kernel (the tensor-core one streams
+    # f16 weights, which hold neither); 40 rows run the tensor-core GEMMs, whose act planes must
+    # carry the NaN too.
+    from deepseek_v4_moe_gb300 import MoeFFN, config_from
+    case, st = tie_free(replace(TINY, rows=rows, name=f"c0_mx_nan_{what}_r{rows}"))
+    c = case.cfg
+    dev = upload(case)
+    mx = upload_mx(case)
+    if what == "code":
+        mx["gate_sh"][3, 17] = 0x7F
+    else:
+        mx["gate_sh_scale"][5, 1] = 0xFF
+    m = MoeFFN(config_from(c, max_rows=rows), {c.layer: dict(dev["weights"])})
+    m.set_mxfp8_experts(c.layer, mx)
+    out = m.forward(dev["state"], dev["token_ids"], c.layer)
+    torch.cuda.synchronize()
+    got, status = out.cpu().numpy(), m.status()
+    m.close()
+    assert status & 0x4
+    assert np.isnan(got).all()
+
+
+@pytest.mark.parametrize("span", [22, 23])
+def test_mx_decode_scale_span(span):
+    # one scale of the shared gate moved `span` binades below the layer's largest: at 22 the f16
+    # weights of the tensor-core decode are still exact (the smallest code times it is 2^-24 in f16);
+    # at 23 the layer decodes on the CUDA-core kernel.  Both match the oracle on the same scales.
+    from deepseek_v4_moe_gb300 import MoeFFN, config_from
+    case, st = tie_free(replace(TINY, rows=2, name=f"c0_mx_span{span}"))
+    c = case.cfg
+    dev = upload(case)
+    mx = upload_mx(case)
+    smax = max(int(v.max()) for k, v in mx.items() if k.endswith("_scale"))
+    q, sc = case.shared_mx("gate")
+    sc = sc.copy()
+    sc[7, 3] = smax - span
+    mx["gate_sh_scale"][7, 3] = smax - span
+    orig = case.shared_mx
+    case.shared_mx = lambda which: (q, sc) if which == "gate" else orig(which)
+    m = MoeFFN(config_from(c, max_rows=c.rows), {c.layer: dict(dev["weights"])})
+    m.set_mxfp8_experts(c.layer, mx)
+    out = m.forward(dev["state"], dev["token_ids"], c.layer)
+    torch.cuda.synchronize()
+    got, status = out.cpu().numpy(), m.status()
+    m.close()
+    assert status == 0
+    compare_state(got, oracle.forward_ffn_rows(case, stages=st)["out_state"])
+
+
 @pytest.mark.parametrize("rows", [1, 40])
 def test_mx_without_bf16_experts(rows):
     case, st, got, idx, status = _run(TINY, rows, with_bf16=False)
