@@ -27,8 +27,14 @@
 // Every CTA draws all of its kind A units before its first kind B unit, and a kind B unit waits only
 // for kind A work, which running CTAs hold: every wait ends.
 //
+// MXFP8 experts: the producer streams the E4M3 code tiles by TMA (64-byte swizzle) into a code ring and
+// copies each unit's E8M0 scales with cp.async; warps 4-7 turn every k-step's codes into exact f16
+// weights (see e4m3x16_scaled_f16) and store them into an A slot in TMEM, which the MMAs read in
+// place of a shared-memory A tile (so the widened weights never pass through shared memory).  The
+// batch rows are then three f16 planes (split3_f16) instead of the bf16 hi / lo pair.
+//
 // Roles: warps 0-7 run the prelude, then the epilogue (two groups of four alternating units, one TMEM
-// lane quarter per warp);
+// lane quarter per warp; MXFP8: warps 0-3 take every unit and warps 4-7 convert);
 // warp 8 is the producer (routing, unit claims, TMA), warp 9 the MMA issuer and TMEM owner.  Phase C
 // (per 32-wide block of hidden: ffn_out and hc_post) is shared by all warps at the end.  Waits are
 // bounded (1 s); after a timeout every later wait fails at once, the producer waits (bounded) for
@@ -42,8 +48,9 @@ namespace moe {
 
 namespace dtc {
 constexpr int kStages = 5;                 // bf16 experts: A ring slots of 32 KB, filled by TMA
-constexpr int kStagesMx = 2;               // MXFP8 experts: A ring slots the converter warps fill
-constexpr int kCodeStages = 5;             // MXFP8 experts: code slots (two 128 x 64 code tiles) filled by TMA
+constexpr int kStagesMx = 4;               // MXFP8 experts: A slots in TMEM (64 columns: two tiles of f16
+                                           // pairs) the converter warps fill
+constexpr int kCodeStages = 8;             // MXFP8 experts: code slots (two 128 x 64 code tiles) filled by TMA
 constexpr int kCodeTile = 128 * 64;        // one code tile, 8 KB
 constexpr int kCodeSlot = 2 * kCodeTile;   // 16 KB
 constexpr int kScaleSlot = 2 * 128 * 16;   // one unit's scales: [tile][row][16 bytes], one byte per 32 k
@@ -57,9 +64,10 @@ constexpr int kConvWarps = 4;              // MXFP8 experts: warps 4-7 convert, 
 constexpr int kMmaWarp = 9;
 constexpr int kTQ = 4;                     // unit queue entries
 constexpr int kTmemCols = 64;              // two accumulator buffers of 32 columns
+constexpr int kTmemColsMx = 512;           // MXFP8: the accumulators, then the A slots from column 64
 constexpr size_t kSmem = (size_t)kStages * kSlotBytes + 3 * kBSlice + 1024;
-constexpr size_t kSmemMx =
-    (size_t)kStagesMx * kSlotBytes + (size_t)kCodeStages * kCodeSlot + 2 * kScaleSlot + 3 * kBSlice + 1024;
+constexpr size_t kSmemMx = (size_t)kCodeStages * kCodeSlot + 2 * kScaleSlot + 3 * kBSlice + 1024;
+static_assert(kTmemCols + kStagesMx * 64 <= kTmemColsMx, "TMEM of the MXFP8 instance");
 static_assert(kSmem <= 227 * 1024 - sizeof(DecSmem) - 512, "shared memory of one CTA");
 static_assert(kSmemMx <= 227 * 1024 - sizeof(DecSmem) - 512, "shared memory of one CTA (MXFP8 experts)");
 static_assert(kEpiWarps + kConvWarps == kWorkerWarps, "the worker warps split into epilogue and converters");
@@ -172,6 +180,28 @@ __device__ __forceinline__ void e4m3x16_scaled_f16(const uint4 q, uint32_t fac, 
   o1 = make_uint4(p[4], p[5], p[6], p[7]);
 }
 
+// 32 consecutive TMEM columns of this thread's lane (32x32b shape: lane 32 (warp % 4) + laneid)
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+// D (+)= A B^T with A (128 rows x 16 k, f16) in TMEM at column a_tmem, B from shared memory
+__device__ __forceinline__ void tc_mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // x as three f16 planes, x ~ 2^16 p0 + 2^5 p1 + 2^-6 p2, each plane the f16 rounding of what the
 // planes before it left (the residuals are exact in f32).  For |x| < 2^32 every plane is in range and
 // |x - sum| <= 2^-33 |x| + 2^-31; beyond, p0 is infinite.  The epilogue weighs the three column
@@ -248,10 +278,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     decode_tc_kernel(const __grid_constant__ DecodeTcMaps tm, DecodeArgs a, DecodeTcArgs t) {
   using namespace dtc;
   constexpr int rows = ROWS;
-  constexpr int NA = MX ? kStagesMx : kStages;  // A ring slots
+  constexpr int NA = MX ? kStagesMx : kStages;  // A slots (bf16: shared memory; MXFP8: TMEM)
+  constexpr int kCols = MX ? kTmemColsMx : kTmemCols;
   extern __shared__ uint8_t dsm_raw[];
   uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *codes = ring + (size_t)NA * kSlotBytes;                 // MXFP8: the code ring
+  uint8_t *codes = ring + (MX ? 0 : (size_t)NA * kSlotBytes);     // MXFP8: the code ring
   uint8_t *scales = codes + (MX ? (size_t)kCodeStages * kCodeSlot : 0);  // MXFP8: two scale slots
   uint8_t *xs = scales + (MX ? 2 * kScaleSlot : 0);  // this CTA's slice of x as B tiles
   uint8_t *as = xs + kBSlice;                          // two act slices
@@ -299,7 +330,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     sm.flag = (int)atomicAdd(&cnt[kCntRole], 1u);
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) tmem_alloc(&tmem_base, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(&tmem_base, kCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -368,10 +399,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
     if (MX && warp >= kEpiWarps) {
       // ---------------- converters (MXFP8 experts): each k-step's two 128 x 64 code tiles times
-      // their scales, as bf16 into an A ring slot in the MMA's swizzled layout.  Thread (warp w,
-      // lane l) takes rows 32 (w - 4) + 8 i + l / 4 (i = 0..3) of both tiles, 16-code chunk l % 4:
-      // its reads of a code tile are conflict-free, and so are its swizzled 16-byte stores. ----------------
-      const int cw = warp - kEpiWarps, ch = lane & 3;
+      // their scales, as f16 weights into an A slot in TMEM, where the MMAs read them (row i of a
+      // tile in TMEM lane i, f16 pair (2c, 2c + 1) in column c of its 32).  Warp w converts rows
+      // 32 (w - 4) .. + 31, its own TMEM lane quarter, one row a thread; TMA leaves the code tiles
+      // with the 64-byte swizzle, so that the 16-byte chunk c of row n sits at chunk c ^ ((n / 2) % 4)
+      // and a warp's reads of one chunk from 32 rows are conflict-free. ----------------
+      const int cw = warp - kEpiWarps, n = cw * 32 + lane;
+      const uint32_t tq_lane = tmem + ((uint32_t)(cw * 32) << 16);
       int j = 0;  // k-steps converted
       for (int u = 0;; ++u) {
         const int q = u % kTQ;
@@ -404,28 +438,30 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             break;
           }
           (void)mbar_try_wait(&code_full[cs], pc);
-          const uint8_t *src = codes + (size_t)cs * kCodeSlot;
-          uint8_t *dst = ring + (size_t)s * kSlotBytes;
-          // all eight items' codes and scales first: the conversions then overlap (the stores into
-          // the A slot would otherwise order every later load behind them)
+          tc_fence_after();  // the MMAs that read this A slot before are complete
+          const uint8_t *src = codes + (size_t)cs * kCodeSlot + n * 64;
+          // the row's codes (both tiles) and scales first, so that the conversions overlap
           uint4 qv[8];
-          unsigned sv[8];
+          unsigned sv[4];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int tt = i >> 2, n = cw * 32 + (i & 3) * 8 + (lane >> 2);
-            qv[i] = *reinterpret_cast<const uint4 *>(src + tt * kCodeTile + n * 64 + ch * 16);
-            sv[i] = sc[tt * 2048 + n * 16 + 2 * c + (ch >> 1)];
-          }
+          for (int i = 0; i < 8; ++i)
+            qv[i] = *reinterpret_cast<const uint4 *>(src + (i >> 2) * kCodeTile + (((i & 3) ^ ((n >> 1) & 3)) << 4));
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int tt = i >> 2, n = cw * 32 + (i & 3) * 8 + (lane >> 2);
-            uint4 o0, o1;
-            e4m3x16_scaled_f16(qv[i], f16x2_pow2((int)sv[i] - 127 + t.mx_c), o0, o1);
-            uint8_t *row = dst + tt * kTile + n * 128;
-            *reinterpret_cast<uint4 *>(row + (((2 * ch) ^ (n & 7)) << 4)) = o0;
-            *reinterpret_cast<uint4 *>(row + (((2 * ch + 1) ^ (n & 7)) << 4)) = o1;
+          for (int i = 0; i < 4; ++i) sv[i] = sc[(i >> 1) * 2048 + n * 16 + 2 * c + (i & 1)];
+#pragma unroll
+          for (int tt = 0; tt < 2; ++tt) {
+            uint32_t v[32];
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+              uint4 o0, o1;
+              e4m3x16_scaled_f16(qv[tt * 4 + ch], f16x2_pow2((int)sv[tt * 2 + (ch >> 1)] - 127 + t.mx_c), o0, o1);
+              v[ch * 8 + 0] = o0.x, v[ch * 8 + 1] = o0.y, v[ch * 8 + 2] = o0.z, v[ch * 8 + 3] = o0.w;
+              v[ch * 8 + 4] = o1.x, v[ch * 8 + 5] = o1.y, v[ch * 8 + 6] = o1.z, v[ch * 8 + 7] = o1.w;
+            }
+            tmem_st32(tq_lane + (uint32_t)(kTmemCols + s * 64 + tt * 32), v);
           }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the MMAs read the tiles
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          tc_fence_before();  // the MMA issuer reads the slot after the barrier
           __syncwarp();
           if (lane == 0) {
             mbar_arrive(&full_bar[s]);
@@ -762,13 +798,25 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t sa = smem_u32(ring + (size_t)s * kSlotBytes), sb = bbase + (uint32_t)(c * kBTile);
+        const uint32_t sb = bbase + (uint32_t)(c * kBTile);
+        if (MX) {  // A from TMEM: slot s, 8 columns (16 k) an MMA
+          const uint32_t ta = tmem + (uint32_t)(kTmemCols + s * 64);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t accum = (c > 0 || k > 0) ? 1u : 0u;
-          const uint64_t bd = smem_desc_sw128(sb + k * 32);
-          tc_mma_f16(d0, smem_desc_sw128(sa + k * 32), bd, idesc, accum);
-          tc_mma_f16(d1, smem_desc_sw128(sa + kTile + k * 32), bd, idesc, accum);
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t accum = (c > 0 || k > 0) ? 1u : 0u;
+            const uint64_t bd = smem_desc_sw128(sb + k * 32);
+            tc_mma_f16_tmem_a(d0, ta + k * 8, bd, idesc, accum);
+            tc_mma_f16_tmem_a(d1, ta + 32 + k * 8, bd, idesc, accum);
+          }
+        } else {
+          const uint32_t sa = smem_u32(ring + (size_t)s * kSlotBytes);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t accum = (c > 0 || k > 0) ? 1u : 0u;
+            const uint64_t bd = smem_desc_sw128(sb + k * 32);
+            tc_mma_f16(d0, smem_desc_sw128(sa + k * 32), bd, idesc, accum);
+            tc_mma_f16(d1, smem_desc_sw128(sa + kTile + k * 32), bd, idesc, accum);
+          }
         }
         tc_commit(&empty_bar[s]);  // the slot is free once these MMAs have read it
       }
@@ -829,7 +877,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, kCols);
   }
   if (tid == 0) sm.flag = atomicAdd(&cnt[kCntExit], 1u) == gridDim.x - 1 ? 1 : 0;
   __syncthreads();

@@ -164,9 +164,10 @@ static bool make_tmap_bf16(CUtensorMap *m, const void *base, uint64_t inner, uin
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D byte matrix [outer, inner] (E4M3 codes), row-major; boxes of 128 rows x 64 bytes, unswizzled
-// (the converter warps of the tensor-core decode read them row by row); rows past `outer` read as
-// zeros.
+// 2-D byte matrix [outer, inner] (E4M3 codes), row-major; boxes of 128 rows x 64 bytes with the
+// 64-byte swizzle (16-byte chunk c of box row n lands at chunk c ^ ((n / 2) % 4), so that the
+// converter warps of the tensor-core decode, one row a thread, read them without bank conflicts);
+// rows past `outer` read as zeros.
 static bool make_tmap_u8(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
@@ -175,7 +176,7 @@ static bool make_tmap_u8(CUtensorMap *m, const void *base, uint64_t inner, uint6
   cuuint32_t box[2] = {64, 128};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
