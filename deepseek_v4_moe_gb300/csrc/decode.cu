@@ -727,10 +727,10 @@ void launch_decode(const Dims &d, const Scratch &s, const LayerDev &w, const flo
   a.eps = d.eps;
   a.wait_ns = dbg.wait_ns ? dbg.wait_ns : kSpinLimitNs;
   a.inject = dbg.inject;
-  // the tensor-core kernel; MXFP8 layers take it from two rows on (on the 4096 x 2048, 256-expert
-  // shapes it measured 229 us against this kernel's 296 us at four rows, and 83 us against 71 us at
-  // one row, where this kernel's cost per weight byte is lowest)
-  if (w.mx ? s.dtc_mx && w.mx_tc && rows >= 2 : s.dtc)
+  // the tensor-core kernel; MXFP8 layers take it at four rows only (on the 4096 x 2048, 256-expert
+  // shapes it measured 229 us against this kernel's 296 us at four rows, but 184 / 136 / 83 us
+  // against 172 / 109 / 72 us at three / two / one rows)
+  if (w.mx ? s.dtc_mx && w.mx_tc && rows == kDecodeRows : s.dtc)
     launch_decode_tc(a, d, s, w, rows, w.mx ? s.decode_ctas_mx[rows] : s.decode_ctas_by_rows[rows], st);
   else
     launch_pdl(decode_kernel_for(rows, w.mx), dim3(w.mx ? s.decode_ctas_mx_cc[rows] : s.decode_ctas_by_rows[rows]),

@@ -259,12 +259,12 @@ int moe_ffn_hc_post(moe_ffn_handle *h, const float *f, const float *state, const
  * 7, 3 mantissa bits; no infinities) in the bf16 matrices' layouts, and one E8M0 scale (2^(s-127))
  * per 32 consecutive elements of a row, so element k of a row is value(code) * 2^(scale[k/32] - 127).
  * The rest of the block is unchanged.  Rows <= 4 stream the codes and scales (about half the bytes
- * of bf16).  The decode kernel turns each tile into exact f16 weights in shared memory for the
- * tensor cores (the batch rows go in as three f16 planes: values of magnitude 2^32 and above come
- * out infinite); that needs every scale of the layer within 22 binades of its largest and no NaN
- * code or scale, and a layer outside that decodes on the CUDA-core kernel instead.  Larger batches
- * run the tensor-core path on a bf16 expansion made at registration, exact wherever code x scale
- * is a normal bf16. */
+ * of bf16).  At four rows the decode kernel turns each tile into exact f16 weights in tensor memory
+ * for the tensor cores (the batch rows go in as three f16 planes: values of magnitude 2^32 and
+ * above come out infinite); that needs every scale of the layer within 22 binades of its largest
+ * and no NaN code or scale, and a layer outside that, or one to three rows, decodes on the
+ * CUDA-core kernel instead.  Larger batches run the tensor-core path on a bf16 expansion made at
+ * registration, exact wherever code x scale is a normal bf16. */
 typedef struct moe_ffn_mxfp8_experts {
   const uint8_t *gate_exps, *gate_exps_scale;  /* E4M3 [experts, inter, hidden], E8M0 [experts, inter, hidden/32] */
   const uint8_t *up_exps, *up_exps_scale;      /* the same layouts */
