@@ -70,11 +70,13 @@ struct Scratch {
   unsigned *dec_counters; // the decode kernel's tickets and completion counters (zero between launches)
   int decode_ctas_by_rows[5];  // co-resident CTAs of the persistent decode kernel, per row count
   int decode_ctas_mx[5];       // the same for its MXFP8-expert instances
-  int decode_ctas_mx_cc[5];    // the CUDA-core kernel's MXFP8 instances (layers with NaN codes)
-  // decode on the tensor cores (bf16 experts)
+  int decode_ctas_mx_cc[5];    // the CUDA-core kernel's MXFP8 instances (one to three rows, and layers
+                               // whose codes the tensor-core instance cannot widen exactly)
+  // decode on the tensor cores
   double *dtc_acc_gu;          // [groups, 2, 4, inter] gate and up partial sums (zero between launches)
   double *dtc_acc_y;           // [4, hidden] the FFN output (zero between launches)
-  uint16_t *dtc_act2;          // [groups, 16, inter] bf16: act hi planes (rows 0-3), lo planes (rows 4-7)
+  uint16_t *dtc_act2;          // [groups, 16, inter]: act as bf16 hi (rows 0-3) and lo (rows 4-7) planes,
+                               // or (MXFP8 experts) as three f16 planes (rows 0-3, 4-7, 8-11)
   CUtensorMap tm_dtc_act2;     // over dtc_act2, boxes of 64 x 16 rows
   bool dtc;                    // the tensor-core decode kernel fits this configuration (bf16 experts)
   bool dtc_mx;                 // ... and its MXFP8 instance

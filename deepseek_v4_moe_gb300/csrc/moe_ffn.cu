@@ -313,7 +313,8 @@ extern "C" int moe_ffn_init(const moe_ffn_config *cfg, const moe_ffn_layer_weigh
   for (int mx = 0; mx < 2; ++mx)
     for (int r = 1; r <= moe::kDecodeRows; ++r) {
       int &n = mx ? s.decode_ctas_mx[r] : s.decode_ctas_by_rows[r];
-      // bf16 experts stream on the tensor cores (one CTA per SM) where the K splits fit the grid
+      // the tensor-core decode (one CTA per SM) where its K splits fit the grid; the CUDA-core
+      // kernel's count is kept for MXFP8 layers, which use it at one to three rows
       const int tc = moe::decode_tc_resident_ctas(r, h->num_sms, mx != 0);
       bool &fits = mx ? s.dtc_mx : s.dtc;
       fits = tc > 0 && moe::decode_tc_fits(d, tc);
