@@ -31,7 +31,8 @@
 // copies each unit's E8M0 scales with cp.async; warps 4-7 turn every k-step's codes into exact f16
 // weights (see e4m3x16_scaled_f16) and store them into an A slot in TMEM, which the MMAs read in
 // place of a shared-memory A tile (so the widened weights never pass through shared memory).  The
-// batch rows are then three f16 planes (split3_f16) instead of the bf16 hi / lo pair.
+// batch rows are then three f16 planes (split3_f16) instead of the bf16 hi / lo pair, in B rows
+// r, 4 + r and 8 + r, and the MMAs run kind::f16 with f16 operands.
 //
 // Roles: warps 0-7 run the prelude, then the epilogue (two groups of four alternating units, one TMEM
 // lane quarter per warp; MXFP8: warps 0-3 take every unit and warps 4-7 convert);
